@@ -1,0 +1,175 @@
+"""Oracle of the fused op: residual add, RMSNorm, block-scaled FP4 quantization.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).
+
+Follows the FlashInfer page ``add_rmsnorm_fp4quant.py``: the module docstring
+(residual updated in place to input + residual, y = residual / sqrt(mean of
+squares + eps) * weight, then FP4 quantization) and ``kernel`` phases 2 and 3,
+written as the plain per-row definition with the rounding rule of
+``oracle.formats``.  Per row m (fp32, each op rounded to nearest even):
+
+  1. h = round_dtype(float(x) + float(r))            (phase 2; new residual)
+  2. ss = sum of h^2 in fp64;  ms = fp32(ss / H);  rstd = 1 / sqrt(ms + eps)
+  3. y = (h * rstd) * w
+  4. per block of b elements: amax = max |y|
+       NVFP4 (b = 16): t = min(amax / 6, 448), scale = E4M3_rne(t)
+       MXFP4 (b = 32): t = amax / 6,             scale = UE8M0 at or above t
+  5. v = y / s (s = decoded scale); code = E2M1_rne(v)  (s == 0: codes 0)
+  6. two codes per byte, element 2j in the low nibble
+  7. scale bytes row-major [m, k] and/or in the 128x4 tile order
+     (m//128)*nkt*512 + (k//4)*512 + (m%32)*16 + ((m%128)//32)*4 + k%4,
+     nkt = ceil(nb / 4), every padding byte of the tiled buffer zero.
+
+Readings where the pages are silent (helper bodies absent):
+  * the sum of squares uses the rounded h (the value written back), fp64 sum;
+  * v is a correctly rounded fp32 division (the page multiplies by an
+    approximate reciprocal; the difference only moves values within an ulp of
+    a rounding boundary);
+  * a block whose scale is zero (amax = 0, or NVFP4 amax/6 below half the
+    smallest E4M3 subnormal) gets all-zero codes;
+  * padding rows [M, 128*ceil(M/128)) and padding k in [nb, 4*nkt) of the
+    tiled buffer are written 0 (the vLLM ``fused_wo_a`` page zero-fills its
+    own padding in the same tile order).
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+from .formats import (
+    F32,
+    e2m1_decode,
+    e2m1_encode,
+    e4m3_decode,
+    e4m3_encode_rne,
+    round_to_dtype,
+    ue8m0_decode,
+    ue8m0_encode_ceil,
+)
+
+E2M1_MAX = F32(6.0)      # FlashInfer page, Notes: FP4 E2M1 maximum
+E4M3_MAX = F32(448.0)    # FlashInfer page, Notes: E4M3 maximum
+
+
+def block_size(fmt: str) -> int:
+    return {"nvfp4": 16, "mxfp4": 32}[fmt]
+
+
+def swizzled_sf_offset(m, k, nkt):
+    """Byte offset of scale (row m, block k) in the 128x4 tiled layout
+    (FlashInfer page, ``add_rmsnorm_fp4quant`` Parameters,
+    ``is_sf_swizzled_layout``; same in-tile order in vLLM ``fused_wo_a``)."""
+    m = np.asarray(m, dtype=np.int64)
+    k = np.asarray(k, dtype=np.int64)
+    return ((m // 128) * nkt * 512 + (k // 4) * 512 + (m % 32) * 16
+            + ((m % 128) // 32) * 4 + (k % 4))
+
+
+def sf_size_bytes(M: int, H: int, fmt: str, layout: str) -> int:
+    """Bytes of one scale buffer (FlashInfer page, output allocation:
+    row-major (M, H/b); tiled ceil(M/128) * ceil((H/b)/4) * 512)."""
+    nb = H // block_size(fmt)
+    if layout == "rowmajor":
+        return M * nb
+    if layout == "swizzled":
+        return ((M + 127) // 128) * ((nb + 3) // 4) * 512
+    raise ValueError(layout)
+
+
+@dataclasses.dataclass
+class OracleResult:
+    residual: np.ndarray          # (M, H) fp32 holding dtype values: new residual
+    packed: np.ndarray            # (M, H/2) uint8
+    scale_codes: np.ndarray       # (M, nb) uint8, row-major
+    sf_rowmajor: Optional[np.ndarray]   # (M*nb,) uint8 when asked
+    sf_swizzled: Optional[np.ndarray]   # tiled buffer when asked
+    codes: np.ndarray             # (M, H) uint8 4-bit codes
+    rstd: np.ndarray              # (M,) fp32
+    y: np.ndarray                 # (M, H) fp32 normalised, weighted
+    t: np.ndarray                 # (M, nb) fp32 value the scale rounds from
+    scale: np.ndarray             # (M, nb) fp32 decoded scale
+    v: np.ndarray                 # (M, H) fp32 value each code rounds from
+
+
+def add_rmsnorm_fp4_quant(x, r, w, eps: float, dtype: str, fmt: str,
+                          layout: str) -> OracleResult:
+    """Run the oracle on one batch.
+
+    x, r: (M, H) arrays of dtype values (any float type; converted exactly to
+    fp32); w: (H,); dtype "bf16"/"fp16"; fmt "nvfp4"/"mxfp4"; layout
+    "rowmajor", "swizzled" or "both".
+    """
+    x = np.asarray(x, dtype=np.float32)
+    r = np.asarray(r, dtype=np.float32)
+    w = np.asarray(w, dtype=np.float32)
+    M, H = x.shape
+    b = block_size(fmt)
+    if H % b or H < 64:
+        raise ValueError("H must be a multiple of the block size and >= 64")
+    nb = H // b
+
+    # 1. residual add, rounded to the storage dtype
+    h = round_to_dtype(x + r, dtype)
+
+    # 2. mean of squares and reciprocal root
+    ss = np.sum(h.astype(np.float64) ** 2, axis=1)
+    ms = (ss / H).astype(np.float32)
+    rstd = F32(1.0) / np.sqrt(ms + F32(eps))
+
+    # 3. normalise and weight, in this order
+    y = (h * rstd[:, None]) * w[None, :]
+
+    # 4. per-block amax and scale
+    yb = y.reshape(M, nb, b)
+    amax = np.max(np.abs(yb), axis=2) if M else np.zeros((0, nb), np.float32)
+    if fmt == "nvfp4":
+        t = np.minimum(amax / E2M1_MAX, E4M3_MAX)
+        scode = e4m3_encode_rne(t)
+        scale = e4m3_decode(scode)
+    else:
+        t = amax / E2M1_MAX
+        scode = ue8m0_encode_ceil(t)
+        scale = ue8m0_decode(scode)
+
+    # 5. element codes
+    with np.errstate(divide="ignore", invalid="ignore"):
+        vb = yb / scale[:, :, None]
+    vb = np.where(scale[:, :, None] == 0, F32(0.0), vb).astype(np.float32)
+    v = vb.reshape(M, H)
+    codes = e2m1_encode(v)
+
+    # 6. pack, element 2j in the low nibble
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << np.uint8(4))).astype(np.uint8)
+
+    # 7. scale layouts
+    sf_rm = scode.reshape(-1).copy() if layout in ("rowmajor", "both") else None
+    sf_sw = None
+    if layout in ("swizzled", "both"):
+        nkt = (nb + 3) // 4
+        sf_sw = np.zeros(sf_size_bytes(M, H, fmt, "swizzled"), dtype=np.uint8)
+        mm, kk = np.meshgrid(np.arange(M), np.arange(nb), indexing="ij")
+        sf_sw[swizzled_sf_offset(mm, kk, nkt)] = scode
+    return OracleResult(h, packed, scode, sf_rm, sf_sw, codes, rstd, y, t, scale, v)
+
+
+def dequant(packed, sf, M: int, H: int, fmt: str, layout: str) -> np.ndarray:
+    """E2M1 value times its block scale, fp32 (exact), from packed bytes and a
+    scale buffer in either layout (FlashRT ``fp4-gemm`` README, Validation:
+    compare through the dequantised values)."""
+    packed = np.asarray(packed, dtype=np.uint8).reshape(M, H // 2)
+    b = block_size(fmt)
+    nb = H // b
+    codes = np.empty((M, H), dtype=np.uint8)
+    codes[:, 0::2] = packed & np.uint8(0xF)
+    codes[:, 1::2] = packed >> np.uint8(4)
+    sf = np.asarray(sf, dtype=np.uint8).reshape(-1)
+    mm, kk = np.meshgrid(np.arange(M), np.arange(nb), indexing="ij")
+    if layout == "rowmajor":
+        scode = sf[mm * nb + kk]
+    else:
+        scode = sf[swizzled_sf_offset(mm, kk, (nb + 3) // 4)]
+    scale = e4m3_decode(scode) if fmt == "nvfp4" else ue8m0_decode(scode)
+    vals = e2m1_decode(codes).reshape(M, nb, b) * scale[:, :, None]
+    return vals.reshape(M, H).astype(np.float32)

@@ -1,0 +1,129 @@
+/*
+ * fp4q.h - C ABI of the GB300 (sm_103a) fused residual-add + RMSNorm +
+ * block-scaled FP4 quantization library (libfp4q.so).
+ *
+ * The operation is the one on the FlashInfer page `add_rmsnorm_fp4quant.py`
+ * (module docstring; `AddRMSNormFP4QuantKernel.kernel` phases 1-3;
+ * `add_rmsnorm_fp4quant` Parameters / Returns / Notes).  Per row m of an
+ * M x H batch, with b = 16 (NVFP4) or 32 (MXFP4), nb = H / b:
+ *
+ *   h        = round_dtype(float(input) + float(residual))   -> residual (in place)
+ *   rstd     = 1 / sqrt(sum(h^2) / H + eps)                   (fp32)
+ *   y        = (h * rstd) * weight                            (fp32, never stored)
+ *   per block of b elements:
+ *     NVFP4: scale = E4M3 nearest-even of min(amax / 6, 448)
+ *     MXFP4: scale = UE8M0, the power of two at or above amax / 6
+ *     code  = E2M1 nearest-even of y / scale on {0,.5,1,1.5,2,3,4,6}, saturating,
+ *             sign in bit 3; a zero scale gives zero codes
+ *   out_packed[m, j] = code[2j] | code[2j+1] << 4
+ *
+ * Scale layouts (same page, `is_sf_swizzled_layout`, `output_both_sf_layouts`):
+ *   row-major : sf[m * nb + k]
+ *   tiled     : sf[(m/128)*nkt*512 + (k/4)*512 + (m%32)*16 + ((m%128)/32)*4 + k%4],
+ *               nkt = ceil(nb / 4), buffer = ceil(M/128) * nkt * 512 bytes, every
+ *               padding byte (rows >= M, k >= nb) written 0.  This is the scale
+ *               layout the FlashRT `fp4-gemm` README (Tensor Contract) names as
+ *               the CUTLASS SFA input of its NVFP4 GEMM.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     allocates nothing and keeps no state between calls.
+ *   - Tensors are dense row-major (row stride = H elements / H/2 bytes).
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream);
+ *     argument errors are detected on the host before anything is launched.
+ *   - Status codes, never exceptions or aborts.
+ */
+#ifndef FP4Q_H_
+#define FP4Q_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* fp4q_stream_t;
+
+typedef enum { FP4_DT_BF16 = 0, FP4_DT_FP16 = 1 } fp4_dtype_t;
+
+/* NVFP4: 16-element blocks, E4M3 scale bytes.  MXFP4: 32-element blocks,
+ * UE8M0 scale bytes (FlashInfer page, `block_size` / `scale_format`). */
+typedef enum { FP4_NVFP4 = 0, FP4_MXFP4 = 1 } fp4_format_t;
+
+typedef enum {
+  FP4_SF_ROWMAJOR = 0, /* (M, nb) bytes                                  */
+  FP4_SF_SWIZZLED = 1, /* 128x4 tiled, padded to whole tiles             */
+  FP4_SF_BOTH = 2      /* tiled into out_sf AND row-major into out_sf_rowmajor */
+} fp4_sf_layout_t;
+
+typedef enum {
+  FP4_OK = 0,
+  FP4_ERR_INVALID_ARG = 1,       /* null pointer, bad enum, negative size, overlap */
+  FP4_ERR_UNSUPPORTED_SHAPE = 2, /* H % b != 0, H < 64, or H above the maximum     */
+  FP4_ERR_MISALIGNED = 3,        /* a pointer breaks the alignment rule below       */
+  FP4_ERR_CUDA = 4               /* the CUDA runtime reported an error on launch    */
+} fp4_status_t;
+
+/* Largest supported H: one CTA holds up to 32768 elements of a row in
+ * registers and a thread-block cluster of up to 8 CTAs shares one row.  Above
+ * 32768, H / 16 must split evenly over the cluster (over chunk pairs for MXFP4). */
+#define FP4Q_MAX_H 262144
+
+/*
+ * fp4_add_rmsnorm_quant - the fused op (FlashInfer page, `add_rmsnorm_fp4quant`).
+ *
+ *   input           [M, H] dtype, read only.                      32-byte aligned.
+ *   residual        [M, H] dtype, read then overwritten with h.   32-byte aligned.
+ *   weight          [H]    dtype, read only.                      32-byte aligned.
+ *   eps             added to the mean of squares (fp32).
+ *   M               rows, >= 0 (M == 0: nothing is launched, FP4_OK).
+ *   H               hidden size: multiple of the block size, 64 <= H <= FP4Q_MAX_H.
+ *   out_packed      [M, H/2] bytes, two E2M1 codes per byte.       8-byte aligned.
+ *   out_sf          row-major scales (FP4_SF_ROWMAJOR) or the tiled buffer
+ *                   (FP4_SF_SWIZZLED / FP4_SF_BOTH, 4-byte aligned); size from
+ *                   fp4_sf_size_bytes.
+ *   out_sf_rowmajor row-major scales for FP4_SF_BOTH, else ignored (may be NULL).
+ *
+ * input must not overlap residual; outputs must not overlap inputs or each
+ * other.  Global scale is 1 (the page's default when none is given).
+ */
+fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void* weight,
+                                   float eps, int64_t M, int64_t H, fp4_dtype_t dtype,
+                                   fp4_format_t format, fp4_sf_layout_t sf_layout,
+                                   uint8_t* out_packed, uint8_t* out_sf,
+                                   uint8_t* out_sf_rowmajor, fp4q_stream_t stream);
+
+/*
+ * fp4_dequant - validation helper: out[m, i] = E2M1 value of code (m, i) times
+ * its block scale, fp32 (exact).  Mirrors the dequantise-and-compare method of
+ * the FlashRT `fp4-gemm` README (Validation; `dequantize_fp4_sfa_fp16`).
+ *
+ *   packed    [M, H/2] bytes.                      8-byte aligned.
+ *   sf        scales in `sf_layout` (FP4_SF_ROWMAJOR or FP4_SF_SWIZZLED).
+ *   out       [M, H] fp32.                         16-byte aligned.
+ * H must be a multiple of the block size (>= 16); M >= 0.
+ */
+fp4_status_t fp4_dequant(const uint8_t* packed, const uint8_t* sf, int64_t M, int64_t H,
+                         fp4_format_t format, fp4_sf_layout_t sf_layout, float* out,
+                         fp4q_stream_t stream);
+
+/*
+ * fp4_sf_size_bytes - bytes of ONE scale buffer in `layout` (FlashInfer page,
+ * output allocation; FlashRT README `sfa_size_bytes`): row-major M * (H/b);
+ * tiled ceil(M/128) * ceil((H/b)/4) * 512.  FP4_SF_BOTH returns the tiled size
+ * (the size of out_sf).  Returns -1 on bad arguments.  Host only; no GPU needed.
+ */
+int64_t fp4_sf_size_bytes(int64_t M, int64_t H, fp4_format_t format, fp4_sf_layout_t layout);
+
+/* Static, NUL-terminated description of a status code. */
+const char* fp4_status_string(fp4_status_t status);
+
+/* cudaError_t value behind the last FP4_ERR_CUDA returned on this thread (0 if none). */
+int fp4_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP4Q_H_ */

@@ -1,0 +1,33 @@
+"""GB300-native fused residual-add + RMSNorm + block-scaled FP4 quantization.
+
+The computation lives in libfp4q.so (hand-written sm_103a CUDA kernels behind
+the C ABI in include/fp4q.h).  This package is a thin ctypes binding: the
+functions named like the C entry points take raw device addresses, and
+``add_rmsnorm_fp4quant`` / ``dequant`` marshal torch tensors (PyTorch provides
+device memory and streams only).  There is no fallback: if the library is not
+built, or a tensor is not on a CUDA device, the call raises.
+
+Operation (FlashInfer page ``add_rmsnorm_fp4quant.py``, ``add_rmsnorm_fp4quant``):
+residual <- input + residual; y = residual / sqrt(mean(residual^2) + eps) * weight;
+y quantized to E2M1 with one scale per 16 (NVFP4, E4M3) or 32 (MXFP4, UE8M0)
+elements, scales row-major and/or in the 128x4 tiled layout.
+"""
+from ._binding import (  # noqa: F401
+    FP4_DT_BF16,
+    FP4_DT_FP16,
+    FP4_MXFP4,
+    FP4_NVFP4,
+    FP4_SF_BOTH,
+    FP4_SF_ROWMAJOR,
+    FP4_SF_SWIZZLED,
+    Fp4Error,
+    add_rmsnorm_fp4quant,
+    dequant,
+    fp4_add_rmsnorm_quant,
+    fp4_dequant,
+    fp4_last_cuda_error,
+    fp4_sf_size_bytes,
+    fp4_status_string,
+    lib,
+    lib_path,
+)

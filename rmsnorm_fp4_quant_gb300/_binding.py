@@ -1,0 +1,174 @@
+"""ctypes binding of libfp4q.so: argument marshalling only, no computation."""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+from .build import LIBPATH
+
+FP4_DT_BF16, FP4_DT_FP16 = 0, 1
+FP4_NVFP4, FP4_MXFP4 = 0, 1
+FP4_SF_ROWMAJOR, FP4_SF_SWIZZLED, FP4_SF_BOTH = 0, 1, 2
+
+_FORMATS = {"nvfp4": FP4_NVFP4, "mxfp4": FP4_MXFP4}
+_LAYOUTS = {"rowmajor": FP4_SF_ROWMAJOR, "swizzled": FP4_SF_SWIZZLED, "both": FP4_SF_BOTH}
+_BLOCK = {FP4_NVFP4: 16, FP4_MXFP4: 32}
+
+_lib = None
+
+
+class Fp4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = f"{where}: {fp4_status_string(status)} (status {status})"
+        if status == 4:
+            msg += f", cudaError {fp4_last_cuda_error()}"
+        super().__init__(msg)
+        self.status = status
+
+
+def lib_path() -> str:
+    return LIBPATH
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libfp4q.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIBPATH):
+        raise RuntimeError(f"{LIBPATH} is missing: build it with "
+                           "`python -m rmsnorm_fp4_quant_gb300.build` (needs nvcc)")
+    L = ctypes.CDLL(LIBPATH)
+    vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    L.fp4_add_rmsnorm_quant.argtypes = [vp, vp, vp, ctypes.c_float, i64, i64, ci, ci, ci,
+                                        vp, vp, vp, vp]
+    L.fp4_add_rmsnorm_quant.restype = ci
+    L.fp4_dequant.argtypes = [vp, vp, i64, i64, ci, ci, vp, vp]
+    L.fp4_dequant.restype = ci
+    L.fp4_sf_size_bytes.argtypes = [i64, i64, ci, ci]
+    L.fp4_sf_size_bytes.restype = i64
+    L.fp4_status_string.argtypes = [ci]
+    L.fp4_status_string.restype = ctypes.c_char_p
+    L.fp4_last_cuda_error.argtypes = []
+    L.fp4_last_cuda_error.restype = ci
+    _lib = L
+    return L
+
+
+# ---------------------------------------------------------------------------
+# Same names as the C ABI; raw integer addresses and a raw stream handle.
+# ---------------------------------------------------------------------------
+def fp4_add_rmsnorm_quant(input_ptr: int, residual_ptr: int, weight_ptr: int, eps: float,
+                          M: int, H: int, dtype: int, fmt: int, sf_layout: int,
+                          out_packed_ptr: int, out_sf_ptr: int, out_sf_rowmajor_ptr: int,
+                          stream: int) -> int:
+    return lib().fp4_add_rmsnorm_quant(input_ptr, residual_ptr, weight_ptr, eps, M, H, dtype,
+                                       fmt, sf_layout, out_packed_ptr, out_sf_ptr,
+                                       out_sf_rowmajor_ptr or None, stream or None)
+
+
+def fp4_dequant(packed_ptr: int, sf_ptr: int, M: int, H: int, fmt: int, sf_layout: int,
+                out_ptr: int, stream: int) -> int:
+    return lib().fp4_dequant(packed_ptr, sf_ptr, M, H, fmt, sf_layout, out_ptr, stream or None)
+
+
+def fp4_sf_size_bytes(M: int, H: int, fmt: int, layout: int) -> int:
+    return lib().fp4_sf_size_bytes(M, H, fmt, layout)
+
+
+def fp4_status_string(status: int) -> str:
+    return lib().fp4_status_string(status).decode()
+
+
+def fp4_last_cuda_error() -> int:
+    return lib().fp4_last_cuda_error()
+
+
+# ---------------------------------------------------------------------------
+# torch-tensor convenience layer (allocation and stream lookup only)
+# ---------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _check_cuda(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def add_rmsnorm_fp4quant(input, residual, weight, eps: float = 1e-6, fmt: str = "nvfp4",
+                         sf_layout: str = "rowmajor", out_packed=None, out_sf=None,
+                         out_sf_rowmajor=None, stream=None) -> Tuple:
+    """residual += input (in place); returns (packed, sf) or, for
+    sf_layout="both", (packed, sf_tiled, sf_rowmajor).  ``input`` may be 2-D
+    (M, H) or 3-D (B, S, H); packed has the same leading shape with H/2 bytes.
+    Scale buffers are uint8: row-major (M, H/b), tiled flat."""
+    torch = _torch()
+    for name, t in (("input", input), ("residual", residual), ("weight", weight)):
+        _check_cuda(t, name)
+    if input.shape != residual.shape or input.dtype != residual.dtype:
+        raise ValueError("input and residual must have the same shape and dtype")
+    if weight.dtype != input.dtype or weight.dim() != 1 or weight.shape[0] != input.shape[-1]:
+        raise ValueError("weight must be (H,) with the input's dtype")
+    if input.dtype == torch.bfloat16:
+        dt = FP4_DT_BF16
+    elif input.dtype == torch.float16:
+        dt = FP4_DT_FP16
+    else:
+        raise ValueError("dtype must be bfloat16 or float16")
+    f = _FORMATS[fmt]
+    lay = _LAYOUTS[sf_layout]
+    H = input.shape[-1]
+    lead = tuple(input.shape[:-1])
+    M = 1
+    for d in lead:
+        M *= d
+    dev = input.device
+    if out_packed is None:
+        out_packed = torch.empty(*lead, H // 2, dtype=torch.uint8, device=dev)
+    nb = H // _BLOCK[f]
+    if out_sf is None:
+        if lay == FP4_SF_ROWMAJOR:
+            out_sf = torch.empty(*lead, nb, dtype=torch.uint8, device=dev)
+        else:
+            out_sf = torch.empty(max(fp4_sf_size_bytes(M, H, f, lay), 0), dtype=torch.uint8,
+                                 device=dev)
+    if lay == FP4_SF_BOTH and out_sf_rowmajor is None:
+        out_sf_rowmajor = torch.empty(*lead, nb, dtype=torch.uint8, device=dev)
+    for name, t in (("out_packed", out_packed), ("out_sf", out_sf)):
+        _check_cuda(t, name)
+    st = fp4_add_rmsnorm_quant(input.data_ptr(), residual.data_ptr(), weight.data_ptr(),
+                               float(eps), M, H, dt, f, lay, out_packed.data_ptr(),
+                               out_sf.data_ptr(),
+                               out_sf_rowmajor.data_ptr() if out_sf_rowmajor is not None else 0,
+                               _stream_handle(stream))
+    if st != 0:
+        raise Fp4Error(st, "fp4_add_rmsnorm_quant")
+    if lay == FP4_SF_BOTH:
+        return out_packed, out_sf, out_sf_rowmajor
+    return out_packed, out_sf
+
+
+def dequant(packed, sf, M: int, H: int, fmt: str = "nvfp4", sf_layout: str = "rowmajor",
+            out=None, stream=None):
+    """fp32 (M, H) = E2M1 value of each code times its block scale."""
+    torch = _torch()
+    _check_cuda(packed, "packed")
+    _check_cuda(sf, "sf")
+    if out is None:
+        out = torch.empty(M, H, dtype=torch.float32, device=packed.device)
+    st = fp4_dequant(packed.data_ptr(), sf.data_ptr(), M, H, _FORMATS[fmt], _LAYOUTS[sf_layout],
+                     out.data_ptr(), _stream_handle(stream))
+    if st != 0:
+        raise Fp4Error(st, "fp4_dequant")
+    return out

@@ -1,0 +1,68 @@
+// fp4q_launch.h - host/device shared parameter blocks and the launch entry
+// points behind the C ABI (include/fp4q.h).  Internal to the library.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp4q {
+
+// Threads per CTA allowed for a kernel instance holding `cpt` chunks per
+// thread: one chunk fits 64 registers (1024 threads), more chunks need up to 128.
+__host__ __device__ constexpr int max_threads_for_cpt(int cpt) { return cpt <= 1 ? 1024 : 512; }
+
+// One fused launch.  All pointers are device pointers; sf_tiled / sf_rm are
+// null when that layout is not written.
+struct FusedParams {
+  const void* x;
+  void* r;
+  const void* w;
+  uint8_t* packed;
+  uint8_t* sf_tiled;
+  uint8_t* sf_rm;
+  float eps;
+  int64_t M;           // valid rows
+  int64_t rows;        // row slots covered by the grid (M, or 128*ceil(M/128) when tiled)
+  int H;
+  int nchunk;          // H / 16
+  int nb;              // H / block
+  int nkt;             // ceil(nb / 4)
+  int tpr;             // threads per row slice
+  int rows_per_cta;    // row slices per CTA (1 with clusters)
+  int cluster;         // CTAs per row (1 = no cluster)
+  int chunks_per_cta;  // nchunk / cluster
+};
+
+// Launch shape chosen on the host for one (M, H, format).
+struct FusedShape {
+  int cpt;             // chunks per thread (template instance)
+  int tpr;
+  int rows_per_cta;
+  int cluster;
+  int chunks_per_cta;
+  int threads;         // tpr * rows_per_cta
+  int64_t grid;        // CTAs
+};
+
+// Picks the launch shape; returns false when H cannot be handled.
+bool choose_fused_shape(int64_t M, int H, int fmt, int num_sms, FusedShape* out);
+
+// Launches the fused kernel (dtype 0 = bf16, 1 = fp16; fmt 0 = NVFP4, 1 = MXFP4).
+cudaError_t launch_fused(int dtype, int fmt, const FusedShape& shape, const FusedParams& p,
+                         cudaStream_t stream);
+
+struct DequantParams {
+  const uint8_t* packed;
+  const uint8_t* sf;
+  float* out;
+  int64_t M;
+  int H;
+  int nchunk;
+  int nb;
+  int nkt;
+  int tiled;           // 1: sf is in the 128x4 tiled layout, 0: row-major
+};
+
+cudaError_t launch_dequant(int fmt, const DequantParams& p, cudaStream_t stream);
+
+}  // namespace fp4q

@@ -1,0 +1,9 @@
+// fp16 instances of the fused kernel (compiled in their own translation unit).
+#include "fused_kernel.cuh"
+
+namespace fp4q {
+cudaError_t launch_fused_fp16(int fmt, const FusedShape& s, const FusedParams& p,
+                              cudaStream_t stream) {
+  return launch_fused_dtype<__half>(fmt, s, p, stream);
+}
+}  // namespace fp4q

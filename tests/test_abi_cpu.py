@@ -1,0 +1,131 @@
+"""Host-side tests of the C ABI (no GPU): the library builds for sm_103a and
+loads, exports every entry point include/*.h declares, sizes scale buffers
+like the oracle, and rejects bad arguments before touching the device.  Only
+calls that fail argument validation are made, so no fake address is ever
+dereferenced or launched on."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import oracle
+import rmsnorm_fp4_quant_gb300 as fq
+from rmsnorm_fp4_quant_gb300 import build as fbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    fbuild.build()
+    return fq.lib()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M):
+            if m.group(1) not in ("if", "defined"):
+                names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for want in ("fp4_add_rmsnorm_quant", "fp4_dequant", "fp4_sf_size_bytes",
+                 "fp4_status_string", "fp4_last_cuda_error"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_library_is_built_for_sm103a(L):
+    # the fatbin section of the .so carries an sm_103a cubin; nvcc names the
+    # arch in the ELF note, readable as plain bytes
+    data = open(fq.lib_path(), "rb").read()
+    assert b"sm_103a" in data or b"sm_103" in data
+
+
+@pytest.mark.parametrize("M", [0, 1, 4, 41, 127, 128, 129, 512, 8192, 32768])
+@pytest.mark.parametrize("H", [64, 80, 256, 1536, 5120, 7168, 17408, 32768])
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+def test_sf_size_matches_oracle(L, M, H, fmt):
+    f = fq.FP4_NVFP4 if fmt == "nvfp4" else fq.FP4_MXFP4
+    b = 16 if fmt == "nvfp4" else 32
+    if H % b:
+        assert fq.fp4_sf_size_bytes(M, H, f, fq.FP4_SF_ROWMAJOR) == -1
+        return
+    assert fq.fp4_sf_size_bytes(M, H, f, fq.FP4_SF_ROWMAJOR) == oracle.sf_size_bytes(M, H, fmt, "rowmajor")
+    assert fq.fp4_sf_size_bytes(M, H, f, fq.FP4_SF_SWIZZLED) == oracle.sf_size_bytes(M, H, fmt, "swizzled")
+    assert fq.fp4_sf_size_bytes(M, H, f, fq.FP4_SF_BOTH) == oracle.sf_size_bytes(M, H, fmt, "swizzled")
+
+
+def test_sf_size_rejects_bad_arguments(L):
+    assert fq.fp4_sf_size_bytes(-1, 256, 0, 0) == -1
+    assert fq.fp4_sf_size_bytes(4, 0, 0, 0) == -1
+    assert fq.fp4_sf_size_bytes(4, 256, 7, 0) == -1
+    assert fq.fp4_sf_size_bytes(4, 256, 0, 9) == -1
+
+
+def test_status_strings(L):
+    for s in range(5):
+        assert fq.fp4_status_string(s) and fq.fp4_status_string(s) != "unknown status"
+    assert fq.fp4_status_string(99) == "unknown status"
+
+
+# Fake, never-dereferenced addresses: every call below must fail validation.
+A = 0x7F0000000000           # 4 KiB-aligned
+B = A + (1 << 32)
+W = A + (2 << 32)
+P = A + (3 << 32)
+S = A + (4 << 32)
+S2 = A + (5 << 32)
+
+
+def _call(x=A, r=B, w=W, eps=1e-6, M=4, H=256, dt=0, f=0, lay=0, p=P, s=S, s2=0):
+    return fq.fp4_add_rmsnorm_quant(x, r, w, eps, M, H, dt, f, lay, p, s, s2, 0)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(dt=2), 1), (dict(f=3), 1), (dict(lay=5), 1), (dict(M=-1), 1), (dict(H=0), 1),
+    (dict(eps=-1.0), 1), (dict(eps=float("nan")), 1),
+    (dict(H=40), 2), (dict(H=48), 2), (dict(H=80, f=1), 2), (dict(H=262144 + 16), 2),
+    (dict(x=0), 1), (dict(r=0), 1), (dict(w=0), 1), (dict(p=0), 1), (dict(s=0), 1),
+    (dict(lay=2, s2=0), 1),
+    (dict(x=A + 16), 3), (dict(r=B + 8), 3), (dict(w=W + 2), 3), (dict(p=P + 4), 3),
+    (dict(r=A + 512), 1),                    # input and residual overlap
+    (dict(p=B + 64), 1),                     # packed inside the residual
+    (dict(s=P + 16), 1),                     # scales inside the packed output
+    (dict(lay=1, s=S + 2), 3),               # tiled scales need 4-byte alignment
+])
+def test_fused_validation(L, kwargs, status):
+    assert _call(**kwargs) == status
+
+
+def test_m_zero_is_a_no_op(L):
+    # nothing is launched and no pointer is looked at
+    assert _call(M=0, x=0, r=0, w=0, p=0, s=0) == 0
+
+
+@pytest.mark.parametrize("args,status", [
+    ((P, S, 4, 256, 2, 0, 0, 0), 1), ((P, S, 4, 256, 0, 2, 0, 0), 1), ((P, S, -1, 256, 0, 0, 0, 0), 1),
+    ((P, S, 4, 40, 0, 0, 0, 0), 2), ((0, S, 4, 256, 0, 0, A, 0), 1), ((P + 4, S, 4, 256, 0, 0, A, 0), 3),
+    ((P, S, 4, 256, 0, 0, A + 8, 0), 3), ((0, 0, 0, 256, 0, 0, 0, 0), 0),
+])
+def test_dequant_validation(L, args, status):
+    assert fq.fp4_dequant(*args) == status
+
+
+def test_tensor_api_refuses_cpu_tensors(L):
+    import torch
+    x = torch.zeros(4, 256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        fq.add_rmsnorm_fp4quant(x, x.clone(), torch.ones(256, dtype=torch.bfloat16))

@@ -1,0 +1,153 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle
+element by element (acceptance rule in tests/parity.py).  Shapes span several
+128-row scale tiles with ragged tails, every dtype / format / scale layout,
+the cluster (split-row) path, and special rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rmsnorm_fp4_quant_gb300 as fq
+import workloads
+from rmsnorm_fp4_quant_gb300 import build as fbuild
+
+import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fbuild.build()
+    fq.lib()
+    torch.cuda.init()
+
+
+def _wl(M, H, dtype, fmt, layout, eps=1e-6, seed=0, **kw):
+    return workloads.Workload(f"t_{M}_{H}", M, H, dtype, fmt, layout, eps, seed=seed, **kw)
+
+
+def _run_full(wl, x=None, r=None, w=None):
+    """Inputs on the CPU (or given), oracle on every row, GPU through the C ABI."""
+    if x is None:
+        x, r, w = workloads.make_inputs(wl, "cpu")
+    o = oracle.add_rmsnorm_fp4_quant(x.float().numpy(), r.float().numpy(), w.float().numpy(),
+                                     wl.eps, wl.dtype, wl.fmt, wl.sf_layout)
+    xd, rd, wd = x.cuda(), r.cuda(), w.cuda()
+    g = parity.run_gpu(xd, rd, wd, wl.eps, wl.fmt, wl.sf_layout)
+    stats = parity.compare(g, o, wl.fmt, wl.sf_layout, wl.dtype, wl.M, wl.H)
+    return g, o, stats
+
+
+SHAPES = [(1, 64), (3, 80), (127, 208), (300, 256), (129, 1536), (300, 4096), (130, 5120),
+          (129, 7168), (41, 17408), (1, 32768), (2, 65536), (5, 6144)]
+
+
+@pytest.mark.parametrize("M,H", SHAPES)
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("layout", ["rowmajor", "swizzled", "both"])
+def test_parity_grid(M, H, fmt, dtype, layout):
+    if H % oracle.block_size(fmt):
+        pytest.skip("H not a multiple of the block")
+    wl = _wl(M, H, dtype, fmt, layout, seed=M * 7 + H)
+    g, o, _ = _run_full(wl)
+    if layout != "both":
+        parity.check_dequant(g, M, H, fmt, layout)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+def test_special_rows(fmt):
+    """Zero rows, a one-hot row, constant rows, an eps-dominated row, negative
+    and signed-zero values, huge and tiny magnitudes in one batch."""
+    H = 256
+    M = 10
+    x = torch.zeros(M, H)
+    r = torch.zeros(M, H)
+    r[1, 0] = 1.0                                  # one-hot
+    r[2] = 1.0                                     # constant
+    r[3] = 2.0 ** -10                              # eps-dominated
+    x[4] = -0.5
+    r[4] = -1.5                                    # negative constant
+    x[5, ::2] = -0.0
+    r[5, ::2] = -0.0                               # -0 + -0 = -0 in the residual
+    r[5, 1::2] = 3.0
+    r[6] = torch.linspace(-1000, 1000, H)          # large magnitudes
+    r[7] = torch.linspace(-1e-20, 1e-20, H)        # tiny magnitudes
+    r[8, :16] = 1e4                                # one huge block among small ones
+    r[8, 16:] = 1e-3
+    x[9] = 1.0
+    r[9] = 2.0 ** -8                               # bf16 tie in the residual add
+    w = torch.ones(H)
+    w[::3] = -1.25                                 # negative weights give -0 in y
+    wl = _wl(M, H, "bf16", fmt, "both")
+    bf = torch.bfloat16
+    g, o, _ = _run_full(wl, x.to(bf), r.to(bf), w.to(bf))
+    assert np.all(g.packed[0] == 0)
+    parity.check_dequant(parity.GpuOut(g.rows, g.residual_bits, g.packed, g.sf, None),
+                         M, H, fmt, "swizzled")
+
+
+def test_determinism_and_stream():
+    """Two runs on the same inputs give identical bytes, on a side stream."""
+    wl = _wl(300, 7168, "bf16", "mxfp4", "swizzled", seed=5)
+    x, r, w = workloads.make_inputs(wl, "cuda")
+    r0 = r.clone()
+    s = torch.cuda.Stream()
+    outs = []
+    for _ in range(2):
+        rr = r0.clone()
+        torch.cuda.current_stream().synchronize()
+        with torch.cuda.stream(s):
+            p, sf = fq.add_rmsnorm_fp4quant(x, rr, w, eps=1e-6, fmt="mxfp4", sf_layout="swizzled",
+                                            stream=s)
+        s.synchronize()
+        outs.append((rr.cpu(), p.cpu(), sf.cpu()))
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
+
+
+def test_outputs_stay_inside_their_buffers():
+    """Canary bytes around every output buffer survive the call."""
+    M, H = 129, 5120
+    wl = _wl(M, H, "fp16", "nvfp4", "both", seed=9)
+    x, r, w = workloads.make_inputs(wl, "cuda")
+    pad = 4096
+    canary = 0xA5
+    n_pk = M * H // 2
+    n_sw = fq.fp4_sf_size_bytes(M, H, fq.FP4_NVFP4, fq.FP4_SF_SWIZZLED)
+    n_rm = M * (H // 16)
+    pk = torch.full((n_pk + 2 * pad,), canary, dtype=torch.uint8, device="cuda")
+    sw = torch.full((n_sw + 2 * pad,), canary, dtype=torch.uint8, device="cuda")
+    rm = torch.full((n_rm + 2 * pad,), canary, dtype=torch.uint8, device="cuda")
+    rbuf = torch.full((M * H + 2 * pad,), 7.0, dtype=torch.float16, device="cuda")
+    rbuf[pad:pad + M * H] = r.reshape(-1)
+    rv = rbuf[pad:pad + M * H].view(M, H)
+    fq.add_rmsnorm_fp4quant(x, rv, w, eps=1e-5, fmt="nvfp4", sf_layout="both",
+                            out_packed=pk[pad:pad + n_pk].view(M, H // 2),
+                            out_sf=sw[pad:pad + n_sw], out_sf_rowmajor=rm[pad:pad + n_rm])
+    torch.cuda.synchronize()
+    for buf, n in ((pk, n_pk), (sw, n_sw), (rm, n_rm)):
+        assert torch.all(buf[:pad] == canary) and torch.all(buf[pad + n:] == canary)
+    assert torch.all(rbuf[:pad] == 7.0) and torch.all(rbuf[pad + M * H:] == 7.0)
+
+
+def test_empty_batch_is_a_no_op():
+    x = torch.empty(0, 256, dtype=torch.bfloat16, device="cuda")
+    r = torch.empty(0, 256, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(256, dtype=torch.bfloat16, device="cuda")
+    p, sf = fq.add_rmsnorm_fp4quant(x, r, w, fmt="nvfp4", sf_layout="swizzled")
+    assert p.shape == (0, 128) and sf.numel() == 0
+
+
+def test_three_d_input_matches_two_d():
+    wl = _wl(6 * 7, 1536, "bf16", "nvfp4", "rowmajor", seed=11)
+    x, r, w = workloads.make_inputs(wl, "cuda")
+    r2 = r.clone()
+    p2, s2 = fq.add_rmsnorm_fp4quant(x, r2, w)
+    r3 = r.clone().view(6, 7, 1536)
+    p3, s3 = fq.add_rmsnorm_fp4quant(x.view(6, 7, 1536), r3, w)
+    torch.cuda.synchronize()
+    assert p3.shape == (6, 7, 768) and s3.shape == (6, 7, 96)
+    assert torch.equal(p2.view(6, 7, 768), p3) and torch.equal(r2.view(6, 7, 1536), r3)
+    assert torch.equal(s2.view(6, 7, 96), s3)

@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Benchmark of the fused residual-add + RMSNorm + FP4 quantization path.
+
+One step = one call of fp4_add_rmsnorm_quant (the whole hot path: add,
+RMSNorm, scales, codes, both writes) over one batch of the workload, inputs
+resident in HBM.  The default workload is M=8192 x H=7168 bf16, MXFP4 with
+tiled scales and 1% x50 outlier columns: 383.5 MB of algorithmic traffic per
+call, three times the 129 MB L2, so no L2 flush is needed between steps.
+Consecutive steps alternate between the input x and -x so the in-place
+residual stays bounded (both copies are read the same way).
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "fused add+RMSNorm+FP4-quant HBM GB/s and % of GB300 HBM roofline (rows/s)"
+DEFAULT_WORKLOAD = workloads.C3.name
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# environment helpers
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "rmsnorm_fp4_quant_gb300", "csrc")
+    for p in sorted(glob.glob(os.path.join(csrc, "*"))):
+        if p.endswith((".cu", ".cuh", ".h")):
+            h.update(os.path.basename(p).encode())
+            h.update(open(p, "rb").read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload_name: str):
+    """dram bytes per launch from a committed ncu summary whose kernel-source
+    hash matches the current sources; None otherwise."""
+    sha = kernel_source_sha()
+    for p in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        text = open(p).read()
+        m_w = re.search(r"^workload:\s*(\S+)", text, re.M)
+        m_s = re.search(r"^source_sha256:\s*([0-9a-f]{64})", text, re.M)
+        m_t = re.search(r"^dram_bytes_per_launch:\s*([0-9]+)", text, re.M)
+        if m_w and m_s and m_t and m_w.group(1) == workload_name and m_s.group(1) == sha:
+            return int(m_t.group(1)), os.path.relpath(p, ROOT)
+    return None, None
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in a background process; each line is
+    stamped on arrival so samples can be matched to the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.samples = []
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        pad = max(0.0, 0.35 - (t1 - t0) / 2)
+        sel = [p for (t, p) in self.samples if t0 - pad <= t <= t1 + pad]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in sel if num(p[0]) is not None]
+        mx = [num(p[1]) for p in sel if num(p[1]) is not None]
+        reasons = set()
+        for p in sel:
+            for name, val in zip(self.NAMES, p[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        pw = [num(p[2]) for p in sel if num(p[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sel),
+                "power_w_max": max(pw) if pw else None}
+
+
+def gpu_smi_id(torch, dev):
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_rows_timing(wl, nrows: int, row0: int = 0):
+    """Time the oracle (as it stands) on rows [row0, row0 + nrows) of `wl`."""
+    import oracle
+    x = workloads.make_rows(wl, "x", row0, row0 + nrows).float().numpy()
+    r = workloads.make_rows(wl, "r", row0, row0 + nrows).float().numpy()
+    w = workloads.make_weight(wl).float().numpy()
+    t = time.perf_counter()
+    oracle.add_rmsnorm_fp4_quant(x, r, w, wl.eps, wl.dtype, wl.fmt, wl.sf_layout)
+    return time.perf_counter() - t
+
+
+def cpu_rows_for(wl, seconds: float) -> int:
+    oracle_rows_timing(wl, 8)                       # warm the allocator
+    probe = min(wl.M, 32)
+    dt = oracle_rows_timing(wl, probe)
+    rows = int(probe * seconds / max(dt, 1e-6))
+    return max(1, min(wl.M, rows))
+
+
+def cpu_baseline(wl, seconds: float):
+    rows = cpu_rows_for(wl, seconds)
+    dt = oracle_rows_timing(wl, rows)
+    bytes_ = wl.with_shape(rows).algorithmic_bytes()
+    return {"value": round(bytes_ / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {rows} of {wl.M} rows of {wl.name}, numpy oracle single-threaded, "
+                      f"{dt:.1f} s", "rows_per_s": round(rows / dt, 2)}
+
+
+def run_reference(args, wl):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    per_step = cpu_rows_for(wl, 2.0)
+    for _ in range(args.warmup):
+        oracle_rows_timing(wl, min(per_step, 8))
+    times = [oracle_rows_timing(wl, per_step, row0=(i * per_step) % max(1, wl.M - per_step))
+             for i in range(args.steps)]
+    bytes_ = wl.with_shape(per_step).algorithmic_bytes()
+    tot = sum(times)
+    val = bytes_ * len(times) / tot / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot / len(times) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "M": wl.M, "H": wl.H, "format": wl.fmt,
+                   "sf_layout": wl.sf_layout, "io_dtype": wl.dtype,
+                   "sample_rows_per_step": per_step},
+        "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} of {wl.M} rows of {wl.name} per step, numpy "
+                                   f"oracle single-threaded"},
+        "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "rows_per_s": round(per_step * len(times) / tot, 2),
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import rmsnorm_fp4_quant_gb300 as fq
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    L = fq.lib()
+    fmt = fq.FP4_NVFP4 if wl.fmt == "nvfp4" else fq.FP4_MXFP4
+    lay = {"rowmajor": fq.FP4_SF_ROWMAJOR, "swizzled": fq.FP4_SF_SWIZZLED,
+           "both": fq.FP4_SF_BOTH}[wl.sf_layout]
+    dt = fq.FP4_DT_BF16 if wl.dtype == "bf16" else fq.FP4_DT_FP16
+
+    # each rank owns an independent batch (weak scaling, no data exchange)
+    import dataclasses
+    wl_r = dataclasses.replace(wl, seed=wl.seed + 1000 * rank)
+    x, r, w = workloads.make_inputs(wl_r, dev)
+    xneg = -x
+    M, H = wl.M, wl.H
+    nb = H // wl.block
+    packed = torch.empty(M, H // 2, dtype=torch.uint8, device=dev)
+    sf = torch.empty(max(1, fq.fp4_sf_size_bytes(M, H, fmt, lay)), dtype=torch.uint8, device=dev)
+    sf_rm = torch.empty(M * nb, dtype=torch.uint8, device=dev) if lay == fq.FP4_SF_BOTH else None
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    ptrs = [x.data_ptr(), xneg.data_ptr()]
+    rp, wp, pp, sp = r.data_ptr(), w.data_ptr(), packed.data_ptr(), sf.data_ptr()
+    s2 = sf_rm.data_ptr() if sf_rm is not None else None
+    call = L.fp4_add_rmsnorm_quant
+    eps = float(wl.eps)
+
+    def step(i):
+        st = call(ptrs[i & 1], rp, wp, eps, M, H, dt, fmt, lay, pp, sp, s2, sh)
+        if st != 0:
+            raise fq.Fp4Error(st, "fp4_add_rmsnorm_quant")
+
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(gpu_smi_id(torch, dev)) if rank == 0 else None
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    stream.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            step(i)
+            ev[i][1].record(stream)
+        t_end.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    kern_ms = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    clocks = sampler.summary(wall0, wall1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    alg = wl.algorithmic_bytes()
+    ms_step = total_ms / K
+    value = world * alg * K / (total_ms * 1e-3) / 1e9
+    kern_mean = statistics.fmean(kern_ms)
+    achieved = alg / (kern_mean * 1e-3) / 1e9
+    peak, peak_src = measured_hbm_peak()
+    traffic, traffic_src = recorded_traffic(wl.name)
+
+    # ---- end-to-end through the C ABI with host buffers --------------------
+    e2e = None
+    if rank == 0 and args.e2e_steps > 0:
+        hx = x.cpu().pin_memory()
+        hr = r.cpu().pin_memory()
+        hw = w.cpu().pin_memory()
+        ho_r = torch.empty_like(hr).pin_memory()
+        ho_p = torch.empty(packed.shape, dtype=torch.uint8).pin_memory()
+        ho_s = torch.empty(sf.shape, dtype=torch.uint8).pin_memory()
+        ho_s2 = torch.empty(sf_rm.shape, dtype=torch.uint8).pin_memory() if sf_rm is not None else None
+        dx = torch.empty_like(x)
+        dr = torch.empty_like(r)
+        dw = torch.empty_like(w)
+        h2d = hx.numel() * 2 + hr.numel() * 2 + hw.numel() * 2
+        d2h = ho_r.numel() * 2 + ho_p.numel() + ho_s.numel() + (ho_s2.numel() if ho_s2 is not None else 0)
+
+        def e2e_step():
+            dx.copy_(hx, non_blocking=True)
+            dr.copy_(hr, non_blocking=True)
+            dw.copy_(hw, non_blocking=True)
+            st = call(dx.data_ptr(), dr.data_ptr(), dw.data_ptr(), eps, M, H, dt, fmt, lay, pp, sp,
+                      s2, sh)
+            if st != 0:
+                raise fq.Fp4Error(st, "fp4_add_rmsnorm_quant")
+            ho_r.copy_(dr, non_blocking=True)
+            ho_p.copy_(packed, non_blocking=True)
+            ho_s.copy_(sf, non_blocking=True)
+            if ho_s2 is not None:
+                ho_s2.copy_(sf_rm, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                e2e_step()
+            stream.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.e2e_steps):
+                e2e_step()
+            b.record(stream)
+        stream.synchronize()
+        e2e_ms = a.elapsed_time(b) / args.e2e_steps
+        e2e = {"value": round(alg / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_ms, 4), "steps": args.e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "M": M, "H": H, "format": wl.fmt,
+                       "sf_layout": wl.sf_layout, "io_dtype": wl.dtype, "eps": wl.eps,
+                       "algorithmic_bytes_per_step": alg,
+                       "l2": ("inputs larger than L2 (%.0f MB per step vs 129 MB), no flush"
+                              % (alg / 1e6)) if alg > L2_BYTES else
+                             "inputs smaller than L2: numbers are L2-assisted",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "rows_per_s": round(world * M * K / (total_ms * 1e-3), 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_src == "measured" else "fallback 6.8 TB/s",
+                         "traffic": traffic, "traffic_source": traffic_src,
+                         "kernel": "fused_add_rmsnorm_fp4_kernel",
+                         "kernel_ms_mean": round(kern_mean, 5),
+                         "kernel_ms_median": round(statistics.median(kern_ms), 5)},
+            "clocks": clocks, "e2e": e2e, "gpu_launches": K, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    wl = workloads.CONFIGS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -14,7 +14,8 @@ written as the plain per-row definition with the rounding rule of
   4. per block of b elements: amax = max |y|
        NVFP4 (b = 16): t = min(amax / 6, 448), scale = E4M3_rne(t)
        MXFP4 (b = 32): t = amax / 6,             scale = UE8M0 at or above t
-  5. v = y / s (s = decoded scale); code = E2M1_rne(v)  (s == 0: codes 0)
+  5. v = y * (1 / s) (s = decoded scale; the reciprocal and the product each
+     rounded to nearest fp32);  code = E2M1_rne(v)   (s == 0: codes 0)
   6. two codes per byte, element 2j in the low nibble
   7. scale bytes row-major [m, k] and/or in the 128x4 tile order
      (m//128)*nkt*512 + (k//4)*512 + (m%32)*16 + ((m%128)//32)*4 + k%4,
@@ -22,9 +23,12 @@ written as the plain per-row definition with the rounding rule of
 
 Readings where the pages are silent (helper bodies absent):
   * the sum of squares uses the rounded h (the value written back), fp64 sum;
-  * v is a correctly rounded fp32 division (the page multiplies by an
-    approximate reciprocal; the difference only moves values within an ulp of
-    a rounding boundary);
+  * the page scales y by the reciprocal of the decoded block scale
+    (``fp8_e4m3_to_f32_and_rcp`` / ``ue8m0_to_output_scale`` feeding
+    ``quantize_and_pack_16`` in kernel phase 3) without saying how the
+    reciprocal is rounded; here it is the correctly rounded fp32 reciprocal,
+    then one rounded product (for MXFP4 the reciprocal of a power of two is
+    exact, so v is the correctly rounded quotient);
   * a block whose scale is zero (amax = 0, or NVFP4 amax/6 below half the
     smallest E4M3 subnormal) gets all-zero codes;
   * padding rows [M, 128*ceil(M/128)) and padding k in [nb, 4*nkt) of the
@@ -133,9 +137,10 @@ def add_rmsnorm_fp4_quant(x, r, w, eps: float, dtype: str, fmt: str,
         scode = ue8m0_encode_ceil(t)
         scale = ue8m0_decode(scode)
 
-    # 5. element codes
+    # 5. element codes: y times the rounded reciprocal of the scale
     with np.errstate(divide="ignore", invalid="ignore"):
-        vb = yb / scale[:, :, None]
+        inv = (F32(1.0) / scale).astype(np.float32)
+        vb = yb * inv[:, :, None]
     vb = np.where(scale[:, :, None] == 0, F32(0.0), vb).astype(np.float32)
     v = vb.reshape(M, H)
     codes = e2m1_encode(v)

@@ -75,18 +75,21 @@ __device__ __forceinline__ void st_u8(void* p, uint32_t v) {
 }
 
 // ---------------------------------------------------------------------------
-// 16-bit storage types: unpack a pair to fp32 (exact), round a pair back
-// (nearest-even, the cvt.rn pair instructions).
+// 16-bit storage types: unpack a pair to fp32 (exact) and add two pairs.
 // ---------------------------------------------------------------------------
 template <typename T> struct Pair;
 
+// add() is the packed add.rn of the storage type: the exact sum rounded once
+// to nearest-even in that type, which is what rounding the fp32 sum gives
+// (fp32 carries more than 2p + 2 bits for p = 8 and 11).
 template <> struct Pair<__nv_bfloat16> {
   static __device__ __forceinline__ float2 to_f32(uint32_t u) {
     return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
   }
-  static __device__ __forceinline__ uint32_t from_f32(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
+  static __device__ __forceinline__ uint32_t add(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
   }
 };
 
@@ -95,29 +98,33 @@ template <> struct Pair<__half> {
     __half2 v = *reinterpret_cast<__half2*>(&u);
     return __half22float2(v);
   }
-  static __device__ __forceinline__ uint32_t from_f32(float lo, float hi) {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
+  static __device__ __forceinline__ uint32_t add(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
   }
 };
 
 // ---------------------------------------------------------------------------
-// Block scales.  Both return the scale byte, the decoded scale s and what the
-// element loop multiplies or divides by.
+// Block scales (FlashInfer kernel phase 3: the block scale is decoded and its
+// reciprocal scales y before E2M1 rounding).  Both return the scale byte and
+// inv_s, the nearest fp32 to 1/s that the element loop multiplies by.
 // ---------------------------------------------------------------------------
 
 // NVFP4: t = min(amax / 6, 448) with a correctly rounded division, then E4M3
 // nearest-even (CUDA's satfinite fp8 conversion).  s is decoded from the byte
 // with exact integer arithmetic: exponent field E (bias 7), mantissa m (3 bits);
-// E = 0 is subnormal, m * 2^-9.
-__device__ __forceinline__ uint32_t nvfp4_scale(float amax, float& s) {
+// E = 0 is subnormal, m * 2^-9.  inv_s = 1/s rounded to nearest (0 when s = 0,
+// which turns every element of the block into code 0).
+__device__ __forceinline__ uint32_t nvfp4_scale(float amax, float& inv_s) {
   const float t = fminf(__fdiv_rn(amax, 6.0f), 448.0f);
   const uint32_t code = static_cast<uint32_t>(__nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3));
   const uint32_t e = (code >> 3) & 0xF;
   const uint32_t m = code & 0x7;
   const float sig = static_cast<float>(e ? (8u + m) : m);          // integer significand
   const float pw = __uint_as_float((((e ? e : 1u) + 117u)) << 23); // 2^(max(E,1) - 10)
-  s = sig * pw;                                                     // exact
+  const float s = sig * pw;                                         // exact
+  inv_s = s > 0.0f ? __frcp_rn(s) : 0.0f;
   return code;
 }
 

@@ -13,10 +13,11 @@
 // barrier orders the st.shared::cluster stores, so no thread ever spins).
 //
 // Per row the kernel:
-//   1. loads x and r (256-bit, streaming), forms h = rn(x + r) in fp32 and
-//      writes h back to the residual at once;
-//   2. reduces sum(h^2): fp32 per thread in chunk order, a shuffle tree in the
-//      warp, warps in order through shared memory, cluster ranks in order;
+//   1. loads x and r (256-bit, streaming), forms h = rn(x + r) with the packed
+//      bf16x2 / f16x2 add and writes h back to the residual at once;
+//   2. reduces sum(h^2): fp32 per thread (two packed f32x2 lanes, chunk
+//      order), a shuffle tree in the warp, warps in order through shared
+//      memory, cluster ranks in order;
 //   3. rstd = 1 / sqrt(ss / H + eps) with correctly rounded division and root;
 //   4. per chunk: y = (h * rstd) * w, block amax (MXFP4: one shuffle joins the
 //      two chunks of a 32-element block), the scale byte, the E2M1 codes of 16
@@ -95,24 +96,23 @@ fused_add_rmsnorm_fp4_kernel(const FusedParams p) {
       rr[k] = ld_stream_rw(rrow + c * 16);
     }
   }
-  float ss = 0.0f;
+  // even elements accumulate in .x, odd ones in .y (packed f32x2 FMA)
+  float2 ss2 = make_float2(0.0f, 0.0f);
 #pragma unroll
   for (int k = 0; k < CPT; ++k) {
     const int c = c_begin + lane + k * tpr;
     if (row_ok && c < c_end) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float2 a = Pair<T>::to_f32(h[k].u[j]);
-        const float2 b = Pair<T>::to_f32(rr[k].u[j]);
-        const uint32_t u = Pair<T>::from_f32(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y));
+        const uint32_t u = Pair<T>::add(h[k].u[j], rr[k].u[j]);
         h[k].u[j] = u;
         const float2 f = Pair<T>::to_f32(u);
-        ss = fmaf(f.x, f.x, ss);   // squares of 8/11-bit significands are exact
-        ss = fmaf(f.y, f.y, ss);
+        ss2 = __ffma2_rn(f, f, ss2);   // squares of 8/11-bit significands are exact
       }
       st_stream(rrow + c * 16, h[k]);
     }
   }
+  float ss = ss2.x + ss2.y;
 
   // ---- 2. sum of squares over the row ------------------------------------
   const int width = tpr < 32 ? tpr : 32;
@@ -140,6 +140,7 @@ fused_add_rmsnorm_fp4_kernel(const FusedParams p) {
   const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, p.eps)));
 
   // ---- 4. normalise, scale, quantize, store --------------------------------
+  const float2 rstd2 = make_float2(rstd, rstd);
   const T* wvec = static_cast<const T*>(p.w);
   uint8_t* prow = p.packed + static_cast<size_t>(row_ok ? row : 0) * static_cast<size_t>(p.H / 2);
 #pragma unroll
@@ -154,9 +155,10 @@ fused_add_rmsnorm_fp4_kernel(const FusedParams p) {
       for (int j = 0; j < 8; ++j) {
         const float2 hf = Pair<T>::to_f32(h[k].u[j]);
         const float2 wf = Pair<T>::to_f32(wc.u[j]);
-        y[2 * j] = __fmul_rn(__fmul_rn(hf.x, rstd), wf.x);
-        y[2 * j + 1] = __fmul_rn(__fmul_rn(hf.y, rstd), wf.y);
-        amax = fmaxf(amax, fmaxf(fabsf(y[2 * j]), fabsf(y[2 * j + 1])));
+        const float2 yy = __fmul2_rn(__fmul2_rn(hf, rstd2), wf);   // (h * rstd) * w
+        y[2 * j] = yy.x;
+        y[2 * j + 1] = yy.y;
+        amax = fmaxf(amax, fmaxf(fabsf(yy.x), fabsf(yy.y)));
       }
     } else {
 #pragma unroll
@@ -165,22 +167,15 @@ fused_add_rmsnorm_fp4_kernel(const FusedParams p) {
     if (FMT == kFmtMX) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
     if (ok) {
       float v[16];
-      uint32_t code;
-      if (FMT == kFmtNV) {
-        float s;
-        code = nvfp4_scale(amax, s);
-        if (s > 0.0f) {
+      float inv_s;
+      const uint32_t code = (FMT == kFmtNV) ? nvfp4_scale(amax, inv_s) : mxfp4_scale(amax, inv_s);
+      // v = y * (1/s); a zero NVFP4 scale has inv_s = 0 and gives +0 codes
+      const float2 inv2 = make_float2(inv_s, inv_s);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = __fdiv_rn(y[i], s);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = 0.0f;
-        }
-      } else {
-        float inv_s;
-        code = mxfp4_scale(amax, inv_s);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(y[i], inv_s);
+      for (int i = 0; i < 16; i += 2) {
+        const float2 vv = __fmul2_rn(make_float2(y[i], y[i + 1]), inv2);
+        v[i] = vv.x;
+        v[i + 1] = vv.y;
       }
       const uint64_t packed = static_cast<uint64_t>(e2m1_pack8(v)) |
                               (static_cast<uint64_t>(e2m1_pack8(v + 8)) << 32);

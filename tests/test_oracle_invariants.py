@@ -111,8 +111,9 @@ def test_dequant_error_within_half_step(fmt, dtype):
 def test_codes_are_nearest_by_brute_force_on_tiny_rows(fmt):
     """H = 64: for each element the oracle's code minimises |E2M1(c) * s - y|
     over all 16 codes (exact fp64 search), ties to the even mantissa, the zero
-    sign following y.  A mismatch is only allowed where y/s sits within one
-    fp32 ulp of an E2M1 midpoint (the oracle rounds y/s to fp32 first)."""
+    sign following y.  A mismatch is only allowed where y/s sits within two
+    fp32 ulps of an E2M1 midpoint (the oracle scales y by the rounded
+    reciprocal of s, then rounds the product to fp32)."""
     x, r, w = _random_case(8, 64, "bf16", 14, scale=2.0)
     o = oracle.add_rmsnorm_fp4_quant(x, r, w, 1e-6, "bf16", fmt, "rowmajor")
     b = oracle.block_size(fmt)
@@ -131,7 +132,7 @@ def test_codes_are_nearest_by_brute_force_on_tiny_rows(fmt):
             if o.codes[i, j] != best[0]:
                 q = abs(y[i, j] / s[i, j])
                 mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
-                assert np.min(np.abs(mids - q) / mids) < 2.0 ** -23
+                assert np.min(np.abs(mids - q) / mids) < 2.0 ** -22
 
 
 # ---------------------------------------------------------------- workloads

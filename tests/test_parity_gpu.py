@@ -82,8 +82,17 @@ def test_special_rows(fmt):
     w[::3] = -1.25                                 # negative weights give -0 in y
     wl = _wl(M, H, "bf16", fmt, "both")
     bf = torch.bfloat16
-    g, o, _ = _run_full(wl, x.to(bf), r.to(bf), w.to(bf))
-    assert np.all(g.packed[0] == 0)
+    x, r, w = x.to(bf), r.to(bf), w.to(bf)
+    # bf16 subnormals (below 2^-126) in the residual add of row 7
+    sub = torch.arange(1, 65, dtype=torch.int16).view(torch.bfloat16)
+    x[7, :64] = sub
+    r[7, :64] = -sub.flip(0)
+    g, o, _ = _run_full(wl, x, r, w)
+    # the zero row: zero magnitudes everywhere; NVFP4 zero scales give 0x0
+    # codes, MXFP4 (scale 2^-127) keeps the sign of -0 products (0x8)
+    assert np.all((g.packed[0] & 0x77) == 0)
+    if fmt == "nvfp4":
+        assert np.all(g.packed[0] == 0)
     parity.check_dequant(parity.GpuOut(g.rows, g.residual_bits, g.packed, g.sf, None),
                          M, H, fmt, "swizzled")
 

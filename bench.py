@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--rows", type=int, default=None,
+                    help="override the workload's M (smaller cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
@@ -282,9 +284,12 @@ def run_ours(args, wl):
             step(i)
     stream.synchronize()
 
+    # Timed region: K steps back to back on one stream between two events.  A
+    # step is exactly one launch of the fused kernel, so the mean launch
+    # duration is the region's time / K (per-launch events would add their own
+    # gaps between launches).  Per-launch event pairs are taken afterwards on
+    # a short separate loop for the spread.
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -294,9 +299,7 @@ def run_ours(args, wl):
     with torch.cuda.stream(stream):
         t_start.record(stream)
         for i in range(K):
-            ev[i][0].record(stream)
             step(i)
-            ev[i][1].record(stream)
         t_end.record(stream)
     stream.synchronize()
     torch.cuda.synchronize(dev)
@@ -304,6 +307,15 @@ def run_ours(args, wl):
     if world > 1:
         dist.barrier()
     total_ms = t_start.elapsed_time(t_end)
+    n_ev = min(K, 200)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n_ev)]
+    with torch.cuda.stream(stream):
+        for i in range(n_ev):
+            ev[i][0].record(stream)
+            step(i)
+            ev[i][1].record(stream)
+    stream.synchronize()
     kern_ms = [a.elapsed_time(b) for a, b in ev]
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64)
@@ -316,9 +328,11 @@ def run_ours(args, wl):
     alg = wl.algorithmic_bytes()
     ms_step = total_ms / K
     value = world * alg * K / (total_ms * 1e-3) / 1e9
-    kern_mean = statistics.fmean(kern_ms)
+    kern_mean = ms_step                       # one launch per step
     achieved = alg / (kern_mean * 1e-3) / 1e9
     peak, peak_src = measured_hbm_peak()
+    shape = fq.fp4_launch_shape(M, H, dt, fmt, lay)
+    kernel_name = shape["kernel"]
     traffic, traffic_src = recorded_traffic(wl.name)
 
     # ---- end-to-end through the C ABI with host buffers --------------------
@@ -390,9 +404,9 @@ def run_ours(args, wl):
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_src == "measured" else "fallback 6.8 TB/s",
                          "traffic": traffic, "traffic_source": traffic_src,
-                         "kernel": "fused_add_rmsnorm_fp4_kernel",
+                         "kernel": kernel_name, "launch": shape,
                          "kernel_ms_mean": round(kern_mean, 5),
-                         "kernel_ms_median": round(statistics.median(kern_ms), 5)},
+                         "kernel_ms_event_pairs_median": round(statistics.median(kern_ms), 5)},
             "clocks": clocks, "e2e": e2e, "gpu_launches": K, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -403,6 +417,8 @@ def run_ours(args, wl):
 def main():
     args = parse_args()
     wl = workloads.CONFIGS[args.workload]
+    if args.rows is not None:
+        wl = wl.with_shape(args.rows)
     if args.impl == "reference":
         run_reference(args, wl)
     else:

@@ -116,6 +116,17 @@ fp4_status_t fp4_dequant(const uint8_t* packed, const uint8_t* sf, int64_t M, in
  */
 int64_t fp4_sf_size_bytes(int64_t M, int64_t H, fp4_format_t format, fp4_sf_layout_t layout);
 
+/*
+ * fp4_launch_shape - the launch the library would make for fp4_add_rmsnorm_quant
+ * with these sizes on the current device (diagnostics; launches nothing).
+ * Fills out[8] = {kernel (0 = persistent TMA-ring kernel, 1 = register-resident
+ * kernel), chunks per thread, threads per row slice, row slices per CTA,
+ * CTAs per cluster, shared-memory ring stages, threads per CTA, CTAs}.
+ * Returns FP4_OK, or the status fp4_add_rmsnorm_quant would return for the sizes.
+ */
+fp4_status_t fp4_launch_shape(int64_t M, int64_t H, fp4_dtype_t dtype, fp4_format_t format,
+                              fp4_sf_layout_t sf_layout, int64_t out[8]);
+
 /* Static, NUL-terminated description of a status code. */
 const char* fp4_status_string(fp4_status_t status);
 

@@ -26,6 +26,7 @@ from ._binding import (  # noqa: F401
     fp4_add_rmsnorm_quant,
     fp4_dequant,
     fp4_last_cuda_error,
+    fp4_launch_shape,
     fp4_sf_size_bytes,
     fp4_status_string,
     lib,

@@ -52,6 +52,8 @@ def lib() -> ctypes.CDLL:
     L.fp4_status_string.restype = ctypes.c_char_p
     L.fp4_last_cuda_error.argtypes = []
     L.fp4_last_cuda_error.restype = ci
+    L.fp4_launch_shape.argtypes = [i64, i64, ci, ci, ci, ctypes.POINTER(ctypes.c_int64)]
+    L.fp4_launch_shape.restype = ci
     _lib = L
     return L
 
@@ -83,6 +85,21 @@ def fp4_status_string(status: int) -> str:
 
 def fp4_last_cuda_error() -> int:
     return lib().fp4_last_cuda_error()
+
+
+_SHAPE_KEYS = ("kernel", "chunks_per_thread", "threads_per_slice", "slices_per_cta",
+               "cluster", "stages", "threads_per_cta", "ctas")
+
+
+def fp4_launch_shape(M: int, H: int, dtype: int, fmt: int, sf_layout: int) -> dict:
+    """The launch fp4_add_rmsnorm_quant would make on the current device."""
+    out = (ctypes.c_int64 * 8)()
+    st = lib().fp4_launch_shape(M, H, dtype, fmt, sf_layout, out)
+    if st != 0:
+        raise Fp4Error(st, "fp4_launch_shape")
+    d = dict(zip(_SHAPE_KEYS, list(out)))
+    d["kernel"] = "fused_tma_kernel" if d["kernel"] == 0 else "fused_direct_kernel"
+    return d
 
 
 # ---------------------------------------------------------------------------

@@ -6,10 +6,33 @@
 
 #include "../../include/fp4q.h"
 #include "fp4q_launch.h"
+#include "fused_tma.cuh"
 
 namespace fp4q {
 cudaError_t launch_fused_bf16(int fmt, const FusedShape& s, const FusedParams& p, cudaStream_t st);
 cudaError_t launch_fused_fp16(int fmt, const FusedShape& s, const FusedParams& p, cudaStream_t st);
+int tma_ctas_per_sm_bf16(int fmt, int cpt, int threads, size_t smem);
+int tma_ctas_per_sm_fp16(int fmt, int cpt, int threads, size_t smem);
+
+// Tuning constants of the launch-shape choice (compile-time, overridable with -D).
+#ifndef FP4Q_TMA_CTA_THREADS
+#define FP4Q_TMA_CTA_THREADS 256        // target threads of a TMA-kernel CTA
+#endif
+#ifndef FP4Q_TMA_SMEM_PER_SM
+#define FP4Q_TMA_SMEM_PER_SM (220 * 1024)   // shared memory the row rings may take per SM
+#endif
+#ifndef FP4Q_TMA_MAX_STAGES
+#define FP4Q_TMA_MAX_STAGES 6
+#endif
+#ifndef FP4Q_TMA_CTAS_PER_SM
+#define FP4Q_TMA_CTAS_PER_SM 2          // CTAs per SM aimed for when the ring allows
+#endif
+#ifndef FP4Q_TMA_MIN_H
+#define FP4Q_TMA_MIN_H 20480            // rows at least this wide use the TMA kernel
+#endif
+#ifndef FP4Q_DIRECT_CTA_THREADS
+#define FP4Q_DIRECT_CTA_THREADS 128     // target threads of a direct-kernel CTA
+#endif
 
 namespace {
 
@@ -17,6 +40,7 @@ thread_local int g_last_cuda_error = 0;
 
 constexpr int kMaxChunksPerCta = 2048;   // 32768 elements held in registers by one CTA
 constexpr int kMaxCluster = 8;           // portable cluster size
+constexpr size_t kMaxSmemPerCta = 227 * 1024;
 
 inline int block_of(fp4_format_t f) { return f == FP4_NVFP4 ? 16 : 32; }
 
@@ -54,56 +78,121 @@ int round_tpr(int chunks, int cpt) {
   return (t + 31) / 32 * 32;
 }
 
+// Chunks per thread and slice width for `chunks` chunks: fewest idle lanes,
+// ties broken in the order 2, 1, 3, 4 (fewer registers first, then more
+// work per thread).  min_tpr forces whole warps where the kernel needs them.
+bool pick_cpt(int chunks, int min_tpr, int* cpt_out, int* tpr_out) {
+  static const int order[4] = {2, 1, 3, 4};
+  int best = -1, best_tpr = 0, best_waste = 1 << 30;
+  for (int i = 0; i < 4; ++i) {
+    const int cpt = order[i];
+    int tpr = round_tpr(chunks, cpt);
+    if (tpr < min_tpr) tpr = min_tpr;
+    if (tpr > max_threads_for_cpt(cpt)) continue;
+    const int waste = tpr * cpt - chunks;
+    if (waste < best_waste) {
+      best_waste = waste;
+      best = cpt;
+      best_tpr = tpr;
+    }
+  }
+  if (best < 0) return false;
+  *cpt_out = best;
+  *tpr_out = best_tpr;
+  return true;
+}
+
 }  // namespace
 
-bool choose_fused_shape(int64_t M, int H, int fmt, int num_sms, FusedShape* out) {
+bool choose_fused_shape(int64_t M, int64_t rows, int H, int fmt, int dtype, int num_sms,
+                        FusedShape* out) {
   const int nchunk = H / 16;
-  // Cluster size: enough CTAs per row that a slice fits one CTA's registers,
-  // and, for short batches, enough CTAs to cover the SMs.
-  // A slice must be a whole number of chunks (of chunk pairs for MXFP4).
+  // A cluster slice must be a whole number of chunks (of chunk pairs for MXFP4).
   auto splits = [&](int c) {
     return nchunk % c == 0 && (fmt == 0 || ((nchunk / c) & 1) == 0);
   };
+  // Cluster size: enough CTAs per row that a slice fits one CTA's registers,
+  // and, for batches shorter than the SM count, enough CTAs to cover the SMs.
   int cluster = 1;
   while (nchunk / cluster > kMaxChunksPerCta) cluster <<= 1;
   if (cluster > kMaxCluster || !splits(cluster)) return false;
   while (cluster < kMaxCluster && M * cluster < num_sms && nchunk / (cluster * 2) >= 128 &&
          splits(cluster * 2))
     cluster <<= 1;
-  const int per_cta = nchunk / cluster;
 
-  // Chunks per thread: least idle lanes, then more chunks per thread.
-  int best_cpt = 0, best_tpr = 0, best_waste = 1 << 30;
-  for (int cpt = 4; cpt >= 1; --cpt) {
-    const int tpr = round_tpr(per_cta, cpt);
-    const int maxt = max_threads_for_cpt(cpt);
-    if (tpr > maxt) continue;
-    const int waste = tpr * cpt - per_cta;
-    if (waste < best_waste) {
-      best_waste = waste;
-      best_cpt = cpt;
-      best_tpr = tpr;
-    }
+  if (cluster > 1) {
+    const int per_cta = nchunk / cluster;
+    int cpt, tpr;
+    if (!pick_cpt(per_cta, 32, &cpt, &tpr)) return false;
+    out->path = kPathDirect;
+    out->cpt = cpt;
+    out->tpr = tpr;
+    out->rows_per_cta = 1;
+    out->cluster = cluster;
+    out->chunks_per_cta = per_cta;
+    out->stages = 0;
+    out->threads = tpr;
+    out->smem = 0;
+    out->grid = rows * cluster;
+    return true;
   }
-  if (best_cpt == 0) return false;
 
-  int rows_per_cta = 1;
-  if (cluster == 1) {
-    rows_per_cta = best_tpr >= 256 ? 1 : 256 / best_tpr;
-    // short batches: spread rows over the SMs first
-    const int64_t per_sm = (M + num_sms - 1) / num_sms;
-    if (per_sm < rows_per_cta) rows_per_cta = static_cast<int>(per_sm < 1 ? 1 : per_sm);
-    // whole warps
-    while ((best_tpr * rows_per_cta) % 32) ++rows_per_cta;
+  if (H < FP4Q_TMA_MIN_H) {
+    // Register-resident rows, several row slices per CTA.
+    int cpt, tpr;
+    if (!pick_cpt(nchunk, 2, &cpt, &tpr)) return false;
+    int R = tpr >= FP4Q_DIRECT_CTA_THREADS ? 1 : FP4Q_DIRECT_CTA_THREADS / tpr;
+    const int64_t per_sm = (M + num_sms - 1) / num_sms;   // short batches: spread rows first
+    if (per_sm < R) R = static_cast<int>(per_sm < 1 ? 1 : per_sm);
+    while ((tpr * R) % 32) ++R;                           // whole warps
+    if (tpr * R > max_threads_for_cpt(cpt)) return false;
+    out->path = kPathDirect;
+    out->cpt = cpt;
+    out->tpr = tpr;
+    out->rows_per_cta = R;
+    out->cluster = 1;
+    out->chunks_per_cta = nchunk;
+    out->stages = 0;
+    out->threads = tpr * R;
+    out->smem = 0;
+    out->grid = (rows + R - 1) / R;
+    return true;
   }
-  if ((best_tpr * rows_per_cta) % 32 != 0) return false;   // whole warps only
-  out->cpt = best_cpt;
-  out->tpr = best_tpr;
-  out->cluster = cluster;
-  out->chunks_per_cta = per_cta;
-  out->rows_per_cta = rows_per_cta;
-  out->threads = best_tpr * rows_per_cta;
-  out->grid = 0;
+
+  // Persistent TMA kernel.
+  int cpt, tpr;
+  if (!pick_cpt(nchunk, 2, &cpt, &tpr)) return false;
+  int R = tpr >= FP4Q_TMA_CTA_THREADS ? 1 : FP4Q_TMA_CTA_THREADS / tpr;
+  // short batches: spread rows over the SMs before stacking them in a stage
+  const int64_t per_sm = (M + num_sms - 1) / num_sms;
+  if (per_sm < R) R = static_cast<int>(per_sm < 1 ? 1 : per_sm);
+  while ((tpr * R) % 32) ++R;               // whole warps
+  if (tpr * R > max_threads_for_cpt(cpt)) return false;
+  const size_t stage = 4u * static_cast<size_t>(R) * H;
+  const int want_ctas = stage * FP4Q_TMA_CTAS_PER_SM <= FP4Q_TMA_SMEM_PER_SM ? FP4Q_TMA_CTAS_PER_SM : 1;
+  size_t budget = FP4Q_TMA_SMEM_PER_SM / want_ctas;
+  if (budget > kMaxSmemPerCta - 1024) budget = kMaxSmemPerCta - 1024;
+  int S = static_cast<int>(budget / stage);
+  if (S > FP4Q_TMA_MAX_STAGES) S = FP4Q_TMA_MAX_STAGES;
+  if (S < 1) S = 1;
+  const size_t smem = tma_smem_bytes(S, R, H);
+  if (smem > kMaxSmemPerCta) return false;
+  const int per = dtype == 0 ? tma_ctas_per_sm_bf16(fmt, cpt, tpr * R, smem)
+                             : tma_ctas_per_sm_fp16(fmt, cpt, tpr * R, smem);
+  if (per <= 0) return false;
+  const int64_t groups = (rows + R - 1) / R;
+  int64_t grid = static_cast<int64_t>(per) * num_sms;
+  if (grid > groups) grid = groups;
+  out->path = kPathTma;
+  out->cpt = cpt;
+  out->tpr = tpr;
+  out->rows_per_cta = R;
+  out->cluster = 1;
+  out->chunks_per_cta = nchunk;
+  out->stages = S;
+  out->threads = tpr * R;
+  out->smem = smem;
+  out->grid = grid;
   return true;
 }
 
@@ -148,6 +237,32 @@ const char* fp4_status_string(fp4_status_t s) {
 
 int fp4_last_cuda_error(void) { return g_last_cuda_error; }
 
+fp4_status_t fp4_launch_shape(int64_t M, int64_t H, fp4_dtype_t dtype, fp4_format_t format,
+                              fp4_sf_layout_t sf_layout, int64_t out[8]) {
+  if (!out) return FP4_ERR_INVALID_ARG;
+  if (dtype != FP4_DT_BF16 && dtype != FP4_DT_FP16) return FP4_ERR_INVALID_ARG;
+  if (format != FP4_NVFP4 && format != FP4_MXFP4) return FP4_ERR_INVALID_ARG;
+  if (sf_layout != FP4_SF_ROWMAJOR && sf_layout != FP4_SF_SWIZZLED && sf_layout != FP4_SF_BOTH)
+    return FP4_ERR_INVALID_ARG;
+  if (M <= 0 || H <= 0) return FP4_ERR_INVALID_ARG;
+  const int b = block_of(format);
+  if (H % b != 0 || H < 64 || H > FP4Q_MAX_H || M > INT32_MAX) return FP4_ERR_UNSUPPORTED_SHAPE;
+  const int64_t rows = sf_layout == FP4_SF_ROWMAJOR ? M : (M + 127) / 128 * 128;
+  FusedShape s;
+  if (!choose_fused_shape(M, rows, static_cast<int>(H), format == FP4_MXFP4 ? 1 : 0,
+                          dtype == FP4_DT_BF16 ? 0 : 1, num_sms_current_device(), &s))
+    return FP4_ERR_UNSUPPORTED_SHAPE;
+  out[0] = s.path;
+  out[1] = s.cpt;
+  out[2] = s.tpr;
+  out[3] = s.rows_per_cta;
+  out[4] = s.cluster;
+  out[5] = s.stages;
+  out[6] = s.threads;
+  out[7] = s.grid;
+  return FP4_OK;
+}
+
 fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void* weight,
                                    float eps, int64_t M, int64_t H, fp4_dtype_t dtype,
                                    fp4_format_t format, fp4_sf_layout_t sf_layout,
@@ -178,9 +293,11 @@ fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void
     return FP4_ERR_INVALID_ARG;
 
   FusedShape shape;
-  if (!choose_fused_shape(M, static_cast<int>(H), format == FP4_MXFP4 ? 1 : 0,
-                          num_sms_current_device(), &shape))
+  const int64_t rows = sf_layout == FP4_SF_ROWMAJOR ? M : (M + 127) / 128 * 128;
+  if (!choose_fused_shape(M, rows, static_cast<int>(H), format == FP4_MXFP4 ? 1 : 0,
+                          dtype == FP4_DT_BF16 ? 0 : 1, num_sms_current_device(), &shape))
     return FP4_ERR_UNSUPPORTED_SHAPE;
+  if (shape.grid > INT32_MAX) return FP4_ERR_UNSUPPORTED_SHAPE;
 
   FusedParams p;
   p.x = input;
@@ -193,7 +310,7 @@ fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void
                                            : nullptr;
   p.eps = eps;
   p.M = M;
-  p.rows = p.sf_tiled ? (M + 127) / 128 * 128 : M;
+  p.rows = rows;
   p.H = static_cast<int>(H);
   p.nchunk = static_cast<int>(H / 16);
   p.nb = static_cast<int>(H / b);
@@ -202,9 +319,8 @@ fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void
   p.rows_per_cta = shape.rows_per_cta;
   p.cluster = shape.cluster;
   p.chunks_per_cta = shape.chunks_per_cta;
-  shape.grid = shape.cluster > 1 ? p.rows * shape.cluster
-                                 : (p.rows + shape.rows_per_cta - 1) / shape.rows_per_cta;
-  if (shape.grid > INT32_MAX) return FP4_ERR_UNSUPPORTED_SHAPE;
+  p.stages = shape.stages;
+  p.groups = (rows + shape.rows_per_cta - 1) / shape.rows_per_cta;
 
   cudaError_t err = launch_fused(dtype == FP4_DT_BF16 ? 0 : 1, format == FP4_MXFP4 ? 1 : 0, shape,
                                  p, reinterpret_cast<cudaStream_t>(stream));

@@ -28,28 +28,41 @@ struct FusedParams {
   int nb;              // H / block
   int nkt;             // ceil(nb / 4)
   int tpr;             // threads per row slice
-  int rows_per_cta;    // row slices per CTA (1 with clusters)
-  int cluster;         // CTAs per row (1 = no cluster)
+  int rows_per_cta;    // row slices per CTA (rows per stage for the TMA kernel)
+  int cluster;         // CTAs per row (direct kernel), 1 otherwise
   int chunks_per_cta;  // nchunk / cluster
+  int stages;          // shared-memory ring depth (TMA kernel)
+  int64_t groups;      // ceil(rows / rows_per_cta) (TMA kernel)
 };
 
-// Launch shape chosen on the host for one (M, H, format).
+constexpr int kPathTma = 0;       // persistent CTAs, TMA bulk-copy row ring
+constexpr int kPathDirect = 1;    // register-resident rows, optionally one row per cluster
+
+// Launch shape chosen on the host for one (M, H, format, dtype).
 struct FusedShape {
+  int path;
   int cpt;             // chunks per thread (template instance)
   int tpr;
   int rows_per_cta;
   int cluster;
   int chunks_per_cta;
+  int stages;
   int threads;         // tpr * rows_per_cta
+  size_t smem;         // dynamic shared memory bytes
   int64_t grid;        // CTAs
 };
 
-// Picks the launch shape; returns false when H cannot be handled.
-bool choose_fused_shape(int64_t M, int H, int fmt, int num_sms, FusedShape* out);
+// Picks the launch shape; returns false when the shape cannot be handled.
+bool choose_fused_shape(int64_t M, int64_t rows, int H, int fmt, int dtype, int num_sms,
+                        FusedShape* out);
 
 // Launches the fused kernel (dtype 0 = bf16, 1 = fp16; fmt 0 = NVFP4, 1 = MXFP4).
 cudaError_t launch_fused(int dtype, int fmt, const FusedShape& shape, const FusedParams& p,
                          cudaStream_t stream);
+
+// CTAs of the TMA kernel instance that fit one SM (0 if none), after raising
+// its dynamic shared-memory limit to `smem`.
+int tma_ctas_per_sm(int dtype, int fmt, int cpt, int threads, size_t smem);
 
 struct DequantParams {
   const uint8_t* packed;

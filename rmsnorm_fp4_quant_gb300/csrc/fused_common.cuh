@@ -1,0 +1,145 @@
+// fused_common.cuh - the per-row phases of the fused residual-add + RMSNorm +
+// FP4 quantization (FlashInfer `add_rmsnorm_fp4quant.py`,
+// `AddRMSNormFP4QuantKernel.kernel`, phases 2 and 3), shared by the persistent
+// TMA kernel and the cluster kernel.
+//
+// Work decomposition.  A row of H elements is cut into 16-element chunks (32
+// bytes of bf16/fp16: one NVFP4 block, half an MXFP4 block).  A "row slice" of
+// `tpr` threads owns chunks c0, c0 + tpr, c0 + 2 tpr, ... (CPT of them, c0 =
+// slice start + lane), so one 256-bit access per thread covers 1 KiB per warp.
+// A thread keeps its chunks of h in registers between the two phases.
+#pragma once
+
+#include "fp4q_device.cuh"
+#include "fp4q_launch.h"
+
+namespace fp4q {
+
+constexpr int kFmtNV = 0;
+constexpr int kFmtMX = 1;
+
+// Phase 2, first half: h = rn(x + r) with the packed bf16x2 / f16x2 add (x
+// arrives in h[], r in rr[]), h written back to the residual row at once, and
+// this thread's partial sum of h^2 (two f32x2 lanes: even / odd elements,
+// chunk order).
+template <typename T, int CPT>
+__device__ __forceinline__ float add_and_write_back(Chunk (&h)[CPT], const Chunk (&rr)[CPT],
+                                                    T* rrow, int c0, int tpr, int c_end,
+                                                    bool row_ok) {
+  float2 ss2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int k = 0; k < CPT; ++k) {
+    const int c = c0 + k * tpr;
+    if (row_ok && c < c_end) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t u = Pair<T>::add(h[k].u[j], rr[k].u[j]);
+        h[k].u[j] = u;
+        const float2 f = Pair<T>::to_f32(u);
+        ss2 = __ffma2_rn(f, f, ss2);   // squares of 8/11-bit significands are exact
+      }
+      st_stream(rrow + c * 16, h[k]);
+    }
+  }
+  return ss2.x + ss2.y;
+}
+
+// rstd = 1 / sqrt(ss / H + eps), each step correctly rounded.
+__device__ __forceinline__ float row_rstd(float ss, int H, float eps) {
+  const float ms = __fdiv_rn(ss, static_cast<float>(H));
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+}
+
+// Phase 3 for one row slice: y = (h * rstd) * w, block amax (MXFP4: a shuffle
+// with the neighbouring lane joins the two chunks of a 32-element block), the
+// scale byte, v = y * (1/s), E2M1 codes of 16 elements in one 64-bit store, and
+// the scale byte in each layout asked for.  Every lane of the warp must call it
+// (the shuffle is unconditional); lanes without a chunk contribute amax 0.
+template <typename T, int FMT, int CPT>
+__device__ __forceinline__ void quantize_and_store(const Chunk (&h)[CPT], float rstd,
+                                                   const FusedParams& p, int64_t row, int c0,
+                                                   int tpr, int c_end, bool row_ok) {
+  const float2 rstd2 = make_float2(rstd, rstd);
+  const T* wvec = static_cast<const T*>(p.w);
+  uint8_t* prow = p.packed + static_cast<size_t>(row_ok ? row : 0) * static_cast<size_t>(p.H / 2);
+#pragma unroll
+  for (int k = 0; k < CPT; ++k) {
+    const int c = c0 + k * tpr;
+    const bool ok = row_ok && c < c_end;
+    float y[16];
+    float amax = 0.0f;
+    if (ok) {
+      const Chunk wc = ld_cached_ro(wvec + c * 16);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float2 hf = Pair<T>::to_f32(h[k].u[j]);
+        const float2 wf = Pair<T>::to_f32(wc.u[j]);
+        const float2 yy = __fmul2_rn(__fmul2_rn(hf, rstd2), wf);   // (h * rstd) * w
+        y[2 * j] = yy.x;
+        y[2 * j + 1] = yy.y;
+        amax = fmaxf(amax, fmaxf(fabsf(yy.x), fabsf(yy.y)));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) y[i] = 0.0f;
+    }
+    if (FMT == kFmtMX) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+    if (ok) {
+      float v[16];
+      float inv_s;
+      const uint32_t code = (FMT == kFmtNV) ? nvfp4_scale(amax, inv_s) : mxfp4_scale(amax, inv_s);
+      // v = y * (1/s); a zero NVFP4 scale (inv_s = 0) gives +0 codes
+      if (inv_s > 0.0f) {
+        const float2 inv2 = make_float2(inv_s, inv_s);
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const float2 vv = __fmul2_rn(make_float2(y[i], y[i + 1]), inv2);
+          v[i] = vv.x;
+          v[i + 1] = vv.y;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+      }
+      const uint64_t packed = static_cast<uint64_t>(e2m1_pack8(v)) |
+                              (static_cast<uint64_t>(e2m1_pack8(v + 8)) << 32);
+      st_u64(prow + static_cast<size_t>(c) * 8, packed);
+
+      const bool owner = (FMT == kFmtNV) || ((c & 1) == 0);
+      if (owner) {
+        const int kb = (FMT == kFmtNV) ? c : (c >> 1);
+        if (p.sf_rm) st_u8(p.sf_rm + static_cast<size_t>(row) * p.nb + kb, code);
+        if (p.sf_tiled) {
+          st_u8(p.sf_tiled + tiled_sf_offset(row, kb, p.nkt), code);
+          if (kb == p.nb - 1) {   // k padding of the last 4-block group
+            for (int kk = p.nb; kk < 4 * p.nkt; ++kk)
+              st_u8(p.sf_tiled + tiled_sf_offset(row, kk, p.nkt), 0u);
+          }
+        }
+      }
+    }
+  }
+}
+
+// A padding row of the tiled layout (M <= row < 128*ceil(M/128)): zero its
+// nkt four-byte groups.
+__device__ __forceinline__ void zero_tiled_row(const FusedParams& p, int64_t row, int lane,
+                                               int tpr) {
+  for (int g = lane; g < p.nkt; g += tpr) st_u32(p.sf_tiled + tiled_sf_offset(row, 4 * g, p.nkt), 0u);
+}
+
+// Marks a row whose inputs never arrived: every scale byte of the slice set
+// to 0xFF (NaN in both E4M3 and UE8M0), so a consumer sees the failure.
+template <int FMT>
+__device__ __forceinline__ void mark_row_failed(const FusedParams& p, int64_t row, int c0,
+                                                int tpr, int c_end) {
+  if (row >= p.M) return;
+  for (int c = c0; c < c_end; c += tpr) {
+    if (FMT == kFmtMX && (c & 1)) continue;
+    const int kb = (FMT == kFmtNV) ? c : (c >> 1);
+    if (p.sf_rm) st_u8(p.sf_rm + static_cast<size_t>(row) * p.nb + kb, 0xFFu);
+    if (p.sf_tiled) st_u8(p.sf_tiled + tiled_sf_offset(row, kb, p.nkt), 0xFFu);
+  }
+}
+
+}  // namespace fp4q

@@ -1,0 +1,93 @@
+// fused_launch.cuh - launch helpers instantiated once per storage dtype.
+#pragma once
+
+#include "fused_direct.cuh"
+#include "fused_tma.cuh"
+
+namespace fp4q {
+
+template <typename T, int FMT, int CPT>
+cudaError_t raise_smem_limit(size_t smem) {
+  // the limit is a per-device function attribute: raise it when a launch
+  // needs more than any earlier one on this device
+  static size_t done[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev] >= smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(fused_tma_kernel<T, FMT, CPT>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = smem;
+  return e;
+}
+
+template <typename T, int FMT, int CPT>
+int ctas_per_sm_one(int threads, size_t smem) {
+  if (raise_smem_limit<T, FMT, CPT>(smem) != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_tma_kernel<T, FMT, CPT>, threads,
+                                                    smem) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+template <typename T, int FMT>
+int ctas_per_sm_fmt(int cpt, int threads, size_t smem) {
+  switch (cpt) {
+    case 1: return ctas_per_sm_one<T, FMT, 1>(threads, smem);
+    case 2: return ctas_per_sm_one<T, FMT, 2>(threads, smem);
+    case 3: return ctas_per_sm_one<T, FMT, 3>(threads, smem);
+    case 4: return ctas_per_sm_one<T, FMT, 4>(threads, smem);
+    default: return 0;
+  }
+}
+
+template <typename T>
+int ctas_per_sm_dtype(int fmt, int cpt, int threads, size_t smem) {
+  return fmt == kFmtNV ? ctas_per_sm_fmt<T, kFmtNV>(cpt, threads, smem)
+                       : ctas_per_sm_fmt<T, kFmtMX>(cpt, threads, smem);
+}
+
+template <typename T, int FMT, int CPT>
+cudaError_t launch_one(const FusedShape& s, const FusedParams& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(s.grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(s.threads), 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  cfg.attrs = attr;
+  cfg.numAttrs = 0;
+  if (s.path == kPathDirect) {
+    if (s.cluster > 1) {
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(s.cluster);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.numAttrs = 1;
+    }
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, fused_direct_kernel<T, FMT, CPT>, p);
+  }
+  const cudaError_t e = raise_smem_limit<T, FMT, CPT>(s.smem);
+  if (e != cudaSuccess) return e;
+  cfg.dynamicSmemBytes = s.smem;
+  return cudaLaunchKernelEx(&cfg, fused_tma_kernel<T, FMT, CPT>, p);
+}
+
+template <typename T, int FMT>
+cudaError_t launch_fmt(const FusedShape& s, const FusedParams& p, cudaStream_t stream) {
+  switch (s.cpt) {
+    case 1: return launch_one<T, FMT, 1>(s, p, stream);
+    case 2: return launch_one<T, FMT, 2>(s, p, stream);
+    case 3: return launch_one<T, FMT, 3>(s, p, stream);
+    case 4: return launch_one<T, FMT, 4>(s, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename T>
+cudaError_t launch_dtype(int fmt, const FusedShape& s, const FusedParams& p, cudaStream_t stream) {
+  return fmt == kFmtNV ? launch_fmt<T, kFmtNV>(s, p, stream) : launch_fmt<T, kFmtMX>(s, p, stream);
+}
+
+}  // namespace fp4q

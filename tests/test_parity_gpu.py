@@ -39,8 +39,12 @@ def _run_full(wl, x=None, r=None, w=None):
     return g, o, stats
 
 
+# short batches (cluster kernel for wide rows), then batches long enough that
+# persistent CTAs loop over several row groups of the TMA ring (ragged last
+# group, tiled padding rows)
 SHAPES = [(1, 64), (3, 80), (127, 208), (300, 256), (129, 1536), (300, 4096), (130, 5120),
-          (129, 7168), (41, 17408), (1, 32768), (2, 65536), (5, 6144)]
+          (129, 7168), (41, 17408), (1, 32768), (2, 65536), (5, 6144),
+          (5000, 64), (2049, 208), (1999, 1536), (700, 7168), (613, 17408), (333, 32768)]
 
 
 @pytest.mark.parametrize("M,H", SHAPES)
@@ -160,3 +164,16 @@ def test_three_d_input_matches_two_d():
     assert p3.shape == (6, 7, 768) and s3.shape == (6, 7, 96)
     assert torch.equal(p2.view(6, 7, 768), p3) and torch.equal(r2.view(6, 7, 1536), r3)
     assert torch.equal(s2.view(6, 7, 96), s3)
+
+
+def test_launch_shapes_cover_every_kernel():
+    """The shapes above reach the TMA-ring kernel, the register-resident kernel
+    and its cluster mode (so the parity grid exercises all three)."""
+    s = fq.fp4_launch_shape(333, 32768, fq.FP4_DT_BF16, fq.FP4_NVFP4, fq.FP4_SF_SWIZZLED)
+    assert s["kernel"] == "fused_tma_kernel" and s["stages"] >= 1
+    s = fq.fp4_launch_shape(700, 7168, fq.FP4_DT_BF16, fq.FP4_MXFP4, fq.FP4_SF_SWIZZLED)
+    assert s["kernel"] == "fused_direct_kernel" and s["cluster"] == 1
+    s = fq.fp4_launch_shape(41, 17408, fq.FP4_DT_BF16, fq.FP4_NVFP4, fq.FP4_SF_SWIZZLED)
+    assert s["kernel"] == "fused_direct_kernel" and s["cluster"] > 1
+    s = fq.fp4_launch_shape(2, 65536, fq.FP4_DT_FP16, fq.FP4_MXFP4, fq.FP4_SF_ROWMAJOR)
+    assert s["cluster"] >= 2

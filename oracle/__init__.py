@@ -38,6 +38,8 @@ from .formats import (  # noqa: F401
 from .add_rmsnorm_quant import (  # noqa: F401
     OracleResult,
     add_rmsnorm_fp4_quant,
+    quantize,
+    e4m3_scaled,
     swizzled_sf_offset,
     sf_size_bytes,
     dequant,

@@ -12,10 +12,12 @@ written as the plain per-row definition with the rounding rule of
   2. ss = sum of h^2 in fp64;  ms = fp32(ss / H);  rstd = 1 / sqrt(ms + eps)
   3. y = (h * rstd) * w
   4. per block of b elements: amax = max |y|
-       NVFP4 (b = 16): t = min(amax / 6, 448), scale = E4M3_rne(t)
-       MXFP4 (b = 32): t = amax / 6,             scale = UE8M0 at or above t
-  5. v = y * (1 / s) (s = decoded scale; the reciprocal and the product each
-     rounded to nearest fp32);  code = E2M1_rne(v)   (s == 0: codes 0)
+       E4M3 scales (NVFP4, b = 16; or b = 32 with E4M3 forced):
+           t = min((gs * amax) / 6, 448),  scale = E4M3_rne(t)
+       UE8M0 scales (MXFP4, b = 32):
+           t = amax / 6,  scale = UE8M0 at or above t   (gs not applied)
+  5. inv = (1 / s) * gs for E4M3 scales, 1 / s for UE8M0 (each op rounded to
+     nearest fp32);  v = y * inv;  code = E2M1_rne(v)   (s == 0: codes 0)
   6. two codes per byte, element 2j in the low nibble
   7. scale bytes row-major [m, k] and/or in the 128x4 tile order
      (m//128)*nkt*512 + (k//4)*512 + (m%32)*16 + ((m%128)//32)*4 + k%4,
@@ -33,7 +35,22 @@ Readings where the pages are silent (helper bodies absent):
     smallest E4M3 subnormal) gets all-zero codes;
   * padding rows [M, 128*ceil(M/128)) and padding k in [nb, 4*nkt) of the
     tiled buffer are written 0 (the vLLM ``fused_wo_a`` page zero-fills its
-    own padding in the same tile order).
+    own padding in the same tile order);
+  * global scale gs (the page's ``global_scale``, one fp32 read on the
+    device, default 1): the kernel code multiplies it into the E4M3 scale
+    (``global_scale_val * max_abs * fp4_max_rcp``) and into the reciprocal
+    (``fp8_e4m3_to_f32_and_rcp(...) * global_scale_val``); the docstring's
+    "divided by global_scale" is not what the code computes, so the code is
+    followed: with gs = 448 * 6 / amax_tensor the block scales use the E4M3
+    range and a consumer divides by gs.  UE8M0 scales ignore gs, as on the
+    page;
+  * ``scale_format="e4m3"`` with 32-element blocks (the page's
+    ``scale_format`` on its block-32 branch) is format "e4m3b32": MXFP4
+    blocking with NVFP4-style scales.
+
+``quantize`` is the same steps 4-7 applied to an input without the residual
+add and the normalisation (y = x), the standalone producer of the FlashRT
+``fp4-gemm`` README (``quantize_fp4_sfa_bf16`` / ``_fp16``).
 """
 from __future__ import annotations
 
@@ -58,7 +75,12 @@ E4M3_MAX = F32(448.0)    # FlashInfer page, Notes: E4M3 maximum
 
 
 def block_size(fmt: str) -> int:
-    return {"nvfp4": 16, "mxfp4": 32}[fmt]
+    return {"nvfp4": 16, "mxfp4": 32, "e4m3b32": 32}[fmt]
+
+
+def e4m3_scaled(fmt: str) -> bool:
+    """True for the formats with E4M3 block scales (global scale applies)."""
+    return fmt in ("nvfp4", "e4m3b32")
 
 
 def swizzled_sf_offset(m, k, nkt):
@@ -98,12 +120,12 @@ class OracleResult:
 
 
 def add_rmsnorm_fp4_quant(x, r, w, eps: float, dtype: str, fmt: str,
-                          layout: str) -> OracleResult:
+                          layout: str, global_scale: float = 1.0) -> OracleResult:
     """Run the oracle on one batch.
 
     x, r: (M, H) arrays of dtype values (any float type; converted exactly to
-    fp32); w: (H,); dtype "bf16"/"fp16"; fmt "nvfp4"/"mxfp4"; layout
-    "rowmajor", "swizzled" or "both".
+    fp32); w: (H,); dtype "bf16"/"fp16"; fmt "nvfp4"/"mxfp4"/"e4m3b32";
+    layout "rowmajor", "swizzled" or "both"; global_scale a positive fp32.
     """
     x = np.asarray(x, dtype=np.float32)
     r = np.asarray(r, dtype=np.float32)
@@ -112,7 +134,6 @@ def add_rmsnorm_fp4_quant(x, r, w, eps: float, dtype: str, fmt: str,
     b = block_size(fmt)
     if H % b or H < 64:
         raise ValueError("H must be a multiple of the block size and >= 64")
-    nb = H // b
 
     # 1. residual add, rounded to the storage dtype
     h = round_to_dtype(x + r, dtype)
@@ -124,12 +145,30 @@ def add_rmsnorm_fp4_quant(x, r, w, eps: float, dtype: str, fmt: str,
 
     # 3. normalise and weight, in this order
     y = (h * rstd[:, None]) * w[None, :]
+    return _quantize_rows(y, h, rstd, fmt, layout, global_scale)
+
+
+def quantize(x, fmt: str, layout: str, global_scale: float = 1.0) -> OracleResult:
+    """Steps 4-7 on x itself (no add, no normalisation): the standalone
+    producer.  `residual` and `rstd` of the result are x and ones."""
+    x = np.asarray(x, dtype=np.float32)
+    M, H = x.shape
+    if H % block_size(fmt) or H < 16:
+        raise ValueError("H must be a multiple of the block size")
+    return _quantize_rows(x.copy(), x, np.ones(M, np.float32), fmt, layout, global_scale)
+
+
+def _quantize_rows(y, h, rstd, fmt, layout, global_scale) -> OracleResult:
+    M, H = y.shape
+    b = block_size(fmt)
+    nb = H // b
+    gs = F32(global_scale)
 
     # 4. per-block amax and scale
     yb = y.reshape(M, nb, b)
     amax = np.max(np.abs(yb), axis=2) if M else np.zeros((0, nb), np.float32)
-    if fmt == "nvfp4":
-        t = np.minimum(amax / E2M1_MAX, E4M3_MAX)
+    if e4m3_scaled(fmt):
+        t = np.minimum((gs * amax) / E2M1_MAX, E4M3_MAX)
         scode = e4m3_encode_rne(t)
         scale = e4m3_decode(scode)
     else:
@@ -137,9 +176,12 @@ def add_rmsnorm_fp4_quant(x, r, w, eps: float, dtype: str, fmt: str,
         scode = ue8m0_encode_ceil(t)
         scale = ue8m0_decode(scode)
 
-    # 5. element codes: y times the rounded reciprocal of the scale
+    # 5. element codes: y times the rounded reciprocal of the scale (times gs
+    #    for E4M3 scales)
     with np.errstate(divide="ignore", invalid="ignore"):
         inv = (F32(1.0) / scale).astype(np.float32)
+        if e4m3_scaled(fmt):
+            inv = (inv * gs).astype(np.float32)
         vb = yb * inv[:, :, None]
     vb = np.where(scale[:, :, None] == 0, F32(0.0), vb).astype(np.float32)
     v = vb.reshape(M, H)
@@ -162,7 +204,8 @@ def add_rmsnorm_fp4_quant(x, r, w, eps: float, dtype: str, fmt: str,
 def dequant(packed, sf, M: int, H: int, fmt: str, layout: str) -> np.ndarray:
     """E2M1 value times its block scale, fp32 (exact), from packed bytes and a
     scale buffer in either layout (FlashRT ``fp4-gemm`` README, Validation:
-    compare through the dequantised values)."""
+    compare through the dequantised values).  With a global scale gs the
+    original values are approximately this divided by gs."""
     packed = np.asarray(packed, dtype=np.uint8).reshape(M, H // 2)
     b = block_size(fmt)
     nb = H // b
@@ -175,6 +218,6 @@ def dequant(packed, sf, M: int, H: int, fmt: str, layout: str) -> np.ndarray:
         scode = sf[mm * nb + kk]
     else:
         scode = sf[swizzled_sf_offset(mm, kk, (nb + 3) // 4)]
-    scale = e4m3_decode(scode) if fmt == "nvfp4" else ue8m0_decode(scode)
+    scale = e4m3_decode(scode) if e4m3_scaled(fmt) else ue8m0_decode(scode)
     vals = e2m1_decode(codes).reshape(M, nb, b) * scale[:, :, None]
     return vals.reshape(M, H).astype(np.float32)

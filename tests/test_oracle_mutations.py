@@ -13,6 +13,7 @@ from oracle import add_rmsnorm_quant as OP
 from oracle import formats as FM
 
 import test_oracle_formats as TF
+import test_oracle_global_scale as TG
 import test_oracle_invariants as TI
 import test_oracle_rows as TR
 
@@ -47,8 +48,14 @@ OP_MUTANTS = {
     "squares of the unrounded sum": ("ss = np.sum(h.astype(np.float64) ** 2, axis=1)",
                                      "ss = np.sum((x + r).astype(np.float64) ** 2, axis=1)"),
     "scale from amax/4": ("t = amax / E2M1_MAX", "t = amax / F32(4.0)"),
-    "no E4M3 clamp, scale from amax/8": ("t = np.minimum(amax / E2M1_MAX, E4M3_MAX)",
-                                         "t = amax / F32(8.0)"),
+    "no E4M3 clamp, scale from amax/8": ("t = np.minimum((gs * amax) / E2M1_MAX, E4M3_MAX)",
+                                         "t = (gs * amax) / F32(8.0)"),
+    "global scale divides": ("t = np.minimum((gs * amax) / E2M1_MAX, E4M3_MAX)",
+                             "t = np.minimum((amax / gs) / E2M1_MAX, E4M3_MAX)"),
+    "global scale left out of the reciprocal": ("inv = (inv * gs).astype(np.float32)",
+                                                "inv = inv.astype(np.float32)"),
+    "global scale applied to UE8M0": ("        t = amax / E2M1_MAX\n",
+                                      "        t = (gs * amax) / E2M1_MAX\n"),
     "weight ignored": ("y = (h * rstd[:, None]) * w[None, :]", "y = h * rstd[:, None]"),
     "mean over H-1": ("ms = (ss / H)", "ms = (ss / (H - 1))"),
     "residual not rounded": ("h = round_to_dtype(x + r, dtype)", "h = x + r"),
@@ -58,15 +65,23 @@ OP_MUTANTS = {
 }
 
 
+def _golden_gs():
+    for spec in TG.ROWS:
+        TG.test_golden_row(spec)
+
+
 @pytest.mark.parametrize("name", list(OP_MUTANTS))
 def test_op_mutant_is_caught(name, monkeypatch):
     old, new = OP_MUTANTS[name]
-    target = "swizzled_sf_offset" if "swizzle" in name else "add_rmsnorm_fp4_quant"
+    target = next(f for f in ("swizzled_sf_offset", "add_rmsnorm_fp4_quant", "_quantize_rows")
+                  if old in inspect.getsource(getattr(OP, f)))
     mut = _mutant(OP, target, old, new)
     monkeypatch.setattr(OP, target, mut)
-    monkeypatch.setattr(oracle, target, mut)
+    if hasattr(oracle, target):
+        monkeypatch.setattr(oracle, target, mut)
     checks = [
         _golden_all,
+        _golden_gs,
         lambda: TR.test_residual_is_rounded_sum(),
         lambda: TR.test_constant_row_rms_closed_form(0.125, "bf16"),
         lambda: TI.test_swizzle_matches_nested_tile_shape(130, 6),

@@ -50,6 +50,11 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--rows", type=int, default=None,
                     help="override the workload's M (smaller cases for profiling)")
+    ap.add_argument("--op", choices=["fused", "quantize"], default="fused",
+                    help="fused add+RMSNorm+quantize (default) or the standalone quantize")
+    ap.add_argument("--global-scale", type=float, default=None,
+                    help="pass this global scale as a device scalar (E4M3 formats)")
+    ap.add_argument("--format", default=None, help="override the workload's format")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
@@ -249,7 +254,7 @@ def run_ours(args, wl):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     L = fq.lib()
-    fmt = fq.FP4_NVFP4 if wl.fmt == "nvfp4" else fq.FP4_MXFP4
+    fmt = {"nvfp4": fq.FP4_NVFP4, "mxfp4": fq.FP4_MXFP4, "e4m3b32": fq.FP4_E4M3_B32}[wl.fmt]
     lay = {"rowmajor": fq.FP4_SF_ROWMAJOR, "swizzled": fq.FP4_SF_SWIZZLED,
            "both": fq.FP4_SF_BOTH}[wl.sf_layout]
     dt = fq.FP4_DT_BF16 if wl.dtype == "bf16" else fq.FP4_DT_FP16
@@ -269,13 +274,25 @@ def run_ours(args, wl):
     ptrs = [x.data_ptr(), xneg.data_ptr()]
     rp, wp, pp, sp = r.data_ptr(), w.data_ptr(), packed.data_ptr(), sf.data_ptr()
     s2 = sf_rm.data_ptr() if sf_rm is not None else None
-    call = L.fp4_add_rmsnorm_quant
     eps = float(wl.eps)
+    gs_t = None
+    if args.global_scale is not None:
+        gs_t = torch.tensor([args.global_scale], dtype=torch.float32, device=dev)
+    gp = gs_t.data_ptr() if gs_t is not None else None
+    if args.op == "quantize":
+        qcall = L.fp4_quantize
 
-    def step(i):
-        st = call(ptrs[i & 1], rp, wp, eps, M, H, dt, fmt, lay, pp, sp, s2, sh)
-        if st != 0:
-            raise fq.Fp4Error(st, "fp4_add_rmsnorm_quant")
+        def step(i):
+            st = qcall(ptrs[i & 1], gp, M, H, dt, fmt, lay, pp, sp, s2, sh)
+            if st != 0:
+                raise fq.Fp4Error(st, "fp4_quantize")
+    else:
+        call = L.fp4_add_rmsnorm_quant_gs
+
+        def step(i):
+            st = call(ptrs[i & 1], rp, wp, gp, eps, M, H, dt, fmt, lay, pp, sp, s2, sh)
+            if st != 0:
+                raise fq.Fp4Error(st, "fp4_add_rmsnorm_quant")
 
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(gpu_smi_id(torch, dev)) if rank == 0 else None
@@ -325,13 +342,16 @@ def run_ours(args, wl):
     if sampler:
         sampler.stop()
 
-    alg = wl.algorithmic_bytes()
+    alg = wl.algorithmic_bytes(args.op)
     ms_step = total_ms / K
     value = world * alg * K / (total_ms * 1e-3) / 1e9
     kern_mean = ms_step                       # one launch per step
     achieved = alg / (kern_mean * 1e-3) / 1e9
     peak, peak_src = measured_hbm_peak()
-    shape = fq.fp4_launch_shape(M, H, dt, fmt, lay)
+    if args.op == "quantize":
+        shape = {"kernel": "quantize_kernel"}
+    else:
+        shape = fq.fp4_launch_shape(M, H, dt, fmt, lay)
     kernel_name = shape["kernel"]
     traffic, traffic_src = recorded_traffic(wl.name)
 
@@ -348,18 +368,25 @@ def run_ours(args, wl):
         dx = torch.empty_like(x)
         dr = torch.empty_like(r)
         dw = torch.empty_like(w)
-        h2d = hx.numel() * 2 + hr.numel() * 2 + hw.numel() * 2
-        d2h = ho_r.numel() * 2 + ho_p.numel() + ho_s.numel() + (ho_s2.numel() if ho_s2 is not None else 0)
+        fused = args.op == "fused"
+        h2d = hx.numel() * 2 + (hr.numel() * 2 + hw.numel() * 2 if fused else 0)
+        d2h = (ho_r.numel() * 2 if fused else 0) + ho_p.numel() + ho_s.numel() + \
+            (ho_s2.numel() if ho_s2 is not None else 0)
 
         def e2e_step():
             dx.copy_(hx, non_blocking=True)
-            dr.copy_(hr, non_blocking=True)
-            dw.copy_(hw, non_blocking=True)
-            st = call(dx.data_ptr(), dr.data_ptr(), dw.data_ptr(), eps, M, H, dt, fmt, lay, pp, sp,
-                      s2, sh)
+            if fused:
+                dr.copy_(hr, non_blocking=True)
+                dw.copy_(hw, non_blocking=True)
+            if args.op == "quantize":
+                st = L.fp4_quantize(dx.data_ptr(), gp, M, H, dt, fmt, lay, pp, sp, s2, sh)
+            else:
+                st = L.fp4_add_rmsnorm_quant_gs(dx.data_ptr(), dr.data_ptr(), dw.data_ptr(), gp,
+                                                eps, M, H, dt, fmt, lay, pp, sp, s2, sh)
             if st != 0:
-                raise fq.Fp4Error(st, "fp4_add_rmsnorm_quant")
-            ho_r.copy_(dr, non_blocking=True)
+                raise fq.Fp4Error(st, "e2e step")
+            if fused:
+                ho_r.copy_(dr, non_blocking=True)
             ho_p.copy_(packed, non_blocking=True)
             ho_s.copy_(sf, non_blocking=True)
             if ho_s2 is not None:
@@ -382,7 +409,7 @@ def run_ours(args, wl):
                "ms_per_step": round(e2e_ms, 4), "steps": args.e2e_steps}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.op == "fused":
         cpu = cpu_baseline(wl, args.cpu_seconds)
 
     if rank == 0:
@@ -391,7 +418,8 @@ def run_ours(args, wl):
             "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": wl.name, "M": M, "H": H, "format": wl.fmt,
+            "config": {"workload": wl.name, "op": args.op, "global_scale": args.global_scale,
+                       "M": M, "H": H, "format": wl.fmt,
                        "sf_layout": wl.sf_layout, "io_dtype": wl.dtype, "eps": wl.eps,
                        "algorithmic_bytes_per_step": alg,
                        "l2": ("inputs larger than L2 (%.0f MB per step vs 129 MB), no flush"
@@ -419,6 +447,9 @@ def main():
     wl = workloads.CONFIGS[args.workload]
     if args.rows is not None:
         wl = wl.with_shape(args.rows)
+    if args.format is not None:
+        import dataclasses
+        wl = dataclasses.replace(wl, fmt=args.format)
     if args.impl == "reference":
         run_reference(args, wl)
     else:

@@ -48,8 +48,10 @@ typedef struct CUstream_st* fp4q_stream_t;
 typedef enum { FP4_DT_BF16 = 0, FP4_DT_FP16 = 1 } fp4_dtype_t;
 
 /* NVFP4: 16-element blocks, E4M3 scale bytes.  MXFP4: 32-element blocks,
- * UE8M0 scale bytes (FlashInfer page, `block_size` / `scale_format`). */
-typedef enum { FP4_NVFP4 = 0, FP4_MXFP4 = 1 } fp4_format_t;
+ * UE8M0 scale bytes.  E4M3_B32: 32-element blocks with E4M3 scale bytes
+ * (FlashInfer page, `block_size` / `scale_format`: "e4m3" on the block-32
+ * branch).  A global scale applies to the two E4M3 formats only. */
+typedef enum { FP4_NVFP4 = 0, FP4_MXFP4 = 1, FP4_E4M3_B32 = 2 } fp4_format_t;
 
 typedef enum {
   FP4_SF_ROWMAJOR = 0, /* (M, nb) bytes                                  */
@@ -93,6 +95,37 @@ fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void
                                    fp4_format_t format, fp4_sf_layout_t sf_layout,
                                    uint8_t* out_packed, uint8_t* out_sf,
                                    uint8_t* out_sf_rowmajor, fp4q_stream_t stream);
+
+/*
+ * fp4_add_rmsnorm_quant_gs - fp4_add_rmsnorm_quant with a device-resident
+ * global scale (FlashInfer page, `global_scale`; read on the device, so a
+ * captured CUDA graph picks up a new value).  global_scale: DEVICE pointer to
+ * one positive finite fp32, or NULL for 1.  For the E4M3 formats each block
+ * scale becomes E4M3(min(gs * amax / 6, 448)) and codes round from
+ * y * (gs / scale) (so dequantised values are y * gs: a consumer divides by gs,
+ * e.g. gs = 448 * 6 / max|y| fills the E4M3 range); UE8M0 scales ignore it.
+ * All other arguments as fp4_add_rmsnorm_quant.
+ */
+fp4_status_t fp4_add_rmsnorm_quant_gs(const void* input, void* residual, const void* weight,
+                                      const float* global_scale, float eps, int64_t M,
+                                      int64_t H, fp4_dtype_t dtype, fp4_format_t format,
+                                      fp4_sf_layout_t sf_layout, uint8_t* out_packed,
+                                      uint8_t* out_sf, uint8_t* out_sf_rowmajor,
+                                      fp4q_stream_t stream);
+
+/*
+ * fp4_quantize - block quantization of `input` [M, H] itself, without the
+ * residual add and the normalisation: the standalone producer of packed E2M1
+ * plus scales (FlashRT `fp4-gemm` README, `quantize_fp4_sfa_bf16` /
+ * `quantize_fp4_sfa_fp16`).  The same layouts serve as the GEMM's A-operand
+ * scales (rows = M) or B-operand scales (rows = N).  input 32-byte aligned,
+ * H a multiple of the block size (>= 16); global_scale as in
+ * fp4_add_rmsnorm_quant_gs; outputs as fp4_add_rmsnorm_quant.
+ */
+fp4_status_t fp4_quantize(const void* input, const float* global_scale, int64_t M, int64_t H,
+                          fp4_dtype_t dtype, fp4_format_t format, fp4_sf_layout_t sf_layout,
+                          uint8_t* out_packed, uint8_t* out_sf, uint8_t* out_sf_rowmajor,
+                          fp4q_stream_t stream);
 
 /*
  * fp4_dequant - validation helper: out[m, i] = E2M1 value of code (m, i) times

@@ -10,7 +10,8 @@ written as the plain per-row definition with the rounding rule of
 
   1. h = round_dtype(float(x) + float(r))            (phase 2; new residual)
   2. ss = sum of h^2 in fp64;  ms = fp32(ss / H);  rstd = 1 / sqrt(ms + eps)
-  3. y = (h * rstd) * w
+  3. y = (h * w) * rstd   (h * w of two 16-bit values is exact in fp32, so
+     y is the single rounding of h * w * rstd)
   4. per block of b elements: amax = max |y|
        E4M3 scales (NVFP4, b = 16; or b = 32 with E4M3 forced):
            t = min((gs * amax) / 6, 448),  scale = E4M3_rne(t)
@@ -25,6 +26,11 @@ written as the plain per-row definition with the rounding rule of
 
 Readings where the pages are silent (helper bodies absent):
   * the sum of squares uses the rounded h (the value written back), fp64 sum;
+  * y multiplies h by w first and then by rstd, the order of the page's
+    cluster branch (``bfloat2_mul_8(h, w)`` then the product times rstd,
+    ``max_abs = max_xw * rstd``), without its rounding of h * w to 16 bits:
+    the product of two bf16/fp16 values is exact in fp32, so y carries one
+    rounding only;
   * the page scales y by the reciprocal of the decoded block scale
     (``fp8_e4m3_to_f32_and_rcp`` / ``ue8m0_to_output_scale`` feeding
     ``quantize_and_pack_16`` in kernel phase 3) without saying how the
@@ -143,8 +149,8 @@ def add_rmsnorm_fp4_quant(x, r, w, eps: float, dtype: str, fmt: str,
     ms = (ss / H).astype(np.float32)
     rstd = F32(1.0) / np.sqrt(ms + F32(eps))
 
-    # 3. normalise and weight, in this order
-    y = (h * rstd[:, None]) * w[None, :]
+    # 3. weight, then normalise (h * w is exact in fp32)
+    y = (h * w[None, :]) * rstd[:, None]
     return _quantize_rows(y, h, rstd, fmt, layout, global_scale)
 
 

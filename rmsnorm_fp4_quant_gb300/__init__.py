@@ -15,6 +15,7 @@ elements, scales row-major and/or in the 128x4 tiled layout.
 from ._binding import (  # noqa: F401
     FP4_DT_BF16,
     FP4_DT_FP16,
+    FP4_E4M3_B32,
     FP4_MXFP4,
     FP4_NVFP4,
     FP4_SF_BOTH,
@@ -24,11 +25,14 @@ from ._binding import (  # noqa: F401
     add_rmsnorm_fp4quant,
     dequant,
     fp4_add_rmsnorm_quant,
+    fp4_add_rmsnorm_quant_gs,
     fp4_dequant,
+    fp4_quantize,
     fp4_last_cuda_error,
     fp4_launch_shape,
     fp4_sf_size_bytes,
     fp4_status_string,
     lib,
     lib_path,
+    quantize_fp4,
 )

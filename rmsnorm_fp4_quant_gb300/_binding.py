@@ -8,12 +8,12 @@ from typing import Optional, Tuple
 from .build import LIBPATH
 
 FP4_DT_BF16, FP4_DT_FP16 = 0, 1
-FP4_NVFP4, FP4_MXFP4 = 0, 1
+FP4_NVFP4, FP4_MXFP4, FP4_E4M3_B32 = 0, 1, 2
 FP4_SF_ROWMAJOR, FP4_SF_SWIZZLED, FP4_SF_BOTH = 0, 1, 2
 
-_FORMATS = {"nvfp4": FP4_NVFP4, "mxfp4": FP4_MXFP4}
+_FORMATS = {"nvfp4": FP4_NVFP4, "mxfp4": FP4_MXFP4, "e4m3b32": FP4_E4M3_B32}
 _LAYOUTS = {"rowmajor": FP4_SF_ROWMAJOR, "swizzled": FP4_SF_SWIZZLED, "both": FP4_SF_BOTH}
-_BLOCK = {FP4_NVFP4: 16, FP4_MXFP4: 32}
+_BLOCK = {FP4_NVFP4: 16, FP4_MXFP4: 32, FP4_E4M3_B32: 32}
 
 _lib = None
 
@@ -44,6 +44,11 @@ def lib() -> ctypes.CDLL:
     L.fp4_add_rmsnorm_quant.argtypes = [vp, vp, vp, ctypes.c_float, i64, i64, ci, ci, ci,
                                         vp, vp, vp, vp]
     L.fp4_add_rmsnorm_quant.restype = ci
+    L.fp4_add_rmsnorm_quant_gs.argtypes = [vp, vp, vp, vp, ctypes.c_float, i64, i64, ci, ci, ci,
+                                           vp, vp, vp, vp]
+    L.fp4_add_rmsnorm_quant_gs.restype = ci
+    L.fp4_quantize.argtypes = [vp, vp, i64, i64, ci, ci, ci, vp, vp, vp, vp]
+    L.fp4_quantize.restype = ci
     L.fp4_dequant.argtypes = [vp, vp, i64, i64, ci, ci, vp, vp]
     L.fp4_dequant.restype = ci
     L.fp4_sf_size_bytes.argtypes = [i64, i64, ci, ci]
@@ -68,6 +73,24 @@ def fp4_add_rmsnorm_quant(input_ptr: int, residual_ptr: int, weight_ptr: int, ep
     return lib().fp4_add_rmsnorm_quant(input_ptr, residual_ptr, weight_ptr, eps, M, H, dtype,
                                        fmt, sf_layout, out_packed_ptr, out_sf_ptr,
                                        out_sf_rowmajor_ptr or None, stream or None)
+
+
+def fp4_add_rmsnorm_quant_gs(input_ptr: int, residual_ptr: int, weight_ptr: int,
+                             global_scale_ptr: int, eps: float, M: int, H: int, dtype: int,
+                             fmt: int, sf_layout: int, out_packed_ptr: int, out_sf_ptr: int,
+                             out_sf_rowmajor_ptr: int, stream: int) -> int:
+    return lib().fp4_add_rmsnorm_quant_gs(input_ptr, residual_ptr, weight_ptr,
+                                          global_scale_ptr or None, eps, M, H, dtype, fmt,
+                                          sf_layout, out_packed_ptr, out_sf_ptr,
+                                          out_sf_rowmajor_ptr or None, stream or None)
+
+
+def fp4_quantize(input_ptr: int, global_scale_ptr: int, M: int, H: int, dtype: int, fmt: int,
+                 sf_layout: int, out_packed_ptr: int, out_sf_ptr: int, out_sf_rowmajor_ptr: int,
+                 stream: int) -> int:
+    return lib().fp4_quantize(input_ptr, global_scale_ptr or None, M, H, dtype, fmt, sf_layout,
+                              out_packed_ptr, out_sf_ptr, out_sf_rowmajor_ptr or None,
+                              stream or None)
 
 
 def fp4_dequant(packed_ptr: int, sf_ptr: int, M: int, H: int, fmt: int, sf_layout: int,
@@ -123,34 +146,27 @@ def _stream_handle(stream) -> int:
     return int(s.cuda_stream)
 
 
-def add_rmsnorm_fp4quant(input, residual, weight, eps: float = 1e-6, fmt: str = "nvfp4",
-                         sf_layout: str = "rowmajor", out_packed=None, out_sf=None,
-                         out_sf_rowmajor=None, stream=None) -> Tuple:
-    """residual += input (in place); returns (packed, sf) or, for
-    sf_layout="both", (packed, sf_tiled, sf_rowmajor).  ``input`` may be 2-D
-    (M, H) or 3-D (B, S, H); packed has the same leading shape with H/2 bytes.
-    Scale buffers are uint8: row-major (M, H/b), tiled flat."""
+def _dtype_code(t):
     torch = _torch()
-    for name, t in (("input", input), ("residual", residual), ("weight", weight)):
-        _check_cuda(t, name)
-    if input.shape != residual.shape or input.dtype != residual.dtype:
-        raise ValueError("input and residual must have the same shape and dtype")
-    if weight.dtype != input.dtype or weight.dim() != 1 or weight.shape[0] != input.shape[-1]:
-        raise ValueError("weight must be (H,) with the input's dtype")
-    if input.dtype == torch.bfloat16:
-        dt = FP4_DT_BF16
-    elif input.dtype == torch.float16:
-        dt = FP4_DT_FP16
-    else:
-        raise ValueError("dtype must be bfloat16 or float16")
-    f = _FORMATS[fmt]
-    lay = _LAYOUTS[sf_layout]
-    H = input.shape[-1]
-    lead = tuple(input.shape[:-1])
-    M = 1
-    for d in lead:
-        M *= d
-    dev = input.device
+    if t.dtype == torch.bfloat16:
+        return FP4_DT_BF16
+    if t.dtype == torch.float16:
+        return FP4_DT_FP16
+    raise ValueError("dtype must be bfloat16 or float16")
+
+
+def _gs_ptr(global_scale) -> int:
+    if global_scale is None:
+        return 0
+    torch = _torch()
+    _check_cuda(global_scale, "global_scale")
+    if global_scale.dtype != torch.float32 or global_scale.numel() != 1:
+        raise ValueError("global_scale must be a CUDA float32 tensor with one element")
+    return global_scale.data_ptr()
+
+
+def _outputs(lead, M, H, f, lay, dev, out_packed, out_sf, out_sf_rowmajor):
+    torch = _torch()
     if out_packed is None:
         out_packed = torch.empty(*lead, H // 2, dtype=torch.uint8, device=dev)
     nb = H // _BLOCK[f]
@@ -164,13 +180,66 @@ def add_rmsnorm_fp4quant(input, residual, weight, eps: float = 1e-6, fmt: str = 
         out_sf_rowmajor = torch.empty(*lead, nb, dtype=torch.uint8, device=dev)
     for name, t in (("out_packed", out_packed), ("out_sf", out_sf)):
         _check_cuda(t, name)
-    st = fp4_add_rmsnorm_quant(input.data_ptr(), residual.data_ptr(), weight.data_ptr(),
-                               float(eps), M, H, dt, f, lay, out_packed.data_ptr(),
-                               out_sf.data_ptr(),
-                               out_sf_rowmajor.data_ptr() if out_sf_rowmajor is not None else 0,
-                               _stream_handle(stream))
+    return out_packed, out_sf, out_sf_rowmajor
+
+
+def add_rmsnorm_fp4quant(input, residual, weight, eps: float = 1e-6, fmt: str = "nvfp4",
+                         sf_layout: str = "rowmajor", out_packed=None, out_sf=None,
+                         out_sf_rowmajor=None, global_scale=None, stream=None) -> Tuple:
+    """residual += input (in place); returns (packed, sf) or, for
+    sf_layout="both", (packed, sf_tiled, sf_rowmajor).  ``input`` may be 2-D
+    (M, H) or 3-D (B, S, H); packed has the same leading shape with H/2 bytes.
+    Scale buffers are uint8: row-major (M, H/b), tiled flat.  ``global_scale``:
+    optional CUDA float32 tensor of one element (E4M3 formats)."""
+    for name, t in (("input", input), ("residual", residual), ("weight", weight)):
+        _check_cuda(t, name)
+    if input.shape != residual.shape or input.dtype != residual.dtype:
+        raise ValueError("input and residual must have the same shape and dtype")
+    if weight.dtype != input.dtype or weight.dim() != 1 or weight.shape[0] != input.shape[-1]:
+        raise ValueError("weight must be (H,) with the input's dtype")
+    dt = _dtype_code(input)
+    f = _FORMATS[fmt]
+    lay = _LAYOUTS[sf_layout]
+    H = input.shape[-1]
+    lead = tuple(input.shape[:-1])
+    M = 1
+    for d in lead:
+        M *= d
+    out_packed, out_sf, out_sf_rowmajor = _outputs(lead, M, H, f, lay, input.device, out_packed,
+                                                   out_sf, out_sf_rowmajor)
+    st = fp4_add_rmsnorm_quant_gs(input.data_ptr(), residual.data_ptr(), weight.data_ptr(),
+                                  _gs_ptr(global_scale), float(eps), M, H, dt, f, lay,
+                                  out_packed.data_ptr(), out_sf.data_ptr(),
+                                  out_sf_rowmajor.data_ptr() if out_sf_rowmajor is not None else 0,
+                                  _stream_handle(stream))
     if st != 0:
         raise Fp4Error(st, "fp4_add_rmsnorm_quant")
+    if lay == FP4_SF_BOTH:
+        return out_packed, out_sf, out_sf_rowmajor
+    return out_packed, out_sf
+
+
+def quantize_fp4(x, fmt: str = "nvfp4", sf_layout: str = "swizzled", global_scale=None,
+                 out_packed=None, out_sf=None, out_sf_rowmajor=None, stream=None) -> Tuple:
+    """Block-quantize x (M, H) or (B, S, H) itself (no add, no norm); returns
+    (packed, sf) or (packed, sf_tiled, sf_rowmajor) for sf_layout="both"."""
+    _check_cuda(x, "x")
+    dt = _dtype_code(x)
+    f = _FORMATS[fmt]
+    lay = _LAYOUTS[sf_layout]
+    H = x.shape[-1]
+    lead = tuple(x.shape[:-1])
+    M = 1
+    for d in lead:
+        M *= d
+    out_packed, out_sf, out_sf_rowmajor = _outputs(lead, M, H, f, lay, x.device, out_packed,
+                                                   out_sf, out_sf_rowmajor)
+    st = fp4_quantize(x.data_ptr(), _gs_ptr(global_scale), M, H, dt, f, lay,
+                      out_packed.data_ptr(), out_sf.data_ptr(),
+                      out_sf_rowmajor.data_ptr() if out_sf_rowmajor is not None else 0,
+                      _stream_handle(stream))
+    if st != 0:
+        raise Fp4Error(st, "fp4_quantize")
     if lay == FP4_SF_BOTH:
         return out_packed, out_sf, out_sf_rowmajor
     return out_packed, out_sf

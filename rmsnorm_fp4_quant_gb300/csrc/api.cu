@@ -43,6 +43,12 @@ constexpr int kMaxCluster = 8;           // portable cluster size
 constexpr size_t kMaxSmemPerCta = 227 * 1024;
 
 inline int block_of(fp4_format_t f) { return f == FP4_NVFP4 ? 16 : 32; }
+inline bool valid_format(fp4_format_t f) {
+  return f == FP4_NVFP4 || f == FP4_MXFP4 || f == FP4_E4M3_B32;
+}
+inline bool valid_layout(fp4_sf_layout_t l) {
+  return l == FP4_SF_ROWMAJOR || l == FP4_SF_SWIZZLED || l == FP4_SF_BOTH;
+}
 
 inline bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
@@ -109,7 +115,7 @@ bool choose_fused_shape(int64_t M, int64_t rows, int H, int fmt, int dtype, int 
   const int nchunk = H / 16;
   // A cluster slice must be a whole number of chunks (of chunk pairs for MXFP4).
   auto splits = [&](int c) {
-    return nchunk % c == 0 && (fmt == 0 || ((nchunk / c) & 1) == 0);
+    return nchunk % c == 0 && (fmt == 0 || ((nchunk / c) & 1) == 0);   // fmt != 0: 32-blocks
   };
   // Cluster size: enough CTAs per row that a slice fits one CTA's registers,
   // and, for batches shorter than the SM count, enough CTAs to cover the SMs.
@@ -209,7 +215,7 @@ extern "C" {
 
 int64_t fp4_sf_size_bytes(int64_t M, int64_t H, fp4_format_t format, fp4_sf_layout_t layout) {
   if (M < 0 || H <= 0) return -1;
-  if (format != FP4_NVFP4 && format != FP4_MXFP4) return -1;
+  if (!valid_format(format)) return -1;
   const int64_t b = block_of(format);
   if (H % b) return -1;
   const int64_t nb = H / b;
@@ -241,15 +247,13 @@ fp4_status_t fp4_launch_shape(int64_t M, int64_t H, fp4_dtype_t dtype, fp4_forma
                               fp4_sf_layout_t sf_layout, int64_t out[8]) {
   if (!out) return FP4_ERR_INVALID_ARG;
   if (dtype != FP4_DT_BF16 && dtype != FP4_DT_FP16) return FP4_ERR_INVALID_ARG;
-  if (format != FP4_NVFP4 && format != FP4_MXFP4) return FP4_ERR_INVALID_ARG;
-  if (sf_layout != FP4_SF_ROWMAJOR && sf_layout != FP4_SF_SWIZZLED && sf_layout != FP4_SF_BOTH)
-    return FP4_ERR_INVALID_ARG;
+  if (!valid_format(format) || !valid_layout(sf_layout)) return FP4_ERR_INVALID_ARG;
   if (M <= 0 || H <= 0) return FP4_ERR_INVALID_ARG;
   const int b = block_of(format);
   if (H % b != 0 || H < 64 || H > FP4Q_MAX_H || M > INT32_MAX) return FP4_ERR_UNSUPPORTED_SHAPE;
   const int64_t rows = sf_layout == FP4_SF_ROWMAJOR ? M : (M + 127) / 128 * 128;
   FusedShape s;
-  if (!choose_fused_shape(M, rows, static_cast<int>(H), format == FP4_MXFP4 ? 1 : 0,
+  if (!choose_fused_shape(M, rows, static_cast<int>(H), static_cast<int>(format),
                           dtype == FP4_DT_BF16 ? 0 : 1, num_sms_current_device(), &s))
     return FP4_ERR_UNSUPPORTED_SHAPE;
   out[0] = s.path;
@@ -263,38 +267,56 @@ fp4_status_t fp4_launch_shape(int64_t M, int64_t H, fp4_dtype_t dtype, fp4_forma
   return FP4_OK;
 }
 
-fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void* weight,
-                                   float eps, int64_t M, int64_t H, fp4_dtype_t dtype,
-                                   fp4_format_t format, fp4_sf_layout_t sf_layout,
-                                   uint8_t* out_packed, uint8_t* out_sf,
-                                   uint8_t* out_sf_rowmajor, fp4q_stream_t stream) {
-  if (dtype != FP4_DT_BF16 && dtype != FP4_DT_FP16) return FP4_ERR_INVALID_ARG;
-  if (format != FP4_NVFP4 && format != FP4_MXFP4) return FP4_ERR_INVALID_ARG;
-  if (sf_layout != FP4_SF_ROWMAJOR && sf_layout != FP4_SF_SWIZZLED && sf_layout != FP4_SF_BOTH)
+static fp4_status_t record_cuda(cudaError_t err) {
+  if (err != cudaSuccess) {
+    g_last_cuda_error = static_cast<int>(err);
+    return FP4_ERR_CUDA;
+  }
+  return FP4_OK;
+}
+
+// Output-side checks shared by the fused op and the standalone quantize.
+static fp4_status_t check_outputs(int64_t M, int64_t H, fp4_format_t format,
+                                  fp4_sf_layout_t sf_layout, const void* act, int64_t act_bytes,
+                                  const uint8_t* out_packed, const uint8_t* out_sf,
+                                  const uint8_t* out_sf_rowmajor) {
+  if (!out_packed || !out_sf) return FP4_ERR_INVALID_ARG;
+  if (sf_layout == FP4_SF_BOTH && !out_sf_rowmajor) return FP4_ERR_INVALID_ARG;
+  if (!aligned(out_packed, 8)) return FP4_ERR_MISALIGNED;
+  // padding of the tiled buffer is zeroed with 4-byte stores
+  if (sf_layout != FP4_SF_ROWMAJOR && !aligned(out_sf, 4)) return FP4_ERR_MISALIGNED;
+  const int64_t sf_bytes = fp4_sf_size_bytes(M, H, format, sf_layout);
+  if (overlap(out_packed, M * H / 2, out_sf, sf_bytes) ||
+      overlap(out_packed, M * H / 2, act, act_bytes) || overlap(out_sf, sf_bytes, act, act_bytes))
     return FP4_ERR_INVALID_ARG;
+  return FP4_OK;
+}
+
+static fp4_status_t fused_call(const void* input, void* residual, const void* weight,
+                               const float* global_scale, float eps, int64_t M, int64_t H,
+                               fp4_dtype_t dtype, fp4_format_t format, fp4_sf_layout_t sf_layout,
+                               uint8_t* out_packed, uint8_t* out_sf, uint8_t* out_sf_rowmajor,
+                               fp4q_stream_t stream) {
+  if (dtype != FP4_DT_BF16 && dtype != FP4_DT_FP16) return FP4_ERR_INVALID_ARG;
+  if (!valid_format(format) || !valid_layout(sf_layout)) return FP4_ERR_INVALID_ARG;
   if (M < 0 || H <= 0 || !(eps >= 0.0f)) return FP4_ERR_INVALID_ARG;
   const int b = block_of(format);
   if (H % b != 0 || H < 64 || H > FP4Q_MAX_H) return FP4_ERR_UNSUPPORTED_SHAPE;
   if (M == 0) return FP4_OK;
   if (M > INT32_MAX) return FP4_ERR_UNSUPPORTED_SHAPE;
-  if (!input || !residual || !weight || !out_packed || !out_sf) return FP4_ERR_INVALID_ARG;
-  if (sf_layout == FP4_SF_BOTH && !out_sf_rowmajor) return FP4_ERR_INVALID_ARG;
+  if (!input || !residual || !weight) return FP4_ERR_INVALID_ARG;
   if (!aligned(input, 32) || !aligned(residual, 32) || !aligned(weight, 32) ||
-      !aligned(out_packed, 8))
+      !aligned(global_scale, 4))
     return FP4_ERR_MISALIGNED;
-  // padding of the tiled buffer is zeroed with 4-byte stores
-  if (sf_layout != FP4_SF_ROWMAJOR && !aligned(out_sf, 4)) return FP4_ERR_MISALIGNED;
   const int64_t act_bytes = M * H * 2;
   if (overlap(input, act_bytes, residual, act_bytes)) return FP4_ERR_INVALID_ARG;
-  const int64_t sf_bytes = fp4_sf_size_bytes(M, H, format, sf_layout);
-  if (overlap(out_packed, M * H / 2, out_sf, sf_bytes) ||
-      overlap(out_packed, M * H / 2, residual, act_bytes) ||
-      overlap(out_sf, sf_bytes, residual, act_bytes))
-    return FP4_ERR_INVALID_ARG;
+  const fp4_status_t st = check_outputs(M, H, format, sf_layout, residual, act_bytes, out_packed,
+                                        out_sf, out_sf_rowmajor);
+  if (st != FP4_OK) return st;
 
   FusedShape shape;
   const int64_t rows = sf_layout == FP4_SF_ROWMAJOR ? M : (M + 127) / 128 * 128;
-  if (!choose_fused_shape(M, rows, static_cast<int>(H), format == FP4_MXFP4 ? 1 : 0,
+  if (!choose_fused_shape(M, rows, static_cast<int>(H), static_cast<int>(format),
                           dtype == FP4_DT_BF16 ? 0 : 1, num_sms_current_device(), &shape))
     return FP4_ERR_UNSUPPORTED_SHAPE;
   if (shape.grid > INT32_MAX) return FP4_ERR_UNSUPPORTED_SHAPE;
@@ -308,6 +330,7 @@ fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void
   p.sf_rm = (sf_layout == FP4_SF_ROWMAJOR) ? out_sf
             : (sf_layout == FP4_SF_BOTH)   ? out_sf_rowmajor
                                            : nullptr;
+  p.gs = global_scale;
   p.eps = eps;
   p.M = M;
   p.rows = rows;
@@ -322,20 +345,69 @@ fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void
   p.stages = shape.stages;
   p.groups = (rows + shape.rows_per_cta - 1) / shape.rows_per_cta;
 
-  cudaError_t err = launch_fused(dtype == FP4_DT_BF16 ? 0 : 1, format == FP4_MXFP4 ? 1 : 0, shape,
+  cudaError_t err = launch_fused(dtype == FP4_DT_BF16 ? 0 : 1, static_cast<int>(format), shape,
                                  p, reinterpret_cast<cudaStream_t>(stream));
   if (err == cudaSuccess) err = cudaGetLastError();
-  if (err != cudaSuccess) {
-    g_last_cuda_error = static_cast<int>(err);
-    return FP4_ERR_CUDA;
-  }
-  return FP4_OK;
+  return record_cuda(err);
+}
+
+fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void* weight,
+                                   float eps, int64_t M, int64_t H, fp4_dtype_t dtype,
+                                   fp4_format_t format, fp4_sf_layout_t sf_layout,
+                                   uint8_t* out_packed, uint8_t* out_sf,
+                                   uint8_t* out_sf_rowmajor, fp4q_stream_t stream) {
+  return fused_call(input, residual, weight, nullptr, eps, M, H, dtype, format, sf_layout,
+                    out_packed, out_sf, out_sf_rowmajor, stream);
+}
+
+fp4_status_t fp4_add_rmsnorm_quant_gs(const void* input, void* residual, const void* weight,
+                                      const float* global_scale, float eps, int64_t M,
+                                      int64_t H, fp4_dtype_t dtype, fp4_format_t format,
+                                      fp4_sf_layout_t sf_layout, uint8_t* out_packed,
+                                      uint8_t* out_sf, uint8_t* out_sf_rowmajor,
+                                      fp4q_stream_t stream) {
+  return fused_call(input, residual, weight, global_scale, eps, M, H, dtype, format, sf_layout,
+                    out_packed, out_sf, out_sf_rowmajor, stream);
+}
+
+fp4_status_t fp4_quantize(const void* input, const float* global_scale, int64_t M, int64_t H,
+                          fp4_dtype_t dtype, fp4_format_t format, fp4_sf_layout_t sf_layout,
+                          uint8_t* out_packed, uint8_t* out_sf, uint8_t* out_sf_rowmajor,
+                          fp4q_stream_t stream) {
+  if (dtype != FP4_DT_BF16 && dtype != FP4_DT_FP16) return FP4_ERR_INVALID_ARG;
+  if (!valid_format(format) || !valid_layout(sf_layout)) return FP4_ERR_INVALID_ARG;
+  if (M < 0 || H <= 0) return FP4_ERR_INVALID_ARG;
+  const int b = block_of(format);
+  if (H % b != 0 || H > INT32_MAX / 2) return FP4_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return FP4_OK;
+  if (!input) return FP4_ERR_INVALID_ARG;
+  if (!aligned(input, 32) || !aligned(global_scale, 4)) return FP4_ERR_MISALIGNED;
+  const fp4_status_t st = check_outputs(M, H, format, sf_layout, input, M * H * 2, out_packed,
+                                        out_sf, out_sf_rowmajor);
+  if (st != FP4_OK) return st;
+  QuantParams p;
+  p.x = input;
+  p.packed = out_packed;
+  p.sf_tiled = (sf_layout == FP4_SF_ROWMAJOR) ? nullptr : out_sf;
+  p.sf_rm = (sf_layout == FP4_SF_ROWMAJOR) ? out_sf
+            : (sf_layout == FP4_SF_BOTH)   ? out_sf_rowmajor
+                                           : nullptr;
+  p.gs = global_scale;
+  p.M = M;
+  p.rows = sf_layout == FP4_SF_ROWMAJOR ? M : (M + 127) / 128 * 128;
+  p.H = static_cast<int>(H);
+  p.nchunk = static_cast<int>(H / 16);
+  p.nb = static_cast<int>(H / b);
+  p.nkt = (p.nb + 3) / 4;
+  return record_cuda(launch_quantize(dtype == FP4_DT_BF16 ? 0 : 1, static_cast<int>(format), p,
+                                     num_sms_current_device(),
+                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
 fp4_status_t fp4_dequant(const uint8_t* packed, const uint8_t* sf, int64_t M, int64_t H,
                          fp4_format_t format, fp4_sf_layout_t sf_layout, float* out,
                          fp4q_stream_t stream) {
-  if (format != FP4_NVFP4 && format != FP4_MXFP4) return FP4_ERR_INVALID_ARG;
+  if (!valid_format(format)) return FP4_ERR_INVALID_ARG;
   if (sf_layout != FP4_SF_ROWMAJOR && sf_layout != FP4_SF_SWIZZLED) return FP4_ERR_INVALID_ARG;
   if (M < 0 || H <= 0) return FP4_ERR_INVALID_ARG;
   const int b = block_of(format);
@@ -353,13 +425,8 @@ fp4_status_t fp4_dequant(const uint8_t* packed, const uint8_t* sf, int64_t M, in
   p.nb = static_cast<int>(H / b);
   p.nkt = (p.nb + 3) / 4;
   p.tiled = sf_layout == FP4_SF_SWIZZLED ? 1 : 0;
-  const cudaError_t err =
-      launch_dequant(format == FP4_MXFP4 ? 1 : 0, p, reinterpret_cast<cudaStream_t>(stream));
-  if (err != cudaSuccess) {
-    g_last_cuda_error = static_cast<int>(err);
-    return FP4_ERR_CUDA;
-  }
-  return FP4_OK;
+  return record_cuda(
+      launch_dequant(static_cast<int>(format), p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -1,4 +1,5 @@
-// dequant.cu - validation kernel: packed E2M1 codes times their block scale,
+// dequant.cu - validation kernel: packed E2M1 codes times their block scale
+// (format 0: 16-element blocks, E4M3; 1: 32, UE8M0; 2: 32, E4M3),
 // fp32 out (FlashRT `fp4-gemm` README, Validation: compare through the
 // dequantised values; `dequantize_fp4_sfa_fp16`).  One thread per 16-element
 // chunk: one 64-bit code load, one scale byte, four 128-bit stores.
@@ -39,12 +40,12 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantParams p) {
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t row = i / p.nchunk;
     const int c = static_cast<int>(i - row * p.nchunk);
-    const int kb = FMT == 0 ? c : (c >> 1);
+    const int kb = FMT == 0 ? c : (c >> 1);          // 16- or 32-element blocks
     const uint8_t* crow = p.packed + row * (p.H / 2);
     const uint64_t codes = *reinterpret_cast<const uint64_t*>(crow + static_cast<int64_t>(c) * 8);
     const int64_t soff = p.tiled ? tiled_sf_offset(row, kb, p.nkt) : row * p.nb + kb;
     const uint32_t sb = p.sf[soff];
-    const float s = FMT == 0 ? e4m3_value(sb) : ue8m0_value(sb);
+    const float s = FMT == 1 ? ue8m0_value(sb) : e4m3_value(sb);
     float4* out = reinterpret_cast<float4*>(p.out + row * p.H + static_cast<int64_t>(c) * 16);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -63,10 +64,13 @@ cudaError_t launch_dequant(int fmt, const DequantParams& p, cudaStream_t stream)
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
   if (blocks > 152 * 64) blocks = 152 * 64;
+  const unsigned g = static_cast<unsigned>(blocks);
   if (fmt == 0)
-    dequant_kernel<0><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(p);
+    dequant_kernel<0><<<g, threads, 0, stream>>>(p);
+  else if (fmt == 1)
+    dequant_kernel<1><<<g, threads, 0, stream>>>(p);
   else
-    dequant_kernel<1><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(p);
+    dequant_kernel<2><<<g, threads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

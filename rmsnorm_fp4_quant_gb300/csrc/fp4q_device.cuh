@@ -111,28 +111,30 @@ template <> struct Pair<__half> {
 // inv_s, the nearest fp32 to 1/s that the element loop multiplies by.
 // ---------------------------------------------------------------------------
 
-// NVFP4: t = min(amax / 6, 448) with a correctly rounded division, then E4M3
-// nearest-even (CUDA's satfinite fp8 conversion).  s is decoded from the byte
-// with exact integer arithmetic: exponent field E (bias 7), mantissa m (3 bits);
-// E = 0 is subnormal, m * 2^-9.  inv_s = 1/s rounded to nearest (0 when s = 0,
-// which turns every element of the block into code 0).
-__device__ __forceinline__ uint32_t nvfp4_scale(float amax, float& inv_s) {
-  const float t = fminf(__fdiv_rn(amax, 6.0f), 448.0f);
+// E4M3 scales (NVFP4, and 32-element blocks with E4M3 forced): t =
+// min((gs * amax) / 6, 448) with correctly rounded ops, then E4M3 nearest-even
+// (CUDA's satfinite fp8 conversion).  s is decoded from the byte with exact
+// integer arithmetic: exponent field E (bias 7), mantissa m (3 bits); E = 0 is
+// subnormal, m * 2^-9.  inv_s = rn(rn(1/s) * gs) (0 when s = 0, which turns
+// every element of the block into code 0).  gs = 1 without a global scale.
+__device__ __forceinline__ uint32_t e4m3_block_scale(float amax, float gs, float& inv_s) {
+  const float t = fminf(__fdiv_rn(__fmul_rn(gs, amax), 6.0f), 448.0f);
   const uint32_t code = static_cast<uint32_t>(__nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3));
   const uint32_t e = (code >> 3) & 0xF;
   const uint32_t m = code & 0x7;
   const float sig = static_cast<float>(e ? (8u + m) : m);          // integer significand
   const float pw = __uint_as_float((((e ? e : 1u) + 117u)) << 23); // 2^(max(E,1) - 10)
   const float s = sig * pw;                                         // exact
-  inv_s = s > 0.0f ? __frcp_rn(s) : 0.0f;
+  inv_s = s > 0.0f ? __fmul_rn(__frcp_rn(s), gs) : 0.0f;
   return code;
 }
 
-// MXFP4: t = amax / 6 (correctly rounded); exponent e = ceil(log2 t) read off
+// UE8M0 scales (MXFP4; the global scale does not apply): t = amax / 6
+// (correctly rounded); exponent e = ceil(log2 t) read off
 // the fp32 encoding (an exact power of two keeps its exponent, anything above
 // it steps up), clamped to [-127, 127]; byte = e + 127.  inv_s = 2^-e exactly,
 // so y * inv_s is the correctly rounded y / s.
-__device__ __forceinline__ uint32_t mxfp4_scale(float amax, float& inv_s) {
+__device__ __forceinline__ uint32_t ue8m0_block_scale(float amax, float& inv_s) {
   const float t = __fdiv_rn(amax, 6.0f);
   const uint32_t bits = __float_as_uint(t);
   const int E = static_cast<int>(bits >> 23);   // t >= 0: no sign bit

@@ -20,6 +20,7 @@ struct FusedParams {
   uint8_t* packed;
   uint8_t* sf_tiled;
   uint8_t* sf_rm;
+  const float* gs;     // device global scale (one fp32) or null for 1
   float eps;
   int64_t M;           // valid rows
   int64_t rows;        // row slots covered by the grid (M, or 128*ceil(M/128) when tiled)
@@ -77,5 +78,23 @@ struct DequantParams {
 };
 
 cudaError_t launch_dequant(int fmt, const DequantParams& p, cudaStream_t stream);
+
+// Standalone block quantization of x (no add, no normalisation).
+struct QuantParams {
+  const void* x;
+  uint8_t* packed;
+  uint8_t* sf_tiled;
+  uint8_t* sf_rm;
+  const float* gs;
+  int64_t M;
+  int64_t rows;        // row slots: M, or 128*ceil(M/128) with the tiled layout
+  int H;
+  int nchunk;
+  int nb;
+  int nkt;
+};
+
+cudaError_t launch_quantize(int dtype, int fmt, const QuantParams& p, int num_sms,
+                            cudaStream_t stream);
 
 }  // namespace fp4q

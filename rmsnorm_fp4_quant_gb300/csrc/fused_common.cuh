@@ -15,8 +15,21 @@
 
 namespace fp4q {
 
+// Formats: NVFP4 (16-element blocks, E4M3 scales), MXFP4 (32, UE8M0), and
+// 32-element blocks with E4M3 scales (FlashInfer `scale_format="e4m3"` on the
+// block-32 branch).
 constexpr int kFmtNV = 0;
 constexpr int kFmtMX = 1;
+constexpr int kFmtE4B32 = 2;
+template <int FMT> struct Fmt {
+  static constexpr bool kBlock32 = FMT != kFmtNV;   // a block is two chunks
+  static constexpr bool kE4M3 = FMT != kFmtMX;      // E4M3 scale, global scale applies
+};
+
+// The global scale: one fp32 on the device (read once per thread), 1 if absent.
+__device__ __forceinline__ float load_global_scale(const float* gs) {
+  return gs ? __ldg(gs) : 1.0f;
+}
 
 // Phase 2, first half: h = rn(x + r) with the packed bf16x2 / f16x2 add (x
 // arrives in h[], r in rr[]), h written back to the residual row at once, and
@@ -50,13 +63,13 @@ __device__ __forceinline__ float row_rstd(float ss, int H, float eps) {
   return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
 }
 
-// Phase 3 for one row slice: y = (h * rstd) * w, block amax (MXFP4: a shuffle
-// with the neighbouring lane joins the two chunks of a 32-element block), the
-// scale byte, v = y * (1/s), E2M1 codes of 16 elements in one 64-bit store, and
+// Phase 3 for one row slice: y = (h * rstd) * w, block amax (32-element
+// blocks: a shuffle with the neighbouring lane joins the two chunks), the
+// scale byte, v = y * inv_s, E2M1 codes of 16 elements in one 64-bit store, and
 // the scale byte in each layout asked for.  Every lane of the warp must call it
 // (the shuffle is unconditional); lanes without a chunk contribute amax 0.
 template <typename T, int FMT, int CPT>
-__device__ __forceinline__ void quantize_and_store(const Chunk (&h)[CPT], float rstd,
+__device__ __forceinline__ void quantize_and_store(const Chunk (&h)[CPT], float rstd, float gs,
                                                    const FusedParams& p, int64_t row, int c0,
                                                    int tpr, int c_end, bool row_ok) {
   const float2 rstd2 = make_float2(rstd, rstd);
@@ -83,12 +96,13 @@ __device__ __forceinline__ void quantize_and_store(const Chunk (&h)[CPT], float 
 #pragma unroll
       for (int i = 0; i < 16; ++i) y[i] = 0.0f;
     }
-    if (FMT == kFmtMX) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+    if (Fmt<FMT>::kBlock32) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
     if (ok) {
       float v[16];
       float inv_s;
-      const uint32_t code = (FMT == kFmtNV) ? nvfp4_scale(amax, inv_s) : mxfp4_scale(amax, inv_s);
-      // v = y * (1/s); a zero NVFP4 scale (inv_s = 0) gives +0 codes
+      const uint32_t code = Fmt<FMT>::kE4M3 ? e4m3_block_scale(amax, gs, inv_s)
+                                            : ue8m0_block_scale(amax, inv_s);
+      // v = y * inv_s; a zero E4M3 scale (inv_s = 0) gives +0 codes
       if (inv_s > 0.0f) {
         const float2 inv2 = make_float2(inv_s, inv_s);
 #pragma unroll
@@ -105,9 +119,9 @@ __device__ __forceinline__ void quantize_and_store(const Chunk (&h)[CPT], float 
                               (static_cast<uint64_t>(e2m1_pack8(v + 8)) << 32);
       st_u64(prow + static_cast<size_t>(c) * 8, packed);
 
-      const bool owner = (FMT == kFmtNV) || ((c & 1) == 0);
+      const bool owner = !Fmt<FMT>::kBlock32 || ((c & 1) == 0);
       if (owner) {
-        const int kb = (FMT == kFmtNV) ? c : (c >> 1);
+        const int kb = Fmt<FMT>::kBlock32 ? (c >> 1) : c;
         if (p.sf_rm) st_u8(p.sf_rm + static_cast<size_t>(row) * p.nb + kb, code);
         if (p.sf_tiled) {
           st_u8(p.sf_tiled + tiled_sf_offset(row, kb, p.nkt), code);
@@ -135,8 +149,8 @@ __device__ __forceinline__ void mark_row_failed(const FusedParams& p, int64_t ro
                                                 int tpr, int c_end) {
   if (row >= p.M) return;
   for (int c = c0; c < c_end; c += tpr) {
-    if (FMT == kFmtMX && (c & 1)) continue;
-    const int kb = (FMT == kFmtNV) ? c : (c >> 1);
+    if (Fmt<FMT>::kBlock32 && (c & 1)) continue;
+    const int kb = Fmt<FMT>::kBlock32 ? (c >> 1) : c;
     if (p.sf_rm) st_u8(p.sf_rm + static_cast<size_t>(row) * p.nb + kb, 0xFFu);
     if (p.sf_tiled) st_u8(p.sf_tiled + tiled_sf_offset(row, kb, p.nkt), 0xFFu);
   }

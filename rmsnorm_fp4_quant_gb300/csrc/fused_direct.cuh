@@ -101,7 +101,8 @@ fused_direct_kernel(const FusedParams p) {
   }
 
   const float rstd = row_rstd(ss, p.H, p.eps);
-  quantize_and_store<T, FMT, CPT>(h, rstd, p, row, c0, tpr, c_end, row_ok);
+  const float gs = load_global_scale(p.gs);
+  quantize_and_store<T, FMT, CPT>(h, rstd, gs, p, row, c0, tpr, c_end, row_ok);
   if (p.sf_tiled && !row_ok && row < p.rows && rank == 0) zero_tiled_row(p, row, lane, tpr);
 }
 

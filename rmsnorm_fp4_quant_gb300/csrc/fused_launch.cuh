@@ -44,8 +44,12 @@ int ctas_per_sm_fmt(int cpt, int threads, size_t smem) {
 
 template <typename T>
 int ctas_per_sm_dtype(int fmt, int cpt, int threads, size_t smem) {
-  return fmt == kFmtNV ? ctas_per_sm_fmt<T, kFmtNV>(cpt, threads, smem)
-                       : ctas_per_sm_fmt<T, kFmtMX>(cpt, threads, smem);
+  switch (fmt) {
+    case kFmtNV: return ctas_per_sm_fmt<T, kFmtNV>(cpt, threads, smem);
+    case kFmtMX: return ctas_per_sm_fmt<T, kFmtMX>(cpt, threads, smem);
+    case kFmtE4B32: return ctas_per_sm_fmt<T, kFmtE4B32>(cpt, threads, smem);
+    default: return 0;
+  }
 }
 
 template <typename T, int FMT, int CPT>
@@ -87,7 +91,12 @@ cudaError_t launch_fmt(const FusedShape& s, const FusedParams& p, cudaStream_t s
 
 template <typename T>
 cudaError_t launch_dtype(int fmt, const FusedShape& s, const FusedParams& p, cudaStream_t stream) {
-  return fmt == kFmtNV ? launch_fmt<T, kFmtNV>(s, p, stream) : launch_fmt<T, kFmtMX>(s, p, stream);
+  switch (fmt) {
+    case kFmtNV: return launch_fmt<T, kFmtNV>(s, p, stream);
+    case kFmtMX: return launch_fmt<T, kFmtMX>(s, p, stream);
+    case kFmtE4B32: return launch_fmt<T, kFmtE4B32>(s, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace fp4q

@@ -41,10 +41,8 @@ __device__ __forceinline__ void mbar_init_fence() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  uint64_t state;
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 %0, [%1], %2;"
-               : "=l"(state) : "r"(smem_addr(bar)), "r"(bytes) : "memory");
-  (void)state;
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+               :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t done;
@@ -132,6 +130,7 @@ fused_tma_kernel(const FusedParams p) {
 
   const int warp = tid >> 5;
   const int wpr = tpr >> 5;                         // warps per slice (tpr >= 32)
+  const float gs = load_global_scale(p.gs);
   for (int64_t it = 0; it < n_iter; ++it) {
     const int s = static_cast<int>(it % S);
     const uint32_t parity = static_cast<uint32_t>((it / S) & 1);
@@ -179,7 +178,7 @@ fused_tma_kernel(const FusedParams p) {
       for (int i = 0; i < wpr; ++i) ss += pp[grp * wpr + i];
     }
     const float rstd = row_rstd(ss, H, p.eps);
-    quantize_and_store<T, FMT, CPT>(h, rstd, p, row, lane, tpr, c_end, row_ok);
+    quantize_and_store<T, FMT, CPT>(h, rstd, gs, p, row, lane, tpr, c_end, row_ok);
     if (p.sf_tiled && !row_ok && row < p.rows) zero_tiled_row(p, row, lane, tpr);
   }
 }

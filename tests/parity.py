@@ -62,23 +62,34 @@ class GpuOut:
     sf_rm: np.ndarray | None  # whole row-major buffer for layout "both", flat
 
 
-def run_gpu(x, r, w, eps, fmt, layout, rows=None, stream=None):
+def run_gpu(x, r, w, eps, fmt, layout, rows=None, stream=None, global_scale=None):
     """x, r, w: CUDA tensors (r is updated in place).  Returns numpy copies
     of the outputs for `rows` (default: every row) and the whole scale
-    buffers."""
-    outs = fq.add_rmsnorm_fp4quant(x, r, w, eps=eps, fmt=fmt, sf_layout=layout, stream=stream)
+    buffers.  global_scale: optional python float, passed as a device scalar."""
+    gs = None if global_scale is None else torch.tensor([global_scale], dtype=torch.float32,
+                                                         device=x.device)
+    outs = fq.add_rmsnorm_fp4quant(x, r, w, eps=eps, fmt=fmt, sf_layout=layout, stream=stream,
+                                   global_scale=gs)
     torch.cuda.synchronize()
     return fetch(outs, r, layout, rows)
 
 
-def fetch(outs, r, layout, rows=None):
+def run_quantize(x, fmt, layout, global_scale=None):
+    gs = None if global_scale is None else torch.tensor([global_scale], dtype=torch.float32,
+                                                         device=x.device)
+    outs = fq.quantize_fp4(x, fmt=fmt, sf_layout=layout, global_scale=gs)
+    torch.cuda.synchronize()
+    return fetch(outs, None, layout, None, M=x.shape[0])
+
+
+def fetch(outs, r, layout, rows=None, M=None):
     packed, sf = outs[0], outs[1]
     sf_rm = outs[2] if layout == "both" else None
-    M = r.shape[0]
+    M = r.shape[0] if M is None else M
     rows = np.arange(M) if rows is None else np.asarray(rows)
-    idx = torch.from_numpy(rows).to(r.device)
-    rb = r.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
-    pk = packed.index_select(0, idx).cpu().numpy()
+    idx = torch.from_numpy(rows).to(packed.device)
+    rb = None if r is None else r.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
+    pk = packed.reshape(M, -1).index_select(0, idx).cpu().numpy()
     return GpuOut(rows, rb, pk, sf.cpu().numpy().reshape(-1),
                   None if sf_rm is None else sf_rm.cpu().numpy().reshape(-1))
 
@@ -102,18 +113,18 @@ def compare(g: GpuOut, o: oracle.OracleResult, fmt, layout, dtype, M_full, H,
     assert o.packed.shape[0] == len(rows)
     b = oracle.block_size(fmt)
     nb = H // b
-    # 1. residual
-    want_bits = (o.residual.view(np.uint32) >> 16).astype(np.uint16) if dtype == "bf16" else \
-        o.residual.astype(np.float16).view(np.uint16)
-    got_bits = g.residual_bits
-    bad_res = np.argwhere(got_bits != want_bits)
-    assert bad_res.size == 0, f"residual differs at {bad_res[:5].tolist()}"
+    # 1. residual (the standalone quantize has none)
+    if g.residual_bits is not None:
+        want_bits = (o.residual.view(np.uint32) >> 16).astype(np.uint16) if dtype == "bf16" \
+            else o.residual.astype(np.float16).view(np.uint16)
+        bad_res = np.argwhere(g.residual_bits != want_bits)
+        assert bad_res.size == 0, f"residual differs at {bad_res[:5].tolist()}"
 
     # 2. scales
     g_sc = gpu_scale_codes(g, M_full, H, fmt, "rowmajor" if layout == "rowmajor" else "swizzled",
                            rows)
     sc_bad = g_sc != o.scale_codes
-    if fmt == "nvfp4":
+    if oracle.e4m3_scaled(fmt):
         sc_excusable = near(o.t, e4m3_midpoints())
     else:
         sc_excusable = near_pow2(o.t)
@@ -164,7 +175,7 @@ def check_dequant(g: GpuOut, M, H, fmt, layout, device="cuda"):
     b = oracle.block_size(fmt)
     nb = H // b
     sc = gpu_scale_codes(g, M, H, fmt, lay)
-    s = oracle.e4m3_decode(sc) if fmt == "nvfp4" else oracle.ue8m0_decode(sc)
+    s = oracle.e4m3_decode(sc) if oracle.e4m3_scaled(fmt) else oracle.ue8m0_decode(sc)
     tol = np.repeat(s.astype(np.float64), b, axis=1) * 1e-6
     assert np.all(np.abs(got.astype(np.float64) - want) <= tol)
     return got

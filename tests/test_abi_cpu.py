@@ -36,7 +36,8 @@ def _declared_functions():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    for want in ("fp4_add_rmsnorm_quant", "fp4_dequant", "fp4_sf_size_bytes",
+    for want in ("fp4_add_rmsnorm_quant", "fp4_add_rmsnorm_quant_gs", "fp4_quantize",
+                 "fp4_dequant", "fp4_sf_size_bytes", "fp4_launch_shape",
                  "fp4_status_string", "fp4_last_cuda_error"):
         assert want in names
 
@@ -56,10 +57,10 @@ def test_library_is_built_for_sm103a(L):
 
 @pytest.mark.parametrize("M", [0, 1, 4, 41, 127, 128, 129, 512, 8192, 32768])
 @pytest.mark.parametrize("H", [64, 80, 256, 1536, 5120, 7168, 17408, 32768])
-@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "e4m3b32"])
 def test_sf_size_matches_oracle(L, M, H, fmt):
-    f = fq.FP4_NVFP4 if fmt == "nvfp4" else fq.FP4_MXFP4
-    b = 16 if fmt == "nvfp4" else 32
+    f = {"nvfp4": fq.FP4_NVFP4, "mxfp4": fq.FP4_MXFP4, "e4m3b32": fq.FP4_E4M3_B32}[fmt]
+    b = oracle.block_size(fmt)
     if H % b:
         assert fq.fp4_sf_size_bytes(M, H, f, fq.FP4_SF_ROWMAJOR) == -1
         return
@@ -96,6 +97,7 @@ def _call(x=A, r=B, w=W, eps=1e-6, M=4, H=256, dt=0, f=0, lay=0, p=P, s=S, s2=0)
 
 @pytest.mark.parametrize("kwargs,status", [
     (dict(dt=2), 1), (dict(f=3), 1), (dict(lay=5), 1), (dict(M=-1), 1), (dict(H=0), 1),
+    (dict(H=80, f=2), 2),
     (dict(eps=-1.0), 1), (dict(eps=float("nan")), 1),
     (dict(H=40), 2), (dict(H=48), 2), (dict(H=80, f=1), 2), (dict(H=262144 + 16), 2),
     (dict(x=0), 1), (dict(r=0), 1), (dict(w=0), 1), (dict(p=0), 1), (dict(s=0), 1),
@@ -129,3 +131,29 @@ def test_tensor_api_refuses_cpu_tensors(L):
     x = torch.zeros(4, 256, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         fq.add_rmsnorm_fp4quant(x, x.clone(), torch.ones(256, dtype=torch.bfloat16))
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(gs=A + 2), 3),            # global scale must be 4-byte aligned
+    (dict(dt=5), 1), (dict(H=40), 2),
+])
+def test_fused_gs_validation(L, kwargs, status):
+    a = dict(x=A, r=B, w=W, gs=0, eps=1e-6, M=4, H=256, dt=0, f=0, lay=0, p=P, s=S, s2=0)
+    a.update(kwargs)
+    st = fq.fp4_add_rmsnorm_quant_gs(a["x"], a["r"], a["w"], a["gs"], a["eps"], a["M"], a["H"],
+                                     a["dt"], a["f"], a["lay"], a["p"], a["s"], a["s2"], 0)
+    assert st == status
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(dt=3), 1), (dict(f=4), 1), (dict(lay=3), 1), (dict(M=-2), 1), (dict(H=24), 2),
+    (dict(H=48, f=1), 2), (dict(x=0), 1), (dict(p=0), 1), (dict(s=0), 1), (dict(x=A + 8), 3),
+    (dict(gs=W + 1), 3), (dict(p=P + 2), 3), (dict(lay=1, s=S + 1), 3), (dict(p=A + 256), 1),
+    (dict(M=0, x=0, p=0, s=0), 0),
+])
+def test_quantize_validation(L, kwargs, status):
+    a = dict(x=A, gs=0, M=4, H=256, dt=0, f=0, lay=0, p=P, s=S, s2=0)
+    a.update(kwargs)
+    st = fq.fp4_quantize(a["x"], a["gs"], a["M"], a["H"], a["dt"], a["f"], a["lay"], a["p"],
+                         a["s"], a["s2"], 0)
+    assert st == status

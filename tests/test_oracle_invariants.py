@@ -153,3 +153,15 @@ def test_algorithmic_bytes_formula():
     assert workloads.C3.algorithmic_bytes() == 383_531_008
     assert workloads.C4.algorithmic_bytes() == 555_755_520
     assert workloads.C1.algorithmic_bytes() == 7_232
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_y_is_one_rounding_of_h_w_rstd(dtype):
+    """h * w * rstd is exact in fp64 (8+8+24 or 11+11+24 significant bits), so
+    the single-rounding reading of y = (h * w) * rstd means y equals that
+    exact product rounded once to fp32, element by element."""
+    x, r, w = _random_case(16, 512, dtype, 21, scale=2.0)
+    o = oracle.add_rmsnorm_fp4_quant(x, r, w, 1e-6, dtype, "nvfp4", "rowmajor")
+    exact = (o.residual.astype(np.float64) * w.astype(np.float64)[None, :]) \
+        * o.rstd.astype(np.float64)[:, None]
+    assert np.array_equal(o.y, exact.astype(np.float32))

@@ -56,7 +56,9 @@ OP_MUTANTS = {
                                                 "inv = inv.astype(np.float32)"),
     "global scale applied to UE8M0": ("        t = amax / E2M1_MAX\n",
                                       "        t = (gs * amax) / E2M1_MAX\n"),
-    "weight ignored": ("y = (h * rstd[:, None]) * w[None, :]", "y = h * rstd[:, None]"),
+    "weight ignored": ("y = (h * w[None, :]) * rstd[:, None]", "y = h * rstd[:, None]"),
+    "two roundings in y": ("y = (h * w[None, :]) * rstd[:, None]",
+                           "y = (h * rstd[:, None]) * w[None, :]"),
     "mean over H-1": ("ms = (ss / H)", "ms = (ss / (H - 1))"),
     "residual not rounded": ("h = round_to_dtype(x + r, dtype)", "h = x + r"),
     "swizzle inner/outer m swapped": (
@@ -88,6 +90,7 @@ def test_op_mutant_is_caught(name, monkeypatch):
         lambda: TI.test_dequant_error_within_half_step("nvfp4", "bf16"),
         lambda: TI.test_mxfp4_scale_brackets_amax(),
         lambda: TI.test_nvfp4_scale_is_nearest_e4m3_to_amax_over_6(),
+        lambda: TI.test_y_is_one_rounding_of_h_w_rstd("bf16"),
     ]
     assert _pins_fail(checks), f"no pin caught: {name}"
 

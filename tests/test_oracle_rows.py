@@ -65,6 +65,9 @@ def test_constant_row_rms_closed_form(c, dtype):
     exact = 1.0 / math.sqrt(c * c + float(np.float32(eps)))
     assert abs(float(o.rstd[0]) - exact) <= 3e-7 * exact
     assert np.allclose(o.y[0], c * exact * w, rtol=4e-7, atol=0)
+    # h * w is exact in fp32, so y is within half an ulp of h * w * rstd
+    yy = (np.float64(c) * w.astype(np.float64)) * np.float64(o.rstd[0])
+    assert np.all(np.abs(o.y[0] - yy) <= np.abs(yy) * 2.0 ** -24)
 
 
 def test_zero_row_gives_zero_codes_and_scales():

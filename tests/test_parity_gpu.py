@@ -27,14 +27,15 @@ def _wl(M, H, dtype, fmt, layout, eps=1e-6, seed=0, **kw):
     return workloads.Workload(f"t_{M}_{H}", M, H, dtype, fmt, layout, eps, seed=seed, **kw)
 
 
-def _run_full(wl, x=None, r=None, w=None):
+def _run_full(wl, x=None, r=None, w=None, global_scale=None):
     """Inputs on the CPU (or given), oracle on every row, GPU through the C ABI."""
     if x is None:
         x, r, w = workloads.make_inputs(wl, "cpu")
     o = oracle.add_rmsnorm_fp4_quant(x.float().numpy(), r.float().numpy(), w.float().numpy(),
-                                     wl.eps, wl.dtype, wl.fmt, wl.sf_layout)
+                                     wl.eps, wl.dtype, wl.fmt, wl.sf_layout,
+                                     1.0 if global_scale is None else global_scale)
     xd, rd, wd = x.cuda(), r.cuda(), w.cuda()
-    g = parity.run_gpu(xd, rd, wd, wl.eps, wl.fmt, wl.sf_layout)
+    g = parity.run_gpu(xd, rd, wd, wl.eps, wl.fmt, wl.sf_layout, global_scale=global_scale)
     stats = parity.compare(g, o, wl.fmt, wl.sf_layout, wl.dtype, wl.M, wl.H)
     return g, o, stats
 
@@ -48,7 +49,7 @@ SHAPES = [(1, 64), (3, 80), (127, 208), (300, 256), (129, 1536), (300, 4096), (1
 
 
 @pytest.mark.parametrize("M,H", SHAPES)
-@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "e4m3b32"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("layout", ["rowmajor", "swizzled", "both"])
 def test_parity_grid(M, H, fmt, dtype, layout):
@@ -177,3 +178,13 @@ def test_launch_shapes_cover_every_kernel():
     assert s["kernel"] == "fused_direct_kernel" and s["cluster"] > 1
     s = fq.fp4_launch_shape(2, 65536, fq.FP4_DT_FP16, fq.FP4_MXFP4, fq.FP4_SF_ROWMAJOR)
     assert s["cluster"] >= 2
+
+
+@pytest.mark.parametrize("M,H", [(129, 1536), (700, 7168), (41, 17408), (333, 32768)])
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "e4m3b32"])
+@pytest.mark.parametrize("gs", [2688.0 / 3.9, 0.37])
+def test_global_scale(M, H, fmt, gs):
+    """Device-resident global scale through every kernel (direct, cluster,
+    TMA ring); UE8M0 scales ignore it."""
+    wl = _wl(M, H, "bf16", fmt, "both", seed=3 * M + H)
+    _run_full(wl, global_scale=gs)

@@ -32,7 +32,8 @@ ROWMAJOR = "rowmajor"
 SWIZZLED = "swizzled"
 BOTH = "both"
 
-BLOCK_SIZE = {NVFP4: 16, MXFP4: 32}
+E4M3_B32 = "e4m3b32"  # 32-element blocks, E4M3 scales
+BLOCK_SIZE = {NVFP4: 16, MXFP4: 32, E4M3_B32: 32}
 
 _ROW_BLOCK = 4096
 
@@ -60,12 +61,15 @@ class Workload:
     def torch_dtype(self) -> torch.dtype:
         return torch.bfloat16 if self.dtype == "bf16" else torch.float16
 
-    def algorithmic_bytes(self) -> int:
-        """HBM bytes one call must move: read x and r, write r, write the
-        packed codes and every scale layout asked for, read the weight once.
+    def algorithmic_bytes(self, op: str = "fused") -> int:
+        """HBM bytes one call must move.  Fused op: read x and r, write r,
+        write the packed codes and every scale layout asked for, read the
+        weight once.  Standalone quantize: read x, write codes and scales.
         Swizzle padding is not counted."""
         nb = self.H // self.block
         n_layouts = 2 if self.sf_layout == BOTH else 1
+        if op == "quantize":
+            return self.M * (2 * self.H + self.H // 2 + n_layouts * nb)
         return self.M * (6 * self.H + self.H // 2 + n_layouts * nb) + 2 * self.H
 
     def with_shape(self, M: int, H: Optional[int] = None) -> "Workload":

@@ -75,22 +75,43 @@ __device__ __forceinline__ void st_u8(void* p, uint32_t v) {
 }
 
 // ---------------------------------------------------------------------------
-// 16-bit storage types: unpack a pair to fp32 (exact) and add two pairs.
+// 16-bit storage types: unpack a pair to fp32 (exact), add two pairs, multiply
+// two pairs into fp32, accumulate squares.
 // ---------------------------------------------------------------------------
 template <typename T> struct Pair;
 
 // add() is the packed add.rn of the storage type: the exact sum rounded once
 // to nearest-even in that type, which is what rounding the fp32 sum gives
 // (fp32 carries more than 2p + 2 bits for p = 8 and 11).
+// mul() gives the two fp32 products of two pairs with the mixed-precision FMA
+// (16-bit sources, fp32 result, addend -0 so a zero product keeps its sign):
+// a product of two 8- or 11-bit significands is exact in fp32.  sq_acc()
+// accumulates the squares of a pair the same way, into two fp32 lanes.
+#define FP4Q_PAIR_OPS(T16, ADD, MIXED)                                                        \
+  static __device__ __forceinline__ uint32_t add(uint32_t a, uint32_t b) {                   \
+    uint32_t d;                                                                               \
+    asm(ADD " %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));                                       \
+    return d;                                                                                 \
+  }                                                                                           \
+  static __device__ __forceinline__ float2 mul(uint32_t a, uint32_t b) {                     \
+    float2 r;                                                                                 \
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"                                                 \
+        "mov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"                                  \
+        MIXED " %0, al, bl, 0f80000000;\n\t" MIXED " %1, ah, bh, 0f80000000;\n\t}"            \
+        : "=f"(r.x), "=f"(r.y) : "r"(a), "r"(b));                                             \
+    return r;                                                                                 \
+  }                                                                                           \
+  static __device__ __forceinline__ void sq_acc(uint32_t a, float2& acc) {                   \
+    asm("{\n\t.reg .b16 al, ah;\n\tmov.b32 {al, ah}, %2;\n\t"                               \
+        MIXED " %0, al, al, %0;\n\t" MIXED " %1, ah, ah, %1;\n\t}"                              \
+        : "+f"(acc.x), "+f"(acc.y) : "r"(a));                                                 \
+  }
+
 template <> struct Pair<__nv_bfloat16> {
   static __device__ __forceinline__ float2 to_f32(uint32_t u) {
     return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
   }
-  static __device__ __forceinline__ uint32_t add(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-  }
+  FP4Q_PAIR_OPS(__nv_bfloat16, "add.rn.bf16x2", "fma.rn.f32.bf16")
 };
 
 template <> struct Pair<__half> {
@@ -98,12 +119,16 @@ template <> struct Pair<__half> {
     __half2 v = *reinterpret_cast<__half2*>(&u);
     return __half22float2(v);
   }
-  static __device__ __forceinline__ uint32_t add(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-  }
+  FP4Q_PAIR_OPS(__half, "add.rn.f16x2", "fma.rn.f32.f16")
 };
+#undef FP4Q_PAIR_OPS
+
+// max(m, |a|, |b|) with the three-input float max of sm_100+.
+__device__ __forceinline__ float max_abs3(float m, float a, float b) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(m), "f"(fabsf(a)), "f"(fabsf(b)));
+  return d;
+}
 
 // ---------------------------------------------------------------------------
 // Block scales (FlashInfer kernel phase 3: the block scale is decoded and its

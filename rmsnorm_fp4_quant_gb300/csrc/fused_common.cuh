@@ -33,8 +33,8 @@ __device__ __forceinline__ float load_global_scale(const float* gs) {
 
 // Phase 2, first half: h = rn(x + r) with the packed bf16x2 / f16x2 add (x
 // arrives in h[], r in rr[]), h written back to the residual row at once, and
-// this thread's partial sum of h^2 (two f32x2 lanes: even / odd elements,
-// chunk order).
+// this thread's partial sum of h^2 (exact squares from the mixed-precision
+// FMA; two fp32 lanes: even / odd elements, chunk order).
 template <typename T, int CPT>
 __device__ __forceinline__ float add_and_write_back(Chunk (&h)[CPT], const Chunk (&rr)[CPT],
                                                     T* rrow, int c0, int tpr, int c_end,
@@ -48,8 +48,7 @@ __device__ __forceinline__ float add_and_write_back(Chunk (&h)[CPT], const Chunk
       for (int j = 0; j < 8; ++j) {
         const uint32_t u = Pair<T>::add(h[k].u[j], rr[k].u[j]);
         h[k].u[j] = u;
-        const float2 f = Pair<T>::to_f32(u);
-        ss2 = __ffma2_rn(f, f, ss2);   // squares of 8/11-bit significands are exact
+        Pair<T>::sq_acc(u, ss2);
       }
       st_stream(rrow + c * 16, h[k]);
     }
@@ -63,7 +62,9 @@ __device__ __forceinline__ float row_rstd(float ss, int H, float eps) {
   return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
 }
 
-// Phase 3 for one row slice: y = (h * rstd) * w, block amax (32-element
+// Phase 3 for one row slice: y = (h * w) * rstd (h * w exact in fp32, so y is
+// one rounding of the product; FlashInfer's cluster branch multiplies in this
+// order), block amax (32-element
 // blocks: a shuffle with the neighbouring lane joins the two chunks), the
 // scale byte, v = y * inv_s, E2M1 codes of 16 elements in one 64-bit store, and
 // the scale byte in each layout asked for.  Every lane of the warp must call it
@@ -85,12 +86,10 @@ __device__ __forceinline__ void quantize_and_store(const Chunk (&h)[CPT], float 
       const Chunk wc = ld_cached_ro(wvec + c * 16);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float2 hf = Pair<T>::to_f32(h[k].u[j]);
-        const float2 wf = Pair<T>::to_f32(wc.u[j]);
-        const float2 yy = __fmul2_rn(__fmul2_rn(hf, rstd2), wf);   // (h * rstd) * w
+        const float2 yy = __fmul2_rn(Pair<T>::mul(h[k].u[j], wc.u[j]), rstd2);   // (h * w) * rstd
         y[2 * j] = yy.x;
         y[2 * j + 1] = yy.y;
-        amax = fmaxf(amax, fmaxf(fabsf(yy.x), fabsf(yy.y)));
+        amax = max_abs3(amax, yy.x, yy.y);
       }
     } else {
 #pragma unroll

@@ -26,7 +26,7 @@ __device__ __forceinline__ void quantize_chunk(const QuantParams& p, const Chunk
       const float2 f = Pair<T>::to_f32(xc.u[j]);
       y[2 * j] = f.x;
       y[2 * j + 1] = f.y;
-      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      amax = max_abs3(amax, f.x, f.y);
     }
   } else {
 #pragma unroll

@@ -136,20 +136,39 @@ __device__ __forceinline__ float max_abs3(float m, float a, float b) {
 // inv_s, the nearest fp32 to 1/s that the element loop multiplies by.
 // ---------------------------------------------------------------------------
 
-// E4M3 scales (NVFP4, and 32-element blocks with E4M3 forced): t =
-// min((gs * amax) / 6, 448) with correctly rounded ops, then E4M3 nearest-even
-// (CUDA's satfinite fp8 conversion).  s is decoded from the byte with exact
-// integer arithmetic: exponent field E (bias 7), mantissa m (3 bits); E = 0 is
-// subnormal, m * 2^-9.  inv_s = rn(rn(1/s) * gs) (0 when s = 0, which turns
-// every element of the block into code 0).  gs = 1 without a global scale.
-__device__ __forceinline__ uint32_t e4m3_block_scale(float amax, float gs, float& inv_s) {
-  const float t = fminf(__fdiv_rn(__fmul_rn(gs, amax), 6.0f), 448.0f);
-  const uint32_t code = static_cast<uint32_t>(__nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3));
+// amax / 6 correctly rounded.  For a in [2^-125, FLT_MAX] the product with
+// rn(1/6), corrected once by its fma remainder (Markstein's correction step),
+// equals the correctly rounded quotient; tests/test_div6_gpu.py checks this
+// against CUDA's __fdiv_rn for every float in that range.  Below it the
+// quotient is subnormal and CUDA's division is used.
+__device__ __forceinline__ float div6_rn(float a) {
+  if (a >= __uint_as_float(0x01000000u) && a <= __uint_as_float(0x7F7FFFFFu)) {
+    const float c6 = __uint_as_float(0x3E2AAAABu);   // rn(1/6)
+    const float q = __fmul_rn(a, c6);
+    return __fmaf_rn(__fmaf_rn(-q, 6.0f, a), c6, q);
+  }
+  return __fdiv_rn(a, 6.0f);
+}
+
+// E4M3 byte -> fp32 (exact): exponent field E (bias 7), mantissa m (3 bits);
+// E = 0 is subnormal, m * 2^-9.
+__device__ __forceinline__ float e4m3_decode(uint32_t code) {
   const uint32_t e = (code >> 3) & 0xF;
   const uint32_t m = code & 0x7;
   const float sig = static_cast<float>(e ? (8u + m) : m);          // integer significand
-  const float pw = __uint_as_float((((e ? e : 1u) + 117u)) << 23); // 2^(max(E,1) - 10)
-  const float s = sig * pw;                                         // exact
+  const float pw = __uint_as_float(((e ? e : 1u) + 117u) << 23);    // 2^(max(E,1) - 10)
+  return sig * pw;
+}
+
+// E4M3 scales (NVFP4, and 32-element blocks with E4M3 forced): t =
+// min((gs * amax) / 6, 448) with correctly rounded ops, then E4M3 nearest-even
+// (CUDA's satfinite fp8 conversion).  inv_s = rn(rn(1/s) * gs) (0 when s = 0,
+// which turns every element of the block into code 0).  gs = 1 without a
+// global scale.
+__device__ __forceinline__ uint32_t e4m3_block_scale(float amax, float gs, float& inv_s) {
+  const float t = fminf(div6_rn(__fmul_rn(gs, amax)), 448.0f);
+  const uint32_t code = static_cast<uint32_t>(__nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3));
+  const float s = e4m3_decode(code);
   inv_s = s > 0.0f ? __fmul_rn(__frcp_rn(s), gs) : 0.0f;
   return code;
 }
@@ -160,7 +179,7 @@ __device__ __forceinline__ uint32_t e4m3_block_scale(float amax, float gs, float
 // it steps up), clamped to [-127, 127]; byte = e + 127.  inv_s = 2^-e exactly,
 // so y * inv_s is the correctly rounded y / s.
 __device__ __forceinline__ uint32_t ue8m0_block_scale(float amax, float& inv_s) {
-  const float t = __fdiv_rn(amax, 6.0f);
+  const float t = div6_rn(amax);
   const uint32_t bits = __float_as_uint(t);
   const int E = static_cast<int>(bits >> 23);   // t >= 0: no sign bit
   const uint32_t man = bits & 0x7FFFFFu;

@@ -20,6 +20,7 @@ written as the plain per-row definition with the rounding rule of
   5. inv = (1 / s) * gs for E4M3 scales, 1 / s for UE8M0 (each op rounded to
      nearest fp32);  v = y * inv;  code = E2M1_rne(v)   (s == 0: codes 0)
   6. two codes per byte, element 2j in the low nibble
+  (side output, on request: y rounded to nearest-even in the storage dtype)
   7. scale bytes row-major [m, k] and/or in the 128x4 tile order
      (m//128)*nkt*512 + (k//4)*512 + (m%32)*16 + ((m%128)//32)*4 + k%4,
      nkt = ceil(nb / 4), every padding byte of the tiled buffer zero.
@@ -123,6 +124,7 @@ class OracleResult:
     t: np.ndarray                 # (M, nb) fp32 value the scale rounds from
     scale: np.ndarray             # (M, nb) fp32 decoded scale
     v: np.ndarray                 # (M, H) fp32 value each code rounds from
+    y_out: Optional[np.ndarray] = None   # (M, H) y rounded to the storage dtype (fused op)
 
 
 def add_rmsnorm_fp4_quant(x, r, w, eps: float, dtype: str, fmt: str,
@@ -151,7 +153,10 @@ def add_rmsnorm_fp4_quant(x, r, w, eps: float, dtype: str, fmt: str,
 
     # 3. weight, then normalise (h * w is exact in fp32)
     y = (h * w[None, :]) * rstd[:, None]
-    return _quantize_rows(y, h, rstd, fmt, layout, global_scale)
+    res = _quantize_rows(y, h, rstd, fmt, layout, global_scale)
+    # optional side output: y itself rounded once to the storage dtype
+    res.y_out = round_to_dtype(y, dtype)
+    return res
 
 
 def quantize(x, fmt: str, layout: str, global_scale: float = 1.0) -> OracleResult:

@@ -96,3 +96,16 @@ def test_residual_is_rounded_sum():
     assert o.residual[0, 1] == 1.0
     assert o.residual[0, 2] == 1 + 2.0 ** -6
     assert o.residual[0, 3] == 1.0
+
+
+def test_y_side_output_is_y_rounded_once():
+    """The optional y output is y rounded to the storage dtype: for the
+    constant row, y = 0.99999952 lies between the bf16 neighbours 0.99609375
+    and 1.0 and rounds to 1.0; for fp16 (spacing 2^-11 below 1) also to 1.0."""
+    for dtype in ("bf16", "fp16"):
+        x = np.zeros((1, 64), np.float32)
+        r = np.ones((1, 64), np.float32)
+        o = oracle.add_rmsnorm_fp4_quant(x, r, np.ones(64, np.float32), 1e-6, dtype, "nvfp4",
+                                         "rowmajor")
+        assert np.all(o.y_out == 1.0)
+        assert np.all(o.y < 1.0)

@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--global-scale", type=float, default=None,
                     help="pass this global scale as a device scalar (E4M3 formats)")
     ap.add_argument("--format", default=None, help="override the workload's format")
+    ap.add_argument("--y-out", action="store_true",
+                    help="also write y (the normalised rows, input dtype): +2H bytes per row")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
@@ -279,6 +281,7 @@ def run_ours(args, wl):
     if args.global_scale is not None:
         gs_t = torch.tensor([args.global_scale], dtype=torch.float32, device=dev)
     gp = gs_t.data_ptr() if gs_t is not None else None
+    y_t, yp = None, None
     if args.op == "quantize":
         qcall = L.fp4_quantize
 
@@ -287,10 +290,12 @@ def run_ours(args, wl):
             if st != 0:
                 raise fq.Fp4Error(st, "fp4_quantize")
     else:
-        call = L.fp4_add_rmsnorm_quant_gs
+        call = L.fp4_add_rmsnorm_quant_ex
+        y_t = torch.empty(M, H, dtype=x.dtype, device=dev) if args.y_out else None
+        yp = y_t.data_ptr() if y_t is not None else None
 
         def step(i):
-            st = call(ptrs[i & 1], rp, wp, gp, eps, M, H, dt, fmt, lay, pp, sp, s2, sh)
+            st = call(ptrs[i & 1], H, rp, H, wp, gp, eps, M, H, dt, fmt, lay, pp, sp, s2, yp, sh)
             if st != 0:
                 raise fq.Fp4Error(st, "fp4_add_rmsnorm_quant")
 
@@ -342,7 +347,7 @@ def run_ours(args, wl):
     if sampler:
         sampler.stop()
 
-    alg = wl.algorithmic_bytes(args.op)
+    alg = wl.algorithmic_bytes(args.op) + (2 * M * H if args.y_out and args.op == "fused" else 0)
     ms_step = total_ms / K
     value = world * alg * K / (total_ms * 1e-3) / 1e9
     kern_mean = ms_step                       # one launch per step
@@ -369,9 +374,10 @@ def run_ours(args, wl):
         dr = torch.empty_like(r)
         dw = torch.empty_like(w)
         fused = args.op == "fused"
+        ho_y = torch.empty(M, H, dtype=x.dtype).pin_memory() if fused and args.y_out else None
         h2d = hx.numel() * 2 + (hr.numel() * 2 + hw.numel() * 2 if fused else 0)
         d2h = (ho_r.numel() * 2 if fused else 0) + ho_p.numel() + ho_s.numel() + \
-            (ho_s2.numel() if ho_s2 is not None else 0)
+            (ho_s2.numel() if ho_s2 is not None else 0) + (ho_y.numel() * 2 if ho_y is not None else 0)
 
         def e2e_step():
             dx.copy_(hx, non_blocking=True)
@@ -381,8 +387,8 @@ def run_ours(args, wl):
             if args.op == "quantize":
                 st = L.fp4_quantize(dx.data_ptr(), gp, M, H, dt, fmt, lay, pp, sp, s2, sh)
             else:
-                st = L.fp4_add_rmsnorm_quant_gs(dx.data_ptr(), dr.data_ptr(), dw.data_ptr(), gp,
-                                                eps, M, H, dt, fmt, lay, pp, sp, s2, sh)
+                st = L.fp4_add_rmsnorm_quant_ex(dx.data_ptr(), H, dr.data_ptr(), H, dw.data_ptr(),
+                                                gp, eps, M, H, dt, fmt, lay, pp, sp, s2, yp, sh)
             if st != 0:
                 raise fq.Fp4Error(st, "e2e step")
             if fused:
@@ -391,6 +397,8 @@ def run_ours(args, wl):
             ho_s.copy_(sf, non_blocking=True)
             if ho_s2 is not None:
                 ho_s2.copy_(sf_rm, non_blocking=True)
+            if ho_y is not None:
+                ho_y.copy_(y_t, non_blocking=True)
 
         with torch.cuda.stream(stream):
             for _ in range(2):
@@ -419,6 +427,7 @@ def run_ours(args, wl):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": wl.name, "op": args.op, "global_scale": args.global_scale,
+                       "y_out": bool(args.y_out),
                        "M": M, "H": H, "format": wl.fmt,
                        "sf_layout": wl.sf_layout, "io_dtype": wl.dtype, "eps": wl.eps,
                        "algorithmic_bytes_per_step": alg,

@@ -114,6 +114,30 @@ fp4_status_t fp4_add_rmsnorm_quant_gs(const void* input, void* residual, const v
                                       fp4q_stream_t stream);
 
 /*
+ * fp4_add_rmsnorm_quant_ex - the general form of the fused op: strided rows
+ * and an optional y output (API variants of the FlashInfer page's
+ * `add_rmsnorm_fp4quant`, which views 3-D input as 2-D rows).
+ *
+ *   input_row_stride, residual_row_stride  elements between consecutive rows
+ *                  (0 = H); >= H and a multiple of 16 (rows start 32-byte
+ *                  aligned).  Outputs stay dense.
+ *   out_y          [M, H] dtype, dense, 32-byte aligned, or NULL: receives y =
+ *                  (h * w) * rstd rounded to the storage dtype (the value the
+ *                  codes quantize), for consumers that want it unquantized.
+ *   global_scale   as in fp4_add_rmsnorm_quant_gs (NULL = 1).
+ * Everything else as fp4_add_rmsnorm_quant; the outputs and y must not
+ * overlap the inputs or each other.
+ */
+fp4_status_t fp4_add_rmsnorm_quant_ex(const void* input, int64_t input_row_stride,
+                                      void* residual, int64_t residual_row_stride,
+                                      const void* weight, const float* global_scale, float eps,
+                                      int64_t M, int64_t H, fp4_dtype_t dtype,
+                                      fp4_format_t format, fp4_sf_layout_t sf_layout,
+                                      uint8_t* out_packed, uint8_t* out_sf,
+                                      uint8_t* out_sf_rowmajor, void* out_y,
+                                      fp4q_stream_t stream);
+
+/*
  * fp4_quantize - block quantization of `input` [M, H] itself, without the
  * residual add and the normalisation: the standalone producer of packed E2M1
  * plus scales (FlashRT `fp4-gemm` README, `quantize_fp4_sfa_bf16` /

@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     add_rmsnorm_fp4quant,
     dequant,
     fp4_add_rmsnorm_quant,
+    fp4_add_rmsnorm_quant_ex,
     fp4_add_rmsnorm_quant_gs,
     fp4_dequant,
     fp4_quantize,

@@ -47,6 +47,9 @@ def lib() -> ctypes.CDLL:
     L.fp4_add_rmsnorm_quant_gs.argtypes = [vp, vp, vp, vp, ctypes.c_float, i64, i64, ci, ci, ci,
                                            vp, vp, vp, vp]
     L.fp4_add_rmsnorm_quant_gs.restype = ci
+    L.fp4_add_rmsnorm_quant_ex.argtypes = [vp, i64, vp, i64, vp, vp, ctypes.c_float, i64, i64,
+                                           ci, ci, ci, vp, vp, vp, vp, vp]
+    L.fp4_add_rmsnorm_quant_ex.restype = ci
     L.fp4_quantize.argtypes = [vp, vp, i64, i64, ci, ci, ci, vp, vp, vp, vp]
     L.fp4_quantize.restype = ci
     L.fp4_dequant.argtypes = [vp, vp, i64, i64, ci, ci, vp, vp]
@@ -83,6 +86,18 @@ def fp4_add_rmsnorm_quant_gs(input_ptr: int, residual_ptr: int, weight_ptr: int,
                                           global_scale_ptr or None, eps, M, H, dtype, fmt,
                                           sf_layout, out_packed_ptr, out_sf_ptr,
                                           out_sf_rowmajor_ptr or None, stream or None)
+
+
+def fp4_add_rmsnorm_quant_ex(input_ptr: int, input_row_stride: int, residual_ptr: int,
+                             residual_row_stride: int, weight_ptr: int, global_scale_ptr: int,
+                             eps: float, M: int, H: int, dtype: int, fmt: int, sf_layout: int,
+                             out_packed_ptr: int, out_sf_ptr: int, out_sf_rowmajor_ptr: int,
+                             out_y_ptr: int, stream: int) -> int:
+    return lib().fp4_add_rmsnorm_quant_ex(input_ptr, input_row_stride, residual_ptr,
+                                          residual_row_stride, weight_ptr, global_scale_ptr or None,
+                                          eps, M, H, dtype, fmt, sf_layout, out_packed_ptr,
+                                          out_sf_ptr, out_sf_rowmajor_ptr or None,
+                                          out_y_ptr or None, stream or None)
 
 
 def fp4_quantize(input_ptr: int, global_scale_ptr: int, M: int, H: int, dtype: int, fmt: int,
@@ -183,20 +198,37 @@ def _outputs(lead, M, H, f, lay, dev, out_packed, out_sf, out_sf_rowmajor):
     return out_packed, out_sf, out_sf_rowmajor
 
 
+def _row_stride(t, name) -> int:
+    """Elements between rows: dense tensors, or 2-D views with unit column stride
+    (e.g. a column slice of a wider matrix)."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.is_contiguous():
+        return t.shape[-1]
+    if t.dim() == 2 and t.stride(1) == 1:
+        return t.stride(0)
+    raise ValueError(f"{name} must be contiguous or a 2-D view with unit column stride")
+
+
 def add_rmsnorm_fp4quant(input, residual, weight, eps: float = 1e-6, fmt: str = "nvfp4",
                          sf_layout: str = "rowmajor", out_packed=None, out_sf=None,
-                         out_sf_rowmajor=None, global_scale=None, stream=None) -> Tuple:
+                         out_sf_rowmajor=None, global_scale=None, return_y: bool = False,
+                         out_y=None, stream=None) -> Tuple:
     """residual += input (in place); returns (packed, sf) or, for
-    sf_layout="both", (packed, sf_tiled, sf_rowmajor).  ``input`` may be 2-D
-    (M, H) or 3-D (B, S, H); packed has the same leading shape with H/2 bytes.
-    Scale buffers are uint8: row-major (M, H/b), tiled flat.  ``global_scale``:
-    optional CUDA float32 tensor of one element (E4M3 formats)."""
-    for name, t in (("input", input), ("residual", residual), ("weight", weight)):
-        _check_cuda(t, name)
+    sf_layout="both", (packed, sf_tiled, sf_rowmajor), with y (the normalised,
+    weighted rows in the input dtype) appended when return_y is set or out_y
+    given.  ``input`` may be 2-D (M, H), a 2-D view with a row stride, or 3-D
+    (B, S, H); packed has the same leading shape with H/2 bytes.  Scale buffers
+    are uint8: row-major (M, H/b), tiled flat.  ``global_scale``: optional CUDA
+    float32 tensor of one element (E4M3 formats)."""
+    xs = _row_stride(input, "input")
+    rs = _row_stride(residual, "residual")
+    _check_cuda(weight, "weight")
     if input.shape != residual.shape or input.dtype != residual.dtype:
         raise ValueError("input and residual must have the same shape and dtype")
     if weight.dtype != input.dtype or weight.dim() != 1 or weight.shape[0] != input.shape[-1]:
         raise ValueError("weight must be (H,) with the input's dtype")
+    torch = _torch()
     dt = _dtype_code(input)
     f = _FORMATS[fmt]
     lay = _LAYOUTS[sf_layout]
@@ -207,16 +239,20 @@ def add_rmsnorm_fp4quant(input, residual, weight, eps: float = 1e-6, fmt: str = 
         M *= d
     out_packed, out_sf, out_sf_rowmajor = _outputs(lead, M, H, f, lay, input.device, out_packed,
                                                    out_sf, out_sf_rowmajor)
-    st = fp4_add_rmsnorm_quant_gs(input.data_ptr(), residual.data_ptr(), weight.data_ptr(),
+    if return_y and out_y is None:
+        out_y = torch.empty(*lead, H, dtype=input.dtype, device=input.device)
+    if out_y is not None:
+        _check_cuda(out_y, "out_y")
+    st = fp4_add_rmsnorm_quant_ex(input.data_ptr(), xs, residual.data_ptr(), rs, weight.data_ptr(),
                                   _gs_ptr(global_scale), float(eps), M, H, dt, f, lay,
                                   out_packed.data_ptr(), out_sf.data_ptr(),
                                   out_sf_rowmajor.data_ptr() if out_sf_rowmajor is not None else 0,
+                                  out_y.data_ptr() if out_y is not None else 0,
                                   _stream_handle(stream))
     if st != 0:
         raise Fp4Error(st, "fp4_add_rmsnorm_quant")
-    if lay == FP4_SF_BOTH:
-        return out_packed, out_sf, out_sf_rowmajor
-    return out_packed, out_sf
+    outs = (out_packed, out_sf, out_sf_rowmajor) if lay == FP4_SF_BOTH else (out_packed, out_sf)
+    return outs + (out_y,) if out_y is not None else outs
 
 
 def quantize_fp4(x, fmt: str = "nvfp4", sf_layout: str = "swizzled", global_scale=None,

@@ -292,27 +292,40 @@ static fp4_status_t check_outputs(int64_t M, int64_t H, fp4_format_t format,
   return FP4_OK;
 }
 
-static fp4_status_t fused_call(const void* input, void* residual, const void* weight,
-                               const float* global_scale, float eps, int64_t M, int64_t H,
-                               fp4_dtype_t dtype, fp4_format_t format, fp4_sf_layout_t sf_layout,
+static fp4_status_t fused_call(const void* input, int64_t x_stride, void* residual,
+                               int64_t r_stride, const void* weight, const float* global_scale,
+                               float eps, int64_t M, int64_t H, fp4_dtype_t dtype,
+                               fp4_format_t format, fp4_sf_layout_t sf_layout,
                                uint8_t* out_packed, uint8_t* out_sf, uint8_t* out_sf_rowmajor,
-                               fp4q_stream_t stream) {
+                               void* out_y, fp4q_stream_t stream) {
   if (dtype != FP4_DT_BF16 && dtype != FP4_DT_FP16) return FP4_ERR_INVALID_ARG;
   if (!valid_format(format) || !valid_layout(sf_layout)) return FP4_ERR_INVALID_ARG;
   if (M < 0 || H <= 0 || !(eps >= 0.0f)) return FP4_ERR_INVALID_ARG;
+  if (x_stride == 0) x_stride = H;
+  if (r_stride == 0) r_stride = H;
+  if (x_stride < H || r_stride < H) return FP4_ERR_INVALID_ARG;
   const int b = block_of(format);
   if (H % b != 0 || H < 64 || H > FP4Q_MAX_H) return FP4_ERR_UNSUPPORTED_SHAPE;
   if (M == 0) return FP4_OK;
   if (M > INT32_MAX) return FP4_ERR_UNSUPPORTED_SHAPE;
   if (!input || !residual || !weight) return FP4_ERR_INVALID_ARG;
+  // rows start on 32-byte boundaries (256-bit accesses, bulk copies)
   if (!aligned(input, 32) || !aligned(residual, 32) || !aligned(weight, 32) ||
-      !aligned(global_scale, 4))
+      !aligned(global_scale, 4) || !aligned(out_y, 32) || x_stride % 16 || r_stride % 16)
     return FP4_ERR_MISALIGNED;
-  const int64_t act_bytes = M * H * 2;
-  if (overlap(input, act_bytes, residual, act_bytes)) return FP4_ERR_INVALID_ARG;
-  const fp4_status_t st = check_outputs(M, H, format, sf_layout, residual, act_bytes, out_packed,
+  const int64_t x_bytes = ((M - 1) * x_stride + H) * 2;
+  const int64_t r_bytes = ((M - 1) * r_stride + H) * 2;
+  const int64_t y_bytes = M * H * 2;
+  if (overlap(input, x_bytes, residual, r_bytes)) return FP4_ERR_INVALID_ARG;
+  const fp4_status_t st = check_outputs(M, H, format, sf_layout, residual, r_bytes, out_packed,
                                         out_sf, out_sf_rowmajor);
   if (st != FP4_OK) return st;
+  if (out_y) {
+    const int64_t sf_bytes = fp4_sf_size_bytes(M, H, format, sf_layout);
+    if (overlap(out_y, y_bytes, input, x_bytes) || overlap(out_y, y_bytes, residual, r_bytes) ||
+        overlap(out_y, y_bytes, out_packed, M * H / 2) || overlap(out_y, y_bytes, out_sf, sf_bytes))
+      return FP4_ERR_INVALID_ARG;
+  }
 
   FusedShape shape;
   const int64_t rows = sf_layout == FP4_SF_ROWMAJOR ? M : (M + 127) / 128 * 128;
@@ -320,6 +333,9 @@ static fp4_status_t fused_call(const void* input, void* residual, const void* we
                           dtype == FP4_DT_BF16 ? 0 : 1, num_sms_current_device(), &shape))
     return FP4_ERR_UNSUPPORTED_SHAPE;
   if (shape.grid > INT32_MAX) return FP4_ERR_UNSUPPORTED_SHAPE;
+  // the TMA ring copies a stage's rows in one piece: strided rows need one row per stage
+  if (shape.path == kPathTma && shape.rows_per_cta > 1 && (x_stride != H || r_stride != H))
+    return FP4_ERR_UNSUPPORTED_SHAPE;
 
   FusedParams p;
   p.x = input;
@@ -331,6 +347,9 @@ static fp4_status_t fused_call(const void* input, void* residual, const void* we
             : (sf_layout == FP4_SF_BOTH)   ? out_sf_rowmajor
                                            : nullptr;
   p.gs = global_scale;
+  p.y = out_y;
+  p.x_stride = x_stride;
+  p.r_stride = r_stride;
   p.eps = eps;
   p.M = M;
   p.rows = rows;
@@ -356,8 +375,8 @@ fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void
                                    fp4_format_t format, fp4_sf_layout_t sf_layout,
                                    uint8_t* out_packed, uint8_t* out_sf,
                                    uint8_t* out_sf_rowmajor, fp4q_stream_t stream) {
-  return fused_call(input, residual, weight, nullptr, eps, M, H, dtype, format, sf_layout,
-                    out_packed, out_sf, out_sf_rowmajor, stream);
+  return fused_call(input, H, residual, H, weight, nullptr, eps, M, H, dtype, format, sf_layout,
+                    out_packed, out_sf, out_sf_rowmajor, nullptr, stream);
 }
 
 fp4_status_t fp4_add_rmsnorm_quant_gs(const void* input, void* residual, const void* weight,
@@ -366,8 +385,21 @@ fp4_status_t fp4_add_rmsnorm_quant_gs(const void* input, void* residual, const v
                                       fp4_sf_layout_t sf_layout, uint8_t* out_packed,
                                       uint8_t* out_sf, uint8_t* out_sf_rowmajor,
                                       fp4q_stream_t stream) {
-  return fused_call(input, residual, weight, global_scale, eps, M, H, dtype, format, sf_layout,
-                    out_packed, out_sf, out_sf_rowmajor, stream);
+  return fused_call(input, H, residual, H, weight, global_scale, eps, M, H, dtype, format,
+                    sf_layout, out_packed, out_sf, out_sf_rowmajor, nullptr, stream);
+}
+
+fp4_status_t fp4_add_rmsnorm_quant_ex(const void* input, int64_t input_row_stride,
+                                      void* residual, int64_t residual_row_stride,
+                                      const void* weight, const float* global_scale, float eps,
+                                      int64_t M, int64_t H, fp4_dtype_t dtype,
+                                      fp4_format_t format, fp4_sf_layout_t sf_layout,
+                                      uint8_t* out_packed, uint8_t* out_sf,
+                                      uint8_t* out_sf_rowmajor, void* out_y,
+                                      fp4q_stream_t stream) {
+  return fused_call(input, input_row_stride, residual, residual_row_stride, weight, global_scale,
+                    eps, M, H, dtype, format, sf_layout, out_packed, out_sf, out_sf_rowmajor,
+                    out_y, stream);
 }
 
 fp4_status_t fp4_quantize(const void* input, const float* global_scale, int64_t M, int64_t H,

@@ -75,8 +75,8 @@ __device__ __forceinline__ void st_u8(void* p, uint32_t v) {
 }
 
 // ---------------------------------------------------------------------------
-// 16-bit storage types: unpack a pair to fp32 (exact), add two pairs, multiply
-// two pairs into fp32, accumulate squares.
+// 16-bit storage types: unpack a pair to fp32 (exact), round a pair of fp32 to
+// the type, add two pairs, multiply two pairs into fp32, accumulate squares.
 // ---------------------------------------------------------------------------
 template <typename T> struct Pair;
 
@@ -111,6 +111,10 @@ template <> struct Pair<__nv_bfloat16> {
   static __device__ __forceinline__ float2 to_f32(uint32_t u) {
     return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
   }
+  static __device__ __forceinline__ uint32_t from_f32(float lo, float hi) {   // nearest-even
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
   FP4Q_PAIR_OPS(__nv_bfloat16, "add.rn.bf16x2", "fma.rn.f32.bf16")
 };
 
@@ -118,6 +122,10 @@ template <> struct Pair<__half> {
   static __device__ __forceinline__ float2 to_f32(uint32_t u) {
     __half2 v = *reinterpret_cast<__half2*>(&u);
     return __half22float2(v);
+  }
+  static __device__ __forceinline__ uint32_t from_f32(float lo, float hi) {   // nearest-even
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
   }
   FP4Q_PAIR_OPS(__half, "add.rn.f16x2", "fma.rn.f32.f16")
 };

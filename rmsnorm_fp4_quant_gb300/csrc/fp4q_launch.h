@@ -21,6 +21,9 @@ struct FusedParams {
   uint8_t* sf_tiled;
   uint8_t* sf_rm;
   const float* gs;     // device global scale (one fp32) or null for 1
+  void* y;             // optional [M, H] dtype output of y (dense), or null
+  int64_t x_stride;    // elements between rows of x
+  int64_t r_stride;    // elements between rows of the residual
   float eps;
   int64_t M;           // valid rows
   int64_t rows;        // row slots covered by the grid (M, or 128*ceil(M/128) when tiled)

@@ -65,9 +65,9 @@ fused_direct_kernel(const FusedParams p) {
   const int c_begin = rank * p.chunks_per_cta;
   const int c_end = c_begin + p.chunks_per_cta;
   const int c0 = c_begin + lane;
-  const size_t row_off = static_cast<size_t>(row_ok ? row : 0) * static_cast<size_t>(p.H);
-  const T* xrow = static_cast<const T*>(p.x) + row_off;
-  T* rrow = static_cast<T*>(p.r) + row_off;
+  const size_t rsafe = static_cast<size_t>(row_ok ? row : 0);
+  const T* xrow = static_cast<const T*>(p.x) + rsafe * static_cast<size_t>(p.x_stride);
+  T* rrow = static_cast<T*>(p.r) + rsafe * static_cast<size_t>(p.r_stride);
 
   Chunk h[CPT];
   Chunk rr[CPT];
@@ -102,7 +102,8 @@ fused_direct_kernel(const FusedParams p) {
 
   const float rstd = row_rstd(ss, p.H, p.eps);
   const float gs = load_global_scale(p.gs);
-  quantize_and_store<T, FMT, CPT>(h, rstd, gs, p, row, c0, tpr, c_end, row_ok);
+  if (p.y) quantize_and_store<T, FMT, CPT, true>(h, rstd, gs, p, row, c0, tpr, c_end, row_ok);
+  else quantize_and_store<T, FMT, CPT, false>(h, rstd, gs, p, row, c0, tpr, c_end, row_ok);
   if (p.sf_tiled && !row_ok && row < p.rows && rank == 0) zero_tiled_row(p, row, lane, tpr);
 }
 

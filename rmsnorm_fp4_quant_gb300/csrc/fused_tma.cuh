@@ -114,8 +114,9 @@ fused_tma_kernel(const FusedParams p) {
     mbar_arrive_expect_tx(&full[s], 2u * bytes);   // zero bytes completes the phase at once
     if (bytes) {
       uint8_t* st = smem + static_cast<size_t>(s) * 2u * half_stage;
-      bulk_g2s(st, static_cast<const T*>(p.x) + row0 * H, bytes, &full[s]);
-      bulk_g2s(st + half_stage, static_cast<const T*>(p.r) + row0 * H, bytes, &full[s]);
+      // rows of a stage are contiguous in memory (strided rows run with R = 1)
+      bulk_g2s(st, static_cast<const T*>(p.x) + row0 * p.x_stride, bytes, &full[s]);
+      bulk_g2s(st + half_stage, static_cast<const T*>(p.r) + row0 * p.r_stride, bytes, &full[s]);
     }
   };
 
@@ -152,8 +153,8 @@ fused_tma_kernel(const FusedParams p) {
         }
       }
     }
-    const size_t row_off = static_cast<size_t>(row_ok ? row : 0) * static_cast<size_t>(H);
-    T* rrow = static_cast<T*>(p.r) + row_off;
+    T* rrow = static_cast<T*>(p.r) + static_cast<size_t>(row_ok ? row : 0) *
+                                         static_cast<size_t>(p.r_stride);
     float ss = add_and_write_back<T, CPT>(h, rr, rrow, lane, tpr, c_end, ok && row_ok);
 
     const int width = tpr < 32 ? tpr : 32;
@@ -178,7 +179,8 @@ fused_tma_kernel(const FusedParams p) {
       for (int i = 0; i < wpr; ++i) ss += pp[grp * wpr + i];
     }
     const float rstd = row_rstd(ss, H, p.eps);
-    quantize_and_store<T, FMT, CPT>(h, rstd, gs, p, row, lane, tpr, c_end, row_ok);
+    if (p.y) quantize_and_store<T, FMT, CPT, true>(h, rstd, gs, p, row, lane, tpr, c_end, row_ok);
+    else quantize_and_store<T, FMT, CPT, false>(h, rstd, gs, p, row, lane, tpr, c_end, row_ok);
     if (p.sf_tiled && !row_ok && row < p.rows) zero_tiled_row(p, row, lane, tpr);
   }
 }

@@ -157,3 +157,23 @@ def test_quantize_validation(L, kwargs, status):
     st = fq.fp4_quantize(a["x"], a["gs"], a["M"], a["H"], a["dt"], a["f"], a["lay"], a["p"],
                          a["s"], a["s2"], 0)
     assert st == status
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(xs=100), 1),                 # row stride below H
+    (dict(rs=200), 1),
+    (dict(xs=264), 3),                 # rows would not start 32-byte aligned
+    (dict(rs=257 * 16 + 8), 3),
+    (dict(y=A + (7 << 32) + 16), 3),   # y must be 32-byte aligned
+    (dict(y=B + 64), 1),               # y inside the residual
+    (dict(y=P + 32), 1),               # y over the packed output
+    (dict(xs=512, r=A + 512), 1),      # strided input overlapping the residual
+])
+def test_fused_ex_validation(L, kwargs, status):
+    a = dict(x=A, xs=0, r=B, rs=0, w=W, gs=0, eps=1e-6, M=4, H=256, dt=0, f=0, lay=0, p=P, s=S,
+             s2=0, y=0)
+    a.update(kwargs)
+    st = fq.fp4_add_rmsnorm_quant_ex(a["x"], a["xs"], a["r"], a["rs"], a["w"], a["gs"], a["eps"],
+                                     a["M"], a["H"], a["dt"], a["f"], a["lay"], a["p"], a["s"],
+                                     a["s2"], a["y"], 0)
+    assert st == status

@@ -188,3 +188,32 @@ def test_global_scale(M, H, fmt, gs):
     TMA ring); UE8M0 scales ignore it."""
     wl = _wl(M, H, "bf16", fmt, "both", seed=3 * M + H)
     _run_full(wl, global_scale=gs)
+
+
+@pytest.mark.parametrize("M,H", [(129, 1536), (700, 7168), (41, 17408), (333, 32768)])
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_strided_rows_and_y_output(M, H, fmt, dtype):
+    """Input and residual as column slices of wider matrices (row strides
+    H + 64 and H + 128), y returned in the storage dtype: codes, scales and
+    residual equal the oracle's, and y is the oracle's fp32 y rounded once
+    (up to the midpoint rule of `parity.compare_y`);
+    every kernel path (direct, cluster, TMA ring)."""
+    wl = _wl(M, H, dtype, fmt, "both", seed=5 * M + H)
+    x, r, w = workloads.make_inputs(wl, "cpu")
+    o = oracle.add_rmsnorm_fp4_quant(x.float().numpy(), r.float().numpy(), w.float().numpy(),
+                                     wl.eps, dtype, fmt, "both")
+    xw = torch.full((M, H + 64), 3.0, dtype=x.dtype, device="cuda")
+    rw = torch.full((M, H + 128), 5.0, dtype=x.dtype, device="cuda")
+    xw[:, :H] = x.cuda()
+    rw[:, 64:64 + H] = r.cuda()
+    xv, rv = xw[:, :H], rw[:, 64:64 + H]
+    packed, sf, sf_rm, y = fq.add_rmsnorm_fp4quant(xv, rv, w.cuda(), eps=wl.eps, fmt=fmt,
+                                                   sf_layout="both", return_y=True)
+    torch.cuda.synchronize()
+    g = parity.fetch((packed, sf, sf_rm), rv, "both")
+    parity.compare(g, o, fmt, "both", dtype, M, H)
+    parity.compare_y(y.view(torch.int16).cpu().numpy().view(np.uint16), o.y, dtype)
+    # the padding columns around the views are untouched
+    assert torch.all(xw[:, H:] == 3.0) and torch.all(rw[:, :64] == 5.0)
+    assert torch.all(rw[:, 64 + H:] == 5.0)

@@ -12,8 +12,9 @@ Sources (web pages; section names as they appear there):
     Parameters / Returns / Notes) - the operation itself;
   * vLLM ``fused_wo_a`` (``FusedWoAKernel`` scale write-out) - the 128x4 scale
     tile order and zero-filled padding;
-  * FlashRT ``fp4-gemm`` README (Tensor Contract, Validation) - the packed FP4
-    and SFA contract, and validation by dequantisation.
+  * FlashRT ``fp4-gemm`` README (Tensor Contract, Available Functions,
+    Validation) - the packed FP4 and SFA contract, validation by
+    dequantisation, and the consumer GEMM (``oracle.gemm``).
 
 Arithmetic is fp32 with every step correctly rounded (numpy float32 ops are
 IEEE-754 round-to-nearest-even); the sum of squares is accumulated in fp64.
@@ -45,3 +46,4 @@ from .add_rmsnorm_quant import (  # noqa: F401
     dequant,
     block_size,
 )
+from .gemm import GemmResult, gemm_bf16  # noqa: F401

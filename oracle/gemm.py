@@ -1,0 +1,66 @@
+"""Oracle of the consumer GEMM: block-scaled FP4 A times FP4 B transposed, bf16 out.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).
+
+Follows the FlashRT ``fp4-gemm`` README:
+  * Tensor Contract: ``a_packed`` uint8 (M, K/2), ``b_packed`` uint8 (N, K/2),
+    ``sfa`` / ``sfb`` the 128x4 tiled scale buffers of (M, K) and (N, K),
+    output bf16 (M, N);
+  * Available Functions: ``nvfp4_gemm_bf16(..., alpha)``, the bias and residual
+    epilogues ``nvfp4_gemm_bias_bf16``, ``nvfp4_gemm_residual_bf16``,
+    ``nvfp4_gemm_bias_residual_bf16``;
+  * Validation: the reference dequantises the very FP4 codes and scales the
+    kernel reads and multiplies the dequantised matrices.
+
+So, with deq() the exact E2M1-value-times-block-scale of ``oracle.dequant``:
+
+    S[m, n]   = sum_k deq(A)[m, k] * deq(B)[n, k]          (fp64)
+    out[m, n] = bf16( fp32( alpha * S[m, n] + bias[n] + residual[m, n] ) )
+
+Readings where the README is silent:
+  * the order of the epilogue terms: alpha scales the product only; bias
+    (length N) and residual (M x N, bf16) are added after it, as the function
+    names list them;
+  * the sum is taken in fp64 (every product of two dequantised values is
+    exact in fp64; the sum is exact up to fp64 rounding), then rounded once to
+    fp32 and once to bf16 - the PyTorch-reference path of the Validation
+    section (fp32 GEMM output cast to bf16).  A GPU accumulating in fp32 is
+    compared against ``exact`` with the fp32 accumulation bound, not
+    bit-for-bit;
+  * ``bound`` = |alpha| * sum_k |deq(A)[m, k]| * |deq(B)[n, k]|, the scale of
+    the rounding error of any summation order.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+from .add_rmsnorm_quant import dequant
+from .formats import bf16_round
+
+
+@dataclasses.dataclass
+class GemmResult:
+    exact: np.ndarray     # (M, N) fp64: alpha * S + bias + residual
+    out: np.ndarray       # (M, N) fp32 holding the bf16 result
+    bound: np.ndarray     # (M, N) fp64: |alpha| * sum_k |a| |b|
+
+
+def gemm_bf16(a_packed, b_packed, sfa, sfb, M: int, N: int, K: int, alpha: float = 1.0,
+              bias: Optional[np.ndarray] = None, residual: Optional[np.ndarray] = None,
+              fmt: str = "nvfp4", sf_layout: str = "swizzled") -> GemmResult:
+    """alpha * deq(A) @ deq(B)^T (+ bias) (+ residual), rounded to bf16."""
+    a = dequant(a_packed, sfa, M, K, fmt, sf_layout).astype(np.float64)
+    b = dequant(b_packed, sfb, N, K, fmt, sf_layout).astype(np.float64)
+    alpha64 = float(np.float32(alpha))
+    s = a @ b.T
+    exact = alpha64 * s
+    if bias is not None:
+        exact = exact + np.asarray(bias, np.float64).reshape(1, N)
+    if residual is not None:
+        exact = exact + np.asarray(residual, np.float64).reshape(M, N)
+    bound = abs(alpha64) * (np.abs(a) @ np.abs(b).T)
+    out = bf16_round(exact.astype(np.float32))
+    return GemmResult(exact, out, bound)

@@ -33,6 +33,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
+
 import workloads  # noqa: E402
 
 METRIC = "fused add+RMSNorm+FP4-quant HBM GB/s and % of GB300 HBM roofline (rows/s)"
@@ -50,8 +52,11 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--rows", type=int, default=None,
                     help="override the workload's M (smaller cases for profiling)")
-    ap.add_argument("--op", choices=["fused", "quantize"], default="fused",
-                    help="fused add+RMSNorm+quantize (default) or the standalone quantize")
+    ap.add_argument("--op", choices=["fused", "quantize", "gemm"], default="fused",
+                    help="fused add+RMSNorm+quantize (default), the standalone quantize, or "
+                         "the NVFP4 GEMM that consumes them (--gemm picks the shape)")
+    ap.add_argument("--gemm", default="G4_M8192_N7168_K7168",
+                    help="GEMM workload for --op gemm")
     ap.add_argument("--global-scale", type=float, default=None,
                     help="pass this global scale as a device scalar (E4M3 formats)")
     ap.add_argument("--format", default=None, help="override the workload's format")
@@ -451,8 +456,213 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# the consumer GEMM
+# ---------------------------------------------------------------------------
+GEMM_METRIC = "NVFP4 GEMM TFLOP/s (bf16 out) and % of the GB300 FP4 tensor roofline"
+FP4_PER_BF16 = 13.5 / 2.25     # nominal dense FP4 / bf16 tensor rates
+
+
+def measured_fp4_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]) * FP4_PER_BF16, \
+            "measured bf16 burst (MEASURED_PEAKS.json bf16_tflops) x 6, the nominal FP4/bf16 ratio"
+    except Exception:
+        return 1900.0 * FP4_PER_BF16, "fallback 1.9 PFLOP/s bf16 x 6"
+
+
+def gemm_operands(gw, device):
+    K = gw.K
+    a = workloads.random_bytes(gw.M * K // 2, gw.seed, 0, device=device).reshape(gw.M, K // 2)
+    b = workloads.random_bytes(gw.N * K // 2, gw.seed, 1, device=device).reshape(gw.N, K // 2)
+    scales = list(range(0x20, 0x51))
+    nsa = ((gw.M + 127) // 128) * (K // 64) * 512
+    nsb = ((gw.N + 127) // 128) * (K // 64) * 512
+    sfa = workloads.random_bytes(nsa, gw.seed, 2, scales, device=device)
+    sfb = workloads.random_bytes(nsb, gw.seed, 3, scales, device=device)
+    return a, b, sfa, sfb
+
+
+def gemm_cpu_baseline(gw, seconds: float):
+    """The GEMM oracle on the first rows of the workload (the whole B operand
+    is dequantised each time, as the oracle stands)."""
+    import oracle
+    a, b, sfa, sfb = gemm_operands(gw, "cpu")
+    an, bn, san, sbn = a.numpy(), b.numpy(), sfa.numpy(), sfb.numpy()
+    rows = 1
+    while True:
+        t = time.perf_counter()
+        oracle.gemm_bf16(an, bn, san, sbn, gw.M, gw.N, gw.K, rows=np.arange(rows))
+        dt = time.perf_counter() - t
+        if dt > seconds / 4 or rows >= gw.M:
+            break
+        rows = min(gw.M, rows * 4)
+    flops = 2 * rows * gw.N * gw.K
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{rows} of {gw.M} rows of {gw.name} (B dequantised in full), numpy "
+                      f"oracle, {dt:.1f} s"}
+
+
+def run_gemm_reference(args):
+    """The GEMM oracle as the reference arm: each step a bounded row sample."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    gw = workloads.GEMM_CONFIGS[args.gemm]
+    steps = [gemm_cpu_baseline(gw, 2.0) for _ in range(max(1, args.steps))]
+    val = statistics.median(s["value"] for s in steps)
+    line = {"impl": "reference", "metric": GEMM_METRIC, "value": val, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": len(steps), "warmup": 0, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": gw.name, "op": "gemm", "M": gw.M, "N": gw.N, "K": gw.K},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": steps[0]["sample"]},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gemm(args):
+    import torch
+
+    import rmsnorm_fp4_quant_gb300 as fq
+
+    world, rank, local = dist_env()
+    gw = workloads.GEMM_CONFIGS[args.gemm]
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    L = fq.lib()
+    a, b, sfa, sfb = gemm_operands(gw, dev)
+    out = torch.empty(gw.M, gw.N, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    ap_, bp_, sap, sbp, op_ = a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(), \
+        out.data_ptr()
+
+    def step(i):
+        st = L.fp4_gemm_nvfp4_bf16(ap_, bp_, sap, sbp, 1.0, None, None, gw.M, gw.N, gw.K, op_, 0,
+                                   sh)
+        if st != 0:
+            raise fq.Fp4Error(st, "fp4_gemm_nvfp4_bf16")
+
+    alg = gw.algorithmic_bytes()
+    flush = alg < 2 * L2_BYTES
+    scrub = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush else None
+    sampler = ClockSampler(gpu_smi_id(torch, dev)) if rank == 0 else None
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    stream.synchronize()
+    K = args.steps
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    if flush:
+        # operands fit in L2: scrub it before every launch, time each launch alone
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                scrub.fill_(i & 0xFF)
+                ev[i][0].record(stream)
+                step(i)
+                ev[i][1].record(stream)
+        stream.synchronize()
+        total_ms = sum(x.elapsed_time(y) for x, y in ev)
+    else:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for i in range(K):
+                step(i)
+            t1.record(stream)
+        stream.synchronize()
+        total_ms = t0.elapsed_time(t1)
+    wall1 = time.time()
+    clocks = sampler.summary(wall0, wall1) if sampler else None
+    if sampler:
+        sampler.stop()
+    ms = total_ms / K
+    tflops = gw.flops() / (ms * 1e-3) / 1e12
+    gbs = alg / (ms * 1e-3) / 1e9
+    fp4_peak, fp4_src = measured_fp4_peak()
+    hbm_peak, hbm_src = measured_hbm_peak()
+    tensor_bound = gw.flops() / alg > fp4_peak * 1e12 / (hbm_peak * 1e9)
+    roof = ({"bound": "tensor", "achieved": round(tflops, 1), "peak": round(fp4_peak, 1),
+             "unit": "TFLOP/s", "frac": round(tflops / fp4_peak, 4), "peak_source": fp4_src}
+            if tensor_bound else
+            {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+             "frac": round(gbs / hbm_peak, 4), "peak_source": f"{hbm_src} hbm_gbs"})
+    roof.update({"traffic": None, "kernel": "gemm_nvfp4_kernel", "kernel_ms_mean": round(ms, 5),
+                 "algorithmic_bytes": alg, "flops": gw.flops()})
+
+    e2e = None
+    if rank == 0 and args.e2e_steps > 0:
+        hs = [t.cpu().pin_memory() for t in (a, b, sfa, sfb)]
+        ds = [torch.empty_like(t) for t in (a, b, sfa, sfb)]
+        ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+        def e2e_step():
+            for d, h in zip(ds, hs):
+                d.copy_(h, non_blocking=True)
+            st = L.fp4_gemm_nvfp4_bf16(ds[0].data_ptr(), ds[1].data_ptr(), ds[2].data_ptr(),
+                                       ds[3].data_ptr(), 1.0, None, None, gw.M, gw.N, gw.K,
+                                       op_, 0, sh)
+            if st != 0:
+                raise fq.Fp4Error(st, "e2e gemm")
+            ho.copy_(out, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            e2e_step()
+            stream.synchronize()
+            x0 = torch.cuda.Event(enable_timing=True)
+            x1 = torch.cuda.Event(enable_timing=True)
+            x0.record(stream)
+            for _ in range(args.e2e_steps):
+                e2e_step()
+            x1.record(stream)
+        stream.synchronize()
+        e2e_ms = x0.elapsed_time(x1) / args.e2e_steps
+        e2e = {"value": round(gw.flops() / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": sum(h.numel() for h in hs),
+               "d2h_bytes_per_step": ho.numel() * 2, "ms_per_step": round(e2e_ms, 4),
+               "steps": args.e2e_steps}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = gemm_cpu_baseline(gw, args.cpu_seconds)
+    if rank == 0:
+        line = {
+            "metric": GEMM_METRIC, "value": round(world * tflops, 2), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e2m1 x e2m1 -> f32 accumulate, bf16 out", "data": "synthetic",
+            "config": {"workload": gw.name, "op": "gemm", "M": gw.M, "N": gw.N, "K": gw.K,
+                       "operands": "uniform random E2M1 bytes, E4M3 scale bytes 0x20..0x50",
+                       "l2": "L2 scrubbed (256 MB write) before every launch, launches "
+                             "timed one by one" if flush else
+                             "operands + output %.0f MB per launch vs 129 MB L2, no flush"
+                             % (alg / 1e6),
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": roof, "clocks": clocks, "e2e": e2e, "gpu_launches": K,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.op == "gemm":
+        if args.impl == "reference":
+            run_gemm_reference(args)
+            return
+        run_gemm(args)
+        return
     wl = workloads.CONFIGS[args.workload]
     if args.rows is not None:
         wl = wl.with_shape(args.rows)

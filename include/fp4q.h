@@ -184,6 +184,36 @@ int64_t fp4_sf_size_bytes(int64_t M, int64_t H, fp4_format_t format, fp4_sf_layo
 fp4_status_t fp4_launch_shape(int64_t M, int64_t H, fp4_dtype_t dtype, fp4_format_t format,
                               fp4_sf_layout_t sf_layout, int64_t out[8]);
 
+/*
+ * fp4_gemm_nvfp4_bf16 - the consumer of the packed codes and tiled scales:
+ * out = bf16(alpha * deq(A) @ deq(B)^T (+ bias) (+ residual)) on the tensor
+ * cores (FlashRT `fp4-gemm` README: Tensor Contract; `nvfp4_gemm_bf16`,
+ * `nvfp4_gemm_bias_bf16`, `nvfp4_gemm_residual_bf16`,
+ * `nvfp4_gemm_bias_residual_bf16`), deq = E2M1 value times its E4M3 block
+ * scale (16 elements per block), accumulation in fp32.
+ *
+ *   a_packed  [M, K/2] bytes: rows of A, two E2M1 codes per byte (element 2j in
+ *             the low nibble), e.g. out_packed of the fused op or fp4_quantize.
+ *   b_packed  [N, K/2] bytes: rows of B (the weight, one row per output column).
+ *   sfa, sfb  NVFP4 scales of A (M rows) and of B (N rows) in the 128x4 tiled
+ *             layout (FP4_SF_SWIZZLED), fp4_sf_size_bytes(M or N, K, ...) bytes.
+ *   alpha     fp32 multiplier of the product (e.g. 1 / (gs_a * gs_b) for
+ *             operands quantized with global scales).
+ *   bias      [N] bf16 or NULL, added after alpha.
+ *   residual  [M, N] bf16 or NULL, added last; may be `out` itself.
+ *   out       [M, N] bf16, row-major.
+ *   pdl       nonzero: launched as a programmatic dependent of the previous
+ *             kernel on `stream`, so its prologue overlaps that kernel's tail
+ *             (it waits for that kernel's results before reading anything).
+ * K must be a multiple of 256 and N of 8; every pointer 16-byte aligned; out
+ * must not overlap the inputs (except residual == out).  A tile whose inputs
+ * never arrive (a bounded wait runs out) is written as NaN.
+ */
+fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
+                                 const uint8_t* sfa, const uint8_t* sfb, float alpha,
+                                 const void* bias, const void* residual, int64_t M, int64_t N,
+                                 int64_t K, void* out, int pdl, fp4q_stream_t stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* fp4_status_string(fp4_status_t status);
 

@@ -50,10 +50,16 @@ class GemmResult:
 
 def gemm_bf16(a_packed, b_packed, sfa, sfb, M: int, N: int, K: int, alpha: float = 1.0,
               bias: Optional[np.ndarray] = None, residual: Optional[np.ndarray] = None,
-              fmt: str = "nvfp4", sf_layout: str = "swizzled") -> GemmResult:
-    """alpha * deq(A) @ deq(B)^T (+ bias) (+ residual), rounded to bf16."""
+              fmt: str = "nvfp4", sf_layout: str = "swizzled", rows=None) -> GemmResult:
+    """alpha * deq(A) @ deq(B)^T (+ bias) (+ residual), rounded to bf16.
+
+    ``rows`` (optional index array) restricts the result to those rows of the
+    output (``residual`` then holds just those rows)."""
     a = dequant(a_packed, sfa, M, K, fmt, sf_layout).astype(np.float64)
     b = dequant(b_packed, sfb, N, K, fmt, sf_layout).astype(np.float64)
+    if rows is not None:
+        a = a[np.asarray(rows)]
+        M = a.shape[0]
     alpha64 = float(np.float32(alpha))
     s = a @ b.T
     exact = alpha64 * s

@@ -24,10 +24,12 @@ from ._binding import (  # noqa: F401
     Fp4Error,
     add_rmsnorm_fp4quant,
     dequant,
+    gemm_nvfp4_bf16,
     fp4_add_rmsnorm_quant,
     fp4_add_rmsnorm_quant_ex,
     fp4_add_rmsnorm_quant_gs,
     fp4_dequant,
+    fp4_gemm_nvfp4_bf16,
     fp4_quantize,
     fp4_last_cuda_error,
     fp4_launch_shape,

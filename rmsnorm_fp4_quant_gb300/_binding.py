@@ -62,6 +62,9 @@ def lib() -> ctypes.CDLL:
     L.fp4_last_cuda_error.restype = ci
     L.fp4_launch_shape.argtypes = [i64, i64, ci, ci, ci, ctypes.POINTER(ctypes.c_int64)]
     L.fp4_launch_shape.restype = ci
+    L.fp4_gemm_nvfp4_bf16.argtypes = [vp, vp, vp, vp, ctypes.c_float, vp, vp, i64, i64, i64,
+                                      vp, ci, vp]
+    L.fp4_gemm_nvfp4_bf16.restype = ci
     _lib = L
     return L
 
@@ -111,6 +114,14 @@ def fp4_quantize(input_ptr: int, global_scale_ptr: int, M: int, H: int, dtype: i
 def fp4_dequant(packed_ptr: int, sf_ptr: int, M: int, H: int, fmt: int, sf_layout: int,
                 out_ptr: int, stream: int) -> int:
     return lib().fp4_dequant(packed_ptr, sf_ptr, M, H, fmt, sf_layout, out_ptr, stream or None)
+
+
+def fp4_gemm_nvfp4_bf16(a_packed_ptr: int, b_packed_ptr: int, sfa_ptr: int, sfb_ptr: int,
+                        alpha: float, bias_ptr: int, residual_ptr: int, M: int, N: int, K: int,
+                        out_ptr: int, pdl: int, stream: int) -> int:
+    return lib().fp4_gemm_nvfp4_bf16(a_packed_ptr, b_packed_ptr, sfa_ptr, sfb_ptr, alpha,
+                                     bias_ptr or None, residual_ptr or None, M, N, K, out_ptr,
+                                     pdl, stream or None)
 
 
 def fp4_sf_size_bytes(M: int, H: int, fmt: int, layout: int) -> int:
@@ -293,4 +304,35 @@ def dequant(packed, sf, M: int, H: int, fmt: str = "nvfp4", sf_layout: str = "ro
                      out.data_ptr(), _stream_handle(stream))
     if st != 0:
         raise Fp4Error(st, "fp4_dequant")
+    return out
+
+
+def gemm_nvfp4_bf16(a_packed, b_packed, sfa, sfb, alpha: float = 1.0, bias=None, residual=None,
+                    out=None, pdl: bool = False, stream=None):
+    """bf16 (M, N) = alpha * deq(A) @ deq(B)^T (+ bias) (+ residual) from packed
+    NVFP4 operands (M, K/2) and (N, K/2) and their tiled scale buffers."""
+    torch = _torch()
+    for name, t in (("a_packed", a_packed), ("b_packed", b_packed), ("sfa", sfa), ("sfb", sfb)):
+        _check_cuda(t, name)
+        if t.dtype != torch.uint8:
+            raise ValueError(f"{name} must be uint8")
+    M, K = a_packed.shape[0], 2 * a_packed.shape[-1]
+    N = b_packed.shape[0]
+    if b_packed.shape[-1] * 2 != K:
+        raise ValueError("a_packed and b_packed disagree on K")
+    for name, t in (("bias", bias), ("residual", residual)):
+        if t is not None:
+            _check_cuda(t, name)
+            if t.dtype != torch.bfloat16:
+                raise ValueError(f"{name} must be bfloat16")
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=a_packed.device)
+    _check_cuda(out, "out")
+    st = fp4_gemm_nvfp4_bf16(a_packed.data_ptr(), b_packed.data_ptr(), sfa.data_ptr(),
+                             sfb.data_ptr(), float(alpha),
+                             bias.data_ptr() if bias is not None else 0,
+                             residual.data_ptr() if residual is not None else 0, M, N, K,
+                             out.data_ptr(), 1 if pdl else 0, _stream_handle(stream))
+    if st != 0:
+        raise Fp4Error(st, "fp4_gemm_nvfp4_bf16")
     return out

@@ -30,6 +30,9 @@ int tma_ctas_per_sm_fp16(int fmt, int cpt, int threads, size_t smem);
 #ifndef FP4Q_TMA_MIN_H
 #define FP4Q_TMA_MIN_H 20480            // rows at least this wide use the TMA kernel
 #endif
+#ifndef FP4Q_GEMM_STAGES
+#define FP4Q_GEMM_STAGES 3              // GEMM shared-memory ring depth (2 CTAs per SM at 3)
+#endif
 #ifndef FP4Q_DIRECT_CTA_THREADS
 #define FP4Q_DIRECT_CTA_THREADS 128     // target threads of a direct-kernel CTA
 #endif
@@ -459,6 +462,48 @@ fp4_status_t fp4_dequant(const uint8_t* packed, const uint8_t* sf, int64_t M, in
   p.tiled = sf_layout == FP4_SF_SWIZZLED ? 1 : 0;
   return record_cuda(
       launch_dequant(static_cast<int>(format), p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
+                                 const uint8_t* sfa, const uint8_t* sfb, float alpha,
+                                 const void* bias, const void* residual, int64_t M, int64_t N,
+                                 int64_t K, void* out, int pdl, fp4q_stream_t stream) {
+  if (M < 0 || N < 0 || K <= 0) return FP4_ERR_INVALID_ARG;
+  if (K % 256 != 0 || N % 8 != 0) return FP4_ERR_UNSUPPORTED_SHAPE;
+  if (M > INT32_MAX - 128 || N > INT32_MAX - 128 || K > INT32_MAX / 2)
+    return FP4_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0 || N == 0) return FP4_OK;
+  if (!a_packed || !b_packed || !sfa || !sfb || !out) return FP4_ERR_INVALID_ARG;
+  if (!aligned(a_packed, 16) || !aligned(b_packed, 16) || !aligned(sfa, 16) ||
+      !aligned(sfb, 16) || !aligned(out, 16) || !aligned(bias, 16) || !aligned(residual, 16))
+    return FP4_ERR_MISALIGNED;
+  const int64_t out_bytes = M * N * 2;
+  const int64_t sfa_bytes = fp4_sf_size_bytes(M, K, FP4_NVFP4, FP4_SF_SWIZZLED);
+  const int64_t sfb_bytes = fp4_sf_size_bytes(N, K, FP4_NVFP4, FP4_SF_SWIZZLED);
+  if (overlap(out, out_bytes, a_packed, M * K / 2) || overlap(out, out_bytes, b_packed, N * K / 2) ||
+      overlap(out, out_bytes, sfa, sfa_bytes) || overlap(out, out_bytes, sfb, sfb_bytes) ||
+      (bias && overlap(out, out_bytes, bias, N * 2)))
+    return FP4_ERR_INVALID_ARG;
+  // the residual may be the output itself (each element is read, then written,
+  // by the same thread), but not partly overlap it
+  if (residual && residual != out && overlap(out, out_bytes, residual, out_bytes))
+    return FP4_ERR_INVALID_ARG;
+  GemmParams p;
+  p.sfa = sfa;
+  p.sfb = sfb;
+  p.bias = static_cast<const uint16_t*>(bias);
+  p.residual = static_cast<const uint16_t*>(residual);
+  p.out = static_cast<uint16_t*>(out);
+  p.alpha = alpha;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.stages = FP4Q_GEMM_STAGES;
+  p.nkt = 0;        // filled by the launcher
+  p.num_kb = 0;
+  p.tmem_cols = 0;
+  return record_cuda(launch_gemm_nvfp4(a_packed, b_packed, p, pdl,
+                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -41,7 +41,7 @@ __device__ __forceinline__ void st_peer_f32(float* local_slot, uint32_t peer, fl
   asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(remote), "f"(v) : "memory");
 }
 
-template <typename T, int FMT, int CPT>
+template <typename T, int FMT, int CPT, bool WITH_Y>
 __global__ void __launch_bounds__(max_threads_for_cpt(CPT))
 fused_direct_kernel(const FusedParams p) {
   __shared__ float warp_part[32];
@@ -102,8 +102,7 @@ fused_direct_kernel(const FusedParams p) {
 
   const float rstd = row_rstd(ss, p.H, p.eps);
   const float gs = load_global_scale(p.gs);
-  if (p.y) quantize_and_store<T, FMT, CPT, true>(h, rstd, gs, p, row, c0, tpr, c_end, row_ok);
-  else quantize_and_store<T, FMT, CPT, false>(h, rstd, gs, p, row, c0, tpr, c_end, row_ok);
+  quantize_and_store<T, FMT, CPT, WITH_Y>(h, rstd, gs, p, row, c0, tpr, c_end, row_ok);
   if (p.sf_tiled && !row_ok && row < p.rows && rank == 0) zero_tiled_row(p, row, lane, tpr);
 }
 

@@ -6,7 +6,7 @@
 
 namespace fp4q {
 
-template <typename T, int FMT, int CPT>
+template <typename T, int FMT, int CPT, bool WITH_Y>
 cudaError_t raise_smem_limit(size_t smem) {
   // the limit is a per-device function attribute: raise it when a launch
   // needs more than any earlier one on this device
@@ -15,7 +15,7 @@ cudaError_t raise_smem_limit(size_t smem) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && done[dev] >= smem) return cudaSuccess;
-  e = cudaFuncSetAttribute(fused_tma_kernel<T, FMT, CPT>,
+  e = cudaFuncSetAttribute(fused_tma_kernel<T, FMT, CPT, WITH_Y>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = smem;
   return e;
@@ -23,9 +23,9 @@ cudaError_t raise_smem_limit(size_t smem) {
 
 template <typename T, int FMT, int CPT>
 int ctas_per_sm_one(int threads, size_t smem) {
-  if (raise_smem_limit<T, FMT, CPT>(smem) != cudaSuccess) return 0;
+  if (raise_smem_limit<T, FMT, CPT, false>(smem) != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_tma_kernel<T, FMT, CPT>, threads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_tma_kernel<T, FMT, CPT, false>, threads,
                                                     smem) != cudaSuccess)
     return 0;
   return n;
@@ -52,7 +52,9 @@ int ctas_per_sm_dtype(int fmt, int cpt, int threads, size_t smem) {
   }
 }
 
-template <typename T, int FMT, int CPT>
+// WITH_Y selects the instance that also stores y; the common instance carries
+// none of that code.
+template <typename T, int FMT, int CPT, bool WITH_Y>
 cudaError_t launch_one(const FusedShape& s, const FusedParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(s.grid), 1, 1);
@@ -70,21 +72,22 @@ cudaError_t launch_one(const FusedShape& s, const FusedParams& p, cudaStream_t s
       cfg.numAttrs = 1;
     }
     cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, fused_direct_kernel<T, FMT, CPT>, p);
+    return cudaLaunchKernelEx(&cfg, fused_direct_kernel<T, FMT, CPT, WITH_Y>, p);
   }
-  const cudaError_t e = raise_smem_limit<T, FMT, CPT>(s.smem);
+  const cudaError_t e = raise_smem_limit<T, FMT, CPT, WITH_Y>(s.smem);
   if (e != cudaSuccess) return e;
   cfg.dynamicSmemBytes = s.smem;
-  return cudaLaunchKernelEx(&cfg, fused_tma_kernel<T, FMT, CPT>, p);
+  return cudaLaunchKernelEx(&cfg, fused_tma_kernel<T, FMT, CPT, WITH_Y>, p);
 }
 
 template <typename T, int FMT>
 cudaError_t launch_fmt(const FusedShape& s, const FusedParams& p, cudaStream_t stream) {
+  const bool y = p.y != nullptr;
   switch (s.cpt) {
-    case 1: return launch_one<T, FMT, 1>(s, p, stream);
-    case 2: return launch_one<T, FMT, 2>(s, p, stream);
-    case 3: return launch_one<T, FMT, 3>(s, p, stream);
-    case 4: return launch_one<T, FMT, 4>(s, p, stream);
+    case 1: return y ? launch_one<T, FMT, 1, true>(s, p, stream) : launch_one<T, FMT, 1, false>(s, p, stream);
+    case 2: return y ? launch_one<T, FMT, 2, true>(s, p, stream) : launch_one<T, FMT, 2, false>(s, p, stream);
+    case 3: return y ? launch_one<T, FMT, 3, true>(s, p, stream) : launch_one<T, FMT, 3, false>(s, p, stream);
+    case 4: return y ? launch_one<T, FMT, 4, true>(s, p, stream) : launch_one<T, FMT, 4, false>(s, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

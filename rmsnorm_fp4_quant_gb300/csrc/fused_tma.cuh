@@ -25,50 +25,11 @@
 // for its copies still in flight, and returns.
 #pragma once
 
+#include "async_copy.cuh"
 #include "fused_common.cuh"
 
 namespace fp4q {
 
-constexpr long long kWaitLimitCycles = 2000000000LL;   // ~1 s at 2 GHz
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_init_fence() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-               :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile("{\n\t.reg .pred p;\n\t"
-               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-               "selp.u32 %0, 1, 0, p;\n\t}"
-               : "=r"(done) : "r"(smem_addr(bar)), "r"(parity) : "memory");
-  return done != 0;
-}
-// Bounded wait for phase `parity` of `bar`; false if it did not complete.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long start = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - start > kWaitLimitCycles) return false;
-  }
-  return true;
-}
-// Global -> shared bulk copy (TMA engine), completion counted on `bar`.
-// dst, src 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
-}
 __device__ __forceinline__ void ld_shared_chunk(const void* p, Chunk& c) {
   const uint32_t a = smem_addr(p);
   asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
@@ -77,13 +38,14 @@ __device__ __forceinline__ void ld_shared_chunk(const void* p, Chunk& c) {
                : "=r"(c.u[4]), "=r"(c.u[5]), "=r"(c.u[6]), "=r"(c.u[7]) : "r"(a));
 }
 
+
 // Dynamic shared memory of one CTA: S stages of {x rows, r rows}, S full
 // barriers, a double-buffered array of 32 warp partials.
 __host__ __device__ constexpr size_t tma_smem_bytes(int stages, int rows_per_cta, int H) {
   return static_cast<size_t>(stages) * 4u * rows_per_cta * H + 8u * stages + 2u * 32u * 4u;
 }
 
-template <typename T, int FMT, int CPT>
+template <typename T, int FMT, int CPT, bool WITH_Y>
 __global__ void __launch_bounds__(max_threads_for_cpt(CPT))
 fused_tma_kernel(const FusedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -179,8 +141,7 @@ fused_tma_kernel(const FusedParams p) {
       for (int i = 0; i < wpr; ++i) ss += pp[grp * wpr + i];
     }
     const float rstd = row_rstd(ss, H, p.eps);
-    if (p.y) quantize_and_store<T, FMT, CPT, true>(h, rstd, gs, p, row, lane, tpr, c_end, row_ok);
-    else quantize_and_store<T, FMT, CPT, false>(h, rstd, gs, p, row, lane, tpr, c_end, row_ok);
+    quantize_and_store<T, FMT, CPT, WITH_Y>(h, rstd, gs, p, row, lane, tpr, c_end, row_ok);
     if (p.sf_tiled && !row_ok && row < p.rows) zero_tiled_row(p, row, lane, tpr);
   }
 }

@@ -38,7 +38,7 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for want in ("fp4_add_rmsnorm_quant", "fp4_add_rmsnorm_quant_gs", "fp4_quantize",
                  "fp4_dequant", "fp4_sf_size_bytes", "fp4_launch_shape",
-                 "fp4_status_string", "fp4_last_cuda_error"):
+                 "fp4_status_string", "fp4_last_cuda_error", "fp4_gemm_nvfp4_bf16"):
         assert want in names
 
 
@@ -176,4 +176,31 @@ def test_fused_ex_validation(L, kwargs, status):
     st = fq.fp4_add_rmsnorm_quant_ex(a["x"], a["xs"], a["r"], a["rs"], a["w"], a["gs"], a["eps"],
                                      a["M"], a["H"], a["dt"], a["f"], a["lay"], a["p"], a["s"],
                                      a["s2"], a["y"], 0)
+    assert st == status
+
+
+G_OUT = A + (6 << 32)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(M=-1), 1), (dict(N=-1), 1), (dict(K=0), 1),
+    (dict(K=128), 2),                  # K not a multiple of 256
+    (dict(N=20), 2),                   # N not a multiple of 8
+    (dict(K=1 << 31), 2),
+    (dict(a=0), 1), (dict(b=0), 1), (dict(sfa=0), 1), (dict(sfb=0), 1), (dict(out=0), 1),
+    (dict(a=A + 8), 3), (dict(sfb=S + 4), 3), (dict(out=G_OUT + 2), 3), (dict(bias=W + 8), 3),
+    (dict(residual=B + 8), 3),
+    (dict(out=A + 1024), 1),           # output over A
+    (dict(out=S + 512), 1),            # output over the scales of A
+    (dict(bias=G_OUT + 64), 1),        # bias inside the output
+    (dict(residual=G_OUT + 64), 1),    # residual partly over the output
+    (dict(M=0, a=0, b=0, out=0), 0),   # empty: nothing launched
+    (dict(N=0), 0),
+])
+def test_gemm_validation(L, kwargs, status):
+    a = dict(a=A, b=B, sfa=S, sfb=S2, alpha=1.0, bias=0, residual=0, M=256, N=256, K=512,
+             out=G_OUT, pdl=0)
+    a.update(kwargs)
+    st = fq.fp4_gemm_nvfp4_bf16(a["a"], a["b"], a["sfa"], a["sfb"], a["alpha"], a["bias"],
+                                a["residual"], a["M"], a["N"], a["K"], a["out"], a["pdl"], 0)
     assert st == status

@@ -1,0 +1,177 @@
+"""GPU parity of the NVFP4 GEMM (fp4_gemm_nvfp4_bf16, through the C ABI via the
+binding) against the oracle (``oracle.gemm_bf16``).
+
+Two kinds of operands, both drawn as bytes by ``workloads.random_bytes``:
+  * "exact": codes in {0, +-0.5, +-1, +-2} and scales in {0.5, 1, 2}.  Every
+    product is a multiple of 2^-4 of magnitude <= 16 and every partial sum
+    stays below 2^17 for K <= 7168, so any fp32 summation order is exact and
+    the bf16 output must equal the oracle's bit for bit;
+  * "random": every E2M1 code, scales 2^-3 .. 9.  The tensor cores sum in fp32
+    in their own order, so the output must lie within
+        2^-8 |exact| + 2^-22 K sum_k |a b| + 2^-22 (|bias| + |residual|)
+    of the oracle's exact value: one bf16 rounding (2^-9, doubled), K fp32
+    additions each off by at most 2^-23 relative to the running magnitude
+    (doubled), and one rounding per epilogue addition.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rmsnorm_fp4_quant_gb300 as fq
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+E2M1_SMALL = [0x0, 0x1, 0x2, 0x4, 0x9, 0xA, 0xC]      # 0, +-0.5, +-1, +-2
+E4M3_POW2 = [0x30, 0x38, 0x40]                         # 0.5, 1, 2
+EXACT_BYTES = [lo | (hi << 4) for lo in E2M1_SMALL for hi in E2M1_SMALL]
+RANDOM_SCALES = list(range(0x20, 0x51))                # 2^-3 .. 9
+
+
+def operands(M, N, K, seed, kind):
+    code_alpha = EXACT_BYTES if kind == "exact" else None
+    sf_alpha = E4M3_POW2 if kind == "exact" else RANDOM_SCALES
+    a = workloads.random_bytes(M * K // 2, seed, 0, code_alpha).reshape(M, K // 2)
+    b = workloads.random_bytes(N * K // 2, seed, 1, code_alpha).reshape(N, K // 2)
+    sfa = workloads.random_bytes(oracle.sf_size_bytes(M, K, "nvfp4", "swizzled"), seed, 2, sf_alpha)
+    sfb = workloads.random_bytes(oracle.sf_size_bytes(N, K, "nvfp4", "swizzled"), seed, 3, sf_alpha)
+    return a, b, sfa, sfb
+
+
+def bf16_values(n, seed, tensor_id, shape):
+    """bf16 tensors whose values are multiples of 2^-4 below 2^9 in magnitude
+    (exact in every fp32 sum of the exact-kind tests)."""
+    ints = workloads.random_bytes(n, seed, tensor_id).to(torch.int32) - 128
+    return (ints.to(torch.float32) * 0.25).to(torch.bfloat16).reshape(shape)
+
+
+def gpu_gemm(a, b, sfa, sfb, alpha=1.0, bias=None, residual=None, out=None, pdl=False):
+    dev = "cuda"
+    res = fq.gemm_nvfp4_bf16(a.to(dev), b.to(dev), sfa.to(dev), sfb.to(dev), alpha=alpha,
+                             bias=None if bias is None else bias.to(dev),
+                             residual=residual, out=out, pdl=pdl)
+    torch.cuda.synchronize()
+    return res
+
+
+def check(got, g, K, kind, bias=None, residual=None):
+    got64 = got.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(got64).all(), "non-finite output (a bounded wait ran out?)"
+    if kind == "exact":
+        bad = got64.astype(np.float32) != g.out
+        assert not bad.any(), (f"{bad.sum()} outputs differ, first at {np.argwhere(bad)[:4].tolist()}: "
+                               f"gpu {got64[bad][:4]} oracle {g.out[bad][:4]}")
+        return
+    tol = 2.0 ** -8 * np.abs(g.exact) + 2.0 ** -22 * K * g.bound
+    if bias is not None:
+        tol = tol + 2.0 ** -22 * np.abs(bias.float().numpy().astype(np.float64))[None, :]
+    if residual is not None:
+        tol = tol + 2.0 ** -22 * np.abs(residual.float().cpu().numpy().astype(np.float64))
+    err = np.abs(got64 - g.exact)
+    bad = err > tol
+    assert not bad.any(), (f"{bad.sum()} outputs outside the bound, first at "
+                           f"{np.argwhere(bad)[:4].tolist()}: gpu {got64[bad][:4]} "
+                           f"exact {g.exact[bad][:4]} tol {tol[bad][:4]}")
+
+
+def oracle_gemm(a, b, sfa, sfb, M, N, K, **kw):
+    return oracle.gemm_bf16(a.numpy(), b.numpy(), sfa.numpy(), sfb.numpy(), M, N, K, **kw)
+
+
+EXACT_SHAPES = [(128, 128, 256), (1, 8, 256), (41, 4608, 1536), (300, 520, 768),
+                (129, 136, 512), (256, 1024, 4096)]
+
+
+@pytest.mark.parametrize("M,N,K", EXACT_SHAPES)
+@pytest.mark.parametrize("alpha", [1.0, 0.5])
+def test_gemm_exact_operands_bit_exact(M, N, K, alpha):
+    """One tile, the minimal shape, a release-gate shape, ragged M and N tails
+    (a partial last row tile and an 8-column last column tile), many K blocks."""
+    a, b, sfa, sfb = operands(M, N, K, seed=M + N + K, kind="exact")
+    got = gpu_gemm(a, b, sfa, sfb, alpha=alpha)
+    check(got, oracle_gemm(a, b, sfa, sfb, M, N, K, alpha=alpha), K, "exact")
+
+
+@pytest.mark.parametrize("name", ["G1_M41_N4608_K1536", "G2_M41_N6144_K1536",
+                                  "G3_M41_N1536_K6144"])
+def test_gemm_release_gate_shapes_random_operands(name):
+    wl = workloads.GEMM_CONFIGS[name]
+    a, b, sfa, sfb = operands(wl.M, wl.N, wl.K, wl.seed, "random")
+    got = gpu_gemm(a, b, sfa, sfb, alpha=0.75)
+    check(got, oracle_gemm(a, b, sfa, sfb, wl.M, wl.N, wl.K, alpha=0.75), wl.K, "random")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 384, 2048), (77, 264, 512)])
+def test_gemm_random_operands(M, N, K):
+    a, b, sfa, sfb = operands(M, N, K, seed=3 * M + N, kind="random")
+    got = gpu_gemm(a, b, sfa, sfb)
+    check(got, oracle_gemm(a, b, sfa, sfb, M, N, K), K, "random")
+
+
+@pytest.mark.parametrize("with_bias,with_residual", [(True, False), (False, True), (True, True)])
+def test_gemm_bias_residual_epilogues(with_bias, with_residual):
+    M, N, K = 200, 264, 1024
+    a, b, sfa, sfb = operands(M, N, K, seed=21, kind="exact")
+    bias = bf16_values(N, 21, 4, (N,)) if with_bias else None
+    res = bf16_values(M * N, 21, 5, (M, N)) if with_residual else None
+    got = gpu_gemm(a, b, sfa, sfb, alpha=0.5, bias=bias,
+                   residual=None if res is None else res.cuda())
+    g = oracle_gemm(a, b, sfa, sfb, M, N, K, alpha=0.5,
+                    bias=None if bias is None else bias.float().numpy(),
+                    residual=None if res is None else res.float().numpy())
+    check(got, g, K, "exact")
+
+
+def test_gemm_residual_in_place():
+    """residual == out: each element read, then overwritten, by one thread."""
+    M, N, K = 130, 256, 512
+    a, b, sfa, sfb = operands(M, N, K, seed=22, kind="exact")
+    res = bf16_values(M * N, 22, 5, (M, N))
+    buf = res.cuda()
+    got = gpu_gemm(a, b, sfa, sfb, residual=buf, out=buf)
+    assert got.data_ptr() == buf.data_ptr()
+    check(got, oracle_gemm(a, b, sfa, sfb, M, N, K, residual=res.float().numpy()), K, "exact")
+
+
+def test_gemm_full_size_sampled_rows():
+    """The 8192 x 7168 x 7168 product in the launch configuration the
+    benchmark times: exact-kind operands, every column of 96 sampled rows
+    (first and last row tile, ragged spread) bit-exact."""
+    wl = workloads.GEMM_CONFIGS["G4_M8192_N7168_K7168"]
+    a, b, sfa, sfb = operands(wl.M, wl.N, wl.K, wl.seed, "exact")
+    got = gpu_gemm(a, b, sfa, sfb)
+    rows = np.unique(np.concatenate([np.arange(0, 32), np.arange(wl.M - 32, wl.M),
+                                     np.random.default_rng(0).integers(0, wl.M, 32)]))
+    g = oracle_gemm(a, b, sfa, sfb, wl.M, wl.N, wl.K, rows=rows)
+    check(got[torch.as_tensor(rows, device=got.device)], g, wl.K, "exact")
+
+
+def test_gemm_consumes_the_fused_producer_with_pdl():
+    """The fused op writes A and its tiled scales, fp4_quantize writes B, and the
+    GEMM is launched as a programmatic dependent of the quantize kernel.  The
+    oracle runs the same chain on the CPU; the producer's bytes equal the
+    oracle's (up to boundary cases, none expected here), so the product is
+    checked against the oracle's bound."""
+    M, N, K = 300, 512, 2048
+    wl = workloads.Workload("chain", M, K, "bf16", "nvfp4", "swizzled", 1e-6, seed=31)
+    x, r, w = workloads.make_inputs(wl, "cpu")
+    wmat = workloads.make_rows(workloads.Workload("wmat", N, K, "bf16", "nvfp4", "swizzled",
+                                                  1e-6, seed=32), "x", 0, N, "cpu")
+    oa = oracle.add_rmsnorm_fp4_quant(x.float().numpy(), r.float().numpy(), w.float().numpy(),
+                                      wl.eps, "bf16", "nvfp4", "swizzled")
+    ob = oracle.quantize(wmat.float().numpy(), "nvfp4", "swizzled")
+    g = oracle.gemm_bf16(oa.packed, ob.packed, oa.sf_swizzled, ob.sf_swizzled, M, N, K)
+
+    xr, rr = x.cuda(), r.clone().cuda()
+    pa, sa = fq.add_rmsnorm_fp4quant(xr, rr, w.cuda(), eps=wl.eps, fmt="nvfp4",
+                                     sf_layout="swizzled")
+    pb, sb = fq.quantize_fp4(wmat.cuda(), fmt="nvfp4", sf_layout="swizzled")
+    got = fq.gemm_nvfp4_bf16(pa, pb, sa, sb, pdl=True)
+    torch.cuda.synchronize()
+    same_a = np.array_equal(pa.cpu().numpy(), oa.packed) and np.array_equal(
+        sa.cpu().numpy(), oa.sf_swizzled)
+    same_b = np.array_equal(pb.cpu().numpy(), ob.packed) and np.array_equal(
+        sb.cpu().numpy(), ob.sf_swizzled)
+    assert same_a and same_b, "producer bytes differ from the oracle's"
+    check(got, g, K, "random")

@@ -154,3 +154,47 @@ def make_inputs(wl: Workload, device="cpu"):
     r = make_rows(wl, "r", 0, wl.M, device)
     w = make_weight(wl, device)
     return x, r, w
+
+
+# ---------------------------------------------------------------------------
+# Consumer GEMM: operand bytes are drawn directly (packed codes and scale
+# bytes), never computed, so the oracle and the kernel read identical bytes.
+# ---------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class GemmWorkload:
+    name: str
+    M: int
+    N: int
+    K: int
+    seed: int = 0
+
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    def algorithmic_bytes(self) -> int:
+        """Operands (codes + tiled scales, padding excluded) read once, bf16
+        output written once."""
+        return (self.M + self.N) * (self.K // 2 + self.K // 16) + 2 * self.M * self.N
+
+
+# The FlashRT fp4-gemm README's release-gate shapes (M = 41 decode rows against
+# 1536 / 6144 wide weights) and a prefill-sized product: the 8192 x 7168
+# activations of the MXFP4 workload above times a square 7168 weight.
+GEMM_CONFIGS: Dict[str, GemmWorkload] = {w.name: w for w in (
+    GemmWorkload("G1_M41_N4608_K1536", 41, 4608, 1536, seed=11),
+    GemmWorkload("G2_M41_N6144_K1536", 41, 6144, 1536, seed=12),
+    GemmWorkload("G3_M41_N1536_K6144", 41, 1536, 6144, seed=13),
+    GemmWorkload("G4_M8192_N7168_K7168", 8192, 7168, 7168, seed=14),
+)}
+
+
+def random_bytes(n: int, seed: int, tensor_id: int, alphabet=None, device="cpu") -> torch.Tensor:
+    """n seeded bytes (uint8), uniform over 0..255 or over `alphabet` (a list of
+    byte values).  Drawn on the CPU, so the bytes do not depend on the device."""
+    g = _gen(seed, 100 + tensor_id, 0, "cpu")
+    if alphabet is None:
+        out = torch.randint(0, 256, (n,), generator=g, dtype=torch.int32)
+    else:
+        table = torch.tensor(list(alphabet), dtype=torch.int32)
+        out = table[torch.randint(0, len(table), (n,), generator=g)]
+    return out.to(torch.uint8).to(device)

@@ -57,6 +57,9 @@ def parse_args():
                          "the NVFP4 GEMM that consumes them (--gemm picks the shape)")
     ap.add_argument("--gemm", default="G4_M8192_N7168_K7168",
                     help="GEMM workload for --op gemm")
+    ap.add_argument("--gemm-variant", type=int, default=-1,
+                    help="GEMM tile schedule: -1 automatic, 0/1 = one CTA per 128x128/128x256 "
+                         "tile, 2/3 = persistent over 128x128/128x256 tiles")
     ap.add_argument("--global-scale", type=float, default=None,
                     help="pass this global scale as a device scalar (E4M3 formats)")
     ap.add_argument("--format", default=None, help="override the workload's format")
@@ -546,8 +549,8 @@ def run_gemm(args):
         out.data_ptr()
 
     def step(i):
-        st = L.fp4_gemm_nvfp4_bf16(ap_, bp_, sap, sbp, 1.0, None, None, gw.M, gw.N, gw.K, op_, 0,
-                                   sh)
+        st = L.fp4_gemm_nvfp4_bf16(ap_, bp_, sap, sbp, 1.0, None, None, gw.M, gw.N, gw.K, op_,
+                                   args.gemm_variant, 0, sh)
         if st != 0:
             raise fq.Fp4Error(st, "fp4_gemm_nvfp4_bf16")
 
@@ -613,7 +616,7 @@ def run_gemm(args):
                 d.copy_(h, non_blocking=True)
             st = L.fp4_gemm_nvfp4_bf16(ds[0].data_ptr(), ds[1].data_ptr(), ds[2].data_ptr(),
                                        ds[3].data_ptr(), 1.0, None, None, gw.M, gw.N, gw.K,
-                                       op_, 0, sh)
+                                       op_, args.gemm_variant, 0, sh)
             if st != 0:
                 raise fq.Fp4Error(st, "e2e gemm")
             ho.copy_(out, non_blocking=True)
@@ -643,6 +646,7 @@ def run_gemm(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e2m1 x e2m1 -> f32 accumulate, bf16 out", "data": "synthetic",
             "config": {"workload": gw.name, "op": "gemm", "M": gw.M, "N": gw.N, "K": gw.K,
+                       "variant": args.gemm_variant,
                        "operands": "uniform random E2M1 bytes, E4M3 scale bytes 0x20..0x50",
                        "l2": "L2 scrubbed (256 MB write) before every launch, launches "
                              "timed one by one" if flush else

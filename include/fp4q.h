@@ -202,6 +202,10 @@ fp4_status_t fp4_launch_shape(int64_t M, int64_t H, fp4_dtype_t dtype, fp4_forma
  *   bias      [N] bf16 or NULL, added after alpha.
  *   residual  [M, N] bf16 or NULL, added last; may be `out` itself.
  *   out       [M, N] bf16, row-major.
+ *   variant   tile schedule (the README's `variant`): -1 automatic; one CTA per
+ *             output tile with 0 = 128 x 128 tiles (two CTAs per SM) or 1 = 128 x 256
+ *             tiles; persistent, one CTA per SM walking the tiles, with 2 = 128 x 128
+ *             (two accumulators in tensor memory) or 3 = 128 x 256.
  *   pdl       nonzero: launched as a programmatic dependent of the previous
  *             kernel on `stream`, so its prologue overlaps that kernel's tail
  *             (it waits for that kernel's results before reading anything).
@@ -212,7 +216,8 @@ fp4_status_t fp4_launch_shape(int64_t M, int64_t H, fp4_dtype_t dtype, fp4_forma
 fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
                                  const uint8_t* sfa, const uint8_t* sfb, float alpha,
                                  const void* bias, const void* residual, int64_t M, int64_t N,
-                                 int64_t K, void* out, int pdl, fp4q_stream_t stream);
+                                 int64_t K, void* out, int variant, int pdl,
+                                 fp4q_stream_t stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char* fp4_status_string(fp4_status_t status);

@@ -63,7 +63,7 @@ def lib() -> ctypes.CDLL:
     L.fp4_launch_shape.argtypes = [i64, i64, ci, ci, ci, ctypes.POINTER(ctypes.c_int64)]
     L.fp4_launch_shape.restype = ci
     L.fp4_gemm_nvfp4_bf16.argtypes = [vp, vp, vp, vp, ctypes.c_float, vp, vp, i64, i64, i64,
-                                      vp, ci, vp]
+                                      vp, ci, ci, vp]
     L.fp4_gemm_nvfp4_bf16.restype = ci
     _lib = L
     return L
@@ -118,10 +118,10 @@ def fp4_dequant(packed_ptr: int, sf_ptr: int, M: int, H: int, fmt: int, sf_layou
 
 def fp4_gemm_nvfp4_bf16(a_packed_ptr: int, b_packed_ptr: int, sfa_ptr: int, sfb_ptr: int,
                         alpha: float, bias_ptr: int, residual_ptr: int, M: int, N: int, K: int,
-                        out_ptr: int, pdl: int, stream: int) -> int:
+                        out_ptr: int, variant: int, pdl: int, stream: int) -> int:
     return lib().fp4_gemm_nvfp4_bf16(a_packed_ptr, b_packed_ptr, sfa_ptr, sfb_ptr, alpha,
                                      bias_ptr or None, residual_ptr or None, M, N, K, out_ptr,
-                                     pdl, stream or None)
+                                     variant, pdl, stream or None)
 
 
 def fp4_sf_size_bytes(M: int, H: int, fmt: int, layout: int) -> int:
@@ -308,9 +308,11 @@ def dequant(packed, sf, M: int, H: int, fmt: str = "nvfp4", sf_layout: str = "ro
 
 
 def gemm_nvfp4_bf16(a_packed, b_packed, sfa, sfb, alpha: float = 1.0, bias=None, residual=None,
-                    out=None, pdl: bool = False, stream=None):
+                    out=None, variant: int = -1, pdl: bool = False, stream=None):
     """bf16 (M, N) = alpha * deq(A) @ deq(B)^T (+ bias) (+ residual) from packed
-    NVFP4 operands (M, K/2) and (N, K/2) and their tiled scale buffers."""
+    NVFP4 operands (M, K/2) and (N, K/2) and their tiled scale buffers.
+    variant: -1 automatic, 0 / 1 = one CTA per 128x128 / 128x256 output tile,
+    2 / 3 = persistent CTAs over 128x128 / 128x256 tiles."""
     torch = _torch()
     for name, t in (("a_packed", a_packed), ("b_packed", b_packed), ("sfa", sfa), ("sfb", sfb)):
         _check_cuda(t, name)
@@ -332,7 +334,8 @@ def gemm_nvfp4_bf16(a_packed, b_packed, sfa, sfb, alpha: float = 1.0, bias=None,
                              sfb.data_ptr(), float(alpha),
                              bias.data_ptr() if bias is not None else 0,
                              residual.data_ptr() if residual is not None else 0, M, N, K,
-                             out.data_ptr(), 1 if pdl else 0, _stream_handle(stream))
+                             out.data_ptr(), int(variant), 1 if pdl else 0,
+                             _stream_handle(stream))
     if st != 0:
         raise Fp4Error(st, "fp4_gemm_nvfp4_bf16")
     return out

@@ -33,6 +33,15 @@ int tma_ctas_per_sm_fp16(int fmt, int cpt, int threads, size_t smem);
 #ifndef FP4Q_GEMM_STAGES
 #define FP4Q_GEMM_STAGES 3              // GEMM shared-memory ring depth (2 CTAs per SM at 3)
 #endif
+#ifndef FP4Q_GEMM_VARIANT
+#define FP4Q_GEMM_VARIANT 0             // the GEMM schedule of the automatic choice
+#endif
+#ifndef FP4Q_GEMM_PSTAGES_128
+#define FP4Q_GEMM_PSTAGES_128 6         // ring depth of the persistent 128-wide schedule
+#endif
+#ifndef FP4Q_GEMM_PSTAGES_256
+#define FP4Q_GEMM_PSTAGES_256 4         // ring depth of the persistent 256-wide schedule
+#endif
 #ifndef FP4Q_DIRECT_CTA_THREADS
 #define FP4Q_DIRECT_CTA_THREADS 128     // target threads of a direct-kernel CTA
 #endif
@@ -467,8 +476,10 @@ fp4_status_t fp4_dequant(const uint8_t* packed, const uint8_t* sf, int64_t M, in
 fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
                                  const uint8_t* sfa, const uint8_t* sfb, float alpha,
                                  const void* bias, const void* residual, int64_t M, int64_t N,
-                                 int64_t K, void* out, int pdl, fp4q_stream_t stream) {
+                                 int64_t K, void* out, int variant, int pdl,
+                                 fp4q_stream_t stream) {
   if (M < 0 || N < 0 || K <= 0) return FP4_ERR_INVALID_ARG;
+  if (variant < -1 || variant > 3) return FP4_ERR_INVALID_ARG;
   if (K % 256 != 0 || N % 8 != 0) return FP4_ERR_UNSUPPORTED_SHAPE;
   if (M > INT32_MAX - 128 || N > INT32_MAX - 128 || K > INT32_MAX / 2)
     return FP4_ERR_UNSUPPORTED_SHAPE;
@@ -498,11 +509,15 @@ fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packe
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  p.stages = FP4Q_GEMM_STAGES;
+  const int v = variant < 0 ? FP4Q_GEMM_VARIANT : variant;
+  const int bn = (v == 1 || v == 3) ? 256 : 128;
+  const bool persistent = v >= 2;
+  p.stages = !persistent ? FP4Q_GEMM_STAGES : bn == 128 ? FP4Q_GEMM_PSTAGES_128
+                                                        : FP4Q_GEMM_PSTAGES_256;
   p.nkt = 0;        // filled by the launcher
   p.num_kb = 0;
   p.tmem_cols = 0;
-  return record_cuda(launch_gemm_nvfp4(a_packed, b_packed, p, pdl,
+  return record_cuda(launch_gemm_nvfp4(a_packed, b_packed, p, bn, persistent, pdl,
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -115,9 +115,10 @@ struct GemmParams {
   uint32_t tmem_cols;          // tensor-memory columns taken per CTA
 };
 
-// K % 256 == 0, N % 8 == 0, a / b 16-byte aligned (checked by the caller).
-cudaError_t launch_gemm_nvfp4(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
-                              cudaStream_t stream);
-size_t gemm_nvfp4_smem_bytes(int stages);
+// K % 256 == 0, N % 8 == 0, a / b 16-byte aligned (checked by the caller);
+// bn = output tile width, 128 or 256; persistent = one CTA per SM walking the
+// tiles (else one CTA per tile).
+cudaError_t launch_gemm_nvfp4(const uint8_t* a, const uint8_t* b, GemmParams p, int bn,
+                              bool persistent, int pdl, cudaStream_t stream);
 
 }  // namespace fp4q

@@ -69,9 +69,9 @@ __device__ __forceinline__ float row_rstd(float ss, int H, float eps) {
 // scale byte, v = y * inv_s, E2M1 codes of 16 elements in one 64-bit store, and
 // the scale byte in each layout asked for.  Every lane of the warp must call it
 // (the shuffle is unconditional); lanes without a chunk contribute amax 0.
-// WITH_Y adds the y side output; a separate instance keeps the common path
-// free of its (otherwise predicated) conversions.
-template <typename T, int FMT, int CPT, bool WITH_Y>
+// EX is the general form (strided rows, optional y side output); the common
+// dense instance carries none of that code.
+template <typename T, int FMT, int CPT, bool EX>
 __device__ __forceinline__ void quantize_and_store(const Chunk (&h)[CPT], float rstd, float gs,
                                                    const FusedParams& p, int64_t row, int c0,
                                                    int tpr, int c_end, bool row_ok) {
@@ -98,7 +98,7 @@ __device__ __forceinline__ void quantize_and_store(const Chunk (&h)[CPT], float 
       for (int i = 0; i < 16; ++i) y[i] = 0.0f;
     }
     if (Fmt<FMT>::kBlock32) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-    if (WITH_Y && ok) {   // side output: y rounded to the storage type
+    if (EX && ok && p.y) {   // side output: y rounded to the storage type
       Chunk yc;
 #pragma unroll
       for (int j = 0; j < 8; ++j) yc.u[j] = Pair<T>::from_f32(y[2 * j], y[2 * j + 1]);

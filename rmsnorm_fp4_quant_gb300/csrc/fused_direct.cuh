@@ -41,7 +41,7 @@ __device__ __forceinline__ void st_peer_f32(float* local_slot, uint32_t peer, fl
   asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(remote), "f"(v) : "memory");
 }
 
-template <typename T, int FMT, int CPT, bool WITH_Y>
+template <typename T, int FMT, int CPT, bool EX>
 __global__ void __launch_bounds__(max_threads_for_cpt(CPT))
 fused_direct_kernel(const FusedParams p) {
   __shared__ float warp_part[32];
@@ -66,8 +66,9 @@ fused_direct_kernel(const FusedParams p) {
   const int c_end = c_begin + p.chunks_per_cta;
   const int c0 = c_begin + lane;
   const size_t rsafe = static_cast<size_t>(row_ok ? row : 0);
-  const T* xrow = static_cast<const T*>(p.x) + rsafe * static_cast<size_t>(p.x_stride);
-  T* rrow = static_cast<T*>(p.r) + rsafe * static_cast<size_t>(p.r_stride);
+  const size_t xoff = rsafe * static_cast<size_t>(EX ? p.x_stride : p.H);
+  const T* xrow = static_cast<const T*>(p.x) + xoff;
+  T* rrow = static_cast<T*>(p.r) + (EX ? rsafe * static_cast<size_t>(p.r_stride) : xoff);
 
   Chunk h[CPT];
   Chunk rr[CPT];
@@ -102,7 +103,7 @@ fused_direct_kernel(const FusedParams p) {
 
   const float rstd = row_rstd(ss, p.H, p.eps);
   const float gs = load_global_scale(p.gs);
-  quantize_and_store<T, FMT, CPT, WITH_Y>(h, rstd, gs, p, row, c0, tpr, c_end, row_ok);
+  quantize_and_store<T, FMT, CPT, EX>(h, rstd, gs, p, row, c0, tpr, c_end, row_ok);
   if (p.sf_tiled && !row_ok && row < p.rows && rank == 0) zero_tiled_row(p, row, lane, tpr);
 }
 

@@ -6,7 +6,7 @@
 
 namespace fp4q {
 
-template <typename T, int FMT, int CPT, bool WITH_Y>
+template <typename T, int FMT, int CPT, bool EX>
 cudaError_t raise_smem_limit(size_t smem) {
   // the limit is a per-device function attribute: raise it when a launch
   // needs more than any earlier one on this device
@@ -15,7 +15,7 @@ cudaError_t raise_smem_limit(size_t smem) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && done[dev] >= smem) return cudaSuccess;
-  e = cudaFuncSetAttribute(fused_tma_kernel<T, FMT, CPT, WITH_Y>,
+  e = cudaFuncSetAttribute(fused_tma_kernel<T, FMT, CPT, EX>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = smem;
   return e;
@@ -52,9 +52,9 @@ int ctas_per_sm_dtype(int fmt, int cpt, int threads, size_t smem) {
   }
 }
 
-// WITH_Y selects the instance that also stores y; the common instance carries
-// none of that code.
-template <typename T, int FMT, int CPT, bool WITH_Y>
+// EX selects the general instance (strided rows and/or y output); dense calls
+// without y run the common instance, which carries none of that code.
+template <typename T, int FMT, int CPT, bool EX>
 cudaError_t launch_one(const FusedShape& s, const FusedParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(s.grid), 1, 1);
@@ -72,17 +72,17 @@ cudaError_t launch_one(const FusedShape& s, const FusedParams& p, cudaStream_t s
       cfg.numAttrs = 1;
     }
     cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, fused_direct_kernel<T, FMT, CPT, WITH_Y>, p);
+    return cudaLaunchKernelEx(&cfg, fused_direct_kernel<T, FMT, CPT, EX>, p);
   }
-  const cudaError_t e = raise_smem_limit<T, FMT, CPT, WITH_Y>(s.smem);
+  const cudaError_t e = raise_smem_limit<T, FMT, CPT, EX>(s.smem);
   if (e != cudaSuccess) return e;
   cfg.dynamicSmemBytes = s.smem;
-  return cudaLaunchKernelEx(&cfg, fused_tma_kernel<T, FMT, CPT, WITH_Y>, p);
+  return cudaLaunchKernelEx(&cfg, fused_tma_kernel<T, FMT, CPT, EX>, p);
 }
 
 template <typename T, int FMT>
 cudaError_t launch_fmt(const FusedShape& s, const FusedParams& p, cudaStream_t stream) {
-  const bool y = p.y != nullptr;
+  const bool y = p.y != nullptr || p.x_stride != p.H || p.r_stride != p.H;
   switch (s.cpt) {
     case 1: return y ? launch_one<T, FMT, 1, true>(s, p, stream) : launch_one<T, FMT, 1, false>(s, p, stream);
     case 2: return y ? launch_one<T, FMT, 2, true>(s, p, stream) : launch_one<T, FMT, 2, false>(s, p, stream);

@@ -45,7 +45,7 @@ __host__ __device__ constexpr size_t tma_smem_bytes(int stages, int rows_per_cta
   return static_cast<size_t>(stages) * 4u * rows_per_cta * H + 8u * stages + 2u * 32u * 4u;
 }
 
-template <typename T, int FMT, int CPT, bool WITH_Y>
+template <typename T, int FMT, int CPT, bool EX>
 __global__ void __launch_bounds__(max_threads_for_cpt(CPT))
 fused_tma_kernel(const FusedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -77,8 +77,9 @@ fused_tma_kernel(const FusedParams p) {
     if (bytes) {
       uint8_t* st = smem + static_cast<size_t>(s) * 2u * half_stage;
       // rows of a stage are contiguous in memory (strided rows run with R = 1)
-      bulk_g2s(st, static_cast<const T*>(p.x) + row0 * p.x_stride, bytes, &full[s]);
-      bulk_g2s(st + half_stage, static_cast<const T*>(p.r) + row0 * p.r_stride, bytes, &full[s]);
+      bulk_g2s(st, static_cast<const T*>(p.x) + row0 * (EX ? p.x_stride : H), bytes, &full[s]);
+      bulk_g2s(st + half_stage, static_cast<const T*>(p.r) + row0 * (EX ? p.r_stride : H), bytes,
+               &full[s]);
     }
   };
 
@@ -116,7 +117,7 @@ fused_tma_kernel(const FusedParams p) {
       }
     }
     T* rrow = static_cast<T*>(p.r) + static_cast<size_t>(row_ok ? row : 0) *
-                                         static_cast<size_t>(p.r_stride);
+                                         static_cast<size_t>(EX ? p.r_stride : H);
     float ss = add_and_write_back<T, CPT>(h, rr, rrow, lane, tpr, c_end, ok && row_ok);
 
     const int width = tpr < 32 ? tpr : 32;
@@ -141,7 +142,7 @@ fused_tma_kernel(const FusedParams p) {
       for (int i = 0; i < wpr; ++i) ss += pp[grp * wpr + i];
     }
     const float rstd = row_rstd(ss, H, p.eps);
-    quantize_and_store<T, FMT, CPT, WITH_Y>(h, rstd, gs, p, row, lane, tpr, c_end, row_ok);
+    quantize_and_store<T, FMT, CPT, EX>(h, rstd, gs, p, row, lane, tpr, c_end, row_ok);
     if (p.sf_tiled && !row_ok && row < p.rows) zero_tiled_row(p, row, lane, tpr);
   }
 }

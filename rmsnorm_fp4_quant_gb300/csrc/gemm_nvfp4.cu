@@ -48,32 +48,38 @@ namespace fp4q {
 namespace {
 
 constexpr int kBM = 128;                    // output rows per CTA (MMA M)
-constexpr int kBN = 128;                    // output columns per CTA (MMA N)
 constexpr int kBKBytes = 128;               // K block: 256 E2M1 codes = one swizzle row
 constexpr int kMmaKBytes = 32;              // K = 64 codes per MMA
-constexpr uint32_t kTileBytes = kBM * kBKBytes;   // 16 KiB, A and B alike
+constexpr uint32_t kTileBytesA = kBM * kBKBytes;  // 16 KiB
 constexpr uint32_t kSfTileBytes = 512;            // 128 rows x 4 scales
-constexpr uint32_t kSfBytes = 4 * kSfTileBytes;   // scales of one K block
-constexpr uint32_t kStageBytes = 2 * kTileBytes + 2 * kSfBytes;
-constexpr uint32_t kAccCols = kBN;          // fp32 accumulator columns
-constexpr uint32_t kSfColsPerStage = 32;    // 16 for A's four tiles, 16 for B's
+constexpr uint32_t kSfBytesA = 4 * kSfTileBytes;  // A's scales of one K block
 
-// Instruction descriptor of the block-scaled MMA: E2M1 A and B (format 1 at
-// bits 7-9 and 10-12), both K-major, N >> 3 at bits 17-22, E4M3 scales (bit 23
-// clear), M >> 7 at bits 27-28, dense K = 64.
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kBN >> 3) << 17) |
-                            (static_cast<uint32_t>(kBM >> 7) << 27);
-
-__host__ __device__ constexpr uint32_t tmem_cols_for(int stages) {
-  // accumulator + per-stage scale columns, rounded up to a power of two
-  return (kAccCols + kSfColsPerStage * stages) <= 256 ? 256u : 512u;
-}
-
-__host__ __device__ constexpr size_t gemm_smem_bytes(int stages) {
-  // 1 KiB of alignment slack (the 128-byte swizzle wants 1 KiB-aligned tiles),
-  // the ring, 2S + 1 mbarriers, the tensor-memory address and a failure flag
-  return 1024 + static_cast<size_t>(stages) * kStageBytes + (2 * stages + 1) * 8 + 8;
-}
+// Per output-tile width BN (the MMA's N: 128 or 256 columns).
+template <int BN>
+struct Cfg {
+  static constexpr uint32_t kTileBytesB = BN * kBKBytes;
+  static constexpr int kSfTilesB = BN / 128;              // 128-row scale tiles of B
+  static constexpr uint32_t kSfBytesB = kSfTilesB * kSfBytesA;
+  static constexpr uint32_t kStageBytes = kTileBytesA + kTileBytesB + kSfBytesA + kSfBytesB;
+  static constexpr uint32_t kAccCols = BN;                // fp32 accumulator columns
+  static constexpr uint32_t kSfColsB = 4 * 4 * kSfTilesB; // B's scale columns per stage
+  static constexpr uint32_t kSfColsPerStage = 16 + kSfColsB;
+  // Instruction descriptor of the block-scaled MMA: E2M1 A and B (format 1 at
+  // bits 7-9 and 10-12), both K-major, N >> 3 at bits 17-22, E4M3 scales (bit
+  // 23 clear), M >> 7 at bits 27-28, dense K = 64.
+  static constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) |
+                                     (static_cast<uint32_t>(BN >> 3) << 17) |
+                                     (static_cast<uint32_t>(kBM >> 7) << 27);
+  static constexpr uint32_t tmem_cols(int stages) {
+    // accumulator + per-stage scale columns, rounded up to a power of two
+    return (kAccCols + kSfColsPerStage * stages) <= 256 ? 256u : 512u;
+  }
+  static constexpr size_t smem_bytes(int stages) {
+    // 1 KiB of alignment slack (the 128-byte swizzle wants 1 KiB-aligned
+    // tiles), the ring, 2S + 1 mbarriers, the tensor-memory address, a flag
+    return 1024 + static_cast<size_t>(stages) * kStageBytes + (2 * stages + 1) * 8 + 8;
+  }
+};
 
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -83,18 +89,62 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
   return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
+// Epilogue of 32 accumulator columns of one output row: alpha, bias, residual
+// in fp32, one rounding to bf16, 16-byte stores (N % 8 == 0).  `bad` stores NaN.
+__device__ __forceinline__ void store_columns32(const GemmParams& p, const uint32_t (&r)[32],
+                                                int row, int n0, bool bad) {
+  const float nan = __int_as_float(0x7fc00000);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int n = n0 + 8 * q;
+    if (n >= p.N) break;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = bad ? nan : __uint_as_float(r[8 * q + i]) * p.alpha;
+    if (p.bias) {
+      const uint4 b = *reinterpret_cast<const uint4*>(p.bias + n);
+      const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = bf16x2_to_float2(bw[i]);
+        v[2 * i] += f.x;
+        v[2 * i + 1] += f.y;
+      }
+    }
+    const size_t off = static_cast<size_t>(row) * static_cast<size_t>(p.N) + n;
+    if (p.residual) {
+      const uint4 rr = *reinterpret_cast<const uint4*>(p.residual + off);
+      const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = bf16x2_to_float2(rw[i]);
+        v[2 * i] += f.x;
+        v[2 * i + 1] += f.y;
+      }
+    }
+    uint4 o;
+    o.x = bf16x2_bits(v[0], v[1]);
+    o.y = bf16x2_bits(v[2], v[3]);
+    o.z = bf16x2_bits(v[4], v[5]);
+    o.w = bf16x2_bits(v[6], v[7]);
+    *reinterpret_cast<uint4*>(p.out + off) = o;
+  }
+}
+
+template <int BN>
 __global__ void __launch_bounds__(128, 1)
 gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
                   const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+  using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
   uint8_t* sA = smem;
-  uint8_t* sB = sA + static_cast<size_t>(S) * kTileBytes;
-  uint8_t* sSFA = sB + static_cast<size_t>(S) * kTileBytes;
-  uint8_t* sSFB = sSFA + static_cast<size_t>(S) * kSfBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + static_cast<size_t>(S) * kSfBytes);
+  uint8_t* sB = sA + static_cast<size_t>(S) * kTileBytesA;
+  uint8_t* sSFA = sB + static_cast<size_t>(S) * C::kTileBytesB;
+  uint8_t* sSFB = sSFA + static_cast<size_t>(S) * kSfBytesA;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + static_cast<size_t>(S) * C::kSfBytesB);
   uint64_t* empty = full + S;
   uint64_t* accum = empty + S;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
@@ -128,7 +178,14 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
   if (warp == 0 && lane == 0) {
     // ---- producer ----
     const uint8_t* sfa_k = p.sfa + static_cast<size_t>(m_tile) * p.nkt * kSfTileBytes;
-    const uint8_t* sfb_k = p.sfb + static_cast<size_t>(n_tile) * p.nkt * kSfTileBytes;
+    // B's 128-row scale tiles of this column tile that exist (the last column
+    // tile may cover fewer rows than BN)
+    const int b_tile0 = n_tile * C::kSfTilesB;
+    const int b_tiles_total = (p.N + 127) / 128;
+    const int b_tiles = b_tiles_total - b_tile0 < C::kSfTilesB ? b_tiles_total - b_tile0
+                                                                : C::kSfTilesB;
+    const uint32_t stage_bytes = kTileBytesA + C::kTileBytesB + kSfBytesA +
+                                 static_cast<uint32_t>(b_tiles) * kSfBytesA;
     int kb = 0;
     for (; kb < p.num_kb; ++kb) {
       const int s = kb % S;
@@ -136,15 +193,18 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
         *failed = 1;
         break;
       }
-      mbar_arrive_expect_tx(&full[s], kStageBytes);
-      tma_load_2d(sA + static_cast<size_t>(s) * kTileBytes, &tmap_a, kb * kBKBytes, m_tile * kBM,
+      mbar_arrive_expect_tx(&full[s], stage_bytes);
+      tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes, m_tile * kBM,
                   &full[s]);
-      tma_load_2d(sB + static_cast<size_t>(s) * kTileBytes, &tmap_b, kb * kBKBytes, n_tile * kBN,
-                  &full[s]);
-      bulk_g2s(sSFA + static_cast<size_t>(s) * kSfBytes, sfa_k + static_cast<size_t>(kb) * kSfBytes,
-               kSfBytes, &full[s]);
-      bulk_g2s(sSFB + static_cast<size_t>(s) * kSfBytes, sfb_k + static_cast<size_t>(kb) * kSfBytes,
-               kSfBytes, &full[s]);
+      tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
+                  n_tile * BN, &full[s]);
+      bulk_g2s(sSFA + static_cast<size_t>(s) * kSfBytesA,
+               sfa_k + static_cast<size_t>(kb) * kSfBytesA, kSfBytesA, &full[s]);
+      for (int t = 0; t < b_tiles; ++t)
+        bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + t * kSfBytesA,
+                 p.sfb + (static_cast<size_t>(b_tile0 + t) * p.nkt) * kSfTileBytes +
+                     static_cast<size_t>(kb) * kSfBytesA,
+                 kSfBytesA, &full[s]);
     }
     if (kb < p.num_kb) {   // gave up: let the copies already issued land first
       for (int j = kb > S ? kb - S : 0; j < kb; ++j)
@@ -159,17 +219,23 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
         break;
       }
       tc_fence_after_sync();
-      const uint32_t sfa_t = tmem + kAccCols + static_cast<uint32_t>(s) * kSfColsPerStage;
+      const uint32_t sfa_t = tmem + C::kAccCols + static_cast<uint32_t>(s) * C::kSfColsPerStage;
       const uint32_t sfb_t = sfa_t + 16;
-      const uint32_t a_s = smem_addr(sA + static_cast<size_t>(s) * kTileBytes);
-      const uint32_t b_s = smem_addr(sB + static_cast<size_t>(s) * kTileBytes);
-      const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(s) * kSfBytes);
-      const uint32_t sfb_s = smem_addr(sSFB + static_cast<size_t>(s) * kSfBytes);
+      const uint32_t a_s = smem_addr(sA + static_cast<size_t>(s) * kTileBytesA);
+      const uint32_t b_s = smem_addr(sB + static_cast<size_t>(s) * C::kTileBytesB);
+      const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(s) * kSfBytesA);
+      const uint32_t sfb_s = smem_addr(sSFB + static_cast<size_t>(s) * C::kSfBytesB);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        // a scale tile: 32 rows of 16 bytes, 8-row groups 128 bytes apart
+        // a scale tile: 32 rows of 16 bytes, 8-row groups 128 bytes apart.
+        // Step j's scales: A's tile at 4j; B's 128-row tiles side by side
+        // from 4 * kSfTilesB * j
         tmem_copy_32x128b_x4(sfa_t + 4 * j, smem_desc(sfa_s + j * kSfTileBytes, 0, 128, kSwizzleNone));
-        tmem_copy_32x128b_x4(sfb_t + 4 * j, smem_desc(sfb_s + j * kSfTileBytes, 0, 128, kSwizzleNone));
+#pragma unroll
+        for (int t = 0; t < C::kSfTilesB; ++t)
+          tmem_copy_32x128b_x4(sfb_t + 4 * (C::kSfTilesB * j + t),
+                               smem_desc(sfb_s + t * kSfBytesA + j * kSfTileBytes, 0, 128,
+                                         kSwizzleNone));
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -177,8 +243,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
         // advances the start address inside the swizzle row
         const uint64_t adesc = smem_desc(a_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
         const uint64_t bdesc = smem_desc(b_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
-        mma_mxf4nvf4(tmem, adesc, bdesc, kIdesc, sfa_t + 4 * j, sfb_t + 4 * j,
-                     (kb | j) != 0 ? 1u : 0u);
+        mma_mxf4nvf4(tmem, adesc, bdesc, C::kIdesc, sfa_t + 4 * j,
+                     sfb_t + 4 * C::kSfTilesB * j, (kb | j) != 0 ? 1u : 0u);
       }
       tc_commit(&empty[s]);   // the stage is free once these MMAs have read it
     }
@@ -194,53 +260,222 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
   const int row = m_tile * kBM + warp * 32 + lane;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  const float nan = __int_as_float(0x7fc00000);
 #pragma unroll 1
-  for (int c = 0; c < kBN; c += 32) {
+  for (int c = 0; c < BN; c += 32) {
     uint32_t r[32];
     tmem_load_32cols(lane_base + static_cast<uint32_t>(c), r);   // whole warp, unconditionally
     if (row >= p.M) continue;
-    const int n0 = n_tile * kBN + c;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int n = n0 + 8 * q;
-      if (n >= p.N) break;
-      float v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = bad ? nan : __uint_as_float(r[8 * q + i]) * p.alpha;
-      if (p.bias) {
-        const uint4 b = *reinterpret_cast<const uint4*>(p.bias + n);
-        const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = bf16x2_to_float2(bw[i]);
-          v[2 * i] += f.x;
-          v[2 * i + 1] += f.y;
-        }
-      }
-      const size_t off = static_cast<size_t>(row) * static_cast<size_t>(p.N) + n;
-      if (p.residual) {
-        const uint4 rr = *reinterpret_cast<const uint4*>(p.residual + off);
-        const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = bf16x2_to_float2(rw[i]);
-          v[2 * i] += f.x;
-          v[2 * i + 1] += f.y;
-        }
-      }
-      uint4 o;
-      o.x = bf16x2_bits(v[0], v[1]);
-      o.y = bf16x2_bits(v[2], v[3]);
-      o.z = bf16x2_bits(v[4], v[5]);
-      o.w = bf16x2_bits(v[6], v[7]);
-      *reinterpret_cast<uint4*>(p.out + off) = o;
-    }
+    store_columns32(p, r, row, n_tile * BN + c, bad);
   }
 
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, p.tmem_cols);
+}
+
+// Persistent form: one CTA per SM walks the output tiles t = blockIdx.x,
+// blockIdx.x + gridDim.x, ... (row tile t / n_tiles, column tile t % n_tiles,
+// so CTAs running together share A's row panel).  Six warps:
+//   warp 0, one lane  producer: one continuous stream of K blocks over all its
+//                     tiles through the S-stage ring (never drains between tiles);
+//   warp 1            tensor-memory allocation; one lane issues the MMAs;
+//   warps 2..5        epilogue, lane quarter = warp % 4.
+// NACC accumulators in tensor memory (2 for 128-wide tiles, 1 for 256): the
+// MMAs of the next tile start as soon as the epilogue has read the previous
+// tile's accumulator out (acc_empty), so loads, MMAs and stores overlap.  The
+// scale tiles use one tensor-memory slot for every stage: tcgen05.cp and
+// tcgen05.mma issued by one thread execute in order, so a copy never
+// overtakes an MMA still reading the slot.
+template <int BN>
+struct PCfg {
+  static constexpr int kAcc = BN == 128 ? 2 : 1;
+  static constexpr uint32_t kSfCol = kAcc * BN;     // the scale slot after the accumulators
+  static constexpr uint32_t tmem_cols() {
+    return (kSfCol + Cfg<BN>::kSfColsPerStage) <= 256 ? 256u : 512u;
+  }
+  static constexpr size_t smem_bytes(int stages) {
+    return 1024 + static_cast<size_t>(stages) * Cfg<BN>::kStageBytes +
+           (2 * stages + 2 * kAcc + 1) * 8 + 8;
+  }
+};
+
+template <int BN>
+__global__ void __launch_bounds__(192, 1)
+gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                             const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+  using C = Cfg<BN>;
+  using P = PCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int S = p.stages;
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + static_cast<size_t>(S) * kTileBytesA;
+  uint8_t* sSFA = sB + static_cast<size_t>(S) * C::kTileBytesB;
+  uint8_t* sSFB = sSFA + static_cast<size_t>(S) * kSfBytesA;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + static_cast<size_t>(S) * C::kSfBytesB);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;
+  uint64_t* acc_empty = acc_full + P::kAcc;
+  uint64_t* mma_done = acc_empty + P::kAcc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* failed = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_tiles = (p.N + BN - 1) / BN;
+  const int tiles = n_tiles * ((p.M + kBM - 1) / kBM);
+  const int G = gridDim.x;
+  const int my_tiles = blockIdx.x < tiles ? (tiles - 1 - blockIdx.x) / G + 1 : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < P::kAcc; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);   // one arrival per epilogue warp
+    }
+    mbar_init(mma_done, 1);
+    *failed = 0;
+    mbar_init_fence();
+    tma_prefetch_map(&tmap_a);
+    tma_prefetch_map(&tmap_b);
+  }
+  griddep_wait();
+  if (warp == 1) tmem_alloc(tmem_slot, p.tmem_cols);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---- producer ----
+    const int b_tiles_total = (p.N + 127) / 128;
+    int it = 0;   // K blocks issued over all tiles
+    bool ok = true;
+    for (int i = 0; i < my_tiles && ok; ++i) {
+      const int t = blockIdx.x + i * G;
+      const int m_tile = t / n_tiles, n_tile = t - (t / n_tiles) * n_tiles;
+      const uint8_t* sfa_k = p.sfa + static_cast<size_t>(m_tile) * p.nkt * kSfTileBytes;
+      const int b_tile0 = n_tile * C::kSfTilesB;
+      const int b_tiles = b_tiles_total - b_tile0 < C::kSfTilesB ? b_tiles_total - b_tile0
+                                                                  : C::kSfTilesB;
+      const uint32_t stage_bytes = kTileBytesA + C::kTileBytesB + kSfBytesA +
+                                   static_cast<uint32_t>(b_tiles) * kSfBytesA;
+      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        const int s = it % S;
+        if (it >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((it / S - 1) & 1))) {
+          *failed = 1;
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes,
+                    m_tile * kBM, &full[s]);
+        tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
+                    n_tile * BN, &full[s]);
+        bulk_g2s(sSFA + static_cast<size_t>(s) * kSfBytesA,
+                 sfa_k + static_cast<size_t>(kb) * kSfBytesA, kSfBytesA, &full[s]);
+        for (int q = 0; q < b_tiles; ++q)
+          bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + q * kSfBytesA,
+                   p.sfb + static_cast<size_t>(b_tile0 + q) * p.nkt * kSfTileBytes +
+                       static_cast<size_t>(kb) * kSfBytesA,
+                   kSfBytesA, &full[s]);
+      }
+    }
+    if (!ok) {   // gave up: let the copies already issued land first
+      for (int j = it > S ? it - S : 0; j < it; ++j)
+        mbar_wait_bounded(&full[j % S], static_cast<uint32_t>((j / S) & 1));
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer ----
+    const uint32_t sfa_t = tmem + P::kSfCol;
+    const uint32_t sfb_t = sfa_t + 16;
+    int it = 0;
+    bool ok = true;
+    for (int i = 0; i < my_tiles && ok; ++i) {
+      const int a = i % P::kAcc;
+      // the epilogue has read this accumulator out (first use: passes at once)
+      if (!mbar_wait_bounded(&acc_empty[a], static_cast<uint32_t>(((i / P::kAcc) & 1) ^ 1))) {
+        *failed = 1;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t d_t = tmem + static_cast<uint32_t>(a * BN);
+      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        const int s = it % S;
+        if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((it / S) & 1))) {
+          *failed = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t a_s = smem_addr(sA + static_cast<size_t>(s) * kTileBytesA);
+        const uint32_t b_s = smem_addr(sB + static_cast<size_t>(s) * C::kTileBytesB);
+        const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(s) * kSfBytesA);
+        const uint32_t sfb_s = smem_addr(sSFB + static_cast<size_t>(s) * C::kSfBytesB);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          tmem_copy_32x128b_x4(sfa_t + 4 * j,
+                               smem_desc(sfa_s + j * kSfTileBytes, 0, 128, kSwizzleNone));
+#pragma unroll
+          for (int q = 0; q < C::kSfTilesB; ++q)
+            tmem_copy_32x128b_x4(sfb_t + 4 * (C::kSfTilesB * j + q),
+                                 smem_desc(sfb_s + q * kSfBytesA + j * kSfTileBytes, 0, 128,
+                                           kSwizzleNone));
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint64_t adesc = smem_desc(a_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
+          const uint64_t bdesc = smem_desc(b_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
+          mma_mxf4nvf4(d_t, adesc, bdesc, C::kIdesc, sfa_t + 4 * j, sfb_t + 4 * C::kSfTilesB * j,
+                       (kb | j) != 0 ? 1u : 0u);
+        }
+        tc_commit(&empty[s]);
+      }
+      tc_commit(&acc_full[a]);   // this tile's MMAs (or those issued before a failure) are done
+    }
+    // tensor memory is freed below only after every MMA issued here has completed
+    tc_commit(mma_done);
+    mbar_wait_bounded(mma_done, 0);
+  } else if (warp >= 2) {
+    // ---- epilogue ----
+    const int quarter = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    bool ok = true;
+    for (int i = 0; i < my_tiles; ++i) {
+      const int t = blockIdx.x + i * G;
+      const int m_tile = t / n_tiles, n_tile = t - (t / n_tiles) * n_tiles;
+      const int a = i % P::kAcc;
+      const int row = m_tile * kBM + quarter * 32 + lane;
+      if (ok) ok = mbar_wait_bounded(&acc_full[a], static_cast<uint32_t>((i / P::kAcc) & 1));
+      ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-wide
+      tc_fence_after_sync();
+      if (i == my_tiles - 1) griddep_launch_dependents();
+      const bool bad = !ok || *failed != 0;
+      if (ok) {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_load_32cols(tmem + lane_off + static_cast<uint32_t>(a * BN + c), r);
+          if (row < p.M) store_columns32(p, r, row, n_tile * BN + c, bad);
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[a]);
+      } else if (row < p.M) {
+        uint32_t r[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) r[c] = 0;
+        for (int c = 0; c < BN; c += 32) store_columns32(p, r, row, n_tile * BN + c, true);
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, p.tmem_cols);
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once (no link to libcuda).
@@ -263,52 +498,62 @@ EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
-// [rows, K/2] bytes, row-major: boxes of 128 rows x 128 bytes, 128-byte swizzle,
-// rows past the end read as zero.
-bool make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t k_bytes) {
+// [rows, K/2] bytes, row-major: boxes of box_rows rows x 128 bytes, 128-byte
+// swizzle, rows past the end read as zero.
+bool make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t k_bytes,
+                      int box_rows) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k_bytes), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k_bytes)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBKBytes), static_cast<cuuint32_t>(kBM)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBKBytes), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-size_t gemm_nvfp4_smem_bytes(int stages) { return gemm_smem_bytes(stages); }
-
-cudaError_t launch_gemm_nvfp4(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
-                              cudaStream_t stream) {
-  if (p.stages < 2 || p.stages > 6) return cudaErrorInvalidValue;
+template <int BN>
+cudaError_t launch_bn(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
+                      cudaStream_t stream) {
+  using C = Cfg<BN>;
   CUtensorMap ta, tb;
-  if (!make_operand_map(&ta, a, p.M, p.K / 2) || !make_operand_map(&tb, b, p.N, p.K / 2))
+  if (!make_operand_map(&ta, a, p.M, p.K / 2, kBM) || !make_operand_map(&tb, b, p.N, p.K / 2, BN))
     return cudaErrorInvalidValue;
-  p.tmem_cols = tmem_cols_for(p.stages);
+  p.tmem_cols = C::tmem_cols(p.stages);
   p.nkt = p.K / 64;
   p.num_kb = p.K / (2 * kBKBytes);
-  const size_t smem = gemm_smem_bytes(p.stages);
+  size_t smem = C::smem_bytes(p.stages);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
   static size_t raised[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || raised[dev] < smem) {
-    e = cudaFuncSetAttribute(gemm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(gemm_nvfp4_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) raised[dev] = smem;
   }
   // resident CTAs must not ask for more than the SM's 512 tensor-memory columns
+  // (an allocation beyond them would wait for a CTA to exit): when shared
+  // memory alone would let more CTAs in, ask for enough to keep them out
+  const int max_ctas = static_cast<int>(512 / p.tmem_cols);
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_nvfp4_kernel, 128, smem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1 || per_sm * p.tmem_cols > 512) return cudaErrorInvalidConfiguration;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_nvfp4_kernel<BN>, 128, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm <= max_ctas) break;
+    smem = (228 * 1024) / (max_ctas + 1) + 1;
+    e = cudaFuncSetAttribute(gemm_nvfp4_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && raised[dev] < smem) raised[dev] = smem;
+  }
+  if (per_sm < 1 || per_sm > max_ctas) return cudaErrorInvalidConfiguration;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((p.N + kBN - 1) / kBN),
+  cfg.gridDim = dim3(static_cast<unsigned>((p.N + BN - 1) / BN),
                      static_cast<unsigned>((p.M + kBM - 1) / kBM), 1);
   cfg.blockDim = dim3(128, 1, 1);
   cfg.dynamicSmemBytes = smem;
@@ -318,7 +563,67 @@ cudaError_t launch_gemm_nvfp4(const uint8_t* a, const uint8_t* b, GemmParams p, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel, ta, tb, p);
+  return cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel<BN>, ta, tb, p);
+}
+
+template <int BN>
+cudaError_t launch_persistent(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
+                              cudaStream_t stream) {
+  using P = PCfg<BN>;
+  CUtensorMap ta, tb;
+  if (!make_operand_map(&ta, a, p.M, p.K / 2, kBM) || !make_operand_map(&tb, b, p.N, p.K / 2, BN))
+    return cudaErrorInvalidValue;
+  p.tmem_cols = P::tmem_cols();
+  p.nkt = p.K / 64;
+  p.num_kb = p.K / (2 * kBKBytes);
+  const size_t smem = P::smem_bytes(p.stages);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  static size_t raised[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || raised[dev] < smem) {
+    e = cudaFuncSetAttribute(gemm_nvfp4_persistent_kernel<BN>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) raised[dev] = smem;
+  }
+  // one CTA per SM: it takes all 512 tensor-memory columns
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_nvfp4_persistent_kernel<BN>, 192,
+                                                    smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1 || per_sm * p.tmem_cols > 512) return cudaErrorInvalidConfiguration;
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = static_cast<int64_t>((p.N + BN - 1) / BN) * ((p.M + kBM - 1) / kBM);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles < sms ? tiles : sms), 1, 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemm_nvfp4_persistent_kernel<BN>, ta, tb, p);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_nvfp4(const uint8_t* a, const uint8_t* b, GemmParams p, int bn,
+                              bool persistent, int pdl, cudaStream_t stream) {
+  if (p.stages < 2 || p.stages > 8) return cudaErrorInvalidValue;
+  if (!persistent) {
+    if (bn == 128) return launch_bn<128>(a, b, p, pdl, stream);
+    if (bn == 256) return launch_bn<256>(a, b, p, pdl, stream);
+  } else {
+    if (bn == 128) return launch_persistent<128>(a, b, p, pdl, stream);
+    if (bn == 256) return launch_persistent<256>(a, b, p, pdl, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fp4q

@@ -46,11 +46,12 @@ def bf16_values(n, seed, tensor_id, shape):
     return (ints.to(torch.float32) * 0.25).to(torch.bfloat16).reshape(shape)
 
 
-def gpu_gemm(a, b, sfa, sfb, alpha=1.0, bias=None, residual=None, out=None, pdl=False):
+def gpu_gemm(a, b, sfa, sfb, alpha=1.0, bias=None, residual=None, out=None, pdl=False,
+             variant=-1):
     dev = "cuda"
     res = fq.gemm_nvfp4_bf16(a.to(dev), b.to(dev), sfa.to(dev), sfb.to(dev), alpha=alpha,
                              bias=None if bias is None else bias.to(dev),
-                             residual=residual, out=out, pdl=pdl)
+                             residual=residual, out=out, pdl=pdl, variant=variant)
     torch.cuda.synchronize()
     return res
 
@@ -83,13 +84,18 @@ EXACT_SHAPES = [(128, 128, 256), (1, 8, 256), (41, 4608, 1536), (300, 520, 768),
                 (129, 136, 512), (256, 1024, 4096)]
 
 
+VARIANTS = [0, 1, 2, 3]   # 128 x 128 / 128 x 256 tiles, one CTA per tile / persistent
+
+
 @pytest.mark.parametrize("M,N,K", EXACT_SHAPES)
 @pytest.mark.parametrize("alpha", [1.0, 0.5])
-def test_gemm_exact_operands_bit_exact(M, N, K, alpha):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_gemm_exact_operands_bit_exact(M, N, K, alpha, variant):
     """One tile, the minimal shape, a release-gate shape, ragged M and N tails
-    (a partial last row tile and an 8-column last column tile), many K blocks."""
+    (a partial last row tile and an 8-column last column tile; with 256-wide
+    tiles a last tile holding one 128-row scale tile of B), many K blocks."""
     a, b, sfa, sfb = operands(M, N, K, seed=M + N + K, kind="exact")
-    got = gpu_gemm(a, b, sfa, sfb, alpha=alpha)
+    got = gpu_gemm(a, b, sfa, sfb, alpha=alpha, variant=variant)
     check(got, oracle_gemm(a, b, sfa, sfb, M, N, K, alpha=alpha), K, "exact")
 
 
@@ -103,20 +109,22 @@ def test_gemm_release_gate_shapes_random_operands(name):
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 384, 2048), (77, 264, 512)])
-def test_gemm_random_operands(M, N, K):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_gemm_random_operands(M, N, K, variant):
     a, b, sfa, sfb = operands(M, N, K, seed=3 * M + N, kind="random")
-    got = gpu_gemm(a, b, sfa, sfb)
+    got = gpu_gemm(a, b, sfa, sfb, variant=variant)
     check(got, oracle_gemm(a, b, sfa, sfb, M, N, K), K, "random")
 
 
 @pytest.mark.parametrize("with_bias,with_residual", [(True, False), (False, True), (True, True)])
-def test_gemm_bias_residual_epilogues(with_bias, with_residual):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_gemm_bias_residual_epilogues(with_bias, with_residual, variant):
     M, N, K = 200, 264, 1024
     a, b, sfa, sfb = operands(M, N, K, seed=21, kind="exact")
     bias = bf16_values(N, 21, 4, (N,)) if with_bias else None
     res = bf16_values(M * N, 21, 5, (M, N)) if with_residual else None
     got = gpu_gemm(a, b, sfa, sfb, alpha=0.5, bias=bias,
-                   residual=None if res is None else res.cuda())
+                   residual=None if res is None else res.cuda(), variant=variant)
     g = oracle_gemm(a, b, sfa, sfb, M, N, K, alpha=0.5,
                     bias=None if bias is None else bias.float().numpy(),
                     residual=None if res is None else res.float().numpy())
@@ -134,13 +142,15 @@ def test_gemm_residual_in_place():
     check(got, oracle_gemm(a, b, sfa, sfb, M, N, K, residual=res.float().numpy()), K, "exact")
 
 
-def test_gemm_full_size_sampled_rows():
+@pytest.mark.parametrize("variant", [-1] + VARIANTS)
+def test_gemm_full_size_sampled_rows(variant):
     """The 8192 x 7168 x 7168 product in the launch configuration the
-    benchmark times: exact-kind operands, every column of 96 sampled rows
-    (first and last row tile, ragged spread) bit-exact."""
+    benchmark times (automatic variant) and in each tile schedule:
+    exact-kind operands, every column of 96 sampled rows (first and last row
+    tile, ragged spread) bit-exact."""
     wl = workloads.GEMM_CONFIGS["G4_M8192_N7168_K7168"]
     a, b, sfa, sfb = operands(wl.M, wl.N, wl.K, wl.seed, "exact")
-    got = gpu_gemm(a, b, sfa, sfb)
+    got = gpu_gemm(a, b, sfa, sfb, variant=variant)
     rows = np.unique(np.concatenate([np.arange(0, 32), np.arange(wl.M - 32, wl.M),
                                      np.random.default_rng(0).integers(0, wl.M, 32)]))
     g = oracle_gemm(a, b, sfa, sfb, wl.M, wl.N, wl.K, rows=rows)

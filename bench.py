@@ -59,7 +59,7 @@ def parse_args():
                     help="GEMM workload for --op gemm")
     ap.add_argument("--gemm-variant", type=int, default=-1,
                     help="GEMM tile schedule: -1 automatic, 0/1 = one CTA per 128x128/128x256 "
-                         "tile, 2/3 = persistent over 128x128/128x256 tiles")
+                         "tile, 2/3 = persistent over 128x128/128x256 tiles, 4 = split K")
     ap.add_argument("--global-scale", type=float, default=None,
                     help="pass this global scale as a device scalar (E4M3 formats)")
     ap.add_argument("--format", default=None, help="override the workload's format")

@@ -205,7 +205,11 @@ fp4_status_t fp4_launch_shape(int64_t M, int64_t H, fp4_dtype_t dtype, fp4_forma
  *   variant   tile schedule (the README's `variant`): -1 automatic; one CTA per
  *             output tile with 0 = 128 x 128 tiles (two CTAs per SM) or 1 = 128 x 256
  *             tiles; persistent, one CTA per SM walking the tiles, with 2 = 128 x 128
- *             (two accumulators in tensor memory) or 3 = 128 x 256.
+ *             (two accumulators in tensor memory) or 3 = 128 x 256; 4 = 128 x 128
+ *             tiles with the K loop of each tile split over a thread-block cluster
+ *             of up to 16 CTAs (partial tiles summed in rank order through
+ *             distributed shared memory; chosen automatically when the output
+ *             has fewer 128 x 128 tiles than half the SMs, e.g. M = 41 decode).
  *   pdl       nonzero: launched as a programmatic dependent of the previous
  *             kernel on `stream`, so its prologue overlaps that kernel's tail
  *             (it waits for that kernel's results before reading anything).

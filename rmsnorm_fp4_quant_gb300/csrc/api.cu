@@ -479,7 +479,7 @@ fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packe
                                  int64_t K, void* out, int variant, int pdl,
                                  fp4q_stream_t stream) {
   if (M < 0 || N < 0 || K <= 0) return FP4_ERR_INVALID_ARG;
-  if (variant < -1 || variant > 3) return FP4_ERR_INVALID_ARG;
+  if (variant < -1 || variant > 4) return FP4_ERR_INVALID_ARG;
   if (K % 256 != 0 || N % 8 != 0) return FP4_ERR_UNSUPPORTED_SHAPE;
   if (M > INT32_MAX - 128 || N > INT32_MAX - 128 || K > INT32_MAX / 2)
     return FP4_ERR_UNSUPPORTED_SHAPE;
@@ -509,16 +509,37 @@ fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packe
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  const int v = variant < 0 ? FP4Q_GEMM_VARIANT : variant;
+  // few output tiles (short, wide products such as decode steps): split the K
+  // loop of each tile over a cluster of CTAs so that most SMs take part
+  const int sms = num_sms_current_device();
+  const int64_t tiles128 = ((N + 127) / 128) * ((M + 127) / 128);
+  const int num_kb = static_cast<int>(K / 256);
+  int v = variant;
+  if (v < 0) v = (tiles128 * 2 <= sms && num_kb >= 2) ? 4 : FP4Q_GEMM_VARIANT;
   const int bn = (v == 1 || v == 3) ? 256 : 128;
-  const bool persistent = v >= 2;
+  const bool persistent = v == 2 || v == 3;
   p.stages = !persistent ? FP4Q_GEMM_STAGES : bn == 128 ? FP4Q_GEMM_PSTAGES_128
                                                         : FP4Q_GEMM_PSTAGES_256;
+  p.split = 1;
+  if (v == 4) {
+    int64_t sk = tiles128 > 0 ? sms / tiles128 : 1;
+    if (sk > 16) sk = 16;
+    if (sk > num_kb) sk = num_kb;
+    p.split = sk < 2 ? 2 : static_cast<int>(sk);
+    if (p.split > num_kb) p.split = 1;
+  }
   p.nkt = 0;        // filled by the launcher
   p.num_kb = 0;
   p.tmem_cols = 0;
-  return record_cuda(launch_gemm_nvfp4(a_packed, b_packed, p, bn, persistent, pdl,
-                                       reinterpret_cast<cudaStream_t>(stream)));
+  cudaError_t e = launch_gemm_nvfp4(a_packed, b_packed, p, bn, persistent, pdl,
+                                    reinterpret_cast<cudaStream_t>(stream));
+  // a cluster of this many CTAs may not fit: halve it until one does
+  while (e == cudaErrorInvalidConfiguration && p.split > 2) {
+    p.split /= 2;
+    e = launch_gemm_nvfp4(a_packed, b_packed, p, bn, persistent, pdl,
+                          reinterpret_cast<cudaStream_t>(stream));
+  }
+  return record_cuda(e);
 }
 
 }  // extern "C"

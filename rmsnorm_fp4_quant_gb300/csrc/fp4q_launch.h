@@ -112,6 +112,7 @@ struct GemmParams {
   int nkt;                     // K / 64: 128x4 scale tiles per 128 rows
   int num_kb;                  // K / 256: K blocks
   int stages;                  // shared-memory ring depth, 2..6
+  int split;                   // CTAs of a cluster sharing one tile's K loop (1 = none)
   uint32_t tmem_cols;          // tensor-memory columns taken per CTA
 };
 

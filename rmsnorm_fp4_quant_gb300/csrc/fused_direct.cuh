@@ -16,24 +16,11 @@
 // layout) only zero their scale bytes.
 #pragma once
 
+#include "async_copy.cuh"
 #include "fused_common.cuh"
 
 namespace fp4q {
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_arrive_release() {
-  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait_acquire() {
-  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
-}
 __device__ __forceinline__ void st_peer_f32(float* local_slot, uint32_t peer, float v) {
   const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(local_slot));
   uint32_t remote;

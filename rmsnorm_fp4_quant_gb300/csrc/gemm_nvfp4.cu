@@ -89,53 +89,71 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
   return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
-// Epilogue of 32 accumulator columns of one output row: alpha, bias, residual
-// in fp32, one rounding to bf16, 16-byte stores (N % 8 == 0).  `bad` stores NaN.
+// Epilogue of 8 accumulator values of one output row at column n (N % 8 == 0,
+// so a group is all in or all out): alpha, bias, residual in fp32, one
+// rounding to bf16, one 16-byte store.  `bad` stores NaN.
+__device__ __forceinline__ void store8(const GemmParams& p, const float (&acc)[8], int row, int n,
+                                       bool bad) {
+  if (n >= p.N) return;
+  const float nan = __int_as_float(0x7fc00000);
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = bad ? nan : acc[i] * p.alpha;
+  if (p.bias) {
+    const uint4 b = *reinterpret_cast<const uint4*>(p.bias + n);
+    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = bf16x2_to_float2(bw[i]);
+      v[2 * i] += f.x;
+      v[2 * i + 1] += f.y;
+    }
+  }
+  const size_t off = static_cast<size_t>(row) * static_cast<size_t>(p.N) + n;
+  if (p.residual) {
+    const uint4 rr = *reinterpret_cast<const uint4*>(p.residual + off);
+    const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = bf16x2_to_float2(rw[i]);
+      v[2 * i] += f.x;
+      v[2 * i + 1] += f.y;
+    }
+  }
+  uint4 o;
+  o.x = bf16x2_bits(v[0], v[1]);
+  o.y = bf16x2_bits(v[2], v[3]);
+  o.z = bf16x2_bits(v[4], v[5]);
+  o.w = bf16x2_bits(v[6], v[7]);
+  *reinterpret_cast<uint4*>(p.out + off) = o;
+}
+
+// 32 accumulator columns (raw fp32 bits from tensor memory) of one row.
 __device__ __forceinline__ void store_columns32(const GemmParams& p, const uint32_t (&r)[32],
                                                 int row, int n0, bool bad) {
-  const float nan = __int_as_float(0x7fc00000);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const int n = n0 + 8 * q;
-    if (n >= p.N) break;
-    float v[8];
+    float acc[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = bad ? nan : __uint_as_float(r[8 * q + i]) * p.alpha;
-    if (p.bias) {
-      const uint4 b = *reinterpret_cast<const uint4*>(p.bias + n);
-      const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = bf16x2_to_float2(bw[i]);
-        v[2 * i] += f.x;
-        v[2 * i + 1] += f.y;
-      }
-    }
-    const size_t off = static_cast<size_t>(row) * static_cast<size_t>(p.N) + n;
-    if (p.residual) {
-      const uint4 rr = *reinterpret_cast<const uint4*>(p.residual + off);
-      const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = bf16x2_to_float2(rw[i]);
-        v[2 * i] += f.x;
-        v[2 * i + 1] += f.y;
-      }
-    }
-    uint4 o;
-    o.x = bf16x2_bits(v[0], v[1]);
-    o.y = bf16x2_bits(v[2], v[3]);
-    o.z = bf16x2_bits(v[4], v[5]);
-    o.w = bf16x2_bits(v[6], v[7]);
-    *reinterpret_cast<uint4*>(p.out + off) = o;
+    for (int i = 0; i < 8; ++i) acc[i] = __uint_as_float(r[8 * q + i]);
+    store8(p, acc, row, n0 + 8 * q, bad);
   }
 }
 
-template <int BN>
+// SPLIT: split-K over a thread-block cluster of p.split CTAs along x, all on
+// the same output tile; CTA rank q takes K blocks [q * nkb / split, (q + 1) *
+// nkb / split), writes its fp32 partial tile into its own shared memory (the
+// drained ring), and after a cluster barrier every rank sums a share of the
+// tile over the ranks' partials in rank order (distributed shared memory
+// loads), so the result does not depend on timing.  A second cluster barrier
+// keeps each partial alive until every peer has read it.  For short, wide
+// products (few output tiles) this spreads the K loop over many SMs.
+template <int BN, bool SPLIT>
 __global__ void __launch_bounds__(128, 1)
 gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
                   const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
   using C = Cfg<BN>;
+  static_assert(!SPLIT || BN == 128, "the split partial tile must fit the drained ring");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -152,8 +170,12 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_tile = blockIdx.x;
+  const int split = SPLIT ? p.split : 1;
+  const int n_tile = SPLIT ? static_cast<int>(blockIdx.x) / split : static_cast<int>(blockIdx.x);
+  const int rank = SPLIT ? static_cast<int>(cluster_ctarank()) : 0;
   const int m_tile = blockIdx.y;
+  const int kb0 = SPLIT ? rank * p.num_kb / split : 0;
+  const int kb1 = SPLIT ? (rank + 1) * p.num_kb / split : p.num_kb;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -186,10 +208,11 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                                 : C::kSfTilesB;
     const uint32_t stage_bytes = kTileBytesA + C::kTileBytesB + kSfBytesA +
                                  static_cast<uint32_t>(b_tiles) * kSfBytesA;
-    int kb = 0;
-    for (; kb < p.num_kb; ++kb) {
-      const int s = kb % S;
-      if (kb >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((kb / S - 1) & 1))) {
+    int i = 0;    // K blocks issued
+    for (; i < kb1 - kb0; ++i) {
+      const int kb = kb0 + i;
+      const int s = i % S;
+      if (i >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((i / S - 1) & 1))) {
         *failed = 1;
         break;
       }
@@ -206,15 +229,15 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      static_cast<size_t>(kb) * kSfBytesA,
                  kSfBytesA, &full[s]);
     }
-    if (kb < p.num_kb) {   // gave up: let the copies already issued land first
-      for (int j = kb > S ? kb - S : 0; j < kb; ++j)
+    if (i < kb1 - kb0) {   // gave up: let the copies already issued land first
+      for (int j = i > S ? i - S : 0; j < i; ++j)
         mbar_wait_bounded(&full[j % S], static_cast<uint32_t>((j / S) & 1));
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
-    for (int kb = 0; kb < p.num_kb; ++kb) {
-      const int s = kb % S;
-      if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((kb / S) & 1))) {
+    for (int i = 0; i < kb1 - kb0; ++i) {
+      const int s = i % S;
+      if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((i / S) & 1))) {
         *failed = 1;
         break;
       }
@@ -244,7 +267,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const uint64_t adesc = smem_desc(a_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
         const uint64_t bdesc = smem_desc(b_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
         mma_mxf4nvf4(tmem, adesc, bdesc, C::kIdesc, sfa_t + 4 * j,
-                     sfb_t + 4 * C::kSfTilesB * j, (kb | j) != 0 ? 1u : 0u);
+                     sfb_t + 4 * C::kSfTilesB * j, (i | j) != 0 ? 1u : 0u);
       }
       tc_commit(&empty[s]);   // the stage is free once these MMAs have read it
     }
@@ -260,12 +283,55 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
   const int row = m_tile * kBM + warp * 32 + lane;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  if constexpr (!SPLIT) {
 #pragma unroll 1
-  for (int c = 0; c < BN; c += 32) {
-    uint32_t r[32];
-    tmem_load_32cols(lane_base + static_cast<uint32_t>(c), r);   // whole warp, unconditionally
-    if (row >= p.M) continue;
-    store_columns32(p, r, row, n_tile * BN + c, bad);
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      tmem_load_32cols(lane_base + static_cast<uint32_t>(c), r);   // whole warp, unconditionally
+      if (row >= p.M) continue;
+      store_columns32(p, r, row, n_tile * BN + c, bad);
+    }
+  } else {
+    // partial tile -> own shared memory, rows 16 bytes apart beyond BN floats
+    constexpr int kStride = BN + 4;
+    float* part = reinterpret_cast<float*>(smem);
+    const int local_row = warp * 32 + lane;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      tmem_load_32cols(lane_base + static_cast<uint32_t>(c), r);
+      if (row >= p.M) continue;
+      float4* dst = reinterpret_cast<float4*>(part + local_row * kStride + c);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                             __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+    }
+    if (bad && threadIdx.x == 0) *failed = 1;
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    bool any_bad = false;
+    for (int q = 0; q < split; ++q)
+      any_bad |= ld_peer_u32(peer_smem_addr(smem_addr(const_cast<int*>(failed)), q)) != 0;
+    const int rows_valid = p.M - m_tile * kBM < kBM ? p.M - m_tile * kBM : kBM;
+    constexpr int kChunks = BN / 8;
+    const int items = rows_valid * kChunks;
+    for (int it = rank + split * static_cast<int>(threadIdx.x); it < items; it += split * 128) {
+      const int rl = it / kChunks;
+      const int ch = it - rl * kChunks;
+      const uint32_t local = smem_addr(part + rl * kStride + ch * 8);
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int q = 0; q < split; ++q) {   // rank order: the same sum on every run
+        const uint32_t a = peer_smem_addr(local, q);
+        const float4 lo = ld_peer_f32x4(a);
+        const float4 hi = ld_peer_f32x4(a + 16);
+        acc[0] += lo.x; acc[1] += lo.y; acc[2] += lo.z; acc[3] += lo.w;
+        acc[4] += hi.x; acc[5] += hi.y; acc[6] += hi.z; acc[7] += hi.w;
+      }
+      store8(p, acc, m_tile * kBM + rl, n_tile * BN + ch * 8, any_bad);
+    }
+    cluster_arrive_release();   // every peer has read this CTA's partial
+    cluster_wait_acquire();
   }
 
   tc_fence_before_sync();
@@ -513,10 +579,11 @@ bool make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN>
+template <int BN, bool SPLIT>
 cudaError_t launch_bn(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
                       cudaStream_t stream) {
   using C = Cfg<BN>;
+  auto kernel = gemm_nvfp4_kernel<BN, SPLIT>;
   CUtensorMap ta, tb;
   if (!make_operand_map(&ta, a, p.M, p.K / 2, kBM) || !make_operand_map(&tb, b, p.N, p.K / 2, BN))
     return cudaErrorInvalidValue;
@@ -530,7 +597,7 @@ cudaError_t launch_bn(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || raised[dev] < smem) {
-    e = cudaFuncSetAttribute(gemm_nvfp4_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) raised[dev] = smem;
@@ -541,11 +608,11 @@ cudaError_t launch_bn(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
   const int max_ctas = static_cast<int>(512 / p.tmem_cols);
   int per_sm = 0;
   for (int attempt = 0; attempt < 2; ++attempt) {
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_nvfp4_kernel<BN>, 128, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 128, smem);
     if (e != cudaSuccess) return e;
     if (per_sm <= max_ctas) break;
     smem = (228 * 1024) / (max_ctas + 1) + 1;
-    e = cudaFuncSetAttribute(gemm_nvfp4_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64 && raised[dev] < smem) raised[dev] = smem;
@@ -553,17 +620,39 @@ cudaError_t launch_bn(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
   if (per_sm < 1 || per_sm > max_ctas) return cudaErrorInvalidConfiguration;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((p.N + BN - 1) / BN),
+  cfg.gridDim = dim3(static_cast<unsigned>((p.N + BN - 1) / BN) * (SPLIT ? p.split : 1),
                      static_cast<unsigned>((p.M + kBM - 1) / kBM), 1);
   cfg.blockDim = dim3(128, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (SPLIT) {
+    if (p.split > 8) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = static_cast<unsigned>(p.split);
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+    // a cluster of this size must fit the GPU at this occupancy
+    cfg.attrs = attr + (pdl ? 1 : 0);
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel<BN>, ta, tb, p);
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kernel, ta, tb, p);
 }
 
 template <int BN>
@@ -616,9 +705,13 @@ cudaError_t launch_persistent(const uint8_t* a, const uint8_t* b, GemmParams p, 
 cudaError_t launch_gemm_nvfp4(const uint8_t* a, const uint8_t* b, GemmParams p, int bn,
                               bool persistent, int pdl, cudaStream_t stream) {
   if (p.stages < 2 || p.stages > 8) return cudaErrorInvalidValue;
+  if (p.split > 1) {
+    if (bn != 128 || persistent || p.split > 16) return cudaErrorInvalidValue;
+    return launch_bn<128, true>(a, b, p, pdl, stream);
+  }
   if (!persistent) {
-    if (bn == 128) return launch_bn<128>(a, b, p, pdl, stream);
-    if (bn == 256) return launch_bn<256>(a, b, p, pdl, stream);
+    if (bn == 128) return launch_bn<128, false>(a, b, p, pdl, stream);
+    if (bn == 256) return launch_bn<256, false>(a, b, p, pdl, stream);
   } else {
     if (bn == 128) return launch_persistent<128>(a, b, p, pdl, stream);
     if (bn == 256) return launch_persistent<256>(a, b, p, pdl, stream);

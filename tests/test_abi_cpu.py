@@ -196,7 +196,7 @@ G_OUT = A + (6 << 32)
     (dict(residual=G_OUT + 64), 1),    # residual partly over the output
     (dict(M=0, a=0, b=0, out=0), 0),   # empty: nothing launched
     (dict(N=0), 0),
-    (dict(variant=4), 1), (dict(variant=-2), 1),
+    (dict(variant=5), 1), (dict(variant=-2), 1),
 ])
 def test_gemm_validation(L, kwargs, status):
     a = dict(a=A, b=B, sfa=S, sfb=S2, alpha=1.0, bias=0, residual=0, M=256, N=256, K=512,

@@ -84,7 +84,7 @@ EXACT_SHAPES = [(128, 128, 256), (1, 8, 256), (41, 4608, 1536), (300, 520, 768),
                 (129, 136, 512), (256, 1024, 4096)]
 
 
-VARIANTS = [0, 1, 2, 3]   # 128 x 128 / 128 x 256 tiles, one CTA per tile / persistent
+VARIANTS = [0, 1, 2, 3, 4]   # 128x128 / 128x256 tiles; one CTA per tile / persistent; split K
 
 
 @pytest.mark.parametrize("M,N,K", EXACT_SHAPES)

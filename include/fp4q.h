@@ -209,7 +209,8 @@ fp4_status_t fp4_launch_shape(int64_t M, int64_t H, fp4_dtype_t dtype, fp4_forma
  *             tiles with the K loop of each tile split over a thread-block cluster
  *             of up to 16 CTAs (partial tiles summed in rank order through
  *             distributed shared memory; chosen automatically when the output
- *             has fewer 128 x 128 tiles than half the SMs, e.g. M = 41 decode).
+ *             has fewer 128 x 128 tiles than half the SMs and K > 1536, e.g. the
+ *             M = 41 decode product with K = 6144).
  *   pdl       nonzero: launched as a programmatic dependent of the previous
  *             kernel on `stream`, so its prologue overlaps that kernel's tail
  *             (it waits for that kernel's results before reading anything).

@@ -515,7 +515,10 @@ fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packe
   const int64_t tiles128 = ((N + 127) / 128) * ((M + 127) / 128);
   const int num_kb = static_cast<int>(K / 256);
   int v = variant;
-  if (v < 0) v = (tiles128 * 2 <= sms && num_kb >= 2) ? 4 : FP4Q_GEMM_VARIANT;
+  // (measured on the decode shapes: with up to 6 K blocks a single CTA per
+  // tile holding them all in flight is faster than a split; with 24 the split
+  // wins by a third)
+  if (v < 0) v = (tiles128 * 2 <= sms && num_kb > 6) ? 4 : FP4Q_GEMM_VARIANT;
   const int bn = (v == 1 || v == 3) ? 256 : 128;
   const bool persistent = v == 2 || v == 3;
   p.stages = !persistent ? FP4Q_GEMM_STAGES : bn == 128 ? FP4Q_GEMM_PSTAGES_128
@@ -527,6 +530,13 @@ fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packe
     if (sk > num_kb) sk = num_kb;
     p.split = sk < 2 ? 2 : static_cast<int>(sk);
     if (p.split > num_kb) p.split = 1;
+  }
+  // a single wave of one-tile CTAs: let each CTA have all (up to 6) of its K
+  // blocks in flight at once instead of sharing its SM with a second CTA
+  if (!persistent && bn == 128) {
+    const int64_t ctas = tiles128 * p.split;
+    const int kb_per_cta = (num_kb + p.split - 1) / p.split;
+    if (ctas <= sms && kb_per_cta > p.stages) p.stages = kb_per_cta < 6 ? kb_per_cta : 6;
   }
   p.nkt = 0;        // filled by the launcher
   p.num_kb = 0;

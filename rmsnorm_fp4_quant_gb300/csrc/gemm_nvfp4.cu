@@ -566,8 +566,8 @@ EncodeTiledFn encode_tiled_fn() {
 
 // [rows, K/2] bytes, row-major: boxes of box_rows rows x 128 bytes, 128-byte
 // swizzle, rows past the end read as zero.
-bool make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t k_bytes,
-                      int box_rows) {
+bool encode_operand_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t k_bytes,
+                        int box_rows) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k_bytes), static_cast<cuuint64_t>(rows)};
@@ -579,52 +579,135 @@ bool make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Recently encoded operand maps of this host thread: a model calls the GEMM on
+// the same weight and activation buffers again and again, so the descriptor
+// of a (buffer, shape) is encoded once.
+bool operand_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t k_bytes,
+                 int box_rows) {
+  struct Entry {
+    const uint8_t* base;
+    int64_t rows, k_bytes;
+    int box_rows;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 16;
+  thread_local Entry cache[kEntries] = {};
+  thread_local int next = 0;
+  for (int i = 0; i < kEntries; ++i) {
+    const Entry& e = cache[i];
+    if (e.base == base && e.rows == rows && e.k_bytes == k_bytes && e.box_rows == box_rows) {
+      *map = e.map;
+      return true;
+    }
+  }
+  if (!encode_operand_map(map, base, rows, k_bytes, box_rows)) return false;
+  Entry& e = cache[next];
+  next = (next + 1) % kEntries;
+  e.base = base;
+  e.rows = rows;
+  e.k_bytes = k_bytes;
+  e.box_rows = box_rows;
+  e.map = *map;
+  return true;
+}
+
+// Per device and ring depth, what a kernel instance needs before its launch,
+// found once: its dynamic shared memory (raised as far as needed to keep the
+// CTAs an SM can hold within its 512 tensor-memory columns: a third CTA's
+// allocation would wait for one of the others to exit) and whether it fits.
+struct Prep {
+  size_t smem = 0;   // 0: not prepared yet
+  cudaError_t err = cudaSuccess;
+  uint32_t cluster_fits = 0;    // bit c: a cluster of c CTAs fits (tested lazily)
+  uint32_t cluster_tested = 0;
+};
+
+using PrepTable = Prep[64][9];   // per device, per ring depth; one table per kernel instance
+
+std::mutex& prep_mutex() {
+  static std::mutex mu;
+  return mu;
+}
+
+template <typename Kernel>
+cudaError_t prepare(PrepTable& table, Kernel kernel, int threads, size_t smem_need,
+                    uint32_t tmem_cols, int stages, Prep** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || stages < 0 || stages > 8) return cudaErrorInvalidValue;
+  std::lock_guard<std::mutex> lock(prep_mutex());
+  Prep& pr = table[dev][stages];
+  *out = &pr;
+  if (pr.smem != 0 || pr.err != cudaSuccess) return pr.err;
+  size_t smem = smem_need;
+  const int max_ctas = static_cast<int>(512 / tmem_cols);
+  int per_sm = 0;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+    if (e != cudaSuccess) break;
+    if (per_sm <= max_ctas) break;
+    smem = (228 * 1024) / (max_ctas + 1) + 1;
+  }
+  if (e == cudaSuccess && (per_sm < 1 || per_sm > max_ctas)) e = cudaErrorInvalidConfiguration;
+  pr.err = e;
+  if (e == cudaSuccess) pr.smem = smem;
+  return e;
+}
+
+template <typename Kernel>
+bool cluster_fits(Prep* pr, Kernel kernel, cudaLaunchConfig_t cfg, int split) {
+  std::lock_guard<std::mutex> lock(prep_mutex());
+  const uint32_t bit = 1u << split;
+  if (pr->cluster_tested & bit) return (pr->cluster_fits & bit) != 0;
+  bool ok = true;
+  if (split > 8)
+    ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+         cudaSuccess;
+  if (ok) {
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = static_cast<unsigned>(split);
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    ok = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) == cudaSuccess && clusters >= 1;
+  }
+  pr->cluster_tested |= bit;
+  if (ok) pr->cluster_fits |= bit;
+  return ok;
+}
+
 template <int BN, bool SPLIT>
 cudaError_t launch_bn(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
                       cudaStream_t stream) {
   using C = Cfg<BN>;
   auto kernel = gemm_nvfp4_kernel<BN, SPLIT>;
   CUtensorMap ta, tb;
-  if (!make_operand_map(&ta, a, p.M, p.K / 2, kBM) || !make_operand_map(&tb, b, p.N, p.K / 2, BN))
+  if (!operand_map(&ta, a, p.M, p.K / 2, kBM) || !operand_map(&tb, b, p.N, p.K / 2, BN))
     return cudaErrorInvalidValue;
   p.tmem_cols = C::tmem_cols(p.stages);
   p.nkt = p.K / 64;
   p.num_kb = p.K / (2 * kBKBytes);
-  size_t smem = C::smem_bytes(p.stages);
-  if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  static size_t raised[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  const size_t smem_need = C::smem_bytes(p.stages);
+  if (smem_need > 227 * 1024) return cudaErrorInvalidValue;
+  static PrepTable table;
+  Prep* pr = nullptr;
+  cudaError_t e = prepare(table, kernel, 128, smem_need, p.tmem_cols, p.stages, &pr);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || raised[dev] < smem) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) raised[dev] = smem;
-  }
-  // resident CTAs must not ask for more than the SM's 512 tensor-memory columns
-  // (an allocation beyond them would wait for a CTA to exit): when shared
-  // memory alone would let more CTAs in, ask for enough to keep them out
-  const int max_ctas = static_cast<int>(512 / p.tmem_cols);
-  int per_sm = 0;
-  for (int attempt = 0; attempt < 2; ++attempt) {
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 128, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm <= max_ctas) break;
-    smem = (228 * 1024) / (max_ctas + 1) + 1;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && raised[dev] < smem) raised[dev] = smem;
-  }
-  if (per_sm < 1 || per_sm > max_ctas) return cudaErrorInvalidConfiguration;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((p.N + BN - 1) / BN) * (SPLIT ? p.split : 1),
                      static_cast<unsigned>((p.M + kBM - 1) / kBM), 1);
   cfg.blockDim = dim3(128, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = pr->smem;
   cfg.stream = stream;
+  if (SPLIT && !cluster_fits(pr, kernel, cfg, p.split)) return cudaErrorInvalidConfiguration;
   cudaLaunchAttribute attr[2];
   int na = 0;
   if (pdl) {
@@ -633,71 +716,61 @@ cudaError_t launch_bn(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
     ++na;
   }
   if (SPLIT) {
-    if (p.split > 8) {
-      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-    }
     attr[na].id = cudaLaunchAttributeClusterDimension;
     attr[na].val.clusterDim.x = static_cast<unsigned>(p.split);
     attr[na].val.clusterDim.y = 1;
     attr[na].val.clusterDim.z = 1;
     ++na;
-    // a cluster of this size must fit the GPU at this occupancy
-    cfg.attrs = attr + (pdl ? 1 : 0);
-    cfg.numAttrs = 1;
-    int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
-    if (e != cudaSuccess) return e;
-    if (clusters < 1) return cudaErrorInvalidConfiguration;
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kernel, ta, tb, p);
 }
 
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 template <int BN>
 cudaError_t launch_persistent(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
                               cudaStream_t stream) {
   using P = PCfg<BN>;
+  auto kernel = gemm_nvfp4_persistent_kernel<BN>;
   CUtensorMap ta, tb;
-  if (!make_operand_map(&ta, a, p.M, p.K / 2, kBM) || !make_operand_map(&tb, b, p.N, p.K / 2, BN))
+  if (!operand_map(&ta, a, p.M, p.K / 2, kBM) || !operand_map(&tb, b, p.N, p.K / 2, BN))
     return cudaErrorInvalidValue;
   p.tmem_cols = P::tmem_cols();
   p.nkt = p.K / 64;
   p.num_kb = p.K / (2 * kBKBytes);
-  const size_t smem = P::smem_bytes(p.stages);
-  if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  static size_t raised[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || raised[dev] < smem) {
-    e = cudaFuncSetAttribute(gemm_nvfp4_persistent_kernel<BN>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) raised[dev] = smem;
-  }
+  const size_t smem_need = P::smem_bytes(p.stages);
+  if (smem_need > 227 * 1024) return cudaErrorInvalidValue;
+  static PrepTable table;
+  Prep* pr = nullptr;
   // one CTA per SM: it takes all 512 tensor-memory columns
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_nvfp4_persistent_kernel<BN>, 192,
-                                                    smem);
+  cudaError_t e = prepare(table, kernel, 192, smem_need, p.tmem_cols, p.stages, &pr);
   if (e != cudaSuccess) return e;
-  if (per_sm < 1 || per_sm * p.tmem_cols > 512) return cudaErrorInvalidConfiguration;
-  int sms = 0;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
+  const int sms = sm_count();
+  if (sms < 1) return cudaErrorInvalidDevice;
   const int64_t tiles = static_cast<int64_t>((p.N + BN - 1) / BN) * ((p.M + kBM - 1) / kBM);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(tiles < sms ? tiles : sms), 1, 1);
   cfg.blockDim = dim3(192, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = pr->smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemm_nvfp4_persistent_kernel<BN>, ta, tb, p);
+  return cudaLaunchKernelEx(&cfg, kernel, ta, tb, p);
 }
 
 }  // namespace

@@ -92,20 +92,30 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_sha() -> str:
+# Sources each measured kernel is built from (its host launch code included):
+# a committed ncu summary applies only while these files are unchanged.
+KERNEL_SOURCES = {
+    "fused": ("api.cu", "async_copy.cuh", "fp4q_device.cuh", "fp4q_launch.h", "fused_bf16.cu",
+              "fused_common.cuh", "fused_direct.cuh", "fused_fp16.cu", "fused_launch.cuh",
+              "fused_tma.cuh"),
+    "quantize": ("api.cu", "fp4q_device.cuh", "fp4q_launch.h", "quantize.cu"),
+    "gemm": ("async_copy.cuh", "fp4q_launch.h", "gemm_api.cu", "gemm_nvfp4.cu", "tcgen05.cuh"),
+}
+
+
+def kernel_source_sha(op: str = "fused") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "rmsnorm_fp4_quant_gb300", "csrc")
-    for p in sorted(glob.glob(os.path.join(csrc, "*"))):
-        if p.endswith((".cu", ".cuh", ".h")):
-            h.update(os.path.basename(p).encode())
-            h.update(open(p, "rb").read())
+    for name in sorted(KERNEL_SOURCES[op]):
+        h.update(name.encode())
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()
 
 
-def recorded_traffic(workload_name: str):
+def recorded_traffic(workload_name: str, op: str = "fused"):
     """dram bytes per launch from a committed ncu summary whose kernel-source
     hash matches the current sources; None otherwise."""
-    sha = kernel_source_sha()
+    sha = kernel_source_sha(op)
     for p in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
         text = open(p).read()
         m_w = re.search(r"^workload:\s*(\S+)", text, re.M)
@@ -366,7 +376,7 @@ def run_ours(args, wl):
     else:
         shape = fq.fp4_launch_shape(M, H, dt, fmt, lay)
     kernel_name = shape["kernel"]
-    traffic, traffic_src = recorded_traffic(wl.name)
+    traffic, traffic_src = recorded_traffic(wl.name, args.op)
 
     # ---- end-to-end through the C ABI with host buffers --------------------
     e2e = None
@@ -610,7 +620,9 @@ def run_gemm(args):
             if tensor_bound else
             {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
              "frac": round(gbs / hbm_peak, 4), "peak_source": f"{hbm_src} hbm_gbs"})
-    roof.update({"traffic": None, "kernel": "gemm_nvfp4_kernel", "kernel_ms_mean": round(ms, 5),
+    traffic, traffic_src = recorded_traffic(gw.name, "gemm")
+    roof.update({"traffic": traffic, "traffic_source": traffic_src,
+                 "kernel": "gemm_nvfp4_kernel", "kernel_ms_mean": round(ms, 5),
                  "algorithmic_bytes": alg, "flops": gw.flops()})
 
     e2e = None

@@ -30,18 +30,6 @@ int tma_ctas_per_sm_fp16(int fmt, int cpt, int threads, size_t smem);
 #ifndef FP4Q_TMA_MIN_H
 #define FP4Q_TMA_MIN_H 20480            // rows at least this wide use the TMA kernel
 #endif
-#ifndef FP4Q_GEMM_STAGES
-#define FP4Q_GEMM_STAGES 3              // GEMM shared-memory ring depth (2 CTAs per SM at 3)
-#endif
-#ifndef FP4Q_GEMM_VARIANT
-#define FP4Q_GEMM_VARIANT 0             // the GEMM schedule of the automatic choice
-#endif
-#ifndef FP4Q_GEMM_PSTAGES_128
-#define FP4Q_GEMM_PSTAGES_128 6         // ring depth of the persistent 128-wide schedule
-#endif
-#ifndef FP4Q_GEMM_PSTAGES_256
-#define FP4Q_GEMM_PSTAGES_256 4         // ring depth of the persistent 256-wide schedule
-#endif
 #ifndef FP4Q_DIRECT_CTA_THREADS
 #define FP4Q_DIRECT_CTA_THREADS 128     // target threads of a direct-kernel CTA
 #endif
@@ -219,6 +207,16 @@ cudaError_t launch_fused(int dtype, int fmt, const FusedShape& s, const FusedPar
   return dtype == 0 ? launch_fused_bf16(fmt, s, p, stream) : launch_fused_fp16(fmt, s, p, stream);
 }
 
+int record_cuda_error(cudaError_t err) {
+  if (err != cudaSuccess) {
+    g_last_cuda_error = static_cast<int>(err);
+    return FP4_ERR_CUDA;
+  }
+  return FP4_OK;
+}
+
+int sm_count_current_device() { return num_sms_current_device(); }
+
 }  // namespace fp4q
 
 using namespace fp4q;
@@ -279,12 +277,8 @@ fp4_status_t fp4_launch_shape(int64_t M, int64_t H, fp4_dtype_t dtype, fp4_forma
   return FP4_OK;
 }
 
-static fp4_status_t record_cuda(cudaError_t err) {
-  if (err != cudaSuccess) {
-    g_last_cuda_error = static_cast<int>(err);
-    return FP4_ERR_CUDA;
-  }
-  return FP4_OK;
+static fp4_status_t record_cuda_status(cudaError_t err) {
+  return static_cast<fp4_status_t>(record_cuda_error(err));
 }
 
 // Output-side checks shared by the fused op and the standalone quantize.
@@ -379,7 +373,7 @@ static fp4_status_t fused_call(const void* input, int64_t x_stride, void* residu
   cudaError_t err = launch_fused(dtype == FP4_DT_BF16 ? 0 : 1, static_cast<int>(format), shape,
                                  p, reinterpret_cast<cudaStream_t>(stream));
   if (err == cudaSuccess) err = cudaGetLastError();
-  return record_cuda(err);
+  return record_cuda_status(err);
 }
 
 fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void* weight,
@@ -443,7 +437,7 @@ fp4_status_t fp4_quantize(const void* input, const float* global_scale, int64_t 
   p.nchunk = static_cast<int>(H / 16);
   p.nb = static_cast<int>(H / b);
   p.nkt = (p.nb + 3) / 4;
-  return record_cuda(launch_quantize(dtype == FP4_DT_BF16 ? 0 : 1, static_cast<int>(format), p,
+  return record_cuda_status(launch_quantize(dtype == FP4_DT_BF16 ? 0 : 1, static_cast<int>(format), p,
                                      num_sms_current_device(),
                                      reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -469,87 +463,8 @@ fp4_status_t fp4_dequant(const uint8_t* packed, const uint8_t* sf, int64_t M, in
   p.nb = static_cast<int>(H / b);
   p.nkt = (p.nb + 3) / 4;
   p.tiled = sf_layout == FP4_SF_SWIZZLED ? 1 : 0;
-  return record_cuda(
+  return record_cuda_status(
       launch_dequant(static_cast<int>(format), p, reinterpret_cast<cudaStream_t>(stream)));
-}
-
-fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
-                                 const uint8_t* sfa, const uint8_t* sfb, float alpha,
-                                 const void* bias, const void* residual, int64_t M, int64_t N,
-                                 int64_t K, void* out, int variant, int pdl,
-                                 fp4q_stream_t stream) {
-  if (M < 0 || N < 0 || K <= 0) return FP4_ERR_INVALID_ARG;
-  if (variant < -1 || variant > 4) return FP4_ERR_INVALID_ARG;
-  if (K % 256 != 0 || N % 8 != 0) return FP4_ERR_UNSUPPORTED_SHAPE;
-  if (M > INT32_MAX - 128 || N > INT32_MAX - 128 || K > INT32_MAX / 2)
-    return FP4_ERR_UNSUPPORTED_SHAPE;
-  if (M == 0 || N == 0) return FP4_OK;
-  if (!a_packed || !b_packed || !sfa || !sfb || !out) return FP4_ERR_INVALID_ARG;
-  if (!aligned(a_packed, 16) || !aligned(b_packed, 16) || !aligned(sfa, 16) ||
-      !aligned(sfb, 16) || !aligned(out, 16) || !aligned(bias, 16) || !aligned(residual, 16))
-    return FP4_ERR_MISALIGNED;
-  const int64_t out_bytes = M * N * 2;
-  const int64_t sfa_bytes = fp4_sf_size_bytes(M, K, FP4_NVFP4, FP4_SF_SWIZZLED);
-  const int64_t sfb_bytes = fp4_sf_size_bytes(N, K, FP4_NVFP4, FP4_SF_SWIZZLED);
-  if (overlap(out, out_bytes, a_packed, M * K / 2) || overlap(out, out_bytes, b_packed, N * K / 2) ||
-      overlap(out, out_bytes, sfa, sfa_bytes) || overlap(out, out_bytes, sfb, sfb_bytes) ||
-      (bias && overlap(out, out_bytes, bias, N * 2)))
-    return FP4_ERR_INVALID_ARG;
-  // the residual may be the output itself (each element is read, then written,
-  // by the same thread), but not partly overlap it
-  if (residual && residual != out && overlap(out, out_bytes, residual, out_bytes))
-    return FP4_ERR_INVALID_ARG;
-  GemmParams p;
-  p.sfa = sfa;
-  p.sfb = sfb;
-  p.bias = static_cast<const uint16_t*>(bias);
-  p.residual = static_cast<const uint16_t*>(residual);
-  p.out = static_cast<uint16_t*>(out);
-  p.alpha = alpha;
-  p.M = static_cast<int>(M);
-  p.N = static_cast<int>(N);
-  p.K = static_cast<int>(K);
-  // few output tiles (short, wide products such as decode steps): split the K
-  // loop of each tile over a cluster of CTAs so that most SMs take part
-  const int sms = num_sms_current_device();
-  const int64_t tiles128 = ((N + 127) / 128) * ((M + 127) / 128);
-  const int num_kb = static_cast<int>(K / 256);
-  int v = variant;
-  // (measured on the decode shapes: with up to 6 K blocks a single CTA per
-  // tile holding them all in flight is faster than a split; with 24 the split
-  // wins by a third)
-  if (v < 0) v = (tiles128 * 2 <= sms && num_kb > 6) ? 4 : FP4Q_GEMM_VARIANT;
-  const int bn = (v == 1 || v == 3) ? 256 : 128;
-  const bool persistent = v == 2 || v == 3;
-  p.stages = !persistent ? FP4Q_GEMM_STAGES : bn == 128 ? FP4Q_GEMM_PSTAGES_128
-                                                        : FP4Q_GEMM_PSTAGES_256;
-  p.split = 1;
-  if (v == 4) {
-    int64_t sk = tiles128 > 0 ? sms / tiles128 : 1;
-    if (sk > 16) sk = 16;
-    if (sk > num_kb) sk = num_kb;
-    p.split = sk < 2 ? 2 : static_cast<int>(sk);
-    if (p.split > num_kb) p.split = 1;
-  }
-  // a single wave of one-tile CTAs: let each CTA have all (up to 6) of its K
-  // blocks in flight at once instead of sharing its SM with a second CTA
-  if (!persistent && bn == 128) {
-    const int64_t ctas = tiles128 * p.split;
-    const int kb_per_cta = (num_kb + p.split - 1) / p.split;
-    if (ctas <= sms && kb_per_cta > p.stages) p.stages = kb_per_cta < 6 ? kb_per_cta : 6;
-  }
-  p.nkt = 0;        // filled by the launcher
-  p.num_kb = 0;
-  p.tmem_cols = 0;
-  cudaError_t e = launch_gemm_nvfp4(a_packed, b_packed, p, bn, persistent, pdl,
-                                    reinterpret_cast<cudaStream_t>(stream));
-  // a cluster of this many CTAs may not fit: halve it until one does
-  while (e == cudaErrorInvalidConfiguration && p.split > 2) {
-    p.split /= 2;
-    e = launch_gemm_nvfp4(a_packed, b_packed, p, bn, persistent, pdl,
-                          reinterpret_cast<cudaStream_t>(stream));
-  }
-  return record_cuda(e);
 }
 
 }  // extern "C"

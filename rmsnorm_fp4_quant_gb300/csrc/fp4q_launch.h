@@ -7,6 +7,17 @@
 
 namespace fp4q {
 
+// Shared by the C entry points (api.cu, gemm_api.cu).
+int record_cuda_error(cudaError_t err);   // 0, or the CUDA-error status after noting err
+int sm_count_current_device();            // SMs of the current device (cached)
+inline bool abi_aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+inline bool abi_overlap(const void* a, int64_t na, const void* b, int64_t nb) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + static_cast<uintptr_t>(nb) && b0 < a0 + static_cast<uintptr_t>(na);
+}
+
 // Threads per CTA allowed for a kernel instance holding `cpt` chunks per
 // thread: one chunk fits 64 registers (1024 threads), more chunks need up to 128.
 __host__ __device__ constexpr int max_threads_for_cpt(int cpt) { return cpt <= 1 ? 1024 : 512; }

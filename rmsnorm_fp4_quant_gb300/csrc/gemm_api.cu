@@ -1,0 +1,111 @@
+// gemm_api.cu - the C entry point of the NVFP4 GEMM (declared in
+// include/fp4q.h): argument checks and the choice of tile schedule; the
+// kernels are in gemm_nvfp4.cu.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <initializer_list>
+
+#include "../../include/fp4q.h"
+#include "fp4q_launch.h"
+
+// Tuning constants of the schedule choice (compile-time, overridable with -D).
+#ifndef FP4Q_GEMM_STAGES
+#define FP4Q_GEMM_STAGES 3              // GEMM shared-memory ring depth (2 CTAs per SM at 3)
+#endif
+#ifndef FP4Q_GEMM_VARIANT
+#define FP4Q_GEMM_VARIANT 0             // the GEMM schedule of the automatic choice
+#endif
+#ifndef FP4Q_GEMM_PSTAGES_128
+#define FP4Q_GEMM_PSTAGES_128 6         // ring depth of the persistent 128-wide schedule
+#endif
+#ifndef FP4Q_GEMM_PSTAGES_256
+#define FP4Q_GEMM_PSTAGES_256 4         // ring depth of the persistent 256-wide schedule
+#endif
+
+using namespace fp4q;
+
+extern "C" {
+
+fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
+                                 const uint8_t* sfa, const uint8_t* sfb, float alpha,
+                                 const void* bias, const void* residual, int64_t M, int64_t N,
+                                 int64_t K, void* out, int variant, int pdl,
+                                 fp4q_stream_t stream) {
+  if (M < 0 || N < 0 || K <= 0) return FP4_ERR_INVALID_ARG;
+  if (variant < -1 || variant > 4) return FP4_ERR_INVALID_ARG;
+  if (K % 256 != 0 || N % 8 != 0) return FP4_ERR_UNSUPPORTED_SHAPE;
+  if (M > INT32_MAX - 128 || N > INT32_MAX - 128 || K > INT32_MAX / 2)
+    return FP4_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0 || N == 0) return FP4_OK;
+  if (!a_packed || !b_packed || !sfa || !sfb || !out) return FP4_ERR_INVALID_ARG;
+  for (const void* ptr : {static_cast<const void*>(a_packed), static_cast<const void*>(b_packed),
+                          static_cast<const void*>(sfa), static_cast<const void*>(sfb),
+                          static_cast<const void*>(out), bias, residual})
+    if (!abi_aligned(ptr, 16)) return FP4_ERR_MISALIGNED;
+  const int64_t out_bytes = M * N * 2;
+  const int64_t sfa_bytes = fp4_sf_size_bytes(M, K, FP4_NVFP4, FP4_SF_SWIZZLED);
+  const int64_t sfb_bytes = fp4_sf_size_bytes(N, K, FP4_NVFP4, FP4_SF_SWIZZLED);
+  if (abi_overlap(out, out_bytes, a_packed, M * K / 2) ||
+      abi_overlap(out, out_bytes, b_packed, N * K / 2) ||
+      abi_overlap(out, out_bytes, sfa, sfa_bytes) || abi_overlap(out, out_bytes, sfb, sfb_bytes) ||
+      (bias && abi_overlap(out, out_bytes, bias, N * 2)))
+    return FP4_ERR_INVALID_ARG;
+  // the residual may be the output itself (each element is read, then written,
+  // by the same thread), but not partly overlap it
+  if (residual && residual != out && abi_overlap(out, out_bytes, residual, out_bytes))
+    return FP4_ERR_INVALID_ARG;
+  GemmParams p;
+  p.sfa = sfa;
+  p.sfb = sfb;
+  p.bias = static_cast<const uint16_t*>(bias);
+  p.residual = static_cast<const uint16_t*>(residual);
+  p.out = static_cast<uint16_t*>(out);
+  p.alpha = alpha;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  // few output tiles (short, wide products such as decode steps): split the K
+  // loop of each tile over a cluster of CTAs so that most SMs take part
+  const int sms = sm_count_current_device();
+  const int64_t tiles128 = ((N + 127) / 128) * ((M + 127) / 128);
+  const int num_kb = static_cast<int>(K / 256);
+  int v = variant;
+  // (measured on the decode shapes: with up to 6 K blocks a single CTA per
+  // tile holding them all in flight is faster than a split; with 24 the split
+  // wins by a third)
+  if (v < 0) v = (tiles128 * 2 <= sms && num_kb > 6) ? 4 : FP4Q_GEMM_VARIANT;
+  const int bn = (v == 1 || v == 3) ? 256 : 128;
+  const bool persistent = v == 2 || v == 3;
+  p.stages = !persistent ? FP4Q_GEMM_STAGES : bn == 128 ? FP4Q_GEMM_PSTAGES_128
+                                                        : FP4Q_GEMM_PSTAGES_256;
+  p.split = 1;
+  if (v == 4) {
+    int64_t sk = tiles128 > 0 ? sms / tiles128 : 1;
+    if (sk > 16) sk = 16;
+    if (sk > num_kb) sk = num_kb;
+    p.split = sk < 2 ? 2 : static_cast<int>(sk);
+    if (p.split > num_kb) p.split = 1;
+  }
+  // a single wave of one-tile CTAs: let each CTA have all (up to 6) of its K
+  // blocks in flight at once instead of sharing its SM with a second CTA
+  if (!persistent && bn == 128) {
+    const int64_t ctas = tiles128 * p.split;
+    const int kb_per_cta = (num_kb + p.split - 1) / p.split;
+    if (ctas <= sms && kb_per_cta > p.stages) p.stages = kb_per_cta < 6 ? kb_per_cta : 6;
+  }
+  p.nkt = 0;        // filled by the launcher
+  p.num_kb = 0;
+  p.tmem_cols = 0;
+  cudaError_t e = launch_gemm_nvfp4(a_packed, b_packed, p, bn, persistent, pdl,
+                                    reinterpret_cast<cudaStream_t>(stream));
+  // a cluster of this many CTAs may not fit: halve it until one does
+  while (e == cudaErrorInvalidConfiguration && p.split > 2) {
+    p.split /= 2;
+    e = launch_gemm_nvfp4(a_packed, b_packed, p, bn, persistent, pdl,
+                          reinterpret_cast<cudaStream_t>(stream));
+  }
+  return static_cast<fp4_status_t>(record_cuda_error(e));
+}
+
+}  // extern "C"

@@ -38,6 +38,14 @@
 
 #include <stdint.h>
 
+/* Only the entry points below are exported from libfp4q.so (built with hidden
+ * visibility). */
+#if defined(__GNUC__)
+#define FP4Q_API __attribute__((visibility("default")))
+#else
+#define FP4Q_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -90,11 +98,11 @@ typedef enum {
  * input must not overlap residual; outputs must not overlap inputs or each
  * other.  Global scale is 1 (the page's default when none is given).
  */
-fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void* weight,
-                                   float eps, int64_t M, int64_t H, fp4_dtype_t dtype,
-                                   fp4_format_t format, fp4_sf_layout_t sf_layout,
-                                   uint8_t* out_packed, uint8_t* out_sf,
-                                   uint8_t* out_sf_rowmajor, fp4q_stream_t stream);
+FP4Q_API fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void* weight,
+                                            float eps, int64_t M, int64_t H, fp4_dtype_t dtype,
+                                            fp4_format_t format, fp4_sf_layout_t sf_layout,
+                                            uint8_t* out_packed, uint8_t* out_sf,
+                                            uint8_t* out_sf_rowmajor, fp4q_stream_t stream);
 
 /*
  * fp4_add_rmsnorm_quant_gs - fp4_add_rmsnorm_quant with a device-resident
@@ -106,12 +114,12 @@ fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void
  * e.g. gs = 448 * 6 / max|y| fills the E4M3 range); UE8M0 scales ignore it.
  * All other arguments as fp4_add_rmsnorm_quant.
  */
-fp4_status_t fp4_add_rmsnorm_quant_gs(const void* input, void* residual, const void* weight,
-                                      const float* global_scale, float eps, int64_t M,
-                                      int64_t H, fp4_dtype_t dtype, fp4_format_t format,
-                                      fp4_sf_layout_t sf_layout, uint8_t* out_packed,
-                                      uint8_t* out_sf, uint8_t* out_sf_rowmajor,
-                                      fp4q_stream_t stream);
+FP4Q_API fp4_status_t fp4_add_rmsnorm_quant_gs(const void* input, void* residual, const void* weight,
+                                               const float* global_scale, float eps, int64_t M,
+                                               int64_t H, fp4_dtype_t dtype, fp4_format_t format,
+                                               fp4_sf_layout_t sf_layout, uint8_t* out_packed,
+                                               uint8_t* out_sf, uint8_t* out_sf_rowmajor,
+                                               fp4q_stream_t stream);
 
 /*
  * fp4_add_rmsnorm_quant_ex - the general form of the fused op: strided rows
@@ -128,14 +136,14 @@ fp4_status_t fp4_add_rmsnorm_quant_gs(const void* input, void* residual, const v
  * Everything else as fp4_add_rmsnorm_quant; the outputs and y must not
  * overlap the inputs or each other.
  */
-fp4_status_t fp4_add_rmsnorm_quant_ex(const void* input, int64_t input_row_stride,
-                                      void* residual, int64_t residual_row_stride,
-                                      const void* weight, const float* global_scale, float eps,
-                                      int64_t M, int64_t H, fp4_dtype_t dtype,
-                                      fp4_format_t format, fp4_sf_layout_t sf_layout,
-                                      uint8_t* out_packed, uint8_t* out_sf,
-                                      uint8_t* out_sf_rowmajor, void* out_y,
-                                      fp4q_stream_t stream);
+FP4Q_API fp4_status_t fp4_add_rmsnorm_quant_ex(const void* input, int64_t input_row_stride,
+                                               void* residual, int64_t residual_row_stride,
+                                               const void* weight, const float* global_scale, float eps,
+                                               int64_t M, int64_t H, fp4_dtype_t dtype,
+                                               fp4_format_t format, fp4_sf_layout_t sf_layout,
+                                               uint8_t* out_packed, uint8_t* out_sf,
+                                               uint8_t* out_sf_rowmajor, void* out_y,
+                                               fp4q_stream_t stream);
 
 /*
  * fp4_quantize - block quantization of `input` [M, H] itself, without the
@@ -146,10 +154,10 @@ fp4_status_t fp4_add_rmsnorm_quant_ex(const void* input, int64_t input_row_strid
  * H a multiple of the block size (>= 16); global_scale as in
  * fp4_add_rmsnorm_quant_gs; outputs as fp4_add_rmsnorm_quant.
  */
-fp4_status_t fp4_quantize(const void* input, const float* global_scale, int64_t M, int64_t H,
-                          fp4_dtype_t dtype, fp4_format_t format, fp4_sf_layout_t sf_layout,
-                          uint8_t* out_packed, uint8_t* out_sf, uint8_t* out_sf_rowmajor,
-                          fp4q_stream_t stream);
+FP4Q_API fp4_status_t fp4_quantize(const void* input, const float* global_scale, int64_t M, int64_t H,
+                                   fp4_dtype_t dtype, fp4_format_t format, fp4_sf_layout_t sf_layout,
+                                   uint8_t* out_packed, uint8_t* out_sf, uint8_t* out_sf_rowmajor,
+                                   fp4q_stream_t stream);
 
 /*
  * fp4_dequant - validation helper: out[m, i] = E2M1 value of code (m, i) times
@@ -161,9 +169,9 @@ fp4_status_t fp4_quantize(const void* input, const float* global_scale, int64_t 
  *   out       [M, H] fp32.                         16-byte aligned.
  * H must be a multiple of the block size (>= 16); M >= 0.
  */
-fp4_status_t fp4_dequant(const uint8_t* packed, const uint8_t* sf, int64_t M, int64_t H,
-                         fp4_format_t format, fp4_sf_layout_t sf_layout, float* out,
-                         fp4q_stream_t stream);
+FP4Q_API fp4_status_t fp4_dequant(const uint8_t* packed, const uint8_t* sf, int64_t M, int64_t H,
+                                  fp4_format_t format, fp4_sf_layout_t sf_layout, float* out,
+                                  fp4q_stream_t stream);
 
 /*
  * fp4_sf_size_bytes - bytes of ONE scale buffer in `layout` (FlashInfer page,
@@ -171,7 +179,7 @@ fp4_status_t fp4_dequant(const uint8_t* packed, const uint8_t* sf, int64_t M, in
  * tiled ceil(M/128) * ceil((H/b)/4) * 512.  FP4_SF_BOTH returns the tiled size
  * (the size of out_sf).  Returns -1 on bad arguments.  Host only; no GPU needed.
  */
-int64_t fp4_sf_size_bytes(int64_t M, int64_t H, fp4_format_t format, fp4_sf_layout_t layout);
+FP4Q_API int64_t fp4_sf_size_bytes(int64_t M, int64_t H, fp4_format_t format, fp4_sf_layout_t layout);
 
 /*
  * fp4_launch_shape - the launch the library would make for fp4_add_rmsnorm_quant
@@ -181,8 +189,8 @@ int64_t fp4_sf_size_bytes(int64_t M, int64_t H, fp4_format_t format, fp4_sf_layo
  * CTAs per cluster, shared-memory ring stages, threads per CTA, CTAs}.
  * Returns FP4_OK, or the status fp4_add_rmsnorm_quant would return for the sizes.
  */
-fp4_status_t fp4_launch_shape(int64_t M, int64_t H, fp4_dtype_t dtype, fp4_format_t format,
-                              fp4_sf_layout_t sf_layout, int64_t out[8]);
+FP4Q_API fp4_status_t fp4_launch_shape(int64_t M, int64_t H, fp4_dtype_t dtype, fp4_format_t format,
+                                       fp4_sf_layout_t sf_layout, int64_t out[8]);
 
 /*
  * fp4_gemm_nvfp4_bf16 - the consumer of the packed codes and tiled scales:
@@ -218,17 +226,17 @@ fp4_status_t fp4_launch_shape(int64_t M, int64_t H, fp4_dtype_t dtype, fp4_forma
  * must not overlap the inputs (except residual == out).  A tile whose inputs
  * never arrive (a bounded wait runs out) is written as NaN.
  */
-fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
-                                 const uint8_t* sfa, const uint8_t* sfb, float alpha,
-                                 const void* bias, const void* residual, int64_t M, int64_t N,
-                                 int64_t K, void* out, int variant, int pdl,
-                                 fp4q_stream_t stream);
+FP4Q_API fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
+                                          const uint8_t* sfa, const uint8_t* sfb, float alpha,
+                                          const void* bias, const void* residual, int64_t M, int64_t N,
+                                          int64_t K, void* out, int variant, int pdl,
+                                          fp4q_stream_t stream);
 
 /* Static, NUL-terminated description of a status code. */
-const char* fp4_status_string(fp4_status_t status);
+FP4Q_API const char* fp4_status_string(fp4_status_t status);
 
 /* cudaError_t value behind the last FP4_ERR_CUDA returned on this thread (0 if none). */
-int fp4_last_cuda_error(void);
+FP4Q_API int fp4_last_cuda_error(void);
 
 #ifdef __cplusplus
 }

@@ -26,7 +26,8 @@ LIBPATH = os.path.join(LIBDIR, LIBNAME)
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
-              "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
+              "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr", "-I", INCLUDE,
+              "-I", CSRC]
 
 
 def nvcc_path() -> str:

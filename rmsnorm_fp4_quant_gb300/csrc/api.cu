@@ -2,6 +2,7 @@
 // checks, launch-shape choice and dispatch to the sm_103a kernels.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "../../include/fp4q.h"
@@ -60,10 +61,10 @@ inline bool overlap(const void* a, int64_t na, const void* b, int64_t nb) {
 }
 
 int num_sms_current_device() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
-  if (cached[dev] == 0) {
+  if (cached[dev].load(std::memory_order_relaxed) == 0) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       n = 152;

@@ -1,6 +1,9 @@
 // fused_launch.cuh - launch helpers instantiated once per storage dtype.
 #pragma once
 
+#include <atomic>
+#include <mutex>
+
 #include "fused_direct.cuh"
 #include "fused_tma.cuh"
 
@@ -10,14 +13,19 @@ template <typename T, int FMT, int CPT, bool EX>
 cudaError_t raise_smem_limit(size_t smem) {
   // the limit is a per-device function attribute: raise it when a launch
   // needs more than any earlier one on this device
-  static size_t done[64] = {0};
+  static std::atomic<size_t> done[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && done[dev] >= smem) return cudaSuccess;
+  if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_relaxed) >= smem)
+    return cudaSuccess;
   e = cudaFuncSetAttribute(fused_tma_kernel<T, FMT, CPT, EX>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = smem;
+  if (e == cudaSuccess && dev >= 0 && dev < 64) {
+    size_t cur = done[dev].load(std::memory_order_relaxed);
+    while (cur < smem && !done[dev].compare_exchange_weak(cur, smem)) {
+    }
+  }
   return e;
 }
 
@@ -26,17 +34,24 @@ int ctas_per_sm_one(int threads, size_t smem) {
   // the last answer per device is kept: calls repeat the same launch shape
   struct Last { int threads; size_t smem; int n; };
   static Last last[64] = {};
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   const bool cacheable = dev >= 0 && dev < 64;
-  if (cacheable && last[dev].n > 0 && last[dev].threads == threads && last[dev].smem == smem)
-    return last[dev].n;
+  if (cacheable) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (last[dev].n > 0 && last[dev].threads == threads && last[dev].smem == smem)
+      return last[dev].n;
+  }
   if (raise_smem_limit<T, FMT, CPT, false>(smem) != cudaSuccess) return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_tma_kernel<T, FMT, CPT, false>, threads,
                                                     smem) != cudaSuccess)
     return 0;
-  if (cacheable) last[dev] = Last{threads, smem, n};
+  if (cacheable) {
+    std::lock_guard<std::mutex> lock(mu);
+    last[dev] = Last{threads, smem, n};
+  }
   return n;
 }
 

@@ -206,3 +206,17 @@ def test_gemm_validation(L, kwargs, status):
                                 a["residual"], a["M"], a["N"], a["K"], a["out"], a["variant"],
                                 a["pdl"], 0)
     assert st == status
+
+
+def test_library_exports_only_the_declared_entry_points(L):
+    """The library is built with hidden visibility: its dynamic symbol table
+    holds exactly the functions include/*.h declares (no internal C++ symbols)."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", fq.lib_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert exported == set(_declared_functions())

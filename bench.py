@@ -57,6 +57,8 @@ def parse_args():
                          "the NVFP4 GEMM that consumes them (--gemm picks the shape)")
     ap.add_argument("--gemm", default="G4_M8192_N7168_K7168",
                     help="GEMM workload for --op gemm")
+    ap.add_argument("--gemm-format", choices=["nvfp4", "mxfp4"], default="nvfp4",
+                    help="GEMM operand format (E4M3 per 16 or UE8M0 per 32 codes)")
     ap.add_argument("--gemm-variant", type=int, default=-1,
                     help="GEMM tile schedule: -1 automatic, 0/1 = one CTA per 128x128/128x256 "
                          "tile, 2/3 = persistent over 128x128/128x256 tiles, 4 = split K")
@@ -515,13 +517,15 @@ def measured_fp4_peak():
         return 1900.0 * FP4_PER_BF16, "fallback 1.9 PFLOP/s bf16 x 6"
 
 
-def gemm_operands(gw, device):
+def gemm_operands(gw, device, fmt="nvfp4"):
     K = gw.K
     a = workloads.random_bytes(gw.M * K // 2, gw.seed, 0, device=device).reshape(gw.M, K // 2)
     b = workloads.random_bytes(gw.N * K // 2, gw.seed, 1, device=device).reshape(gw.N, K // 2)
-    scales = list(range(0x20, 0x51))
-    nsa = ((gw.M + 127) // 128) * (K // 64) * 512
-    nsb = ((gw.N + 127) // 128) * (K // 64) * 512
+    # scale bytes: E4M3 2^-3..9 or UE8M0 2^-5..2^5; tiled buffers of 4-scale groups
+    scales = list(range(0x20, 0x51)) if fmt == "nvfp4" else list(range(122, 133))
+    group = 64 if fmt == "nvfp4" else 128
+    nsa = ((gw.M + 127) // 128) * (K // group) * 512
+    nsb = ((gw.N + 127) // 128) * (K // group) * 512
     sfa = workloads.random_bytes(nsa, gw.seed, 2, scales, device=device)
     sfb = workloads.random_bytes(nsb, gw.seed, 3, scales, device=device)
     return a, b, sfa, sfb
@@ -580,7 +584,8 @@ def run_gemm(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     L = fq.lib()
-    a, b, sfa, sfb = gemm_operands(gw, dev)
+    a, b, sfa, sfb = gemm_operands(gw, dev, args.gemm_format)
+    gemm_call = L.fp4_gemm_nvfp4_bf16 if args.gemm_format == "nvfp4" else L.fp4_gemm_mxfp4_bf16
     out = torch.empty(gw.M, gw.N, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
@@ -597,9 +602,9 @@ def run_gemm(args):
 
     def launch(k):
         s_ = sets[k % rot]
-        st = L.fp4_gemm_nvfp4_bf16(s_[0].data_ptr(), s_[1].data_ptr(), s_[2].data_ptr(),
-                                   s_[3].data_ptr(), 1.0, None, None, gw.M, gw.N, gw.K,
-                                   s_[4].data_ptr(), args.gemm_variant, 0, sh)
+        st = gemm_call(s_[0].data_ptr(), s_[1].data_ptr(), s_[2].data_ptr(), s_[3].data_ptr(),
+                       1.0, None, None, gw.M, gw.N, gw.K, s_[4].data_ptr(), args.gemm_variant,
+                       0, sh)
         if st != 0:
             raise fq.Fp4Error(st, "fp4_gemm_nvfp4_bf16")
 
@@ -663,9 +668,9 @@ def run_gemm(args):
         def e2e_step():
             for d, h in zip(ds, hs):
                 d.copy_(h, non_blocking=True)
-            st = L.fp4_gemm_nvfp4_bf16(ds[0].data_ptr(), ds[1].data_ptr(), ds[2].data_ptr(),
-                                       ds[3].data_ptr(), 1.0, None, None, gw.M, gw.N, gw.K,
-                                       op_, args.gemm_variant, 0, sh)
+            st = gemm_call(ds[0].data_ptr(), ds[1].data_ptr(), ds[2].data_ptr(),
+                           ds[3].data_ptr(), 1.0, None, None, gw.M, gw.N, gw.K, op_,
+                           args.gemm_variant, 0, sh)
             if st != 0:
                 raise fq.Fp4Error(st, "e2e gemm")
             ho.copy_(out, non_blocking=True)
@@ -690,13 +695,15 @@ def run_gemm(args):
         cpu = gemm_cpu_baseline(gw, args.cpu_seconds)
     if rank == 0:
         line = {
-            "metric": GEMM_METRIC, "value": round(world * tflops, 2), "unit": "TFLOP/s",
+            "metric": GEMM_METRIC.replace("NVFP4", args.gemm_format.upper()),
+            "value": round(world * tflops, 2), "unit": "TFLOP/s",
             "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e2m1 x e2m1 -> f32 accumulate, bf16 out", "data": "synthetic",
             "config": {"workload": gw.name, "op": "gemm", "M": gw.M, "N": gw.N, "K": gw.K,
-                       "variant": args.gemm_variant,
-                       "operands": "uniform random E2M1 bytes, E4M3 scale bytes 0x20..0x50",
+                       "variant": args.gemm_variant, "format": args.gemm_format,
+                       "operands": "uniform random E2M1 bytes, scale bytes 2^-3..9 (E4M3) or "
+                                   "2^-5..2^5 (UE8M0)",
                        "l2": ("%d operand copies rotated (%.0f MB per pass vs 129 MB L2), "
                               "one pass captured as a CUDA graph and replayed" % (rot, rot * alg / 1e6))
                              if rot > 1 else

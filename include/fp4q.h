@@ -232,6 +232,21 @@ FP4Q_API fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t
                                           int64_t K, void* out, int variant, int pdl,
                                           fp4q_stream_t stream);
 
+/*
+ * fp4_gemm_mxfp4_bf16 - the same product for MXFP4 operands: E2M1 codes with
+ * one UE8M0 scale per 32 elements (the fused op's and fp4_quantize's MXFP4
+ * output, tiled layout, fp4_sf_size_bytes(M or N, K, FP4_MXFP4, ...) bytes).
+ * Not on the FlashRT page (its GEMM is NVFP4 only): the consumer of this
+ * library's own MXFP4 producer.  Arguments, checks and variants as
+ * fp4_gemm_nvfp4_bf16, except that the persistent variants 2 and 3 are
+ * NVFP4 only (FP4_ERR_INVALID_ARG).
+ */
+FP4Q_API fp4_status_t fp4_gemm_mxfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
+                                          const uint8_t* sfa, const uint8_t* sfb, float alpha,
+                                          const void* bias, const void* residual, int64_t M,
+                                          int64_t N, int64_t K, void* out, int variant, int pdl,
+                                          fp4q_stream_t stream);
+
 /* Static, NUL-terminated description of a status code. */
 FP4Q_API const char* fp4_status_string(fp4_status_t status);
 

@@ -29,6 +29,7 @@ from ._binding import (  # noqa: F401
     fp4_add_rmsnorm_quant_ex,
     fp4_add_rmsnorm_quant_gs,
     fp4_dequant,
+    fp4_gemm_mxfp4_bf16,
     fp4_gemm_nvfp4_bf16,
     fp4_quantize,
     fp4_last_cuda_error,

@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
     L.fp4_gemm_nvfp4_bf16.argtypes = [vp, vp, vp, vp, ctypes.c_float, vp, vp, i64, i64, i64,
                                       vp, ci, ci, vp]
     L.fp4_gemm_nvfp4_bf16.restype = ci
+    L.fp4_gemm_mxfp4_bf16.argtypes = L.fp4_gemm_nvfp4_bf16.argtypes
+    L.fp4_gemm_mxfp4_bf16.restype = ci
     _lib = L
     return L
 
@@ -120,6 +122,14 @@ def fp4_gemm_nvfp4_bf16(a_packed_ptr: int, b_packed_ptr: int, sfa_ptr: int, sfb_
                         alpha: float, bias_ptr: int, residual_ptr: int, M: int, N: int, K: int,
                         out_ptr: int, variant: int, pdl: int, stream: int) -> int:
     return lib().fp4_gemm_nvfp4_bf16(a_packed_ptr, b_packed_ptr, sfa_ptr, sfb_ptr, alpha,
+                                     bias_ptr or None, residual_ptr or None, M, N, K, out_ptr,
+                                     variant, pdl, stream or None)
+
+
+def fp4_gemm_mxfp4_bf16(a_packed_ptr: int, b_packed_ptr: int, sfa_ptr: int, sfb_ptr: int,
+                        alpha: float, bias_ptr: int, residual_ptr: int, M: int, N: int, K: int,
+                        out_ptr: int, variant: int, pdl: int, stream: int) -> int:
+    return lib().fp4_gemm_mxfp4_bf16(a_packed_ptr, b_packed_ptr, sfa_ptr, sfb_ptr, alpha,
                                      bias_ptr or None, residual_ptr or None, M, N, K, out_ptr,
                                      variant, pdl, stream or None)
 
@@ -308,9 +318,10 @@ def dequant(packed, sf, M: int, H: int, fmt: str = "nvfp4", sf_layout: str = "ro
 
 
 def gemm_nvfp4_bf16(a_packed, b_packed, sfa, sfb, alpha: float = 1.0, bias=None, residual=None,
-                    out=None, variant: int = -1, pdl: bool = False, stream=None):
+                    out=None, variant: int = -1, pdl: bool = False, stream=None, fmt="nvfp4"):
     """bf16 (M, N) = alpha * deq(A) @ deq(B)^T (+ bias) (+ residual) from packed
     NVFP4 operands (M, K/2) and (N, K/2) and their tiled scale buffers.
+    fmt "mxfp4" takes MXFP4 operands (UE8M0 scale per 32 codes) instead.
     variant: -1 automatic, 0 / 1 = one CTA per 128x128 / 128x256 output tile,
     2 / 3 = persistent CTAs over 128x128 / 128x256 tiles, 4 = 128x128 tiles with
     the K loop split over a cluster (automatic for few output tiles)."""
@@ -331,12 +342,13 @@ def gemm_nvfp4_bf16(a_packed, b_packed, sfa, sfb, alpha: float = 1.0, bias=None,
     if out is None:
         out = torch.empty(M, N, dtype=torch.bfloat16, device=a_packed.device)
     _check_cuda(out, "out")
-    st = fp4_gemm_nvfp4_bf16(a_packed.data_ptr(), b_packed.data_ptr(), sfa.data_ptr(),
-                             sfb.data_ptr(), float(alpha),
-                             bias.data_ptr() if bias is not None else 0,
-                             residual.data_ptr() if residual is not None else 0, M, N, K,
-                             out.data_ptr(), int(variant), 1 if pdl else 0,
-                             _stream_handle(stream))
+    if fmt not in ("nvfp4", "mxfp4"):
+        raise ValueError("fmt must be 'nvfp4' or 'mxfp4'")
+    call = fp4_gemm_nvfp4_bf16 if fmt == "nvfp4" else fp4_gemm_mxfp4_bf16
+    st = call(a_packed.data_ptr(), b_packed.data_ptr(), sfa.data_ptr(), sfb.data_ptr(),
+              float(alpha), bias.data_ptr() if bias is not None else 0,
+              residual.data_ptr() if residual is not None else 0, M, N, K, out.data_ptr(),
+              int(variant), 1 if pdl else 0, _stream_handle(stream))
     if st != 0:
-        raise Fp4Error(st, "fp4_gemm_nvfp4_bf16")
+        raise Fp4Error(st, f"fp4_gemm_{fmt}_bf16")
     return out

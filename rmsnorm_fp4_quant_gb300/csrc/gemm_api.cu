@@ -25,15 +25,16 @@
 
 using namespace fp4q;
 
-extern "C" {
+namespace {
 
-fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
-                                 const uint8_t* sfa, const uint8_t* sfb, float alpha,
-                                 const void* bias, const void* residual, int64_t M, int64_t N,
-                                 int64_t K, void* out, int variant, int pdl,
-                                 fp4q_stream_t stream) {
+// Both formats: NVFP4 (mx = false) or MXFP4 operands.
+fp4_status_t gemm_call(bool mx, const uint8_t* a_packed, const uint8_t* b_packed,
+                       const uint8_t* sfa, const uint8_t* sfb, float alpha, const void* bias,
+                       const void* residual, int64_t M, int64_t N, int64_t K, void* out,
+                       int variant, int pdl, fp4q_stream_t stream) {
   if (M < 0 || N < 0 || K <= 0) return FP4_ERR_INVALID_ARG;
   if (variant < -1 || variant > 4) return FP4_ERR_INVALID_ARG;
+  if (mx && (variant == 2 || variant == 3)) return FP4_ERR_INVALID_ARG;   // NVFP4 only
   if (K % 256 != 0 || N % 8 != 0) return FP4_ERR_UNSUPPORTED_SHAPE;
   if (M > INT32_MAX - 128 || N > INT32_MAX - 128 || K > INT32_MAX / 2)
     return FP4_ERR_UNSUPPORTED_SHAPE;
@@ -44,8 +45,9 @@ fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packe
                           static_cast<const void*>(out), bias, residual})
     if (!abi_aligned(ptr, 16)) return FP4_ERR_MISALIGNED;
   const int64_t out_bytes = M * N * 2;
-  const int64_t sfa_bytes = fp4_sf_size_bytes(M, K, FP4_NVFP4, FP4_SF_SWIZZLED);
-  const int64_t sfb_bytes = fp4_sf_size_bytes(N, K, FP4_NVFP4, FP4_SF_SWIZZLED);
+  const fp4_format_t fmt = mx ? FP4_MXFP4 : FP4_NVFP4;
+  const int64_t sfa_bytes = fp4_sf_size_bytes(M, K, fmt, FP4_SF_SWIZZLED);
+  const int64_t sfb_bytes = fp4_sf_size_bytes(N, K, fmt, FP4_SF_SWIZZLED);
   if (abi_overlap(out, out_bytes, a_packed, M * K / 2) ||
       abi_overlap(out, out_bytes, b_packed, N * K / 2) ||
       abi_overlap(out, out_bytes, sfa, sfa_bytes) || abi_overlap(out, out_bytes, sfb, sfb_bytes) ||
@@ -97,15 +99,37 @@ fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packe
   p.nkt = 0;        // filled by the launcher
   p.num_kb = 0;
   p.tmem_cols = 0;
-  cudaError_t e = launch_gemm_nvfp4(a_packed, b_packed, p, bn, persistent, pdl,
+  cudaError_t e = launch_gemm_nvfp4(a_packed, b_packed, p, bn, persistent, mx, pdl,
                                     reinterpret_cast<cudaStream_t>(stream));
   // a cluster of this many CTAs may not fit: halve it until one does
   while (e == cudaErrorInvalidConfiguration && p.split > 2) {
     p.split /= 2;
-    e = launch_gemm_nvfp4(a_packed, b_packed, p, bn, persistent, pdl,
+    e = launch_gemm_nvfp4(a_packed, b_packed, p, bn, persistent, mx, pdl,
                           reinterpret_cast<cudaStream_t>(stream));
   }
   return static_cast<fp4_status_t>(record_cuda_error(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
+                                 const uint8_t* sfa, const uint8_t* sfb, float alpha,
+                                 const void* bias, const void* residual, int64_t M, int64_t N,
+                                 int64_t K, void* out, int variant, int pdl,
+                                 fp4q_stream_t stream) {
+  return gemm_call(false, a_packed, b_packed, sfa, sfb, alpha, bias, residual, M, N, K, out,
+                   variant, pdl, stream);
+}
+
+fp4_status_t fp4_gemm_mxfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
+                                 const uint8_t* sfa, const uint8_t* sfb, float alpha,
+                                 const void* bias, const void* residual, int64_t M, int64_t N,
+                                 int64_t K, void* out, int variant, int pdl,
+                                 fp4q_stream_t stream) {
+  return gemm_call(true, a_packed, b_packed, sfa, sfb, alpha, bias, residual, M, N, K, out,
+                   variant, pdl, stream);
 }
 
 }  // extern "C"

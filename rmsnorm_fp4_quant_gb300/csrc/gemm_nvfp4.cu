@@ -53,24 +53,38 @@ constexpr int kBKBytes = 128;               // K block: 256 E2M1 codes = one swi
 constexpr int kMmaKBytes = 32;              // K = 64 codes per MMA
 constexpr uint32_t kTileBytesA = kBM * kBKBytes;  // 16 KiB
 constexpr uint32_t kSfTileBytes = 512;            // 128 rows x 4 scales
-constexpr uint32_t kSfBytesA = 4 * kSfTileBytes;  // A's scales of one K block
 
-// Per output-tile width BN (the MMA's N: 128 or 256 columns).
-template <int BN>
+// Per output-tile width BN (the MMA's N: 128 or 256 columns) and scale format:
+// NVFP4 (E4M3 scale per 16 codes, four 512-byte scale tiles per K block, one
+// per MMA) or MXFP4 (UE8M0 per 32 codes, two tiles per K block, each holding
+// the scales of two MMAs: bytes 0-1 and 2-3 of a row's 4-byte group).
+template <int BN, bool MX = false>
 struct Cfg {
   static constexpr uint32_t kTileBytesB = BN * kBKBytes;
   static constexpr int kSfTilesB = BN / 128;              // 128-row scale tiles of B
+  static constexpr int kSfAtoms = MX ? 2 : 4;             // scale tiles per 128 rows per K block
+  static constexpr uint32_t kSfBytesA = kSfAtoms * kSfTileBytes;
   static constexpr uint32_t kSfBytesB = kSfTilesB * kSfBytesA;
   static constexpr uint32_t kStageBytes = kTileBytesA + kTileBytesB + kSfBytesA + kSfBytesB;
   static constexpr uint32_t kAccCols = BN;                // fp32 accumulator columns
-  static constexpr uint32_t kSfColsB = 4 * 4 * kSfTilesB; // B's scale columns per stage
-  static constexpr uint32_t kSfColsPerStage = 16 + kSfColsB;
+  static constexpr uint32_t kSfColsA = 4 * kSfAtoms;      // tensor-memory columns per stage
+  static constexpr uint32_t kSfColsB = 4 * kSfAtoms * kSfTilesB;
+  static constexpr uint32_t kSfColsPerStage = kSfColsA + kSfColsB;
   // Instruction descriptor of the block-scaled MMA: E2M1 A and B (format 1 at
-  // bits 7-9 and 10-12), both K-major, N >> 3 at bits 17-22, E4M3 scales (bit
-  // 23 clear), M >> 7 at bits 27-28, dense K = 64.
+  // bits 7-9 and 10-12), both K-major, N >> 3 at bits 17-22, scale type at bit
+  // 23 (0 = E4M3, 1 = UE8M0), M >> 7 at bits 27-28, dense K = 64; the scale
+  // byte pair of an MXFP4 step is chosen at bits 4-5 (B) and 29-30 (A).
   static constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) |
                                      (static_cast<uint32_t>(BN >> 3) << 17) |
+                                     ((MX ? 1u : 0u) << 23) |
                                      (static_cast<uint32_t>(kBM >> 7) << 27);
+  // K step j (of 4 per K block): its scale tile and instruction descriptor
+  __host__ __device__ static constexpr int atom(int j) { return MX ? j / 2 : j; }
+  __host__ __device__ static constexpr uint32_t idesc(int j) {
+    return MX ? kIdesc | (static_cast<uint32_t>((j & 1) * 2) << 4) |
+                    (static_cast<uint32_t>((j & 1) * 2) << 29)
+              : kIdesc;
+  }
   static constexpr uint32_t tmem_cols(int stages) {
     // accumulator + per-stage scale columns, rounded up to a power of two
     return (kAccCols + kSfColsPerStage * stages) <= 256 ? 256u : 512u;
@@ -149,11 +163,11 @@ __device__ __forceinline__ void store_columns32(const GemmParams& p, const uint3
 // loads), so the result does not depend on timing.  A second cluster barrier
 // keeps each partial alive until every peer has read it.  For short, wide
 // products (few output tiles) this spreads the K loop over many SMs.
-template <int BN, bool SPLIT>
+template <int BN, bool SPLIT, bool MX>
 __global__ void __launch_bounds__(128, 1)
 gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
                   const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, MX>;
   static_assert(!SPLIT || BN == 128, "the split partial tile must fit the drained ring");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -162,7 +176,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
   uint8_t* sA = smem;
   uint8_t* sB = sA + static_cast<size_t>(S) * kTileBytesA;
   uint8_t* sSFA = sB + static_cast<size_t>(S) * C::kTileBytesB;
-  uint8_t* sSFB = sSFA + static_cast<size_t>(S) * kSfBytesA;
+  uint8_t* sSFB = sSFA + static_cast<size_t>(S) * C::kSfBytesA;
   uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + static_cast<size_t>(S) * C::kSfBytesB);
   uint64_t* empty = full + S;
   uint64_t* accum = empty + S;
@@ -207,8 +221,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const int b_tiles_total = (p.N + 127) / 128;
     const int b_tiles = b_tiles_total - b_tile0 < C::kSfTilesB ? b_tiles_total - b_tile0
                                                                 : C::kSfTilesB;
-    const uint32_t stage_bytes = kTileBytesA + C::kTileBytesB + kSfBytesA +
-                                 static_cast<uint32_t>(b_tiles) * kSfBytesA;
+    const uint32_t stage_bytes = kTileBytesA + C::kTileBytesB + C::kSfBytesA +
+                                 static_cast<uint32_t>(b_tiles) * C::kSfBytesA;
     int i = 0;    // K blocks issued
     for (; i < kb1 - kb0; ++i) {
       const int kb = kb0 + i;
@@ -222,13 +236,13 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
                   &full[s]);
       tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
                   n_tile * BN, &full[s]);
-      bulk_g2s(sSFA + static_cast<size_t>(s) * kSfBytesA,
-               sfa_k + static_cast<size_t>(kb) * kSfBytesA, kSfBytesA, &full[s]);
+      bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA,
+               sfa_k + static_cast<size_t>(kb) * C::kSfBytesA, C::kSfBytesA, &full[s]);
       for (int t = 0; t < b_tiles; ++t)
-        bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + t * kSfBytesA,
+        bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + t * C::kSfBytesA,
                  p.sfb + (static_cast<size_t>(b_tile0 + t) * p.nkt) * kSfTileBytes +
-                     static_cast<size_t>(kb) * kSfBytesA,
-                 kSfBytesA, &full[s]);
+                     static_cast<size_t>(kb) * C::kSfBytesA,
+                 C::kSfBytesA, &full[s]);
     }
     if (i < kb1 - kb0) {   // gave up: let the copies already issued land first
       for (int j = i > S ? i - S : 0; j < i; ++j)
@@ -244,21 +258,21 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
       }
       tc_fence_after_sync();
       const uint32_t sfa_t = tmem + C::kAccCols + static_cast<uint32_t>(s) * C::kSfColsPerStage;
-      const uint32_t sfb_t = sfa_t + 16;
+      const uint32_t sfb_t = sfa_t + C::kSfColsA;
       const uint32_t a_s = smem_addr(sA + static_cast<size_t>(s) * kTileBytesA);
       const uint32_t b_s = smem_addr(sB + static_cast<size_t>(s) * C::kTileBytesB);
-      const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(s) * kSfBytesA);
+      const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(s) * C::kSfBytesA);
       const uint32_t sfb_s = smem_addr(sSFB + static_cast<size_t>(s) * C::kSfBytesB);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int q = 0; q < C::kSfAtoms; ++q) {
         // a scale tile: 32 rows of 16 bytes, 8-row groups 128 bytes apart.
-        // Step j's scales: A's tile at 4j; B's 128-row tiles side by side
-        // from 4 * kSfTilesB * j
-        tmem_copy_32x128b_x4(sfa_t + 4 * j, smem_desc(sfa_s + j * kSfTileBytes, 0, 128, kSwizzleNone));
+        // Tile q: A's at column 4q; B's 128-row tiles side by side from
+        // 4 * kSfTilesB * q
+        tmem_copy_32x128b_x4(sfa_t + 4 * q, smem_desc(sfa_s + q * kSfTileBytes, 0, 128, kSwizzleNone));
 #pragma unroll
         for (int t = 0; t < C::kSfTilesB; ++t)
-          tmem_copy_32x128b_x4(sfb_t + 4 * (C::kSfTilesB * j + t),
-                               smem_desc(sfb_s + t * kSfBytesA + j * kSfTileBytes, 0, 128,
+          tmem_copy_32x128b_x4(sfb_t + 4 * (C::kSfTilesB * q + t),
+                               smem_desc(sfb_s + t * C::kSfBytesA + q * kSfTileBytes, 0, 128,
                                          kSwizzleNone));
       }
 #pragma unroll
@@ -267,8 +281,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
         // advances the start address inside the swizzle row
         const uint64_t adesc = smem_desc(a_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
         const uint64_t bdesc = smem_desc(b_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
-        mma_mxf4nvf4(tmem, adesc, bdesc, C::kIdesc, sfa_t + 4 * j,
-                     sfb_t + 4 * C::kSfTilesB * j, (i | j) != 0 ? 1u : 0u);
+        mma_fp4_block_scaled<MX>(tmem, adesc, bdesc, C::idesc(j), sfa_t + 4 * C::atom(j),
+                                 sfb_t + 4 * C::kSfTilesB * C::atom(j), (i | j) != 0 ? 1u : 0u);
       }
       tc_commit(&empty[s]);   // the stage is free once these MMAs have read it
     }
@@ -379,7 +393,7 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
   uint8_t* sA = smem;
   uint8_t* sB = sA + static_cast<size_t>(S) * kTileBytesA;
   uint8_t* sSFA = sB + static_cast<size_t>(S) * C::kTileBytesB;
-  uint8_t* sSFB = sSFA + static_cast<size_t>(S) * kSfBytesA;
+  uint8_t* sSFB = sSFA + static_cast<size_t>(S) * C::kSfBytesA;
   uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + static_cast<size_t>(S) * C::kSfBytesB);
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;
@@ -429,8 +443,8 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const int b_tile0 = n_tile * C::kSfTilesB;
       const int b_tiles = b_tiles_total - b_tile0 < C::kSfTilesB ? b_tiles_total - b_tile0
                                                                   : C::kSfTilesB;
-      const uint32_t stage_bytes = kTileBytesA + C::kTileBytesB + kSfBytesA +
-                                   static_cast<uint32_t>(b_tiles) * kSfBytesA;
+      const uint32_t stage_bytes = kTileBytesA + C::kTileBytesB + C::kSfBytesA +
+                                   static_cast<uint32_t>(b_tiles) * C::kSfBytesA;
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
         const int s = it % S;
         if (it >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((it / S - 1) & 1))) {
@@ -443,13 +457,13 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     m_tile * kBM, &full[s]);
         tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
                     n_tile * BN, &full[s]);
-        bulk_g2s(sSFA + static_cast<size_t>(s) * kSfBytesA,
-                 sfa_k + static_cast<size_t>(kb) * kSfBytesA, kSfBytesA, &full[s]);
+        bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA,
+                 sfa_k + static_cast<size_t>(kb) * C::kSfBytesA, C::kSfBytesA, &full[s]);
         for (int q = 0; q < b_tiles; ++q)
-          bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + q * kSfBytesA,
+          bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + q * C::kSfBytesA,
                    p.sfb + static_cast<size_t>(b_tile0 + q) * p.nkt * kSfTileBytes +
-                       static_cast<size_t>(kb) * kSfBytesA,
-                   kSfBytesA, &full[s]);
+                       static_cast<size_t>(kb) * C::kSfBytesA,
+                   C::kSfBytesA, &full[s]);
       }
     }
     if (!ok) {   // gave up: let the copies already issued land first
@@ -459,7 +473,7 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
     const uint32_t sfa_t = tmem + P::kSfCol;
-    const uint32_t sfb_t = sfa_t + 16;
+    const uint32_t sfb_t = sfa_t + C::kSfColsA;
     int it = 0;
     bool ok = true;
     for (int i = 0; i < my_tiles && ok; ++i) {
@@ -481,7 +495,7 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
         tc_fence_after_sync();
         const uint32_t a_s = smem_addr(sA + static_cast<size_t>(s) * kTileBytesA);
         const uint32_t b_s = smem_addr(sB + static_cast<size_t>(s) * C::kTileBytesB);
-        const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(s) * kSfBytesA);
+        const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(s) * C::kSfBytesA);
         const uint32_t sfb_s = smem_addr(sSFB + static_cast<size_t>(s) * C::kSfBytesB);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -490,15 +504,15 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
 #pragma unroll
           for (int q = 0; q < C::kSfTilesB; ++q)
             tmem_copy_32x128b_x4(sfb_t + 4 * (C::kSfTilesB * j + q),
-                                 smem_desc(sfb_s + q * kSfBytesA + j * kSfTileBytes, 0, 128,
+                                 smem_desc(sfb_s + q * C::kSfBytesA + j * kSfTileBytes, 0, 128,
                                            kSwizzleNone));
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint64_t adesc = smem_desc(a_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
           const uint64_t bdesc = smem_desc(b_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
-          mma_mxf4nvf4(d_t, adesc, bdesc, C::kIdesc, sfa_t + 4 * j, sfb_t + 4 * C::kSfTilesB * j,
-                       (kb | j) != 0 ? 1u : 0u);
+          mma_fp4_block_scaled<false>(d_t, adesc, bdesc, C::kIdesc, sfa_t + 4 * j,
+                                      sfb_t + 4 * C::kSfTilesB * j, (kb | j) != 0 ? 1u : 0u);
         }
         tc_commit(&empty[s]);
       }
@@ -684,16 +698,16 @@ bool cluster_fits(Prep* pr, Kernel kernel, cudaLaunchConfig_t cfg, int split) {
   return ok;
 }
 
-template <int BN, bool SPLIT>
+template <int BN, bool SPLIT, bool MX>
 cudaError_t launch_bn(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
                       cudaStream_t stream) {
-  using C = Cfg<BN>;
-  auto kernel = gemm_nvfp4_kernel<BN, SPLIT>;
+  using C = Cfg<BN, MX>;
+  auto kernel = gemm_nvfp4_kernel<BN, SPLIT, MX>;
   CUtensorMap ta, tb;
   if (!operand_map(&ta, a, p.M, p.K / 2, kBM) || !operand_map(&tb, b, p.N, p.K / 2, BN))
     return cudaErrorInvalidValue;
   p.tmem_cols = C::tmem_cols(p.stages);
-  p.nkt = p.K / 64;
+  p.nkt = p.K / (MX ? 128 : 64);   // 4-scale groups per row: K / (4 * block)
   p.num_kb = p.K / (2 * kBKBytes);
   const size_t smem_need = C::smem_bytes(p.stages);
   if (smem_need > 227 * 1024) return cudaErrorInvalidValue;
@@ -777,15 +791,24 @@ cudaError_t launch_persistent(const uint8_t* a, const uint8_t* b, GemmParams p, 
 }  // namespace
 
 cudaError_t launch_gemm_nvfp4(const uint8_t* a, const uint8_t* b, GemmParams p, int bn,
-                              bool persistent, int pdl, cudaStream_t stream) {
+                              bool persistent, bool mx, int pdl, cudaStream_t stream) {
   if (p.stages < 2 || p.stages > 8) return cudaErrorInvalidValue;
+  if (mx) {
+    if (persistent) return cudaErrorInvalidValue;
+    if (p.split > 1)
+      return bn == 128 && p.split <= 16 ? launch_bn<128, true, true>(a, b, p, pdl, stream)
+                                        : cudaErrorInvalidValue;
+    if (bn == 128) return launch_bn<128, false, true>(a, b, p, pdl, stream);
+    if (bn == 256) return launch_bn<256, false, true>(a, b, p, pdl, stream);
+    return cudaErrorInvalidValue;
+  }
   if (p.split > 1) {
     if (bn != 128 || persistent || p.split > 16) return cudaErrorInvalidValue;
-    return launch_bn<128, true>(a, b, p, pdl, stream);
+    return launch_bn<128, true, false>(a, b, p, pdl, stream);
   }
   if (!persistent) {
-    if (bn == 128) return launch_bn<128, false>(a, b, p, pdl, stream);
-    if (bn == 256) return launch_bn<256, false>(a, b, p, pdl, stream);
+    if (bn == 128) return launch_bn<128, false, false>(a, b, p, pdl, stream);
+    if (bn == 256) return launch_bn<256, false, false>(a, b, p, pdl, stream);
   } else {
     if (bn == 128) return launch_persistent<128>(a, b, p, pdl, stream);
     if (bn == 256) return launch_persistent<256>(a, b, p, pdl, stream);

@@ -46,19 +46,34 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 
 // --- MMA ----------------------------------------------------------------------
 // D[tmem] (+)= A[smem] * B[smem]^T with E2M1 operands (K = 64 per instruction)
-// and one E4M3 scale per 16 elements of each row of A and of B (4 per row per
-// instruction), read from tensor memory at sfa / sfb.
-__device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                             uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                             uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
-      "[%0], %1, %2, %3, [%5], [%6], p;\n\t}"
-      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem),
-         "r"(sfb_tmem)
-      : "memory");
+// and block scales read from tensor memory at sfa / sfb: NVFP4 (MX = false),
+// one E4M3 scale per 16 elements (4 per row per instruction), or MXFP4 (MX =
+// true), one UE8M0 scale per 32 elements (2 per row per instruction, the byte
+// pair chosen by the instruction descriptor).
+template <bool MX>
+__device__ __forceinline__ void mma_fp4_block_scaled(uint32_t d_tmem, uint64_t adesc,
+                                                     uint64_t bdesc, uint32_t idesc,
+                                                     uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                     uint32_t accumulate) {
+  if constexpr (MX) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X "
+        "[%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+        :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem),
+           "r"(sfb_tmem)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+        "[%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+        :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem),
+           "r"(sfb_tmem)
+        : "memory");
+  }
 }
 
 // 32 rows x 16 bytes of shared memory into 32 lanes x 4 columns of tensor

@@ -38,7 +38,8 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for want in ("fp4_add_rmsnorm_quant", "fp4_add_rmsnorm_quant_gs", "fp4_quantize",
                  "fp4_dequant", "fp4_sf_size_bytes", "fp4_launch_shape",
-                 "fp4_status_string", "fp4_last_cuda_error", "fp4_gemm_nvfp4_bf16"):
+                 "fp4_status_string", "fp4_last_cuda_error", "fp4_gemm_nvfp4_bf16",
+                 "fp4_gemm_mxfp4_bf16"):
         assert want in names
 
 
@@ -220,3 +221,19 @@ def test_library_exports_only_the_declared_entry_points(L):
                          text=True, check=True).stdout
     exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
     assert exported == set(_declared_functions())
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(variant=2), 1), (dict(variant=3), 1),   # the persistent schedules are NVFP4 only
+    (dict(K=128), 2), (dict(a=0), 1), (dict(sfa=S + 8), 3),
+    (dict(out=S + 256), 1),                         # output over the MXFP4 scales of A
+    (dict(M=0, a=0), 0),
+])
+def test_gemm_mxfp4_validation(L, kwargs, status):
+    a = dict(a=A, b=B, sfa=S, sfb=S2, alpha=1.0, bias=0, residual=0, M=256, N=256, K=512,
+             out=G_OUT, variant=-1, pdl=0)
+    a.update(kwargs)
+    st = fq.fp4_gemm_mxfp4_bf16(a["a"], a["b"], a["sfa"], a["sfb"], a["alpha"], a["bias"],
+                                a["residual"], a["M"], a["N"], a["K"], a["out"], a["variant"],
+                                a["pdl"], 0)
+    assert st == status

@@ -24,18 +24,19 @@ import workloads
 pytestmark = pytest.mark.gpu
 
 E2M1_SMALL = [0x0, 0x1, 0x2, 0x4, 0x9, 0xA, 0xC]      # 0, +-0.5, +-1, +-2
-E4M3_POW2 = [0x30, 0x38, 0x40]                         # 0.5, 1, 2
 EXACT_BYTES = [lo | (hi << 4) for lo in E2M1_SMALL for hi in E2M1_SMALL]
-RANDOM_SCALES = list(range(0x20, 0x51))                # 2^-3 .. 9
+# scale bytes per format: powers of two 0.5, 1, 2 (exact kind) and a range
+SCALES = {"nvfp4": {"exact": [0x30, 0x38, 0x40], "random": list(range(0x20, 0x51))},   # 2^-3..9
+          "mxfp4": {"exact": [126, 127, 128], "random": list(range(122, 133))}}       # 2^-5..2^5
 
 
-def operands(M, N, K, seed, kind):
+def operands(M, N, K, seed, kind, fmt="nvfp4"):
     code_alpha = EXACT_BYTES if kind == "exact" else None
-    sf_alpha = E4M3_POW2 if kind == "exact" else RANDOM_SCALES
+    sf_alpha = SCALES[fmt][kind]
     a = workloads.random_bytes(M * K // 2, seed, 0, code_alpha).reshape(M, K // 2)
     b = workloads.random_bytes(N * K // 2, seed, 1, code_alpha).reshape(N, K // 2)
-    sfa = workloads.random_bytes(oracle.sf_size_bytes(M, K, "nvfp4", "swizzled"), seed, 2, sf_alpha)
-    sfb = workloads.random_bytes(oracle.sf_size_bytes(N, K, "nvfp4", "swizzled"), seed, 3, sf_alpha)
+    sfa = workloads.random_bytes(oracle.sf_size_bytes(M, K, fmt, "swizzled"), seed, 2, sf_alpha)
+    sfb = workloads.random_bytes(oracle.sf_size_bytes(N, K, fmt, "swizzled"), seed, 3, sf_alpha)
     return a, b, sfa, sfb
 
 
@@ -47,11 +48,11 @@ def bf16_values(n, seed, tensor_id, shape):
 
 
 def gpu_gemm(a, b, sfa, sfb, alpha=1.0, bias=None, residual=None, out=None, pdl=False,
-             variant=-1):
+             variant=-1, fmt="nvfp4"):
     dev = "cuda"
     res = fq.gemm_nvfp4_bf16(a.to(dev), b.to(dev), sfa.to(dev), sfb.to(dev), alpha=alpha,
                              bias=None if bias is None else bias.to(dev),
-                             residual=residual, out=out, pdl=pdl, variant=variant)
+                             residual=residual, out=out, pdl=pdl, variant=variant, fmt=fmt)
     torch.cuda.synchronize()
     return res
 
@@ -82,6 +83,32 @@ def oracle_gemm(a, b, sfa, sfb, M, N, K, **kw):
 
 EXACT_SHAPES = [(128, 128, 256), (1, 8, 256), (41, 4608, 1536), (300, 520, 768),
                 (129, 136, 512), (256, 1024, 4096)]
+
+MX_VARIANTS = [0, 1, 4]   # MXFP4: one CTA per 128x128 / 128x256 tile, split K
+
+
+@pytest.mark.parametrize("M,N,K", EXACT_SHAPES)
+@pytest.mark.parametrize("variant", MX_VARIANTS)
+def test_gemm_mxfp4_exact_operands_bit_exact(M, N, K, variant):
+    """MXFP4 operands (UE8M0 per 32 codes; two 128x4 scale tiles per K block,
+    each holding two K steps' scales)."""
+    a, b, sfa, sfb = operands(M, N, K, seed=7 * M + N + K, kind="exact", fmt="mxfp4")
+    got = gpu_gemm(a, b, sfa, sfb, alpha=0.5, variant=variant, fmt="mxfp4")
+    check(got, oracle_gemm(a, b, sfa, sfb, M, N, K, alpha=0.5, fmt="mxfp4"), K, "exact")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 384, 2048), (41, 1536, 6144)])
+@pytest.mark.parametrize("variant", MX_VARIANTS)
+def test_gemm_mxfp4_random_operands(M, N, K, variant):
+    a, b, sfa, sfb = operands(M, N, K, seed=5 * M + N, kind="random", fmt="mxfp4")
+    got = gpu_gemm(a, b, sfa, sfb, variant=variant, fmt="mxfp4")
+    check(got, oracle_gemm(a, b, sfa, sfb, M, N, K, fmt="mxfp4"), K, "random")
+
+
+def test_gemm_mxfp4_rejects_persistent_variants():
+    a, b, sfa, sfb = operands(128, 128, 256, 1, "exact", "mxfp4")
+    with pytest.raises(fq.Fp4Error):
+        gpu_gemm(a, b, sfa, sfb, variant=2, fmt="mxfp4")
 
 
 VARIANTS = [0, 1, 2, 3, 4]   # 128x128 / 128x256 tiles; one CTA per tile / persistent; split K
@@ -184,4 +211,31 @@ def test_gemm_consumes_the_fused_producer_with_pdl():
     same_b = np.array_equal(pb.cpu().numpy(), ob.packed) and np.array_equal(
         sb.cpu().numpy(), ob.sf_swizzled)
     assert same_a and same_b, "producer bytes differ from the oracle's"
+    check(got, g, K, "random")
+
+
+def test_gemm_consumes_the_mxfp4_producer():
+    """The headline producer configuration (bf16 rows with outlier columns,
+    MXFP4, tiled scales) feeding the MXFP4 GEMM with PDL, against the oracle's
+    chain."""
+    M, N, K = 256, 384, 7168
+    wl = workloads.Workload("chain_mx", M, K, "bf16", "mxfp4", "swizzled", 1e-6,
+                            outlier_frac=0.01, seed=33)
+    x, r, w = workloads.make_inputs(wl, "cpu")
+    wmat = workloads.make_rows(workloads.Workload("wmat_mx", N, K, "bf16", "mxfp4", "swizzled",
+                                                  1e-6, seed=34), "x", 0, N, "cpu")
+    oa = oracle.add_rmsnorm_fp4_quant(x.float().numpy(), r.float().numpy(), w.float().numpy(),
+                                      wl.eps, "bf16", "mxfp4", "swizzled")
+    ob = oracle.quantize(wmat.float().numpy(), "mxfp4", "swizzled")
+    g = oracle.gemm_bf16(oa.packed, ob.packed, oa.sf_swizzled, ob.sf_swizzled, M, N, K,
+                         fmt="mxfp4")
+    pa, sa = fq.add_rmsnorm_fp4quant(x.cuda(), r.clone().cuda(), w.cuda(), eps=wl.eps,
+                                     fmt="mxfp4", sf_layout="swizzled")
+    pb, sb = fq.quantize_fp4(wmat.cuda(), fmt="mxfp4", sf_layout="swizzled")
+    got = fq.gemm_nvfp4_bf16(pa, pb, sa, sb, pdl=True, fmt="mxfp4")
+    torch.cuda.synchronize()
+    assert np.array_equal(pa.cpu().numpy(), oa.packed)
+    assert np.array_equal(sa.cpu().numpy(), oa.sf_swizzled)
+    assert np.array_equal(pb.cpu().numpy(), ob.packed)
+    assert np.array_equal(sb.cpu().numpy(), ob.sf_swizzled)
     check(got, g, K, "random")

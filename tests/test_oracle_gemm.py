@@ -134,6 +134,50 @@ def test_brute_force_tiny():
             assert g.exact[m, n] == pytest.approx(1.5 * s, rel=1e-14, abs=1e-300)
 
 
+UE8M0_ONE = 127
+
+
+def tiled_mx(scale_codes):
+    """UE8M0 scale bytes (rows, nb) into a zeroed 128x4 tiled buffer (32-blocks)."""
+    sc = np.asarray(scale_codes, np.uint8)
+    R, nb = sc.shape
+    buf = np.zeros(oracle.sf_size_bytes(R, nb * 32, "mxfp4", "swizzled"), np.uint8)
+    mm, kk = np.meshgrid(np.arange(R), np.arange(nb), indexing="ij")
+    buf[oracle.swizzled_sf_offset(mm, kk, (nb + 3) // 4)] = sc
+    return buf
+
+
+def test_mxfp4_row_and_block_scales_multiply():
+    """MXFP4 operands (UE8M0 scale per 32 codes): per-row and per-block powers
+    of two multiply as in the NVFP4 case, 32 elements per block."""
+    M, N, K = 3, 5, 128
+    ea = np.array([[(m % 3) - 1 + (k % 2) for k in range(K // 32)] for m in range(M)])
+    eb = np.array([[-(n % 2) - (k // 2) + 2 for k in range(K // 32)] for n in range(N)])
+    a = np.full((M, K), E2M1_ONE, np.uint8)
+    b = np.full((N, K), E2M1_TWO, np.uint8)
+    g = oracle.gemm_bf16(pack(a), pack(b), tiled_mx(UE8M0_ONE + ea), tiled_mx(UE8M0_ONE + eb),
+                         M, N, K, fmt="mxfp4")
+    want = np.array([[sum(32 * 2.0 * 2.0 ** (ea[m, k] + eb[n, k]) for k in range(K // 32))
+                      for n in range(N)] for m in range(M)])
+    assert np.array_equal(g.exact, want)
+
+
+def test_mxfp4_brute_force_tiny():
+    rng = np.random.default_rng(9)
+    M, N, K = 2, 3, 64
+    a = rng.integers(0, 16, (M, K)).astype(np.uint8)
+    b = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    a_sc = rng.integers(120, 135, (M, K // 32))
+    b_sc = rng.integers(120, 135, (N, K // 32))
+    g = oracle.gemm_bf16(pack(a), pack(b), tiled_mx(a_sc), tiled_mx(b_sc), M, N, K, alpha=0.5,
+                         fmt="mxfp4")
+    for m in range(M):
+        for n in range(N):
+            s = sum(_e2m1(a[m, k]) * 2.0 ** (int(a_sc[m, k // 32]) - 127) *
+                    _e2m1(b[n, k]) * 2.0 ** (int(b_sc[n, k // 32]) - 127) for k in range(K))
+            assert g.exact[m, n] == pytest.approx(0.5 * s, rel=1e-14, abs=1e-300)
+
+
 def test_quantized_product_within_quantization_bound():
     """x and w quantized by the producer oracle, then multiplied: the result
     is x @ w^T up to the per-element quantization errors, each at most one

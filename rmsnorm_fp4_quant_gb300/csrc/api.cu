@@ -344,7 +344,7 @@ static fp4_status_t fused_call(const void* input, int64_t x_stride, void* residu
   if (shape.path == kPathTma && shape.rows_per_cta > 1 && (x_stride != H || r_stride != H))
     return FP4_ERR_UNSUPPORTED_SHAPE;
 
-  FusedParams p;
+  FusedParams p{};
   p.x = input;
   p.r = residual;
   p.w = weight;
@@ -424,7 +424,7 @@ fp4_status_t fp4_quantize(const void* input, const float* global_scale, int64_t 
   const fp4_status_t st = check_outputs(M, H, format, sf_layout, input, M * H * 2, out_packed,
                                         out_sf, out_sf_rowmajor);
   if (st != FP4_OK) return st;
-  QuantParams p;
+  QuantParams p{};
   p.x = input;
   p.packed = out_packed;
   p.sf_tiled = (sf_layout == FP4_SF_ROWMAJOR) ? nullptr : out_sf;
@@ -454,7 +454,7 @@ fp4_status_t fp4_dequant(const uint8_t* packed, const uint8_t* sf, int64_t M, in
   if (M == 0) return FP4_OK;
   if (!packed || !sf || !out) return FP4_ERR_INVALID_ARG;
   if (!aligned(packed, 8) || !aligned(out, 16)) return FP4_ERR_MISALIGNED;
-  DequantParams p;
+  DequantParams p{};
   p.packed = packed;
   p.sf = sf;
   p.out = out;

@@ -34,6 +34,18 @@ __device__ __forceinline__ Chunk ld_stream_ro(const void* p) {
   return c;
 }
 
+// Streaming read that should also leave L2 first (evict-first): the
+// standalone quantize reads each input byte once and writes far less, so
+// its input should not push out lines still being written back.
+__device__ __forceinline__ Chunk ld_stream_ro_evict_first(const void* p) {
+  Chunk c;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(c.u[0]), "=r"(c.u[1]), "=r"(c.u[2]), "=r"(c.u[3]),
+                 "=r"(c.u[4]), "=r"(c.u[5]), "=r"(c.u[6]), "=r"(c.u[7])
+               : "l"(p));
+  return c;
+}
+
 // Streaming read of data the same thread overwrites later (the residual):
 // coherent load, no L1 allocation.
 __device__ __forceinline__ Chunk ld_stream_rw(const void* p) {

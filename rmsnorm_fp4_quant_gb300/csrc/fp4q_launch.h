@@ -106,6 +106,7 @@ struct QuantParams {
   int nchunk;
   int nb;
   int nkt;
+  int evict_first;     // read the input with the L2 evict-first policy (set by the launcher)
 };
 
 cudaError_t launch_quantize(int dtype, int fmt, const QuantParams& p, int num_sms,

@@ -57,7 +57,7 @@ fp4_status_t gemm_call(bool mx, const uint8_t* a_packed, const uint8_t* b_packed
   // by the same thread), but not partly overlap it
   if (residual && residual != out && abi_overlap(out, out_bytes, residual, out_bytes))
     return FP4_ERR_INVALID_ARG;
-  GemmParams p;
+  GemmParams p{};
   p.sfa = sfa;
   p.sfb = sfb;
   p.bias = static_cast<const uint16_t*>(bias);

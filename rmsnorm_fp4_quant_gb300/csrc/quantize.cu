@@ -81,7 +81,9 @@ __global__ void __launch_bounds__(256) quantize_kernel(const QuantParams p) {
   for (int u = 0; u < SEGS; ++u) {                    // all loads first
     c[u] = (blockIdx.y * SEGS + u) * 32 + lane;
     have[u] = have_row && c[u] < p.nchunk;
-    if (have[u]) xc[u] = ld_stream_ro(xrow + c[u] * 16);
+    if (have[u])
+      xc[u] = p.evict_first ? ld_stream_ro_evict_first(xrow + c[u] * 16)
+                            : ld_stream_ro(xrow + c[u] * 16);
   }
 #pragma unroll
   for (int u = 0; u < SEGS; ++u) quantize_chunk<T, FMT>(p, xc[u], have[u], row, c[u], gs);
@@ -120,7 +122,12 @@ cudaError_t launch_quantize(int dtype, int fmt, const QuantParams& p, int num_sm
   if (p.rows == 0) return cudaSuccess;
   if ((p.rows + 7) / 8 > INT32_MAX || (p.nchunk + 31) / 32 > 65535)
     return cudaErrorInvalidConfiguration;
-  return dtype == 0 ? launch_q<__nv_bfloat16>(fmt, p, stream) : launch_q<__half>(fmt, p, stream);
+  // Inputs read with L2 evict-first for rows up to 8192 elements: measured
+  // 6-9 % faster there (C3 / C4 shapes, 1536-wide rows), 1-2 % slower on
+  // 17408- and 32768-wide rows.
+  QuantParams q = p;
+  q.evict_first = p.H <= 8192 ? 1 : 0;
+  return dtype == 0 ? launch_q<__nv_bfloat16>(fmt, q, stream) : launch_q<__half>(fmt, q, stream);
 }
 
 }  // namespace fp4q

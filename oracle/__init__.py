@@ -46,4 +46,4 @@ from .add_rmsnorm_quant import (  # noqa: F401
     dequant,
     block_size,
 )
-from .gemm import GemmResult, gemm_bf16  # noqa: F401
+from .gemm import GemmResult, gelu, gemm_bf16, gemm_gelu_nvfp4  # noqa: F401

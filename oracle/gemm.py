@@ -28,7 +28,15 @@ Readings where the README is silent:
     compared against ``exact`` with the fp32 accumulation bound, not
     bit-for-bit;
   * ``bound`` = |alpha| * sum_k |deq(A)[m, k]| * |deq(B)[n, k]|, the scale of
-    the rounding error of any summation order.
+    the rounding error of any summation order;
+  * GELU (``nvfp4_gemm_bias_gelu_bf16`` / ``_nvfp4``; the README names it, the
+    form is not given): the exact one, x * Phi(x) = x/2 * (1 + erf(x / sqrt 2)),
+    applied to alpha * S + bias;
+  * the FP4-output epilogue (``nvfp4_gemm_bias_gelu_nvfp4`` "emits packed FP4
+    plus CUTLASS SFA so the following projection can consume it"): the
+    GELU values rounded once to fp32, then quantized by this oracle's
+    producer rules (``oracle.quantize``, NVFP4, tiled scales), rows of the
+    output as the rows of the next GEMM's A.
 """
 from __future__ import annotations
 
@@ -37,7 +45,7 @@ from typing import Optional
 
 import numpy as np
 
-from .add_rmsnorm_quant import dequant
+from .add_rmsnorm_quant import OracleResult, dequant, quantize
 from .formats import bf16_round
 
 
@@ -48,13 +56,24 @@ class GemmResult:
     bound: np.ndarray     # (M, N) fp64: |alpha| * sum_k |a| |b|
 
 
+def gelu(x) -> np.ndarray:
+    """x * Phi(x) with the exact normal CDF, in fp64."""
+    from scipy.special import erf
+    x = np.asarray(x, np.float64)
+    return 0.5 * x * (1.0 + erf(x / np.sqrt(2.0)))
+
+
 def gemm_bf16(a_packed, b_packed, sfa, sfb, M: int, N: int, K: int, alpha: float = 1.0,
               bias: Optional[np.ndarray] = None, residual: Optional[np.ndarray] = None,
-              fmt: str = "nvfp4", sf_layout: str = "swizzled", rows=None) -> GemmResult:
-    """alpha * deq(A) @ deq(B)^T (+ bias) (+ residual), rounded to bf16.
+              fmt: str = "nvfp4", sf_layout: str = "swizzled", rows=None,
+              gelu_act: bool = False) -> GemmResult:
+    """alpha * deq(A) @ deq(B)^T (+ bias) (+ residual), rounded to bf16; with
+    ``gelu_act``, GELU(alpha * deq(A) @ deq(B)^T + bias) (no residual).
 
     ``rows`` (optional index array) restricts the result to those rows of the
     output (``residual`` then holds just those rows)."""
+    if gelu_act and residual is not None:
+        raise ValueError("the GELU epilogue takes no residual")
     a = dequant(a_packed, sfa, M, K, fmt, sf_layout).astype(np.float64)
     b = dequant(b_packed, sfb, N, K, fmt, sf_layout).astype(np.float64)
     if rows is not None:
@@ -67,6 +86,18 @@ def gemm_bf16(a_packed, b_packed, sfa, sfb, M: int, N: int, K: int, alpha: float
         exact = exact + np.asarray(bias, np.float64).reshape(1, N)
     if residual is not None:
         exact = exact + np.asarray(residual, np.float64).reshape(M, N)
+    if gelu_act:
+        exact = gelu(exact)
     bound = abs(alpha64) * (np.abs(a) @ np.abs(b).T)
     out = bf16_round(exact.astype(np.float32))
     return GemmResult(exact, out, bound)
+
+
+def gemm_gelu_nvfp4(a_packed, b_packed, sfa, sfb, M: int, N: int, K: int, alpha: float = 1.0,
+                    bias: Optional[np.ndarray] = None, fmt: str = "nvfp4",
+                    rows=None) -> OracleResult:
+    """GELU(alpha * deq(A) @ deq(B)^T + bias) rounded to fp32 and quantized to
+    NVFP4 with tiled scales (rows = output rows, H = N)."""
+    g = gemm_bf16(a_packed, b_packed, sfa, sfb, M, N, K, alpha=alpha, bias=bias, fmt=fmt,
+                  rows=rows, gelu_act=True)
+    return quantize(g.exact.astype(np.float32), "nvfp4", "swizzled")

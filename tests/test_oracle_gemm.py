@@ -237,3 +237,87 @@ def test_gemm_mutant_is_caught(name, monkeypatch):
             caught = True
             break
     assert caught, f"no pin caught: {name}"
+
+
+# ---------------------------------------------------------------------------
+# GELU epilogues
+# ---------------------------------------------------------------------------
+# standard normal CDF at 0.5, 1, 2 (printed tables of Phi)
+PHI = {0.5: 0.6914624612740131, 1.0: 0.8413447460685429, 2.0: 0.9772498680518208}
+
+
+def test_gelu_is_x_times_normal_cdf():
+    for x, phi in PHI.items():
+        assert oracle.gelu(x) == pytest.approx(x * phi, rel=1e-15)
+        # Phi(-x) = 1 - Phi(x)
+        assert oracle.gelu(-x) == pytest.approx(-x * (1 - phi), rel=1e-14)
+    assert oracle.gelu(0.0) == 0.0
+    xs = np.linspace(-6, 6, 97)
+    assert np.allclose(oracle.gelu(xs) - oracle.gelu(-xs), xs, rtol=0, atol=1e-15)
+
+
+def test_gemm_gelu_applies_to_alpha_product_plus_bias():
+    """One-hot rows select a column of deq(B): out = GELU(alpha * b + bias)."""
+    rng = np.random.default_rng(4)
+    M, N, K = 3, 8, 64
+    a = np.zeros((M, K), np.uint8)
+    for m in range(M):
+        a[m, 5 * m] = E2M1_ONE
+    b = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    b_sc = np.full((N, K // 16), E4M3_ONE)
+    bias = np.linspace(-1, 1, N).astype(np.float32)
+    g = oracle.gemm_bf16(pack(a), pack(b), tiled(np.full((M, K // 16), E4M3_ONE)), tiled(b_sc),
+                         M, N, K, alpha=0.5, bias=bias, gelu_act=True)
+    deq_b = oracle.dequant(pack(b), tiled(b_sc), N, K, "nvfp4", "swizzled").astype(np.float64)
+    for m in range(M):
+        x = 0.5 * deq_b[:, 5 * m] + bias
+        assert np.allclose(g.exact[m], x * 0.5 * (1 + np.vectorize(__import__("math").erf)(
+            x / np.sqrt(2))), rtol=1e-14, atol=1e-300)
+    with pytest.raises(ValueError):
+        oracle.gemm_bf16(pack(a), pack(b), tiled(np.full((M, K // 16), E4M3_ONE)), tiled(b_sc),
+                         M, N, K, residual=np.zeros((M, N)), gelu_act=True)
+
+
+def test_gemm_gelu_nvfp4_output_dequantises_near_gelu():
+    """The FP4-output epilogue: every code, times its block scale, is within
+    half an E2M1 step (times the scale) of the GELU value it encodes."""
+    rng = np.random.default_rng(6)
+    M, N, K = 5, 64, 128
+    a = rng.integers(0, 16, (M, K)).astype(np.uint8)
+    b = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    a_sc = rng.integers(0x30, 0x40, (M, K // 16))
+    b_sc = rng.integers(0x30, 0x40, (N, K // 16))
+    bias = rng.standard_normal(N).astype(np.float32)
+    q = oracle.gemm_gelu_nvfp4(pack(a), pack(b), tiled(a_sc), tiled(b_sc), M, N, K, alpha=0.25,
+                               bias=bias)
+    g = oracle.gemm_bf16(pack(a), pack(b), tiled(a_sc), tiled(b_sc), M, N, K, alpha=0.25,
+                         bias=bias, gelu_act=True)
+    deq = oracle.dequant(q.packed, q.sf_swizzled, M, N, "nvfp4", "swizzled").astype(np.float64)
+    s = np.repeat(oracle.e4m3_decode(q.scale_codes), 16, axis=1).astype(np.float64)
+    v = g.exact / np.where(s > 0, s, 1)
+    step = np.where(np.abs(v) < 2, 0.5, np.where(np.abs(v) < 4, 1.0, 2.0))
+    err = np.abs(deq - g.exact)
+    assert np.all(err <= np.maximum(0.5 * step * s * (1 + 1e-6), (np.abs(v) - 6) * s + 1e-12))
+
+
+GELU_MUTANTS = {
+    "tanh approximation": ("return 0.5 * x * (1.0 + erf(x / np.sqrt(2.0)))",
+                           "return 0.5 * x * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * "
+                           "(x + 0.044715 * x ** 3)))"),
+    "erf argument not scaled": ("erf(x / np.sqrt(2.0))", "erf(x)"),
+    "Phi instead of x * Phi": ("return 0.5 * x * (1.0 + erf(x / np.sqrt(2.0)))",
+                               "return 0.5 * (1.0 + erf(x / np.sqrt(2.0)))"),
+}
+
+
+@pytest.mark.parametrize("name", list(GELU_MUTANTS))
+def test_gelu_mutant_is_caught(name, monkeypatch):
+    old, new = GELU_MUTANTS[name]
+    src = inspect.getsource(OG.gelu)
+    assert old in src
+    ns = dict(vars(OG))
+    exec(compile(src.replace(old, new, 1), "<mutant gelu>", "exec"), ns)
+    monkeypatch.setattr(oracle, "gelu", ns["gelu"])
+    monkeypatch.setattr(OG, "gelu", ns["gelu"])
+    with pytest.raises(AssertionError):
+        test_gelu_is_x_times_normal_cdf()

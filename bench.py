@@ -101,7 +101,8 @@ KERNEL_SOURCES = {
               "fused_common.cuh", "fused_direct.cuh", "fused_fp16.cu", "fused_launch.cuh",
               "fused_tma.cuh"),
     "quantize": ("api.cu", "fp4q_device.cuh", "fp4q_launch.h", "quantize.cu"),
-    "gemm": ("async_copy.cuh", "fp4q_launch.h", "gemm_api.cu", "gemm_nvfp4.cu", "tcgen05.cuh"),
+    "gemm": ("async_copy.cuh", "fp4q_device.cuh", "gemm_api.cu", "gemm_launch.h", "gemm_nvfp4.cu",
+             "tcgen05.cuh"),
 }
 
 

@@ -247,6 +247,39 @@ FP4Q_API fp4_status_t fp4_gemm_mxfp4_bf16(const uint8_t* a_packed, const uint8_t
                                           int64_t N, int64_t K, void* out, int variant, int pdl,
                                           fp4q_stream_t stream);
 
+/*
+ * fp4_gemm_nvfp4_gelu_bf16 - out = bf16(GELU(alpha * deq(A) @ deq(B)^T + bias))
+ * (FlashRT `fp4-gemm` README, `nvfp4_gemm_bias_gelu_bf16`; GELU is the exact
+ * x * Phi(x), computed with erff; bias may be NULL).  Arguments as
+ * fp4_gemm_nvfp4_bf16 without the residual.
+ */
+FP4Q_API fp4_status_t fp4_gemm_nvfp4_gelu_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
+                                               const uint8_t* sfa, const uint8_t* sfb,
+                                               float alpha, const void* bias, int64_t M,
+                                               int64_t N, int64_t K, void* out, int variant,
+                                               int pdl, fp4q_stream_t stream);
+
+/*
+ * fp4_gemm_nvfp4_gelu_nvfp4 - the same GELU values, rounded to fp32 and
+ * quantized in the epilogue to NVFP4 for the next GEMM (README,
+ * `nvfp4_gemm_bias_gelu_nvfp4`: "packed FP4 plus CUTLASS SFA"): the
+ * producer's rules (E4M3 scale of amax / 6 per 16 values, codes of
+ * v * rn(1/s), no global scale).
+ *   out_packed  [M, N/2] bytes, 16-byte aligned.
+ *   out_sf      tiled scales of the M x N output (fp4_sf_size_bytes(M, N,
+ *               FP4_NVFP4, FP4_SF_SWIZZLED) bytes), padding rows and k padding
+ *               written 0.
+ * N must be a multiple of 16; variant 4 (split K) is not available
+ * (FP4_ERR_INVALID_ARG); outputs must not overlap the inputs or each other.
+ */
+FP4Q_API fp4_status_t fp4_gemm_nvfp4_gelu_nvfp4(const uint8_t* a_packed,
+                                                const uint8_t* b_packed, const uint8_t* sfa,
+                                                const uint8_t* sfb, float alpha,
+                                                const void* bias, int64_t M, int64_t N,
+                                                int64_t K, uint8_t* out_packed,
+                                                uint8_t* out_sf, int variant, int pdl,
+                                                fp4q_stream_t stream);
+
 /* Static, NUL-terminated description of a status code. */
 FP4Q_API const char* fp4_status_string(fp4_status_t status);
 

@@ -25,11 +25,14 @@ from ._binding import (  # noqa: F401
     add_rmsnorm_fp4quant,
     dequant,
     gemm_nvfp4_bf16,
+    gemm_nvfp4_gelu,
     fp4_add_rmsnorm_quant,
     fp4_add_rmsnorm_quant_ex,
     fp4_add_rmsnorm_quant_gs,
     fp4_dequant,
     fp4_gemm_mxfp4_bf16,
+    fp4_gemm_nvfp4_gelu_bf16,
+    fp4_gemm_nvfp4_gelu_nvfp4,
     fp4_gemm_nvfp4_bf16,
     fp4_quantize,
     fp4_last_cuda_error,

@@ -67,6 +67,12 @@ def lib() -> ctypes.CDLL:
     L.fp4_gemm_nvfp4_bf16.restype = ci
     L.fp4_gemm_mxfp4_bf16.argtypes = L.fp4_gemm_nvfp4_bf16.argtypes
     L.fp4_gemm_mxfp4_bf16.restype = ci
+    L.fp4_gemm_nvfp4_gelu_bf16.argtypes = [vp, vp, vp, vp, ctypes.c_float, vp, i64, i64, i64,
+                                           vp, ci, ci, vp]
+    L.fp4_gemm_nvfp4_gelu_bf16.restype = ci
+    L.fp4_gemm_nvfp4_gelu_nvfp4.argtypes = [vp, vp, vp, vp, ctypes.c_float, vp, i64, i64, i64,
+                                            vp, vp, ci, ci, vp]
+    L.fp4_gemm_nvfp4_gelu_nvfp4.restype = ci
     _lib = L
     return L
 
@@ -132,6 +138,23 @@ def fp4_gemm_mxfp4_bf16(a_packed_ptr: int, b_packed_ptr: int, sfa_ptr: int, sfb_
     return lib().fp4_gemm_mxfp4_bf16(a_packed_ptr, b_packed_ptr, sfa_ptr, sfb_ptr, alpha,
                                      bias_ptr or None, residual_ptr or None, M, N, K, out_ptr,
                                      variant, pdl, stream or None)
+
+
+def fp4_gemm_nvfp4_gelu_bf16(a_packed_ptr: int, b_packed_ptr: int, sfa_ptr: int, sfb_ptr: int,
+                             alpha: float, bias_ptr: int, M: int, N: int, K: int, out_ptr: int,
+                             variant: int, pdl: int, stream: int) -> int:
+    return lib().fp4_gemm_nvfp4_gelu_bf16(a_packed_ptr, b_packed_ptr, sfa_ptr, sfb_ptr, alpha,
+                                          bias_ptr or None, M, N, K, out_ptr, variant, pdl,
+                                          stream or None)
+
+
+def fp4_gemm_nvfp4_gelu_nvfp4(a_packed_ptr: int, b_packed_ptr: int, sfa_ptr: int, sfb_ptr: int,
+                              alpha: float, bias_ptr: int, M: int, N: int, K: int,
+                              out_packed_ptr: int, out_sf_ptr: int, variant: int, pdl: int,
+                              stream: int) -> int:
+    return lib().fp4_gemm_nvfp4_gelu_nvfp4(a_packed_ptr, b_packed_ptr, sfa_ptr, sfb_ptr, alpha,
+                                           bias_ptr or None, M, N, K, out_packed_ptr,
+                                           out_sf_ptr, variant, pdl, stream or None)
 
 
 def fp4_sf_size_bytes(M: int, H: int, fmt: int, layout: int) -> int:
@@ -352,3 +375,40 @@ def gemm_nvfp4_bf16(a_packed, b_packed, sfa, sfb, alpha: float = 1.0, bias=None,
     if st != 0:
         raise Fp4Error(st, f"fp4_gemm_{fmt}_bf16")
     return out
+
+
+def gemm_nvfp4_gelu(a_packed, b_packed, sfa, sfb, alpha: float = 1.0, bias=None,
+                    out_format: str = "bf16", variant: int = -1, pdl: bool = False, stream=None):
+    """GELU(alpha * deq(A) @ deq(B)^T + bias) from NVFP4 operands; out_format
+    "bf16" returns a (M, N) bf16 tensor, "nvfp4" returns (packed (M, N/2),
+    tiled scales) ready to be the next GEMM's A operand."""
+    torch = _torch()
+    for name, t in (("a_packed", a_packed), ("b_packed", b_packed), ("sfa", sfa), ("sfb", sfb)):
+        _check_cuda(t, name)
+    if bias is not None:
+        _check_cuda(bias, "bias")
+        if bias.dtype != torch.bfloat16:
+            raise ValueError("bias must be bfloat16")
+    M, K, N = a_packed.shape[0], 2 * a_packed.shape[-1], b_packed.shape[0]
+    bp = bias.data_ptr() if bias is not None else 0
+    dev = a_packed.device
+    if out_format == "bf16":
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        st = fp4_gemm_nvfp4_gelu_bf16(a_packed.data_ptr(), b_packed.data_ptr(), sfa.data_ptr(),
+                                      sfb.data_ptr(), float(alpha), bp, M, N, K, out.data_ptr(),
+                                      int(variant), 1 if pdl else 0, _stream_handle(stream))
+        if st != 0:
+            raise Fp4Error(st, "fp4_gemm_nvfp4_gelu_bf16")
+        return out
+    if out_format != "nvfp4":
+        raise ValueError("out_format must be 'bf16' or 'nvfp4'")
+    packed = torch.empty(M, N // 2, dtype=torch.uint8, device=dev)
+    sf = torch.empty(max(1, fp4_sf_size_bytes(M, N, FP4_NVFP4, FP4_SF_SWIZZLED)), dtype=torch.uint8,
+                     device=dev)
+    st = fp4_gemm_nvfp4_gelu_nvfp4(a_packed.data_ptr(), b_packed.data_ptr(), sfa.data_ptr(),
+                                   sfb.data_ptr(), float(alpha), bp, M, N, K, packed.data_ptr(),
+                                   sf.data_ptr(), int(variant), 1 if pdl else 0,
+                                   _stream_handle(stream))
+    if st != 0:
+        raise Fp4Error(st, "fp4_gemm_nvfp4_gelu_nvfp4")
+    return packed, sf

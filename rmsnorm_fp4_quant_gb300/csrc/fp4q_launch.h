@@ -112,27 +112,4 @@ struct QuantParams {
 cudaError_t launch_quantize(int dtype, int fmt, const QuantParams& p, int num_sms,
                             cudaStream_t stream);
 
-// NVFP4 x NVFP4 -> bf16 GEMM (bf16 tensors as raw 16-bit words).
-struct GemmParams {
-  const uint8_t* sfa;          // tiled scales of A, ceil(M/128) * nkt * 512 bytes
-  const uint8_t* sfb;          // tiled scales of B, ceil(N/128) * nkt * 512 bytes
-  const uint16_t* bias;        // [N] bf16 or null
-  const uint16_t* residual;    // [M, N] bf16 or null
-  uint16_t* out;               // [M, N] bf16
-  float alpha;
-  int M, N, K;
-  int nkt;                     // 128x4 scale tiles per 128 rows: K / 64 (NVFP4), K / 128 (MXFP4)
-  int num_kb;                  // K / 256: K blocks
-  int stages;                  // shared-memory ring depth, 2..6
-  int split;                   // CTAs of a cluster sharing one tile's K loop (1 = none)
-  uint32_t tmem_cols;          // tensor-memory columns taken per CTA
-};
-
-// K % 256 == 0, N % 8 == 0, a / b 16-byte aligned (checked by the caller);
-// bn = output tile width, 128 or 256; persistent = one CTA per SM walking the
-// tiles (else one CTA per tile); mx = MXFP4 operands (UE8M0 scale per 32
-// codes) instead of NVFP4 (E4M3 per 16).
-cudaError_t launch_gemm_nvfp4(const uint8_t* a, const uint8_t* b, GemmParams p, int bn,
-                              bool persistent, bool mx, int pdl, cudaStream_t stream);
-
 }  // namespace fp4q

@@ -8,6 +8,7 @@
 
 #include "../../include/fp4q.h"
 #include "fp4q_launch.h"
+#include "gemm_launch.h"
 
 // Tuning constants of the schedule choice (compile-time, overridable with -D).
 #ifndef FP4Q_GEMM_STAGES
@@ -27,24 +28,45 @@ using namespace fp4q;
 
 namespace {
 
-// Both formats: NVFP4 (mx = false) or MXFP4 operands.
-fp4_status_t gemm_call(bool mx, const uint8_t* a_packed, const uint8_t* b_packed,
+// Every form: NVFP4 (mx = false) or MXFP4 operands; epilogue kEpiPlain /
+// kEpiGelu into `out` (bf16), or kEpiGeluFp4 into out_packed + out_sf.
+fp4_status_t gemm_call(bool mx, int epilogue, const uint8_t* a_packed, const uint8_t* b_packed,
                        const uint8_t* sfa, const uint8_t* sfb, float alpha, const void* bias,
                        const void* residual, int64_t M, int64_t N, int64_t K, void* out,
-                       int variant, int pdl, fp4q_stream_t stream) {
+                       uint8_t* out_packed, uint8_t* out_sf, int variant, int pdl,
+                       fp4q_stream_t stream) {
+  const bool fp4_out = epilogue == kEpiGeluFp4;
   if (M < 0 || N < 0 || K <= 0) return FP4_ERR_INVALID_ARG;
   if (variant < -1 || variant > 4) return FP4_ERR_INVALID_ARG;
   if (mx && (variant == 2 || variant == 3)) return FP4_ERR_INVALID_ARG;   // NVFP4 only
-  if (K % 256 != 0 || N % 8 != 0) return FP4_ERR_UNSUPPORTED_SHAPE;
+  if (fp4_out && variant == 4) return FP4_ERR_INVALID_ARG;   // split K stores 8-column groups
+  if (K % 256 != 0 || N % (fp4_out ? 16 : 8) != 0) return FP4_ERR_UNSUPPORTED_SHAPE;
   if (M > INT32_MAX - 128 || N > INT32_MAX - 128 || K > INT32_MAX / 2)
     return FP4_ERR_UNSUPPORTED_SHAPE;
   if (M == 0 || N == 0) return FP4_OK;
-  if (!a_packed || !b_packed || !sfa || !sfb || !out) return FP4_ERR_INVALID_ARG;
+  if (!a_packed || !b_packed || !sfa || !sfb) return FP4_ERR_INVALID_ARG;
+  if (fp4_out ? (!out_packed || !out_sf) : !out) return FP4_ERR_INVALID_ARG;
   for (const void* ptr : {static_cast<const void*>(a_packed), static_cast<const void*>(b_packed),
                           static_cast<const void*>(sfa), static_cast<const void*>(sfb),
-                          static_cast<const void*>(out), bias, residual})
+                          static_cast<const void*>(out), bias, residual,
+                          static_cast<const void*>(out_packed)})
     if (!abi_aligned(ptr, 16)) return FP4_ERR_MISALIGNED;
-  const int64_t out_bytes = M * N * 2;
+  if (fp4_out) {
+    const int64_t pk = M * N / 2;
+    const int64_t sfo = fp4_sf_size_bytes(M, N, FP4_NVFP4, FP4_SF_SWIZZLED);
+    const void* ins[4] = {a_packed, b_packed, sfa, sfb};
+    const int64_t in_bytes[4] = {M * K / 2, N * K / 2,
+                                 fp4_sf_size_bytes(M, K, FP4_NVFP4, FP4_SF_SWIZZLED),
+                                 fp4_sf_size_bytes(N, K, FP4_NVFP4, FP4_SF_SWIZZLED)};
+    if (abi_overlap(out_packed, pk, out_sf, sfo)) return FP4_ERR_INVALID_ARG;
+    for (int i = 0; i < 4; ++i)
+      if (abi_overlap(out_packed, pk, ins[i], in_bytes[i]) ||
+          abi_overlap(out_sf, sfo, ins[i], in_bytes[i]))
+        return FP4_ERR_INVALID_ARG;
+    if (bias && (abi_overlap(out_packed, pk, bias, N * 2) || abi_overlap(out_sf, sfo, bias, N * 2)))
+      return FP4_ERR_INVALID_ARG;
+  }
+  const int64_t out_bytes = fp4_out ? 0 : M * N * 2;
   const fp4_format_t fmt = mx ? FP4_MXFP4 : FP4_NVFP4;
   const int64_t sfa_bytes = fp4_sf_size_bytes(M, K, fmt, FP4_SF_SWIZZLED);
   const int64_t sfb_bytes = fp4_sf_size_bytes(N, K, fmt, FP4_SF_SWIZZLED);
@@ -63,6 +85,11 @@ fp4_status_t gemm_call(bool mx, const uint8_t* a_packed, const uint8_t* b_packed
   p.bias = static_cast<const uint16_t*>(bias);
   p.residual = static_cast<const uint16_t*>(residual);
   p.out = static_cast<uint16_t*>(out);
+  p.out_packed = out_packed;
+  p.out_sf = out_sf;
+  p.epilogue = epilogue;
+  p.out_nkt = static_cast<int>((N / 16 + 3) / 4);
+  p.rows_out = static_cast<int>(fp4_out ? (M + 127) / 128 * 128 : M);
   p.alpha = alpha;
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
@@ -76,7 +103,7 @@ fp4_status_t gemm_call(bool mx, const uint8_t* a_packed, const uint8_t* b_packed
   // (measured on the decode shapes: with up to 6 K blocks a single CTA per
   // tile holding them all in flight is faster than a split; with 24 the split
   // wins by a third)
-  if (v < 0) v = (tiles128 * 2 <= sms && num_kb > 6) ? 4 : FP4Q_GEMM_VARIANT;
+  if (v < 0) v = (tiles128 * 2 <= sms && num_kb > 6 && !fp4_out) ? 4 : FP4Q_GEMM_VARIANT;
   const int bn = (v == 1 || v == 3) ? 256 : 128;
   const bool persistent = v == 2 || v == 3;
   p.stages = !persistent ? FP4Q_GEMM_STAGES : bn == 128 ? FP4Q_GEMM_PSTAGES_128
@@ -119,8 +146,8 @@ fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packe
                                  const void* bias, const void* residual, int64_t M, int64_t N,
                                  int64_t K, void* out, int variant, int pdl,
                                  fp4q_stream_t stream) {
-  return gemm_call(false, a_packed, b_packed, sfa, sfb, alpha, bias, residual, M, N, K, out,
-                   variant, pdl, stream);
+  return gemm_call(false, kEpiPlain, a_packed, b_packed, sfa, sfb, alpha, bias, residual, M, N,
+                   K, out, nullptr, nullptr, variant, pdl, stream);
 }
 
 fp4_status_t fp4_gemm_mxfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
@@ -128,8 +155,25 @@ fp4_status_t fp4_gemm_mxfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packe
                                  const void* bias, const void* residual, int64_t M, int64_t N,
                                  int64_t K, void* out, int variant, int pdl,
                                  fp4q_stream_t stream) {
-  return gemm_call(true, a_packed, b_packed, sfa, sfb, alpha, bias, residual, M, N, K, out,
-                   variant, pdl, stream);
+  return gemm_call(true, kEpiPlain, a_packed, b_packed, sfa, sfb, alpha, bias, residual, M, N, K,
+                   out, nullptr, nullptr, variant, pdl, stream);
+}
+
+fp4_status_t fp4_gemm_nvfp4_gelu_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
+                                      const uint8_t* sfa, const uint8_t* sfb, float alpha,
+                                      const void* bias, int64_t M, int64_t N, int64_t K,
+                                      void* out, int variant, int pdl, fp4q_stream_t stream) {
+  return gemm_call(false, kEpiGelu, a_packed, b_packed, sfa, sfb, alpha, bias, nullptr, M, N, K,
+                   out, nullptr, nullptr, variant, pdl, stream);
+}
+
+fp4_status_t fp4_gemm_nvfp4_gelu_nvfp4(const uint8_t* a_packed, const uint8_t* b_packed,
+                                       const uint8_t* sfa, const uint8_t* sfb, float alpha,
+                                       const void* bias, int64_t M, int64_t N, int64_t K,
+                                       uint8_t* out_packed, uint8_t* out_sf, int variant,
+                                       int pdl, fp4q_stream_t stream) {
+  return gemm_call(false, kEpiGeluFp4, a_packed, b_packed, sfa, sfb, alpha, bias, nullptr, M, N,
+                   K, nullptr, out_packed, out_sf, variant, pdl, stream);
 }
 
 }  // extern "C"

@@ -41,7 +41,9 @@
 #include <cstdint>
 #include <mutex>
 
+#include "fp4q_device.cuh"
 #include "fp4q_launch.h"
+#include "gemm_launch.h"
 #include "tcgen05.cuh"
 
 namespace fp4q {
@@ -104,14 +106,15 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
   return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
-// Epilogue of 8 accumulator values of one output row at column n (N % 8 == 0,
-// so a group is all in or all out): alpha, bias, residual in fp32, one
-// rounding to bf16, one 16-byte store.  `bad` stores NaN.
-__device__ __forceinline__ void store8(const GemmParams& p, const float (&acc)[8], int row, int n,
-                                       bool bad) {
-  if (n >= p.N) return;
+// x * Phi(x) with the exact normal CDF (CUDA's erff).
+__device__ __forceinline__ float gelu_exact(float x) {
+  return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+}
+
+// alpha * acc + bias (fp32) for 8 columns starting at n, GELU when asked.
+__device__ __forceinline__ void epilogue_values(const GemmParams& p, const float (&acc)[8], int n,
+                                                bool bad, float (&v)[8]) {
   const float nan = __int_as_float(0x7fc00000);
-  float v[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = bad ? nan : acc[i] * p.alpha;
   if (p.bias) {
@@ -124,6 +127,20 @@ __device__ __forceinline__ void store8(const GemmParams& p, const float (&acc)[8
       v[2 * i + 1] += f.y;
     }
   }
+  if (p.epilogue != kEpiPlain) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = gelu_exact(v[i]);
+  }
+}
+
+// Epilogue of 8 accumulator values of one output row at column n (N % 8 == 0,
+// so a group is all in or all out): alpha, bias, GELU or residual in fp32,
+// one rounding to bf16, one 16-byte store.  `bad` stores NaN.
+__device__ __forceinline__ void store8(const GemmParams& p, const float (&acc)[8], int row, int n,
+                                       bool bad) {
+  if (n >= p.N) return;
+  float v[8];
+  epilogue_values(p, acc, n, bad, v);
   const size_t off = static_cast<size_t>(row) * static_cast<size_t>(p.N) + n;
   if (p.residual) {
     const uint4 rr = *reinterpret_cast<const uint4*>(p.residual + off);
@@ -143,9 +160,63 @@ __device__ __forceinline__ void store8(const GemmParams& p, const float (&acc)[8
   *reinterpret_cast<uint4*>(p.out + off) = o;
 }
 
-// 32 accumulator columns (raw fp32 bits from tensor memory) of one row.
+// FP4 output of 16 values (one NVFP4 block) of one row at column n: the
+// producer's rules (E4M3 scale of amax / 6, codes of v * rn(1/s)), codes to
+// the packed output, the scale byte to the tiled scale buffer (k padding of
+// the row's last group zeroed by the last block).  `row_valid` false writes
+// the zero scale byte of a padding row.
+__device__ __forceinline__ void store_fp4_block16(const GemmParams& p, const float (&v)[16],
+                                                  int row, int n, bool row_valid) {
+  const int kb = n >> 4;
+  uint32_t code = 0;
+  if (row_valid) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) amax = max_abs3(amax, v[i], v[i + 1]);
+    float inv_s;
+    code = e4m3_block_scale(amax, 1.0f, inv_s);
+    float q[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = inv_s > 0.0f ? v[i] * inv_s : 0.0f;
+    const uint64_t packed = static_cast<uint64_t>(e2m1_pack8(q)) |
+                            (static_cast<uint64_t>(e2m1_pack8(q + 8)) << 32);
+    st_u64(p.out_packed + static_cast<size_t>(row) * static_cast<size_t>(p.N / 2) + n / 2,
+           packed);
+  }
+  st_u8(p.out_sf + tiled_sf_offset(row, kb, p.out_nkt), code);
+  if (kb == p.N / 16 - 1)
+    for (int kk = kb + 1; kk < 4 * p.out_nkt; ++kk)
+      st_u8(p.out_sf + tiled_sf_offset(row, kk, p.out_nkt), 0u);
+}
+
+// 32 accumulator columns (raw fp32 bits from tensor memory) of one row.  Rows
+// past M (the last row tile's padding) only write zero scale bytes, and only
+// in the FP4-output epilogue.
 __device__ __forceinline__ void store_columns32(const GemmParams& p, const uint32_t (&r)[32],
                                                 int row, int n0, bool bad) {
+  if (p.epilogue == kEpiGeluFp4) {
+    const bool row_valid = row < p.M;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int n = n0 + 16 * h;
+      if (n >= p.N) break;
+      float v[16];
+      if (row_valid) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          float acc[8], out8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = __uint_as_float(r[16 * h + 8 * q + i]);
+          epilogue_values(p, acc, n + 8 * q, bad, out8);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[8 * q + i] = out8[i];
+        }
+      }
+      store_fp4_block16(p, v, row, n, row_valid);
+    }
+    return;
+  }
+  if (row >= p.M) return;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     float acc[8];
@@ -303,7 +374,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     for (int c = 0; c < BN; c += 32) {
       uint32_t r[32];
       tmem_load_32cols(lane_base + static_cast<uint32_t>(c), r);   // whole warp, unconditionally
-      if (row >= p.M) continue;
+      if (row >= p.rows_out) continue;
       store_columns32(p, r, row, n_tile * BN + c, bad);
     }
   } else {
@@ -541,12 +612,12 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
         for (int c = 0; c < BN; c += 32) {
           uint32_t r[32];
           tmem_load_32cols(tmem + lane_off + static_cast<uint32_t>(a * BN + c), r);
-          if (row < p.M) store_columns32(p, r, row, n_tile * BN + c, bad);
+          if (row < p.rows_out) store_columns32(p, r, row, n_tile * BN + c, bad);
         }
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[a]);
-      } else if (row < p.M) {
+      } else if (row < p.rows_out) {
         uint32_t r[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) r[c] = 0;
@@ -637,7 +708,14 @@ struct Prep {
   uint32_t cluster_tested = 0;
 };
 
-using PrepTable = Prep[64][9];   // per device, per ring depth; one table per kernel instance
+// One table per kernel instance: an entry per device and ring depth, and the
+// largest dynamic shared-memory limit set on the instance per device (the
+// limit is a property of the kernel, so it is only ever raised: lowering it
+// for a shallower ring would break a deeper one prepared earlier).
+struct PrepTable {
+  Prep entry[64][9];
+  size_t attr[64] = {};
+};
 
 std::mutex& prep_mutex() {
   static std::mutex mu;
@@ -652,17 +730,20 @@ cudaError_t prepare(PrepTable& table, Kernel kernel, int threads, size_t smem_ne
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || stages < 0 || stages > 8) return cudaErrorInvalidValue;
   std::lock_guard<std::mutex> lock(prep_mutex());
-  Prep& pr = table[dev][stages];
+  Prep& pr = table.entry[dev][stages];
   *out = &pr;
   if (pr.smem != 0 || pr.err != cudaSuccess) return pr.err;
   size_t smem = smem_need;
   const int max_ctas = static_cast<int>(512 / tmem_cols);
   int per_sm = 0;
   for (int attempt = 0; attempt < 2; ++attempt) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+    if (smem > table.attr[dev]) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+      if (e != cudaSuccess) break;
+      table.attr[dev] = smem;
+    }
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
     if (e != cudaSuccess) break;
     if (per_sm <= max_ctas) break;
     smem = (228 * 1024) / (max_ctas + 1) + 1;

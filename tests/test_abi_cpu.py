@@ -39,7 +39,7 @@ def test_header_declares_the_boundary():
     for want in ("fp4_add_rmsnorm_quant", "fp4_add_rmsnorm_quant_gs", "fp4_quantize",
                  "fp4_dequant", "fp4_sf_size_bytes", "fp4_launch_shape",
                  "fp4_status_string", "fp4_last_cuda_error", "fp4_gemm_nvfp4_bf16",
-                 "fp4_gemm_mxfp4_bf16"):
+                 "fp4_gemm_mxfp4_bf16", "fp4_gemm_nvfp4_gelu_bf16", "fp4_gemm_nvfp4_gelu_nvfp4"):
         assert want in names
 
 
@@ -236,4 +236,23 @@ def test_gemm_mxfp4_validation(L, kwargs, status):
     st = fq.fp4_gemm_mxfp4_bf16(a["a"], a["b"], a["sfa"], a["sfb"], a["alpha"], a["bias"],
                                 a["residual"], a["M"], a["N"], a["K"], a["out"], a["variant"],
                                 a["pdl"], 0)
+    assert st == status
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(variant=4), 1),                 # split K cannot quantize 16-wide blocks
+    (dict(N=264), 2),                     # N not a multiple of 16
+    (dict(p=0), 1), (dict(s=0), 1),
+    (dict(p=A + 64), 1),                  # packed output over A
+    (dict(s=P + 128), 1),                 # scales over the packed output
+    (dict(p=P + 8), 3),
+    (dict(M=0, a=0, p=0, s=0), 0),
+])
+def test_gemm_gelu_nvfp4_validation(L, kwargs, status):
+    a = dict(a=A, b=B, sfa=S, sfb=S2, alpha=1.0, bias=0, M=256, N=256, K=512, p=P,
+             s=G_OUT, variant=-1, pdl=0)
+    a.update(kwargs)
+    st = fq.fp4_gemm_nvfp4_gelu_nvfp4(a["a"], a["b"], a["sfa"], a["sfb"], a["alpha"], a["bias"],
+                                      a["M"], a["N"], a["K"], a["p"], a["s"], a["variant"],
+                                      a["pdl"], 0)
     assert st == status

@@ -239,3 +239,83 @@ def test_gemm_consumes_the_mxfp4_producer():
     assert np.array_equal(pb.cpu().numpy(), ob.packed)
     assert np.array_equal(sb.cpu().numpy(), ob.sf_swizzled)
     check(got, g, K, "random")
+
+
+# ---------------------------------------------------------------------------
+# GELU epilogues
+# ---------------------------------------------------------------------------
+import parity  # noqa: E402
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (41, 4608, 1536), (300, 520, 768)])
+@pytest.mark.parametrize("variant", [0, 1, 4])
+def test_gemm_gelu_bf16(M, N, K, variant):
+    """GELU(alpha * product + bias) in bf16.  Exact-kind operands make the
+    GELU argument exact; the GPU's erff-based GELU and one bf16 rounding keep
+    every output within one bf16 step of the exact value."""
+    a, b, sfa, sfb = operands(M, N, K, seed=11 * M + N, kind="exact")
+    bias = bf16_values(N, 13, 4, (N,))
+    got = fq.gemm_nvfp4_gelu(a.cuda(), b.cuda(), sfa.cuda(), sfb.cuda(), alpha=0.125,
+                             bias=bias.cuda(), variant=variant)
+    torch.cuda.synchronize()
+    g = oracle_gemm(a, b, sfa, sfb, M, N, K, alpha=0.125, bias=bias.float().numpy(),
+                    gelu_act=True)
+    got64 = got.float().cpu().numpy().astype(np.float64)
+    err = np.abs(got64 - g.exact)
+    tol = 2.0 ** -8 * np.abs(g.exact) + 2.0 ** -20
+    assert np.all(err <= tol), f"{(err > tol).sum()} outputs off, first {np.argwhere(err > tol)[:4]}"
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (300, 528, 768), (41, 4608, 1536)])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+def test_gemm_gelu_nvfp4_output(M, N, K, variant):
+    """The FP4-output epilogue against the oracle's quantization of the same
+    GELU values, with the producer's acceptance rule (codes and scale bytes
+    exact except within 1e-5 of a rounding boundary; tiled padding zero).  N =
+    528 leaves a partial last group of four scales (k padding), M = 300 and 41
+    leave padding rows."""
+    a, b, sfa, sfb = operands(M, N, K, seed=17 * M + N, kind="exact")
+    bias = bf16_values(N, 19, 4, (N,))
+    outs = fq.gemm_nvfp4_gelu(a.cuda(), b.cuda(), sfa.cuda(), sfb.cuda(), alpha=0.25,
+                              bias=bias.cuda(), out_format="nvfp4", variant=variant)
+    torch.cuda.synchronize()
+    o = oracle.gemm_gelu_nvfp4(a.numpy(), b.numpy(), sfa.numpy(), sfb.numpy(), M, N, K,
+                               alpha=0.25, bias=bias.float().numpy())
+    g = parity.fetch(outs, None, "swizzled", None, M=M)
+    parity.compare(g, o, "nvfp4", "swizzled", "bf16", M, N)
+
+
+def test_gemm_gelu_nvfp4_feeds_the_next_gemm():
+    """Two chained projections: the first emits NVFP4 + tiled scales, the
+    second consumes them as its A operand (PDL), against the oracle's chain."""
+    M, N1, N2, K = 192, 512, 256, 1024
+    a, b1, sfa, sfb1 = operands(M, N1, K, seed=23, kind="exact")
+    _, b2, _, sfb2 = operands(N2, N2, N1, seed=29, kind="random")
+    b2 = b2[:N2]
+    pk, sf = fq.gemm_nvfp4_gelu(a.cuda(), b1.cuda(), sfa.cuda(), sfb1.cuda(), alpha=0.25,
+                                out_format="nvfp4")
+    got = fq.gemm_nvfp4_bf16(pk, b2.cuda(), sf, sfb2.cuda(), pdl=True)
+    torch.cuda.synchronize()
+    o1 = oracle.gemm_gelu_nvfp4(a.numpy(), b1.numpy(), sfa.numpy(), sfb1.numpy(), M, N1, K,
+                                alpha=0.25)
+    assert np.array_equal(pk.cpu().numpy(), o1.packed), "first projection's codes differ"
+    assert np.array_equal(sf.cpu().numpy(), o1.sf_swizzled), "first projection's scales differ"
+    g2 = oracle.gemm_bf16(o1.packed, b2.numpy(), o1.sf_swizzled, sfb2.numpy(), M, N2, N1)
+    check(got, g2, N1, "random")
+
+
+def test_gemm_gelu_nvfp4_rejects_split_k():
+    a, b, sfa, sfb = operands(128, 128, 256, 1, "exact")
+    with pytest.raises(fq.Fp4Error):
+        fq.gemm_nvfp4_gelu(a.cuda(), b.cuda(), sfa.cuda(), sfb.cuda(), out_format="nvfp4",
+                           variant=4)
+
+
+def test_gemm_alternating_ring_depths():
+    """A launch needing a deep ring (41 x 4608 x 1536: one wave, six stages),
+    then a shallow one, then the deep one again: the kernel's shared-memory
+    limit must not have been lowered in between."""
+    for (M, N, K) in [(41, 4608, 1536), (300, 520, 768), (41, 4608, 1536), (8, 16, 256)]:
+        a, b, sfa, sfb = operands(M, N, K, seed=M + K, kind="exact")
+        got = gpu_gemm(a, b, sfa, sfb, variant=0)
+        check(got, oracle_gemm(a, b, sfa, sfb, M, N, K), K, "exact")

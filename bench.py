@@ -320,11 +320,60 @@ def run_ours(args, wl):
             if st != 0:
                 raise fq.Fp4Error(st, "fp4_add_rmsnorm_quant")
 
+    # Workloads smaller than twice the L2 (C1, C2, short batches): rotate
+    # through enough copies of the inputs and outputs that one pass touches
+    # more than twice the L2, and replay the pass as a CUDA graph, so neither
+    # warm caches nor host launch cost enter the number.  Each copy is called
+    # with x and then -x in a pass, so its residual returns to where it was.
+    alg_step = wl.algorithmic_bytes(args.op) + (2 * M * H if args.y_out and args.op == "fused"
+                                                else 0)
+    rot = 1 if alg_step >= 2 * L2_BYTES else min(256, -(-2 * L2_BYTES // alg_step))
+    graph = None
+    if rot > 1:
+        copies = []
+        for _ in range(rot):
+            c = {"x": x.clone(), "xn": xneg.clone(), "r": r.clone(), "p": torch.empty_like(packed),
+                 "s": torch.empty_like(sf),
+                 "s2": torch.empty_like(sf_rm) if sf_rm is not None else None,
+                 "y": torch.empty(M, H, dtype=x.dtype, device=dev) if args.y_out else None}
+            copies.append(c)
+
+        def step_copy(c, xs):
+            s2p = c["s2"].data_ptr() if c["s2"] is not None else None
+            if args.op == "quantize":
+                st = L.fp4_quantize(xs.data_ptr(), gp, M, H, dt, fmt, lay, c["p"].data_ptr(),
+                                    c["s"].data_ptr(), s2p, sh)
+            else:
+                st = L.fp4_add_rmsnorm_quant_ex(
+                    xs.data_ptr(), H, c["r"].data_ptr(), H, wp, gp, eps, M, H, dt, fmt, lay,
+                    c["p"].data_ptr(), c["s"].data_ptr(), s2p,
+                    c["y"].data_ptr() if c["y"] is not None else None, sh)
+            if st != 0:
+                raise fq.Fp4Error(st, "graph step")
+
+        def one_pass():
+            for c in copies:
+                step_copy(c, c["x"])
+            for c in copies:
+                step_copy(c, c["xn"])
+
+        with torch.cuda.stream(stream):
+            one_pass()
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                one_pass()
+
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(gpu_smi_id(torch, dev)) if rank == 0 else None
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            step(i)
+            if graph is None:
+                step(i)
+        if graph is not None:
+            for _ in range(3):
+                graph.replay()
     stream.synchronize()
 
     # Timed region: K steps back to back on one stream between two events.  A
@@ -332,7 +381,7 @@ def run_ours(args, wl):
     # duration is the region's time / K (per-launch events would add their own
     # gaps between launches).  Per-launch event pairs are taken afterwards on
     # a short separate loop for the spread.
-    K = args.steps
+    K = args.steps if graph is None else -(-args.steps // (2 * rot)) * 2 * rot
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -341,8 +390,12 @@ def run_ours(args, wl):
     wall0 = time.time()
     with torch.cuda.stream(stream):
         t_start.record(stream)
-        for i in range(K):
-            step(i)
+        if graph is None:
+            for i in range(K):
+                step(i)
+        else:
+            for _ in range(K // (2 * rot)):
+                graph.replay()
         t_end.record(stream)
     stream.synchronize()
     torch.cuda.synchronize(dev)
@@ -482,8 +535,13 @@ def run_ours(args, wl):
                        "sf_layout": wl.sf_layout, "io_dtype": wl.dtype, "eps": wl.eps,
                        "algorithmic_bytes_per_step": alg,
                        "l2": ("inputs larger than L2 (%.0f MB per step vs 129 MB), no flush"
-                              % (alg / 1e6)) if alg > L2_BYTES else
-                             "inputs smaller than L2: numbers are L2-assisted",
+                              % (alg / 1e6)) if rot == 1 else
+                             ("%d input/output copies rotated (%.0f MB per pass vs 129 MB L2%s), "
+                              "one pass of %d calls captured as a CUDA graph and replayed"
+                              % (rot, 2 * rot * alg / 1e6,
+                                 "" if 2 * rot * alg >= 2 * L2_BYTES else
+                                 "; fewer bytes than L2: the number is L2-assisted",
+                                 2 * rot)),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "rows_per_s": round(world * M * K / (total_ms * 1e-3), 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,

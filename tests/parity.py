@@ -74,12 +74,12 @@ def run_gpu(x, r, w, eps, fmt, layout, rows=None, stream=None, global_scale=None
     return fetch(outs, r, layout, rows)
 
 
-def run_quantize(x, fmt, layout, global_scale=None):
+def run_quantize(x, fmt, layout, global_scale=None, rows=None):
     gs = None if global_scale is None else torch.tensor([global_scale], dtype=torch.float32,
                                                          device=x.device)
     outs = fq.quantize_fp4(x, fmt=fmt, sf_layout=layout, global_scale=gs)
     torch.cuda.synchronize()
-    return fetch(outs, None, layout, None, M=x.shape[0])
+    return fetch(outs, None, layout, rows, M=x.shape[0])
 
 
 def fetch(outs, r, layout, rows=None, M=None):

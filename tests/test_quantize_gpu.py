@@ -21,7 +21,7 @@ def _lib():
 
 
 @pytest.mark.parametrize("M,H", [(1, 32), (3, 80), (130, 208), (1000, 1536), (257, 5120),
-                                 (64, 17408), (5, 65536)])
+                                 (41, 7168), (129, 8224), (64, 17408), (5, 65536)])
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "e4m3b32"])
 @pytest.mark.parametrize("layout", ["rowmajor", "swizzled", "both"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
@@ -58,3 +58,29 @@ def test_quantize_three_d_and_empty():
     e = torch.empty(0, 256, device="cuda", dtype=torch.float16)
     p, s = fq.quantize_fp4(e, fmt="mxfp4", sf_layout="swizzled")
     assert p.numel() == 0 and s.numel() == 0
+
+
+def _sample_rows(M, seed, n=96):
+    fixed = {0, 1, 31, 32, 127, 128, 129, M // 2, M - 129, M - 128, M - 2, M - 1}
+    rng = np.random.default_rng(seed)
+    rand = set(rng.choice(M, size=min(n, M), replace=False).tolist())
+    return np.array(sorted(r for r in fixed | rand if 0 <= r < M), dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", ["C3_M8192_H7168_bf16_mxfp4_swizzled_outliers",
+                                  "C4_M16384_H5120_fp16_nvfp4_both",
+                                  "C5_M32768_H1536_bf16_nvfp4_swizzled",
+                                  "C5_M32768_H6144_bf16_nvfp4_swizzled",
+                                  "C5_M32768_H17408_bf16_mxfp4_swizzled",
+                                  "C5_M32768_H32768_bf16_nvfp4_swizzled"])
+def test_quantize_full_size_sampled(name):
+    """The benchmarked quantize shapes at full size, in the launch the
+    benchmark times: sampled rows (tile edges, first/last, seeded random)
+    against the oracle, every padding byte of the tiled buffer checked."""
+    wl = workloads.CONFIGS[name]
+    x = workloads.make_inputs(wl, "cuda")[0]
+    rows = _sample_rows(wl.M, wl.seed)
+    xs = x.index_select(0, torch.from_numpy(rows).cuda()).float().cpu().numpy()
+    g = parity.run_quantize(x, wl.fmt, wl.sf_layout, rows=rows)
+    o = oracle.quantize(xs, wl.fmt, wl.sf_layout)
+    parity.compare(g, o, wl.fmt, wl.sf_layout, wl.dtype, wl.M, wl.H)

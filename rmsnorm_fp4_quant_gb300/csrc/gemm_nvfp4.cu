@@ -19,12 +19,18 @@
 //                      arriving once per stage (two threads issue a stage's
 //                      copies in about half the time one takes: 4 % on a
 //                      large product).
-//   warp 1, one lane   MMA issuer.  Copies the stage's eight scale tiles into
-//                      tensor memory (tcgen05.cp 32x128b, repeated over the four
-//                      lane quarters: a 512-byte tile is exactly the image of
-//                      128 rows x 4 scales the block-scaled MMA reads), issues
-//                      four K = 64 MMAs of kind mxf4nvf4 with one E4M3 scale per
-//                      16 elements, and commits the stage back (empty[s]).
+//   warp 3, one lane   scale mover.  Copies the stage's eight scale tiles into
+//                      the stage's tensor-memory slot (tcgen05.cp 32x128b,
+//                      repeated over the four lane quarters: a 512-byte tile is
+//                      exactly the image of 128 rows x 4 scales the
+//                      block-scaled MMA reads) and commits them to sf_ready[s],
+//                      so the copies of stage s + 1 run while stage s
+//                      multiplies (8 % on a large product against issuing them
+//                      from the MMA thread).
+//   warp 1, one lane   MMA issuer.  Once the stage's scales are in tensor
+//                      memory, issues four K = 64 MMAs of kind mxf4nvf4 with
+//                      one E4M3 scale per 16 elements, and commits the stage
+//                      back (empty[s]).
 //   all four warps     epilogue.  Warp w owns accumulator lanes 32w..32w+31 (one
 //                      output row per thread): 32 columns at a time from tensor
 //                      memory, alpha, bias and residual in fp32, one rounding to
@@ -97,8 +103,8 @@ struct Cfg {
   }
   static constexpr size_t smem_bytes(int stages) {
     // 1 KiB of alignment slack (the 128-byte swizzle wants 1 KiB-aligned
-    // tiles), the ring, 2S + 1 mbarriers, the tensor-memory address, a flag
-    return 1024 + static_cast<size_t>(stages) * kStageBytes + (2 * stages + 1) * 8 + 8;
+    // tiles), the ring, 3S + 2 mbarriers, the tensor-memory address, a flag
+    return 1024 + static_cast<size_t>(stages) * kStageBytes + (3 * stages + 2) * 8 + 8;
   }
 };
 
@@ -255,7 +261,9 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
   uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + static_cast<size_t>(S) * C::kSfBytesB);
   uint64_t* empty = full + S;
   uint64_t* accum = empty + S;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  uint64_t* sf_ready = accum + 1;     // the stage's scales are in tensor memory
+  uint64_t* sf_done = sf_ready + S;   // every scale copy has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_done + 1);
   volatile int* failed = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -271,7 +279,9 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 2);   // one arrival per producer
       mbar_init(&empty[s], 1);
+      mbar_init(&sf_ready[s], 1);
     }
+    mbar_init(sf_done, 1);
     mbar_init(accum, 1);
     *failed = 0;
     mbar_init_fence();
@@ -332,7 +342,10 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     // ---- MMA issuer ----
     for (int i = 0; i < kb1 - kb0; ++i) {
       const int s = i % S;
-      if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((i / S) & 1))) {
+      // the scale mover waited for full[s] before its copies; waiting for it
+      // here too (already complete) orders the TMA writes before the MMAs
+      if (!mbar_wait_bounded(&sf_ready[s], static_cast<uint32_t>((i / S) & 1)) ||
+          !mbar_wait_bounded(&full[s], static_cast<uint32_t>((i / S) & 1))) {
         *failed = 1;
         break;
       }
@@ -341,6 +354,31 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const uint32_t sfb_t = sfa_t + C::kSfColsA;
       const uint32_t a_s = smem_addr(sA + static_cast<size_t>(s) * kTileBytesA);
       const uint32_t b_s = smem_addr(sB + static_cast<size_t>(s) * C::kTileBytesB);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        // K-major, 128-byte swizzle: 8-row groups 1024 bytes apart; the K step
+        // advances the start address inside the swizzle row
+        const uint64_t adesc = smem_desc(a_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
+        const uint64_t bdesc = smem_desc(b_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
+        mma_fp4_block_scaled<MX>(tmem, adesc, bdesc, C::idesc(j), sfa_t + 4 * C::atom(j),
+                                 sfb_t + 4 * C::kSfTilesB * C::atom(j), (i | j) != 0 ? 1u : 0u);
+      }
+      tc_commit(&empty[s]);   // the stage is free once these MMAs have read it
+    }
+    tc_commit(accum);         // every MMA issued above has completed
+  } else if (warp == 3 && lane == 0) {
+    // ---- scale mover ----
+    // Slot s is free for stage i: full[s] of stage i means the producers
+    // refilled the stage, which waited for the MMAs of stage i - S.
+    for (int i = 0; i < kb1 - kb0; ++i) {
+      const int s = i % S;
+      if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((i / S) & 1))) {
+        *failed = 1;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t sfa_t = tmem + C::kAccCols + static_cast<uint32_t>(s) * C::kSfColsPerStage;
+      const uint32_t sfb_t = sfa_t + C::kSfColsA;
       const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(s) * C::kSfBytesA);
       const uint32_t sfb_s = smem_addr(sSFB + static_cast<size_t>(s) * C::kSfBytesB);
 #pragma unroll
@@ -355,18 +393,10 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                smem_desc(sfb_s + t * C::kSfBytesA + q * kSfTileBytes, 0, 128,
                                          kSwizzleNone));
       }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        // K-major, 128-byte swizzle: 8-row groups 1024 bytes apart; the K step
-        // advances the start address inside the swizzle row
-        const uint64_t adesc = smem_desc(a_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
-        const uint64_t bdesc = smem_desc(b_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
-        mma_fp4_block_scaled<MX>(tmem, adesc, bdesc, C::idesc(j), sfa_t + 4 * C::atom(j),
-                                 sfb_t + 4 * C::kSfTilesB * C::atom(j), (i | j) != 0 ? 1u : 0u);
-      }
-      tc_commit(&empty[s]);   // the stage is free once these MMAs have read it
+      tc_commit(&sf_ready[s]);
     }
-    tc_commit(accum);         // every MMA issued above has completed
+    tc_commit(sf_done);       // no copy may still be running when tensor memory is freed
+    mbar_wait_bounded(sf_done, 0);
   }
   __syncthreads();            // roles done; a failure flag is visible to all
 

@@ -466,32 +466,36 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
 // Persistent form: one CTA per SM walks the output tiles t = blockIdx.x,
 // blockIdx.x + gridDim.x, ... (row tile t / n_tiles, column tile t % n_tiles,
-// so CTAs running together share A's row panel).  Six warps:
-//   warp 0, one lane  producer: one continuous stream of K blocks over all its
-//                     tiles through the S-stage ring (never drains between tiles);
+// so CTAs running together share A's row panel).  Eight warps:
+//   warps 0 and 6,    producers (A and its scales / B and its scales): one
+//   one lane each     continuous stream of K blocks over all the CTA's tiles
+//                     through the S-stage ring (never drains between tiles);
 //   warp 1            tensor-memory allocation; one lane issues the MMAs;
-//   warps 2..5        epilogue, lane quarter = warp % 4.
+//   warps 2..5        epilogue, lane quarter = warp % 4;
+//   warp 7, one lane  scale mover: each stage's scale tiles into that stage's
+//                     tensor-memory slot, committed to sf_ready[s].
 // NACC accumulators in tensor memory (2 for 128-wide tiles, 1 for 256): the
 // MMAs of the next tile start as soon as the epilogue has read the previous
-// tile's accumulator out (acc_empty), so loads, MMAs and stores overlap.  The
-// scale tiles use one tensor-memory slot for every stage: tcgen05.cp and
-// tcgen05.mma issued by one thread execute in order, so a copy never
-// overtakes an MMA still reading the slot.
+// tile's accumulator out (acc_empty), so loads, MMAs and stores overlap.
+// (Splitting the producer and moving the scale copies off the MMA thread took
+// the 128-wide form from 404 to 318 us and the 256-wide from 287-308 to 265 us
+// on an 8192 x 7168 x 7168 product; the one-tile-per-CTA kernel above, two
+// CTAs per SM, stays faster there.)
 template <int BN>
 struct PCfg {
   static constexpr int kAcc = BN == 128 ? 2 : 1;
-  static constexpr uint32_t kSfCol = kAcc * BN;     // the scale slot after the accumulators
-  static constexpr uint32_t tmem_cols() {
-    return (kSfCol + Cfg<BN>::kSfColsPerStage) <= 256 ? 256u : 512u;
+  static constexpr uint32_t kSfCol = kAcc * BN;     // the scale slots after the accumulators
+  static constexpr uint32_t tmem_cols(int stages) {
+    return (kSfCol + Cfg<BN>::kSfColsPerStage * stages) <= 256 ? 256u : 512u;
   }
   static constexpr size_t smem_bytes(int stages) {
     return 1024 + static_cast<size_t>(stages) * Cfg<BN>::kStageBytes +
-           (2 * stages + 2 * kAcc + 1) * 8 + 8;
+           (3 * stages + 2 * kAcc + 2) * 8 + 8;
   }
 };
 
 template <int BN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(256, 1)
 gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
                              const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
   using C = Cfg<BN>;
@@ -509,7 +513,9 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
   uint64_t* acc_full = empty + S;
   uint64_t* acc_empty = acc_full + P::kAcc;
   uint64_t* mma_done = acc_empty + P::kAcc;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* sf_ready = mma_done + 1;
+  uint64_t* sf_done = sf_ready + S;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_done + 1);
   volatile int* failed = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -521,9 +527,11 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 2);
       mbar_init(&empty[s], 1);
+      mbar_init(&sf_ready[s], 1);
     }
+    mbar_init(sf_done, 1);
     for (int a = 0; a < P::kAcc; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], 4);   // one arrival per epilogue warp
@@ -541,8 +549,9 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
-    // ---- producer ----
+  if ((warp == 0 || warp == 6) && lane == 0) {
+    // ---- producers: warp 0 A and its scales, warp 6 B and its scales ----
+    const bool load_a = warp == 0;
     const int b_tiles_total = (p.N + 127) / 128;
     int it = 0;   // K blocks issued over all tiles
     bool ok = true;
@@ -553,8 +562,9 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const int b_tile0 = n_tile * C::kSfTilesB;
       const int b_tiles = b_tiles_total - b_tile0 < C::kSfTilesB ? b_tiles_total - b_tile0
                                                                   : C::kSfTilesB;
-      const uint32_t stage_bytes = kTileBytesA + C::kTileBytesB + C::kSfBytesA +
-                                   static_cast<uint32_t>(b_tiles) * C::kSfBytesA;
+      const uint32_t stage_bytes =
+          load_a ? kTileBytesA + C::kSfBytesA
+                 : C::kTileBytesB + static_cast<uint32_t>(b_tiles) * C::kSfBytesA;
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
         const int s = it % S;
         if (it >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((it / S - 1) & 1))) {
@@ -563,17 +573,20 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
           break;
         }
         mbar_arrive_expect_tx(&full[s], stage_bytes);
-        tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes,
-                    m_tile * kBM, &full[s]);
-        tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
-                    n_tile * BN, &full[s]);
-        bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA,
-                 sfa_k + static_cast<size_t>(kb) * C::kSfBytesA, C::kSfBytesA, &full[s]);
-        for (int q = 0; q < b_tiles; ++q)
-          bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + q * C::kSfBytesA,
-                   p.sfb + static_cast<size_t>(b_tile0 + q) * p.nkt * kSfTileBytes +
-                       static_cast<size_t>(kb) * C::kSfBytesA,
-                   C::kSfBytesA, &full[s]);
+        if (load_a) {
+          tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes,
+                      m_tile * kBM, &full[s]);
+          bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA,
+                   sfa_k + static_cast<size_t>(kb) * C::kSfBytesA, C::kSfBytesA, &full[s]);
+        } else {
+          tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
+                      n_tile * BN, &full[s]);
+          for (int q = 0; q < b_tiles; ++q)
+            bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + q * C::kSfBytesA,
+                     p.sfb + static_cast<size_t>(b_tile0 + q) * p.nkt * kSfTileBytes +
+                         static_cast<size_t>(kb) * C::kSfBytesA,
+                     C::kSfBytesA, &full[s]);
+        }
       }
     }
     if (!ok) {   // gave up: let the copies already issued land first
@@ -582,8 +595,6 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
-    const uint32_t sfa_t = tmem + P::kSfCol;
-    const uint32_t sfb_t = sfa_t + C::kSfColsA;
     int it = 0;
     bool ok = true;
     for (int i = 0; i < my_tiles && ok; ++i) {
@@ -597,26 +608,17 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const uint32_t d_t = tmem + static_cast<uint32_t>(a * BN);
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
         const int s = it % S;
-        if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((it / S) & 1))) {
+        if (!mbar_wait_bounded(&sf_ready[s], static_cast<uint32_t>((it / S) & 1)) ||
+            !mbar_wait_bounded(&full[s], static_cast<uint32_t>((it / S) & 1))) {
           *failed = 1;
           ok = false;
           break;
         }
         tc_fence_after_sync();
+        const uint32_t sfa_t = tmem + P::kSfCol + static_cast<uint32_t>(s) * C::kSfColsPerStage;
+        const uint32_t sfb_t = sfa_t + C::kSfColsA;
         const uint32_t a_s = smem_addr(sA + static_cast<size_t>(s) * kTileBytesA);
         const uint32_t b_s = smem_addr(sB + static_cast<size_t>(s) * C::kTileBytesB);
-        const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(s) * C::kSfBytesA);
-        const uint32_t sfb_s = smem_addr(sSFB + static_cast<size_t>(s) * C::kSfBytesB);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          tmem_copy_32x128b_x4(sfa_t + 4 * j,
-                               smem_desc(sfa_s + j * kSfTileBytes, 0, 128, kSwizzleNone));
-#pragma unroll
-          for (int q = 0; q < C::kSfTilesB; ++q)
-            tmem_copy_32x128b_x4(sfb_t + 4 * (C::kSfTilesB * j + q),
-                                 smem_desc(sfb_s + q * C::kSfBytesA + j * kSfTileBytes, 0, 128,
-                                           kSwizzleNone));
-        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint64_t adesc = smem_desc(a_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
@@ -631,7 +633,35 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
     // tensor memory is freed below only after every MMA issued here has completed
     tc_commit(mma_done);
     mbar_wait_bounded(mma_done, 0);
-  } else if (warp >= 2) {
+  } else if (warp == 7 && lane == 0) {
+    // ---- scale mover: stage it's scales into its tensor-memory slot ----
+    const int total = my_tiles * p.num_kb;
+    for (int it = 0; it < total; ++it) {
+      const int s = it % S;
+      if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((it / S) & 1))) {
+        *failed = 1;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t sfa_t = tmem + P::kSfCol + static_cast<uint32_t>(s) * C::kSfColsPerStage;
+      const uint32_t sfb_t = sfa_t + C::kSfColsA;
+      const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(s) * C::kSfBytesA);
+      const uint32_t sfb_s = smem_addr(sSFB + static_cast<size_t>(s) * C::kSfBytesB);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        tmem_copy_32x128b_x4(sfa_t + 4 * j,
+                             smem_desc(sfa_s + j * kSfTileBytes, 0, 128, kSwizzleNone));
+#pragma unroll
+        for (int q = 0; q < C::kSfTilesB; ++q)
+          tmem_copy_32x128b_x4(sfb_t + 4 * (C::kSfTilesB * j + q),
+                               smem_desc(sfb_s + q * C::kSfBytesA + j * kSfTileBytes, 0, 128,
+                                         kSwizzleNone));
+      }
+      tc_commit(&sf_ready[s]);
+    }
+    tc_commit(sf_done);
+    mbar_wait_bounded(sf_done, 0);
+  } else if (warp >= 2 && warp <= 5) {
     // ---- epilogue ----
     const int quarter = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -877,12 +907,15 @@ int sm_count() {
 template <int BN>
 cudaError_t launch_persistent(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
                               cudaStream_t stream) {
+  using C = Cfg<BN>;
   using P = PCfg<BN>;
   auto kernel = gemm_nvfp4_persistent_kernel<BN>;
   CUtensorMap ta, tb;
   if (!operand_map(&ta, a, p.M, p.K / 2, kBM) || !operand_map(&tb, b, p.N, p.K / 2, BN))
     return cudaErrorInvalidValue;
-  p.tmem_cols = P::tmem_cols();
+  if (P::kSfCol + C::kSfColsPerStage * static_cast<uint32_t>(p.stages) > 512)
+    return cudaErrorInvalidValue;   // accumulators and scale slots must fit tensor memory
+  p.tmem_cols = P::tmem_cols(p.stages);
   p.nkt = p.K / 64;
   p.num_kb = p.K / (2 * kBKBytes);
   const size_t smem_need = P::smem_bytes(p.stages);
@@ -890,14 +923,14 @@ cudaError_t launch_persistent(const uint8_t* a, const uint8_t* b, GemmParams p, 
   static PrepTable table;
   Prep* pr = nullptr;
   // one CTA per SM: it takes all 512 tensor-memory columns
-  cudaError_t e = prepare(table, kernel, 192, smem_need, p.tmem_cols, p.stages, &pr);
+  cudaError_t e = prepare(table, kernel, 256, smem_need, p.tmem_cols, p.stages, &pr);
   if (e != cudaSuccess) return e;
   const int sms = sm_count();
   if (sms < 1) return cudaErrorInvalidDevice;
   const int64_t tiles = static_cast<int64_t>((p.N + BN - 1) / BN) * ((p.M + kBM - 1) / kBM);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(tiles < sms ? tiles : sms), 1, 1);
-  cfg.blockDim = dim3(192, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = pr->smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -222,9 +222,13 @@ FP4Q_API fp4_status_t fp4_launch_shape(int64_t M, int64_t H, fp4_dtype_t dtype, 
  *   pdl       nonzero: launched as a programmatic dependent of the previous
  *             kernel on `stream`, so its prologue overlaps that kernel's tail
  *             (it waits for that kernel's results before reading anything).
- * K must be a multiple of 256 and N of 8; every pointer 16-byte aligned; out
- * must not overlap the inputs (except residual == out).  A tile whose inputs
- * never arrive (a bounded wait runs out) is written as NaN.
+ * K must be a multiple of 32 (a packed row a whole number of 16-byte units;
+ * the FlashRT contract's K % 16 otherwise) and N of 8; every pointer 16-byte
+ * aligned; out must not overlap the inputs (except residual == out).  When K
+ * is not a multiple of 64, the last K = 64 step reads the k-padding scales of
+ * the tiled layout against zero codes: they must be finite (this library's
+ * producers write them as 0).  A tile whose inputs never arrive (a bounded
+ * wait runs out) is written as NaN.
  */
 FP4Q_API fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
                                           const uint8_t* sfa, const uint8_t* sfb, float alpha,

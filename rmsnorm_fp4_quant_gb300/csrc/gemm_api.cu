@@ -40,7 +40,7 @@ fp4_status_t gemm_call(bool mx, int epilogue, const uint8_t* a_packed, const uin
   if (variant < -1 || variant > 4) return FP4_ERR_INVALID_ARG;
   if (mx && (variant == 2 || variant == 3)) return FP4_ERR_INVALID_ARG;   // NVFP4 only
   if (fp4_out && variant == 4) return FP4_ERR_INVALID_ARG;   // split K stores 8-column groups
-  if (K % 256 != 0 || N % (fp4_out ? 16 : 8) != 0) return FP4_ERR_UNSUPPORTED_SHAPE;
+  if (K % 32 != 0 || N % (fp4_out ? 16 : 8) != 0) return FP4_ERR_UNSUPPORTED_SHAPE;
   if (M > INT32_MAX - 128 || N > INT32_MAX - 128 || K > INT32_MAX / 2)
     return FP4_ERR_UNSUPPORTED_SHAPE;
   if (M == 0 || N == 0) return FP4_OK;
@@ -98,7 +98,7 @@ fp4_status_t gemm_call(bool mx, int epilogue, const uint8_t* a_packed, const uin
   // loop of each tile over a cluster of CTAs so that most SMs take part
   const int sms = sm_count_current_device();
   const int64_t tiles128 = ((N + 127) / 128) * ((M + 127) / 128);
-  const int num_kb = static_cast<int>(K / 256);
+  const int num_kb = static_cast<int>((K + 255) / 256);
   int v = variant;
   // (measured on the decode shapes: with up to 6 K blocks a single CTA per
   // tile holding them all in flight is faster than a split; with 24 the split

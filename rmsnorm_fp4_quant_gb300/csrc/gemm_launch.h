@@ -24,14 +24,17 @@ struct GemmParams {
   int rows_out;                // rows the epilogue visits: M, or 128 * ceil(M / 128) (kEpiGeluFp4)
   float alpha;
   int M, N, K;
-  int nkt;                     // 128x4 scale tiles per 128 rows: K / 64 (NVFP4), K / 128 (MXFP4)
-  int num_kb;                  // K / 256: K blocks
+  int nkt;                     // 128x4 scale tiles per 128 rows: ceil(K / 64) (NVFP4),
+                               // ceil(K / 128) (MXFP4)
+  int num_kb;                  // ceil(K / 256): K blocks, the last one possibly ragged
+  int mma_last;                // K = 64 MMAs in the last K block (1..4)
+  int sf_tiles_last;           // scale tiles per 128 rows in the last K block
   int stages;                  // shared-memory ring depth, 2..6
   int split;                   // CTAs of a cluster sharing one tile's K loop (1 = none)
   uint32_t tmem_cols;          // tensor-memory columns taken per CTA
 };
 
-// K % 256 == 0, N % 8 == 0, a / b 16-byte aligned (checked by the caller);
+// K % 32 == 0, N % 8 == 0, a / b 16-byte aligned (checked by the caller);
 // bn = output tile width, 128 or 256; persistent = one CTA per SM walking the
 // tiles (else one CTA per tile); mx = MXFP4 operands (UE8M0 scale per 32
 // codes) instead of NVFP4 (E4M3 per 16).

@@ -307,9 +307,6 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const int b_tiles_total = (p.N + 127) / 128;
     const int b_tiles = b_tiles_total - b_tile0 < C::kSfTilesB ? b_tiles_total - b_tile0
                                                                 : C::kSfTilesB;
-    const uint32_t stage_bytes =
-        load_a ? kTileBytesA + C::kSfBytesA
-               : C::kTileBytesB + static_cast<uint32_t>(b_tiles) * C::kSfBytesA;
     int i = 0;    // K blocks issued
     for (; i < kb1 - kb0; ++i) {
       const int kb = kb0 + i;
@@ -318,12 +315,18 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
         *failed = 1;
         break;
       }
-      mbar_arrive_expect_tx(&full[s], stage_bytes);
+      // the last K block may hold fewer scale tiles (a ragged K)
+      const uint32_t sf_bytes =
+          (kb == p.num_kb - 1 ? static_cast<uint32_t>(p.sf_tiles_last) : C::kSfAtoms) *
+          kSfTileBytes;
+      mbar_arrive_expect_tx(&full[s], load_a ? kTileBytesA + sf_bytes
+                                             : C::kTileBytesB +
+                                                   static_cast<uint32_t>(b_tiles) * sf_bytes);
       if (load_a) {
         tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes,
                     m_tile * kBM, &full[s]);
         bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA,
-                 sfa_k + static_cast<size_t>(kb) * C::kSfBytesA, C::kSfBytesA, &full[s]);
+                 sfa_k + static_cast<size_t>(kb) * C::kSfBytesA, sf_bytes, &full[s]);
       } else {
         tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
                     n_tile * BN, &full[s]);
@@ -331,7 +334,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
           bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + t * C::kSfBytesA,
                    p.sfb + (static_cast<size_t>(b_tile0 + t) * p.nkt) * kSfTileBytes +
                        static_cast<size_t>(kb) * C::kSfBytesA,
-                   C::kSfBytesA, &full[s]);
+                   sf_bytes, &full[s]);
       }
     }
     if (i < kb1 - kb0) {   // gave up: let the copies already issued land first
@@ -354,8 +357,10 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const uint32_t sfb_t = sfa_t + C::kSfColsA;
       const uint32_t a_s = smem_addr(sA + static_cast<size_t>(s) * kTileBytesA);
       const uint32_t b_s = smem_addr(sB + static_cast<size_t>(s) * C::kTileBytesB);
+      const int steps = kb0 + i == p.num_kb - 1 ? p.mma_last : 4;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
+        if (j >= steps) break;
         // K-major, 128-byte swizzle: 8-row groups 1024 bytes apart; the K step
         // advances the start address inside the swizzle row
         const uint64_t adesc = smem_desc(a_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
@@ -381,8 +386,10 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const uint32_t sfb_t = sfa_t + C::kSfColsA;
       const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(s) * C::kSfBytesA);
       const uint32_t sfb_s = smem_addr(sSFB + static_cast<size_t>(s) * C::kSfBytesB);
+      const int tiles = kb0 + i == p.num_kb - 1 ? p.sf_tiles_last : C::kSfAtoms;
 #pragma unroll
       for (int q = 0; q < C::kSfAtoms; ++q) {
+        if (q >= tiles) break;
         // a scale tile: 32 rows of 16 bytes, 8-row groups 128 bytes apart.
         // Tile q: A's at column 4q; B's 128-row tiles side by side from
         // 4 * kSfTilesB * q
@@ -562,9 +569,6 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const int b_tile0 = n_tile * C::kSfTilesB;
       const int b_tiles = b_tiles_total - b_tile0 < C::kSfTilesB ? b_tiles_total - b_tile0
                                                                   : C::kSfTilesB;
-      const uint32_t stage_bytes =
-          load_a ? kTileBytesA + C::kSfBytesA
-                 : C::kTileBytesB + static_cast<uint32_t>(b_tiles) * C::kSfBytesA;
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
         const int s = it % S;
         if (it >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((it / S - 1) & 1))) {
@@ -572,12 +576,17 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        const uint32_t sf_bytes =
+            (kb == p.num_kb - 1 ? static_cast<uint32_t>(p.sf_tiles_last) : C::kSfAtoms) *
+            kSfTileBytes;
+        mbar_arrive_expect_tx(&full[s], load_a ? kTileBytesA + sf_bytes
+                                               : C::kTileBytesB +
+                                                     static_cast<uint32_t>(b_tiles) * sf_bytes);
         if (load_a) {
           tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes,
                       m_tile * kBM, &full[s]);
           bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA,
-                   sfa_k + static_cast<size_t>(kb) * C::kSfBytesA, C::kSfBytesA, &full[s]);
+                   sfa_k + static_cast<size_t>(kb) * C::kSfBytesA, sf_bytes, &full[s]);
         } else {
           tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
                       n_tile * BN, &full[s]);
@@ -585,7 +594,7 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
             bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + q * C::kSfBytesA,
                      p.sfb + static_cast<size_t>(b_tile0 + q) * p.nkt * kSfTileBytes +
                          static_cast<size_t>(kb) * C::kSfBytesA,
-                     C::kSfBytesA, &full[s]);
+                     sf_bytes, &full[s]);
         }
       }
     }
@@ -619,8 +628,10 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const uint32_t sfb_t = sfa_t + C::kSfColsA;
         const uint32_t a_s = smem_addr(sA + static_cast<size_t>(s) * kTileBytesA);
         const uint32_t b_s = smem_addr(sB + static_cast<size_t>(s) * C::kTileBytesB);
+        const int steps = kb == p.num_kb - 1 ? p.mma_last : 4;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
+          if (j >= steps) break;
           const uint64_t adesc = smem_desc(a_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
           const uint64_t bdesc = smem_desc(b_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
           mma_fp4_block_scaled<false>(d_t, adesc, bdesc, C::kIdesc, sfa_t + 4 * j,
@@ -647,8 +658,10 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const uint32_t sfb_t = sfa_t + C::kSfColsA;
       const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(s) * C::kSfBytesA);
       const uint32_t sfb_s = smem_addr(sSFB + static_cast<size_t>(s) * C::kSfBytesB);
+      const int tiles = it % p.num_kb == p.num_kb - 1 ? p.sf_tiles_last : 4;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
+        if (j >= tiles) break;
         tmem_copy_32x128b_x4(sfa_t + 4 * j,
                              smem_desc(sfa_s + j * kSfTileBytes, 0, 128, kSwizzleNone));
 #pragma unroll
@@ -848,6 +861,18 @@ bool cluster_fits(Prep* pr, Kernel kernel, cudaLaunchConfig_t cfg, int split) {
   return ok;
 }
 
+// K blocks of 256 codes, the last one ragged when K % 256 != 0: its K = 64
+// steps and its scale tiles (one per step for NVFP4, one per two for MXFP4).
+// Codes past K read as zero (the TMA box runs past the row), so a partial step
+// multiplies zeros by the k-padding scales of the tiled layout.
+void set_k_blocks(GemmParams& p, bool mx) {
+  p.nkt = (p.K + (mx ? 127 : 63)) / (mx ? 128 : 64);   // ceil(K / (4 * block))
+  p.num_kb = (p.K + 255) / 256;
+  const int rem = p.K - (p.num_kb - 1) * 256;          // 32..256 codes in the last block
+  p.mma_last = (rem + 63) / 64;
+  p.sf_tiles_last = mx ? (rem + 127) / 128 : p.mma_last;
+}
+
 template <int BN, bool SPLIT, bool MX>
 cudaError_t launch_bn(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
                       cudaStream_t stream) {
@@ -857,8 +882,7 @@ cudaError_t launch_bn(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
   if (!operand_map(&ta, a, p.M, p.K / 2, kBM) || !operand_map(&tb, b, p.N, p.K / 2, BN))
     return cudaErrorInvalidValue;
   p.tmem_cols = C::tmem_cols(p.stages);
-  p.nkt = p.K / (MX ? 128 : 64);   // 4-scale groups per row: K / (4 * block)
-  p.num_kb = p.K / (2 * kBKBytes);
+  set_k_blocks(p, MX);
   const size_t smem_need = C::smem_bytes(p.stages);
   if (smem_need > 227 * 1024) return cudaErrorInvalidValue;
   static PrepTable table;
@@ -916,8 +940,7 @@ cudaError_t launch_persistent(const uint8_t* a, const uint8_t* b, GemmParams p, 
   if (P::kSfCol + C::kSfColsPerStage * static_cast<uint32_t>(p.stages) > 512)
     return cudaErrorInvalidValue;   // accumulators and scale slots must fit tensor memory
   p.tmem_cols = P::tmem_cols(p.stages);
-  p.nkt = p.K / 64;
-  p.num_kb = p.K / (2 * kBKBytes);
+  set_k_blocks(p, false);
   const size_t smem_need = P::smem_bytes(p.stages);
   if (smem_need > 227 * 1024) return cudaErrorInvalidValue;
   static PrepTable table;

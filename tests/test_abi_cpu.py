@@ -185,7 +185,8 @@ G_OUT = A + (6 << 32)
 
 @pytest.mark.parametrize("kwargs,status", [
     (dict(M=-1), 1), (dict(N=-1), 1), (dict(K=0), 1),
-    (dict(K=128), 2),                  # K not a multiple of 256
+    (dict(K=48), 2),                   # K not a multiple of 32
+    (dict(K=16), 2),
     (dict(N=20), 2),                   # N not a multiple of 8
     (dict(K=1 << 31), 2),
     (dict(a=0), 1), (dict(b=0), 1), (dict(sfa=0), 1), (dict(sfb=0), 1), (dict(out=0), 1),
@@ -225,7 +226,7 @@ def test_library_exports_only_the_declared_entry_points(L):
 
 @pytest.mark.parametrize("kwargs,status", [
     (dict(variant=2), 1), (dict(variant=3), 1),   # the persistent schedules are NVFP4 only
-    (dict(K=128), 2), (dict(a=0), 1), (dict(sfa=S + 8), 3),
+    (dict(K=80), 2), (dict(a=0), 1), (dict(sfa=S + 8), 3),   # K not a multiple of 32
     (dict(out=S + 256), 1),                         # output over the MXFP4 scales of A
     (dict(M=0, a=0), 0),
 ])

@@ -126,6 +126,45 @@ def test_gemm_exact_operands_bit_exact(M, N, K, alpha, variant):
     check(got, oracle_gemm(a, b, sfa, sfb, M, N, K, alpha=alpha), K, "exact")
 
 
+# K not a multiple of 256: a ragged last K block of 1-4 K = 64 steps, the last
+# of them possibly half past K (codes there read as zero, scales are the
+# k-padding of the tiled layout)
+RAGGED_K_SHAPES = [(128, 128, 32), (1, 8, 96), (128, 128, 224), (41, 520, 288),
+                   (77, 264, 352), (300, 136, 800), (129, 264, 1600), (256, 384, 4160)]
+
+
+@pytest.mark.parametrize("M,N,K", RAGGED_K_SHAPES)
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_gemm_ragged_k_bit_exact(M, N, K, variant):
+    a, b, sfa, sfb = operands(M, N, K, seed=3 * M + N + K, kind="exact")
+    got = gpu_gemm(a, b, sfa, sfb, alpha=0.5, variant=variant)
+    check(got, oracle_gemm(a, b, sfa, sfb, M, N, K, alpha=0.5), K, "exact")
+
+
+@pytest.mark.parametrize("M,N,K", RAGGED_K_SHAPES)
+@pytest.mark.parametrize("variant", MX_VARIANTS)
+def test_gemm_mxfp4_ragged_k_bit_exact(M, N, K, variant):
+    a, b, sfa, sfb = operands(M, N, K, seed=5 * M + N + K, kind="exact", fmt="mxfp4")
+    got = gpu_gemm(a, b, sfa, sfb, variant=variant, fmt="mxfp4")
+    check(got, oracle_gemm(a, b, sfa, sfb, M, N, K, fmt="mxfp4"), K, "exact")
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+def test_gemm_ragged_k_random_operands(fmt):
+    M, N, K = 200, 392, 2144          # 8 full K blocks and one of 96 codes
+    a, b, sfa, sfb = operands(M, N, K, seed=11, kind="random", fmt=fmt)
+    got = gpu_gemm(a, b, sfa, sfb, alpha=1.25, fmt=fmt)
+    check(got, oracle_gemm(a, b, sfa, sfb, M, N, K, alpha=1.25, fmt=fmt), K, "random")
+
+
+def test_gemm_rejects_k_not_multiple_of_32():
+    """K = 240 is a whole number of NVFP4 blocks, but a row of 120 bytes is no
+    multiple of 16 bytes, which the tiled loads need."""
+    a, b, sfa, sfb = operands(128, 128, 240, 1, "exact")
+    with pytest.raises(fq.Fp4Error):
+        gpu_gemm(a, b, sfa, sfb)
+
+
 @pytest.mark.parametrize("name", ["G1_M41_N4608_K1536", "G2_M41_N6144_K1536",
                                   "G3_M41_N1536_K6144"])
 def test_gemm_release_gate_shapes_random_operands(name):
@@ -184,13 +223,16 @@ def test_gemm_full_size_sampled_rows(variant):
     check(got[torch.as_tensor(rows, device=got.device)], g, wl.K, "exact")
 
 
-def test_gemm_consumes_the_fused_producer_with_pdl():
+@pytest.mark.parametrize("K", [2048, 1568])
+def test_gemm_consumes_the_fused_producer_with_pdl(K):
     """The fused op writes A and its tiled scales, fp4_quantize writes B, and the
     GEMM is launched as a programmatic dependent of the quantize kernel.  The
     oracle runs the same chain on the CPU; the producer's bytes equal the
     oracle's (up to boundary cases, none expected here), so the product is
-    checked against the oracle's bound."""
-    M, N, K = 300, 512, 2048
+    checked against the oracle's bound.  K = 1568: 98 scale blocks per row
+    (two k-padding scales in the last tile, written as zero by the producers)
+    and a last K block of 32 codes."""
+    M, N = 300, 512
     wl = workloads.Workload("chain", M, K, "bf16", "nvfp4", "swizzled", 1e-6, seed=31)
     x, r, w = workloads.make_inputs(wl, "cpu")
     wmat = workloads.make_rows(workloads.Workload("wmat", N, K, "bf16", "nvfp4", "swizzled",
@@ -247,7 +289,8 @@ def test_gemm_consumes_the_mxfp4_producer():
 import parity  # noqa: E402
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (41, 4608, 1536), (300, 520, 768)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (41, 4608, 1536), (300, 520, 768),
+                                   (77, 264, 352)])
 @pytest.mark.parametrize("variant", [0, 1, 4])
 def test_gemm_gelu_bf16(M, N, K, variant):
     """GELU(alpha * product + bias) in bf16.  Exact-kind operands make the
@@ -266,7 +309,8 @@ def test_gemm_gelu_bf16(M, N, K, variant):
     assert np.all(err <= tol), f"{(err > tol).sum()} outputs off, first {np.argwhere(err > tol)[:4]}"
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (300, 528, 768), (41, 4608, 1536)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (300, 528, 768), (41, 4608, 1536),
+                                   (77, 272, 352)])
 @pytest.mark.parametrize("variant", [0, 1, 2, 3])
 def test_gemm_gelu_nvfp4_output(M, N, K, variant):
     """The FP4-output epilogue against the oracle's quantization of the same

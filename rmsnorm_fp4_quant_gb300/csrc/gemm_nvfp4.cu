@@ -244,7 +244,12 @@ __device__ __forceinline__ void store_columns32(const GemmParams& p, const uint3
 // loads), so the result does not depend on timing.  A second cluster barrier
 // keeps each partial alive until every peer has read it.  For short, wide
 // products (few output tiles) this spreads the K loop over many SMs.
-template <int BN, bool SPLIT, bool MX>
+//
+// RAG: K % 256 != 0, so the last K block is ragged: only its K = 64 steps and
+// scale tiles that exist are issued (codes past K read as zero, so a half
+// step meets the tiled layout's k-padding scales).  A separate instance, so
+// the full-block loops of every other product stay as they are.
+template <int BN, bool SPLIT, bool MX, bool RAG>
 __global__ void __launch_bounds__(128, 1)
 gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
                   const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
@@ -307,6 +312,9 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const int b_tiles_total = (p.N + 127) / 128;
     const int b_tiles = b_tiles_total - b_tile0 < C::kSfTilesB ? b_tiles_total - b_tile0
                                                                 : C::kSfTilesB;
+    const uint32_t stage_bytes =
+        load_a ? kTileBytesA + C::kSfBytesA
+               : C::kTileBytesB + static_cast<uint32_t>(b_tiles) * C::kSfBytesA;
     int i = 0;    // K blocks issued
     for (; i < kb1 - kb0; ++i) {
       const int kb = kb0 + i;
@@ -315,13 +323,16 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
         *failed = 1;
         break;
       }
-      // the last K block may hold fewer scale tiles (a ragged K)
-      const uint32_t sf_bytes =
-          (kb == p.num_kb - 1 ? static_cast<uint32_t>(p.sf_tiles_last) : C::kSfAtoms) *
-          kSfTileBytes;
-      mbar_arrive_expect_tx(&full[s], load_a ? kTileBytesA + sf_bytes
-                                             : C::kTileBytesB +
-                                                   static_cast<uint32_t>(b_tiles) * sf_bytes);
+      uint32_t sf_bytes = C::kSfBytesA;
+      uint32_t bytes = stage_bytes;
+      if constexpr (RAG) {
+        if (kb == p.num_kb - 1) {   // fewer scale tiles in the ragged last block
+          sf_bytes = static_cast<uint32_t>(p.sf_tiles_last) * kSfTileBytes;
+          bytes = load_a ? kTileBytesA + sf_bytes
+                         : C::kTileBytesB + static_cast<uint32_t>(b_tiles) * sf_bytes;
+        }
+      }
+      mbar_arrive_expect_tx(&full[s], bytes);
       if (load_a) {
         tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes,
                     m_tile * kBM, &full[s]);
@@ -357,10 +368,11 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const uint32_t sfb_t = sfa_t + C::kSfColsA;
       const uint32_t a_s = smem_addr(sA + static_cast<size_t>(s) * kTileBytesA);
       const uint32_t b_s = smem_addr(sB + static_cast<size_t>(s) * C::kTileBytesB);
-      const int steps = kb0 + i == p.num_kb - 1 ? p.mma_last : 4;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        if (j >= steps) break;
+        if constexpr (RAG) {
+          if (kb0 + i == p.num_kb - 1 && j >= p.mma_last) break;
+        }
         // K-major, 128-byte swizzle: 8-row groups 1024 bytes apart; the K step
         // advances the start address inside the swizzle row
         const uint64_t adesc = smem_desc(a_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
@@ -386,10 +398,11 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const uint32_t sfb_t = sfa_t + C::kSfColsA;
       const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(s) * C::kSfBytesA);
       const uint32_t sfb_s = smem_addr(sSFB + static_cast<size_t>(s) * C::kSfBytesB);
-      const int tiles = kb0 + i == p.num_kb - 1 ? p.sf_tiles_last : C::kSfAtoms;
 #pragma unroll
       for (int q = 0; q < C::kSfAtoms; ++q) {
-        if (q >= tiles) break;
+        if constexpr (RAG) {
+          if (kb0 + i == p.num_kb - 1 && q >= p.sf_tiles_last) break;
+        }
         // a scale tile: 32 rows of 16 bytes, 8-row groups 128 bytes apart.
         // Tile q: A's at column 4q; B's 128-row tiles side by side from
         // 4 * kSfTilesB * q
@@ -501,7 +514,7 @@ struct PCfg {
   }
 };
 
-template <int BN>
+template <int BN, bool RAG>
 __global__ void __launch_bounds__(256, 1)
 gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
                              const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
@@ -569,6 +582,9 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const int b_tile0 = n_tile * C::kSfTilesB;
       const int b_tiles = b_tiles_total - b_tile0 < C::kSfTilesB ? b_tiles_total - b_tile0
                                                                   : C::kSfTilesB;
+      const uint32_t stage_bytes =
+          load_a ? kTileBytesA + C::kSfBytesA
+                 : C::kTileBytesB + static_cast<uint32_t>(b_tiles) * C::kSfBytesA;
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
         const int s = it % S;
         if (it >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((it / S - 1) & 1))) {
@@ -576,12 +592,16 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
           ok = false;
           break;
         }
-        const uint32_t sf_bytes =
-            (kb == p.num_kb - 1 ? static_cast<uint32_t>(p.sf_tiles_last) : C::kSfAtoms) *
-            kSfTileBytes;
-        mbar_arrive_expect_tx(&full[s], load_a ? kTileBytesA + sf_bytes
-                                               : C::kTileBytesB +
-                                                     static_cast<uint32_t>(b_tiles) * sf_bytes);
+        uint32_t sf_bytes = C::kSfBytesA;
+        uint32_t bytes = stage_bytes;
+        if constexpr (RAG) {
+          if (kb == p.num_kb - 1) {   // fewer scale tiles in the ragged last block
+            sf_bytes = static_cast<uint32_t>(p.sf_tiles_last) * kSfTileBytes;
+            bytes = load_a ? kTileBytesA + sf_bytes
+                           : C::kTileBytesB + static_cast<uint32_t>(b_tiles) * sf_bytes;
+          }
+        }
+        mbar_arrive_expect_tx(&full[s], bytes);
         if (load_a) {
           tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes,
                       m_tile * kBM, &full[s]);
@@ -628,10 +648,11 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const uint32_t sfb_t = sfa_t + C::kSfColsA;
         const uint32_t a_s = smem_addr(sA + static_cast<size_t>(s) * kTileBytesA);
         const uint32_t b_s = smem_addr(sB + static_cast<size_t>(s) * C::kTileBytesB);
-        const int steps = kb == p.num_kb - 1 ? p.mma_last : 4;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          if (j >= steps) break;
+          if constexpr (RAG) {
+            if (kb == p.num_kb - 1 && j >= p.mma_last) break;
+          }
           const uint64_t adesc = smem_desc(a_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
           const uint64_t bdesc = smem_desc(b_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
           mma_fp4_block_scaled<false>(d_t, adesc, bdesc, C::kIdesc, sfa_t + 4 * j,
@@ -658,10 +679,11 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const uint32_t sfb_t = sfa_t + C::kSfColsA;
       const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(s) * C::kSfBytesA);
       const uint32_t sfb_s = smem_addr(sSFB + static_cast<size_t>(s) * C::kSfBytesB);
-      const int tiles = it % p.num_kb == p.num_kb - 1 ? p.sf_tiles_last : 4;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        if (j >= tiles) break;
+        if constexpr (RAG) {
+          if (it % p.num_kb == p.num_kb - 1 && j >= p.sf_tiles_last) break;
+        }
         tmem_copy_32x128b_x4(sfa_t + 4 * j,
                              smem_desc(sfa_s + j * kSfTileBytes, 0, 128, kSwizzleNone));
 #pragma unroll
@@ -863,8 +885,6 @@ bool cluster_fits(Prep* pr, Kernel kernel, cudaLaunchConfig_t cfg, int split) {
 
 // K blocks of 256 codes, the last one ragged when K % 256 != 0: its K = 64
 // steps and its scale tiles (one per step for NVFP4, one per two for MXFP4).
-// Codes past K read as zero (the TMA box runs past the row), so a partial step
-// multiplies zeros by the k-padding scales of the tiled layout.
 void set_k_blocks(GemmParams& p, bool mx) {
   p.nkt = (p.K + (mx ? 127 : 63)) / (mx ? 128 : 64);   // ceil(K / (4 * block))
   p.num_kb = (p.K + 255) / 256;
@@ -873,11 +893,11 @@ void set_k_blocks(GemmParams& p, bool mx) {
   p.sf_tiles_last = mx ? (rem + 127) / 128 : p.mma_last;
 }
 
-template <int BN, bool SPLIT, bool MX>
+template <int BN, bool SPLIT, bool MX, bool RAG>
 cudaError_t launch_bn(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
                       cudaStream_t stream) {
   using C = Cfg<BN, MX>;
-  auto kernel = gemm_nvfp4_kernel<BN, SPLIT, MX>;
+  auto kernel = gemm_nvfp4_kernel<BN, SPLIT, MX, RAG>;
   CUtensorMap ta, tb;
   if (!operand_map(&ta, a, p.M, p.K / 2, kBM) || !operand_map(&tb, b, p.N, p.K / 2, BN))
     return cudaErrorInvalidValue;
@@ -928,12 +948,12 @@ int sm_count() {
   return cached[dev];
 }
 
-template <int BN>
+template <int BN, bool RAG>
 cudaError_t launch_persistent(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
                               cudaStream_t stream) {
   using C = Cfg<BN>;
   using P = PCfg<BN>;
-  auto kernel = gemm_nvfp4_persistent_kernel<BN>;
+  auto kernel = gemm_nvfp4_persistent_kernel<BN, RAG>;
   CUtensorMap ta, tb;
   if (!operand_map(&ta, a, p.M, p.K / 2, kBM) || !operand_map(&tb, b, p.N, p.K / 2, BN))
     return cudaErrorInvalidValue;
@@ -964,32 +984,40 @@ cudaError_t launch_persistent(const uint8_t* a, const uint8_t* b, GemmParams p, 
   return cudaLaunchKernelEx(&cfg, kernel, ta, tb, p);
 }
 
+// One dispatch per operand format, ring shape and K raggedness.
+template <bool RAG>
+cudaError_t launch_k(const uint8_t* a, const uint8_t* b, const GemmParams& p, int bn,
+                     bool persistent, bool mx, int pdl, cudaStream_t stream) {
+  if (mx) {
+    if (persistent) return cudaErrorInvalidValue;
+    if (p.split > 1)
+      return bn == 128 && p.split <= 16 ? launch_bn<128, true, true, RAG>(a, b, p, pdl, stream)
+                                        : cudaErrorInvalidValue;
+    if (bn == 128) return launch_bn<128, false, true, RAG>(a, b, p, pdl, stream);
+    if (bn == 256) return launch_bn<256, false, true, RAG>(a, b, p, pdl, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (p.split > 1) {
+    if (bn != 128 || persistent || p.split > 16) return cudaErrorInvalidValue;
+    return launch_bn<128, true, false, RAG>(a, b, p, pdl, stream);
+  }
+  if (!persistent) {
+    if (bn == 128) return launch_bn<128, false, false, RAG>(a, b, p, pdl, stream);
+    if (bn == 256) return launch_bn<256, false, false, RAG>(a, b, p, pdl, stream);
+  } else {
+    if (bn == 128) return launch_persistent<128, RAG>(a, b, p, pdl, stream);
+    if (bn == 256) return launch_persistent<256, RAG>(a, b, p, pdl, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_nvfp4(const uint8_t* a, const uint8_t* b, GemmParams p, int bn,
                               bool persistent, bool mx, int pdl, cudaStream_t stream) {
   if (p.stages < 2 || p.stages > 8) return cudaErrorInvalidValue;
-  if (mx) {
-    if (persistent) return cudaErrorInvalidValue;
-    if (p.split > 1)
-      return bn == 128 && p.split <= 16 ? launch_bn<128, true, true>(a, b, p, pdl, stream)
-                                        : cudaErrorInvalidValue;
-    if (bn == 128) return launch_bn<128, false, true>(a, b, p, pdl, stream);
-    if (bn == 256) return launch_bn<256, false, true>(a, b, p, pdl, stream);
-    return cudaErrorInvalidValue;
-  }
-  if (p.split > 1) {
-    if (bn != 128 || persistent || p.split > 16) return cudaErrorInvalidValue;
-    return launch_bn<128, true, false>(a, b, p, pdl, stream);
-  }
-  if (!persistent) {
-    if (bn == 128) return launch_bn<128, false, false>(a, b, p, pdl, stream);
-    if (bn == 256) return launch_bn<256, false, false>(a, b, p, pdl, stream);
-  } else {
-    if (bn == 128) return launch_persistent<128>(a, b, p, pdl, stream);
-    if (bn == 256) return launch_persistent<256>(a, b, p, pdl, stream);
-  }
-  return cudaErrorInvalidValue;
+  return p.K % 256 != 0 ? launch_k<true>(a, b, p, bn, persistent, mx, pdl, stream)
+                        : launch_k<false>(a, b, p, bn, persistent, mx, pdl, stream);
 }
 
 }  // namespace fp4q

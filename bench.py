@@ -115,6 +115,11 @@ def kernel_source_sha(op: str = "fused") -> str:
     return h.hexdigest()
 
 
+def gemm_profile_key(workload_name: str, fmt: str, kernel: str) -> str:
+    """The `workload:` key of a GEMM capture: shape, operand format, kernel."""
+    return f"{workload_name}_{fmt}_{kernel}"
+
+
 def recorded_traffic(workload_name: str, op: str = "fused"):
     """dram bytes per launch from a committed ncu summary whose kernel-source
     hash matches the current sources; None otherwise."""
@@ -713,9 +718,13 @@ def run_gemm(args):
             if tensor_bound else
             {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
              "frac": round(gbs / hbm_peak, 4), "peak_source": f"{hbm_src} hbm_gbs"})
-    traffic, traffic_src = recorded_traffic(gw.name, "gemm")
+    sched = fq.fp4_gemm_variant(gw.M, gw.N, gw.K, 0 if args.gemm_format == "nvfp4" else 1,
+                                False, args.gemm_variant)
+    # a GEMM capture is keyed by shape, operand format and kernel
+    traffic, traffic_src = recorded_traffic(gemm_profile_key(gw.name, args.gemm_format,
+                                                             sched["kernel"]), "gemm")
     roof.update({"traffic": traffic, "traffic_source": traffic_src,
-                 "kernel": "gemm_nvfp4_kernel", "kernel_ms_mean": round(ms, 5),
+                 "kernel": sched["kernel"], "schedule": sched, "kernel_ms_mean": round(ms, 5),
                  "algorithmic_bytes": alg, "flops": gw.flops()})
 
     e2e = None

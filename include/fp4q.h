@@ -193,6 +193,19 @@ FP4Q_API fp4_status_t fp4_launch_shape(int64_t M, int64_t H, fp4_dtype_t dtype, 
                                        fp4_sf_layout_t sf_layout, int64_t out[8]);
 
 /*
+ * fp4_gemm_variant - the schedule (the `variant` numbers of
+ * fp4_gemm_nvfp4_bf16 below) the GEMM entry points would run for an
+ * M x N x K product of `format` operands (FP4_NVFP4 or FP4_MXFP4); fp4_out
+ * nonzero for fp4_gemm_nvfp4_gelu_nvfp4.  `variant` -1 asks for the
+ * automatic choice; any other accepted value is returned as given.  Returns
+ * -1 for sizes or a variant the GEMM would reject.  Host only (diagnostics;
+ * launches nothing): the choice depends on the current device's SM count,
+ * taken as 152 when no device is visible.
+ */
+FP4Q_API int fp4_gemm_variant(int64_t M, int64_t N, int64_t K, fp4_format_t format, int fp4_out,
+                              int variant);
+
+/*
  * fp4_gemm_nvfp4_bf16 - the consumer of the packed codes and tiled scales:
  * out = bf16(alpha * deq(A) @ deq(B)^T (+ bias) (+ residual)) on the tensor
  * cores (FlashRT `fp4-gemm` README: Tensor Contract; `nvfp4_gemm_bf16`,

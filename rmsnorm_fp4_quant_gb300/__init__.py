@@ -37,6 +37,7 @@ from ._binding import (  # noqa: F401
     fp4_quantize,
     fp4_last_cuda_error,
     fp4_launch_shape,
+    fp4_gemm_variant,
     fp4_sf_size_bytes,
     fp4_status_string,
     lib,

@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
     L.fp4_gemm_nvfp4_gelu_nvfp4.argtypes = [vp, vp, vp, vp, ctypes.c_float, vp, i64, i64, i64,
                                             vp, vp, ci, ci, vp]
     L.fp4_gemm_nvfp4_gelu_nvfp4.restype = ci
+    L.fp4_gemm_variant.argtypes = [i64, i64, i64, ci, ci, ci]
+    L.fp4_gemm_variant.restype = ci
     _lib = L
     return L
 
@@ -182,6 +184,23 @@ def fp4_launch_shape(M: int, H: int, dtype: int, fmt: int, sf_layout: int) -> di
     d = dict(zip(_SHAPE_KEYS, list(out)))
     d["kernel"] = "fused_tma_kernel" if d["kernel"] == 0 else "fused_direct_kernel"
     return d
+
+
+# GEMM schedules by `variant` number: (kernel, output tile width)
+_GEMM_SCHEDULES = {0: ("gemm_nvfp4_kernel", 128), 1: ("gemm_nvfp4_kernel", 256),
+                   2: ("gemm_nvfp4_persistent_kernel", 128),
+                   3: ("gemm_nvfp4_persistent_kernel", 256), 4: ("gemm_nvfp4_kernel", 128)}
+
+
+def fp4_gemm_variant(M: int, N: int, K: int, fmt: int = 0, fp4_out: bool = False,
+                     variant: int = -1) -> dict:
+    """The schedule the GEMM entry points would run for an M x N x K product
+    on the current device: {"variant", "kernel", "tile_n", "split_k"}."""
+    v = lib().fp4_gemm_variant(M, N, K, fmt, 1 if fp4_out else 0, variant)
+    if v < 0:
+        raise ValueError("the GEMM rejects these sizes or this variant")
+    kernel, tile_n = _GEMM_SCHEDULES[v]
+    return {"variant": v, "kernel": kernel, "tile_n": tile_n, "split_k": v == 4}
 
 
 # ---------------------------------------------------------------------------

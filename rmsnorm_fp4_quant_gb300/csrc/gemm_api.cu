@@ -18,8 +18,8 @@
 #define FP4Q_GEMM_VARIANT 0             // the GEMM schedule of the automatic choice
 #endif
 #ifndef FP4Q_GEMM_PSTAGES_128
-#define FP4Q_GEMM_PSTAGES_128 6         // ring depth of the persistent 128-wide schedule
-#endif
+#define FP4Q_GEMM_PSTAGES_128 3         // ring depth of the persistent 128-wide schedule
+#endif                                  // (2 CTAs per SM at 3)
 #ifndef FP4Q_GEMM_PSTAGES_256
 #define FP4Q_GEMM_PSTAGES_256 4         // ring depth of the persistent 256-wide schedule
 #endif
@@ -27,6 +27,23 @@
 using namespace fp4q;
 
 namespace {
+
+// The schedule of an M x N x K product: `variant` if given (>= 0), else the
+// automatic choice.  Measured on the decode shapes: with up to 6 K blocks a
+// single CTA per tile holding them all in flight is faster than a split; with
+// 24 the split wins by a third.  Measured on an 8192 x 7168 x 7168 product:
+// with more tiles than two CTAs per SM take at once, persistent CTAs that load
+// the next tile during the epilogue run 2.5 % faster than one CTA per tile
+// (that schedule is NVFP4 only).
+int choose_variant(int64_t M, int64_t N, int64_t K, bool mx, bool fp4_out, int variant,
+                   int sms) {
+  if (variant >= 0) return variant;
+  const int64_t tiles128 = ((N + 127) / 128) * ((M + 127) / 128);
+  const int64_t num_kb = (K + 255) / 256;
+  if (tiles128 * 2 <= sms && num_kb > 6 && !fp4_out) return 4;
+  if (!mx && tiles128 > 2 * static_cast<int64_t>(sms)) return 2;
+  return FP4Q_GEMM_VARIANT;
+}
 
 // Every form: NVFP4 (mx = false) or MXFP4 operands; epilogue kEpiPlain /
 // kEpiGelu into `out` (bf16), or kEpiGeluFp4 into out_packed + out_sf.
@@ -99,11 +116,7 @@ fp4_status_t gemm_call(bool mx, int epilogue, const uint8_t* a_packed, const uin
   const int sms = sm_count_current_device();
   const int64_t tiles128 = ((N + 127) / 128) * ((M + 127) / 128);
   const int num_kb = static_cast<int>((K + 255) / 256);
-  int v = variant;
-  // (measured on the decode shapes: with up to 6 K blocks a single CTA per
-  // tile holding them all in flight is faster than a split; with 24 the split
-  // wins by a third)
-  if (v < 0) v = (tiles128 * 2 <= sms && num_kb > 6 && !fp4_out) ? 4 : FP4Q_GEMM_VARIANT;
+  const int v = choose_variant(M, N, K, mx, fp4_out, variant, sms);
   const int bn = (v == 1 || v == 3) ? 256 : 128;
   const bool persistent = v == 2 || v == 3;
   p.stages = !persistent ? FP4Q_GEMM_STAGES : bn == 128 ? FP4Q_GEMM_PSTAGES_128
@@ -174,6 +187,18 @@ fp4_status_t fp4_gemm_nvfp4_gelu_nvfp4(const uint8_t* a_packed, const uint8_t* b
                                        int pdl, fp4q_stream_t stream) {
   return gemm_call(false, kEpiGeluFp4, a_packed, b_packed, sfa, sfb, alpha, bias, nullptr, M, N,
                    K, nullptr, out_packed, out_sf, variant, pdl, stream);
+}
+
+int fp4_gemm_variant(int64_t M, int64_t N, int64_t K, fp4_format_t format, int fp4_out,
+                     int variant) {
+  if (format != FP4_NVFP4 && format != FP4_MXFP4) return -1;
+  const bool mx = format == FP4_MXFP4;
+  if (M < 0 || N < 0 || K <= 0 || variant < -1 || variant > 4) return -1;
+  if (mx && (variant == 2 || variant == 3)) return -1;
+  if (fp4_out && (mx || variant == 4)) return -1;
+  if (K % 32 != 0 || N % (fp4_out ? 16 : 8) != 0) return -1;
+  if (M > INT32_MAX - 128 || N > INT32_MAX - 128 || K > INT32_MAX / 2) return -1;
+  return choose_variant(M, N, K, mx, fp4_out != 0, variant, sm_count_current_device());
 }
 
 }  // extern "C"

@@ -484,9 +484,10 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
   if (warp == 0) tmem_dealloc(tmem, p.tmem_cols);
 }
 
-// Persistent form: one CTA per SM walks the output tiles t = blockIdx.x,
-// blockIdx.x + gridDim.x, ... (row tile t / n_tiles, column tile t % n_tiles,
-// so CTAs running together share A's row panel).  Eight warps:
+// Persistent form: resident CTAs (two per SM for 128-wide tiles, one for
+// 256-wide) walk the output tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...
+// (row tile t / n_tiles, column tile t % n_tiles, so CTAs running together
+// share A's row panel).  Eight warps:
 //   warps 0 and 6,    producers (A and its scales / B and its scales): one
 //   one lane each     continuous stream of K blocks over all the CTA's tiles
 //                     through the S-stage ring (never drains between tiles);
@@ -494,16 +495,19 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
 //   warps 2..5        epilogue, lane quarter = warp % 4;
 //   warp 7, one lane  scale mover: each stage's scale tiles into that stage's
 //                     tensor-memory slot, committed to sf_ready[s].
-// NACC accumulators in tensor memory (2 for 128-wide tiles, 1 for 256): the
-// MMAs of the next tile start as soon as the epilogue has read the previous
-// tile's accumulator out (acc_empty), so loads, MMAs and stores overlap.
-// (Splitting the producer and moving the scale copies off the MMA thread took
-// the 128-wide form from 404 to 318 us and the 256-wide from 287-308 to 265 us
-// on an 8192 x 7168 x 7168 product; the one-tile-per-CTA kernel above, two
-// CTAs per SM, stays faster there.)
+// While the epilogue reads a tile's accumulator out (acc_empty), the
+// producers already fill the ring with the next tile's K blocks, so a new
+// tile never waits for a CTA launch or a first load; with two CTAs per SM the
+// other CTA's MMAs run meanwhile.  This is the automatic schedule for large
+// NVFP4 products (238 us on 8192 x 7168 x 7168 against 244 us for one CTA
+// per tile in the same run).
 template <int BN>
 struct PCfg {
-  static constexpr int kAcc = BN == 128 ? 2 : 1;
+  // One accumulator: a 128-wide tile then needs 128 + S * 32 <= 256 tensor-
+  // memory columns, so two CTAs share an SM and one's epilogue overlaps the
+  // other's MMAs (measured faster than one CTA per SM with two accumulators
+  // and six stages: 238 against 315 us on an 8192 x 7168 x 7168 product).
+  static constexpr int kAcc = 1;
   static constexpr uint32_t kSfCol = kAcc * BN;     // the scale slots after the accumulators
   static constexpr uint32_t tmem_cols(int stages) {
     return (kSfCol + Cfg<BN>::kSfColsPerStage * stages) <= 256 ? 256u : 512u;
@@ -965,14 +969,15 @@ cudaError_t launch_persistent(const uint8_t* a, const uint8_t* b, GemmParams p, 
   if (smem_need > 227 * 1024) return cudaErrorInvalidValue;
   static PrepTable table;
   Prep* pr = nullptr;
-  // one CTA per SM: it takes all 512 tensor-memory columns
+  // as many CTAs per SM as tensor memory holds: two 128-wide, one 256-wide
   cudaError_t e = prepare(table, kernel, 256, smem_need, p.tmem_cols, p.stages, &pr);
   if (e != cudaSuccess) return e;
   const int sms = sm_count();
   if (sms < 1) return cudaErrorInvalidDevice;
   const int64_t tiles = static_cast<int64_t>((p.N + BN - 1) / BN) * ((p.M + kBM - 1) / kBM);
+  const int64_t resident = static_cast<int64_t>(sms) * static_cast<int64_t>(512 / p.tmem_cols);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(tiles < sms ? tiles : sms), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles < resident ? tiles : resident), 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = pr->smem;
   cfg.stream = stream;

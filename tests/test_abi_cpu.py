@@ -257,3 +257,22 @@ def test_gemm_gelu_nvfp4_validation(L, kwargs, status):
                                       a["M"], a["N"], a["K"], a["p"], a["s"], a["variant"],
                                       a["pdl"], 0)
     assert st == status
+
+
+def test_gemm_variant_query(L):
+    """The schedule query: host only (152 SMs without a device); a given
+    variant comes back as given, rejected sizes give -1."""
+    import rmsnorm_fp4_quant_gb300 as fq
+    v = fq.fp4_gemm_variant
+    assert v(8192, 7168, 7168)["variant"] == 2                       # many tiles, NVFP4
+    assert v(8192, 7168, 7168)["kernel"] == "gemm_nvfp4_persistent_kernel"
+    assert v(8192, 7168, 7168, fmt=1)["variant"] == 0                # MXFP4: no persistent form
+    assert v(41, 1536, 6144)["split_k"]                              # few tiles, long K
+    assert v(41, 4608, 1536)["variant"] == 0                         # few tiles, 6 K blocks
+    assert v(8192, 7168, 7168, fp4_out=True)["variant"] == 2
+    assert v(41, 1536, 6144, fp4_out=True)["variant"] == 0           # no split for FP4 output
+    assert v(256, 256, 512, variant=3)["variant"] == 3
+    assert L.fp4_gemm_variant(256, 256, 240, 0, 0, -1) == -1         # K % 32
+    assert L.fp4_gemm_variant(256, 256, 512, 1, 0, 2) == -1          # MXFP4 persistent
+    assert L.fp4_gemm_variant(256, 264, 512, 0, 1, -1) == -1         # FP4 output: N % 16
+    assert L.fp4_gemm_variant(256, 256, 512, 2, 0, -1) == -1         # E4M3-B32 operands

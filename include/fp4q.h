@@ -255,8 +255,7 @@ FP4Q_API fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t
  * output, tiled layout, fp4_sf_size_bytes(M or N, K, FP4_MXFP4, ...) bytes).
  * Not on the FlashRT page (its GEMM is NVFP4 only): the consumer of this
  * library's own MXFP4 producer.  Arguments, checks and variants as
- * fp4_gemm_nvfp4_bf16, except that the persistent variants 2 and 3 are
- * NVFP4 only (FP4_ERR_INVALID_ARG).
+ * fp4_gemm_nvfp4_bf16 (every variant).
  */
 FP4Q_API fp4_status_t fp4_gemm_mxfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
                                           const uint8_t* sfa, const uint8_t* sfb, float alpha,

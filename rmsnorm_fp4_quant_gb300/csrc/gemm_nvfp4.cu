@@ -501,7 +501,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
 // other CTA's MMAs run meanwhile.  This is the automatic schedule for large
 // NVFP4 products (238 us on 8192 x 7168 x 7168 against 244 us for one CTA
 // per tile in the same run).
-template <int BN>
+template <int BN, bool MX>
 struct PCfg {
   // One accumulator: a 128-wide tile then needs 128 + S * 32 <= 256 tensor-
   // memory columns, so two CTAs share an SM and one's epilogue overlaps the
@@ -510,20 +510,20 @@ struct PCfg {
   static constexpr int kAcc = 1;
   static constexpr uint32_t kSfCol = kAcc * BN;     // the scale slots after the accumulators
   static constexpr uint32_t tmem_cols(int stages) {
-    return (kSfCol + Cfg<BN>::kSfColsPerStage * stages) <= 256 ? 256u : 512u;
+    return (kSfCol + Cfg<BN, MX>::kSfColsPerStage * stages) <= 256 ? 256u : 512u;
   }
   static constexpr size_t smem_bytes(int stages) {
-    return 1024 + static_cast<size_t>(stages) * Cfg<BN>::kStageBytes +
+    return 1024 + static_cast<size_t>(stages) * Cfg<BN, MX>::kStageBytes +
            (3 * stages + 2 * kAcc + 2) * 8 + 8;
   }
 };
 
-template <int BN, bool RAG>
+template <int BN, bool MX, bool RAG>
 __global__ void __launch_bounds__(256, 1)
 gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
                              const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
-  using C = Cfg<BN>;
-  using P = PCfg<BN>;
+  using C = Cfg<BN, MX>;
+  using P = PCfg<BN, MX>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -659,8 +659,8 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
           }
           const uint64_t adesc = smem_desc(a_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
           const uint64_t bdesc = smem_desc(b_s + j * kMmaKBytes, 0, 1024, kSwizzle128B);
-          mma_fp4_block_scaled<false>(d_t, adesc, bdesc, C::kIdesc, sfa_t + 4 * j,
-                                      sfb_t + 4 * C::kSfTilesB * j, (kb | j) != 0 ? 1u : 0u);
+          mma_fp4_block_scaled<MX>(d_t, adesc, bdesc, C::idesc(j), sfa_t + 4 * C::atom(j),
+                                   sfb_t + 4 * C::kSfTilesB * C::atom(j), (kb | j) != 0 ? 1u : 0u);
         }
         tc_commit(&empty[s]);
       }
@@ -684,7 +684,7 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(s) * C::kSfBytesA);
       const uint32_t sfb_s = smem_addr(sSFB + static_cast<size_t>(s) * C::kSfBytesB);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < C::kSfAtoms; ++j) {
         if constexpr (RAG) {
           if (it % p.num_kb == p.num_kb - 1 && j >= p.sf_tiles_last) break;
         }
@@ -952,19 +952,19 @@ int sm_count() {
   return cached[dev];
 }
 
-template <int BN, bool RAG>
+template <int BN, bool MX, bool RAG>
 cudaError_t launch_persistent(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
                               cudaStream_t stream) {
-  using C = Cfg<BN>;
-  using P = PCfg<BN>;
-  auto kernel = gemm_nvfp4_persistent_kernel<BN, RAG>;
+  using C = Cfg<BN, MX>;
+  using P = PCfg<BN, MX>;
+  auto kernel = gemm_nvfp4_persistent_kernel<BN, MX, RAG>;
   CUtensorMap ta, tb;
   if (!operand_map(&ta, a, p.M, p.K / 2, kBM) || !operand_map(&tb, b, p.N, p.K / 2, BN))
     return cudaErrorInvalidValue;
   if (P::kSfCol + C::kSfColsPerStage * static_cast<uint32_t>(p.stages) > 512)
     return cudaErrorInvalidValue;   // accumulators and scale slots must fit tensor memory
   p.tmem_cols = P::tmem_cols(p.stages);
-  set_k_blocks(p, false);
+  set_k_blocks(p, MX);
   const size_t smem_need = P::smem_bytes(p.stages);
   if (smem_need > 227 * 1024) return cudaErrorInvalidValue;
   static PrepTable table;
@@ -994,7 +994,12 @@ template <bool RAG>
 cudaError_t launch_k(const uint8_t* a, const uint8_t* b, const GemmParams& p, int bn,
                      bool persistent, bool mx, int pdl, cudaStream_t stream) {
   if (mx) {
-    if (persistent) return cudaErrorInvalidValue;
+    if (persistent) {
+      if (p.split > 1) return cudaErrorInvalidValue;
+      if (bn == 128) return launch_persistent<128, true, RAG>(a, b, p, pdl, stream);
+      if (bn == 256) return launch_persistent<256, true, RAG>(a, b, p, pdl, stream);
+      return cudaErrorInvalidValue;
+    }
     if (p.split > 1)
       return bn == 128 && p.split <= 16 ? launch_bn<128, true, true, RAG>(a, b, p, pdl, stream)
                                         : cudaErrorInvalidValue;
@@ -1010,8 +1015,8 @@ cudaError_t launch_k(const uint8_t* a, const uint8_t* b, const GemmParams& p, in
     if (bn == 128) return launch_bn<128, false, false, RAG>(a, b, p, pdl, stream);
     if (bn == 256) return launch_bn<256, false, false, RAG>(a, b, p, pdl, stream);
   } else {
-    if (bn == 128) return launch_persistent<128, RAG>(a, b, p, pdl, stream);
-    if (bn == 256) return launch_persistent<256, RAG>(a, b, p, pdl, stream);
+    if (bn == 128) return launch_persistent<128, false, RAG>(a, b, p, pdl, stream);
+    if (bn == 256) return launch_persistent<256, false, RAG>(a, b, p, pdl, stream);
   }
   return cudaErrorInvalidValue;
 }

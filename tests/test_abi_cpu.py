@@ -225,7 +225,7 @@ def test_library_exports_only_the_declared_entry_points(L):
 
 
 @pytest.mark.parametrize("kwargs,status", [
-    (dict(variant=2), 1), (dict(variant=3), 1),   # the persistent schedules are NVFP4 only
+    (dict(variant=5), 1),
     (dict(K=80), 2), (dict(a=0), 1), (dict(sfa=S + 8), 3),   # K not a multiple of 32
     (dict(out=S + 256), 1),                         # output over the MXFP4 scales of A
     (dict(M=0, a=0), 0),
@@ -266,13 +266,13 @@ def test_gemm_variant_query(L):
     v = fq.fp4_gemm_variant
     assert v(8192, 7168, 7168)["variant"] == 2                       # many tiles, NVFP4
     assert v(8192, 7168, 7168)["kernel"] == "gemm_nvfp4_persistent_kernel"
-    assert v(8192, 7168, 7168, fmt=1)["variant"] == 0                # MXFP4: no persistent form
+    assert v(8192, 7168, 7168, fmt=1)["variant"] == 2                # MXFP4 as well
     assert v(41, 1536, 6144)["split_k"]                              # few tiles, long K
     assert v(41, 4608, 1536)["variant"] == 0                         # few tiles, 6 K blocks
     assert v(8192, 7168, 7168, fp4_out=True)["variant"] == 2
     assert v(41, 1536, 6144, fp4_out=True)["variant"] == 0           # no split for FP4 output
     assert v(256, 256, 512, variant=3)["variant"] == 3
     assert L.fp4_gemm_variant(256, 256, 240, 0, 0, -1) == -1         # K % 32
-    assert L.fp4_gemm_variant(256, 256, 512, 1, 0, 2) == -1          # MXFP4 persistent
+    assert L.fp4_gemm_variant(256, 256, 512, 1, 0, 2) == 2           # MXFP4 persistent
     assert L.fp4_gemm_variant(256, 264, 512, 0, 1, -1) == -1         # FP4 output: N % 16
     assert L.fp4_gemm_variant(256, 256, 512, 2, 0, -1) == -1         # E4M3-B32 operands

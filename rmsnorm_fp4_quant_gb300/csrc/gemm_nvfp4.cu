@@ -14,12 +14,13 @@
 //                      128-byte swizzle, and 2 KiB of each scale buffer by a
 //                      bulk copy - the four 512-byte scale tiles of this K
 //                      block, contiguous in the 128x4 layout - into a ring of
-//                      S stages, completion counted on full[s].  Warp 0 loads
-//                      A and its scales, warp 2 B and its scales, each
-//                      arriving once per stage (two threads issue a stage's
-//                      copies in about half the time one takes: 4 % on a
-//                      large product).
-//   warp 3, one lane   scale mover.  Copies the stage's eight scale tiles into
+//                      S stages, the operand tiles counted on full[s], the
+//                      scales on sf_full[s].  Warp 0 loads A and its scales,
+//                      warp 2 B and its scales, each arriving once per stage
+//                      on each barrier (two threads issue a stage's copies in
+//                      about half the time one takes: 4 % on a large product).
+//   warp 3, one lane   scale mover.  As soon as a stage's scales have landed
+//                      (sf_full[s], before its operand tiles), copies its eight scale tiles into
 //                      the stage's tensor-memory slot (tcgen05.cp 32x128b,
 //                      repeated over the four lane quarters: a 512-byte tile is
 //                      exactly the image of 128 rows x 4 scales the
@@ -103,8 +104,8 @@ struct Cfg {
   }
   static constexpr size_t smem_bytes(int stages) {
     // 1 KiB of alignment slack (the 128-byte swizzle wants 1 KiB-aligned
-    // tiles), the ring, 3S + 2 mbarriers, the tensor-memory address, a flag
-    return 1024 + static_cast<size_t>(stages) * kStageBytes + (3 * stages + 2) * 8 + 8;
+    // tiles), the ring, 4S + 2 mbarriers, the tensor-memory address, a flag
+    return 1024 + static_cast<size_t>(stages) * kStageBytes + (4 * stages + 2) * 8 + 8;
   }
 };
 
@@ -268,7 +269,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
   uint64_t* accum = empty + S;
   uint64_t* sf_ready = accum + 1;     // the stage's scales are in tensor memory
   uint64_t* sf_done = sf_ready + S;   // every scale copy has completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_done + 1);
+  uint64_t* sf_full = sf_done + 1;    // the stage's scale bytes have landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_full + S);
   volatile int* failed = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -285,6 +287,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
       mbar_init(&full[s], 2);   // one arrival per producer
       mbar_init(&empty[s], 1);
       mbar_init(&sf_ready[s], 1);
+      mbar_init(&sf_full[s], 2);   // one arrival per producer
     }
     mbar_init(sf_done, 1);
     mbar_init(accum, 1);
@@ -312,9 +315,6 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const int b_tiles_total = (p.N + 127) / 128;
     const int b_tiles = b_tiles_total - b_tile0 < C::kSfTilesB ? b_tiles_total - b_tile0
                                                                 : C::kSfTilesB;
-    const uint32_t stage_bytes =
-        load_a ? kTileBytesA + C::kSfBytesA
-               : C::kTileBytesB + static_cast<uint32_t>(b_tiles) * C::kSfBytesA;
     int i = 0;    // K blocks issued
     for (; i < kb1 - kb0; ++i) {
       const int kb = kb0 + i;
@@ -324,40 +324,41 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
         break;
       }
       uint32_t sf_bytes = C::kSfBytesA;
-      uint32_t bytes = stage_bytes;
       if constexpr (RAG) {
-        if (kb == p.num_kb - 1) {   // fewer scale tiles in the ragged last block
+        if (kb == p.num_kb - 1)     // fewer scale tiles in the ragged last block
           sf_bytes = static_cast<uint32_t>(p.sf_tiles_last) * kSfTileBytes;
-          bytes = load_a ? kTileBytesA + sf_bytes
-                         : C::kTileBytesB + static_cast<uint32_t>(b_tiles) * sf_bytes;
-        }
       }
-      mbar_arrive_expect_tx(&full[s], bytes);
+      // the scales land on their own barrier, so the scale mover copies them
+      // into tensor memory while the operand tiles are still arriving
+      mbar_arrive_expect_tx(&sf_full[s], load_a ? sf_bytes
+                                                : static_cast<uint32_t>(b_tiles) * sf_bytes);
+      mbar_arrive_expect_tx(&full[s], load_a ? kTileBytesA : C::kTileBytesB);
       if (load_a) {
+        bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA,
+                 sfa_k + static_cast<size_t>(kb) * C::kSfBytesA, sf_bytes, &sf_full[s]);
         tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes,
                     m_tile * kBM, &full[s]);
-        bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA,
-                 sfa_k + static_cast<size_t>(kb) * C::kSfBytesA, sf_bytes, &full[s]);
       } else {
-        tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
-                    n_tile * BN, &full[s]);
         for (int t = 0; t < b_tiles; ++t)
           bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + t * C::kSfBytesA,
                    p.sfb + (static_cast<size_t>(b_tile0 + t) * p.nkt) * kSfTileBytes +
                        static_cast<size_t>(kb) * C::kSfBytesA,
-                   sf_bytes, &full[s]);
+                   sf_bytes, &sf_full[s]);
+        tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
+                    n_tile * BN, &full[s]);
       }
     }
     if (i < kb1 - kb0) {   // gave up: let the copies already issued land first
-      for (int j = i > S ? i - S : 0; j < i; ++j)
+      for (int j = i > S ? i - S : 0; j < i; ++j) {
         mbar_wait_bounded(&full[j % S], static_cast<uint32_t>((j / S) & 1));
+        mbar_wait_bounded(&sf_full[j % S], static_cast<uint32_t>((j / S) & 1));
+      }
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
     for (int i = 0; i < kb1 - kb0; ++i) {
       const int s = i % S;
-      // the scale mover waited for full[s] before its copies; waiting for it
-      // here too (already complete) orders the TMA writes before the MMAs
+      // the operand tiles (full[s]) and the scales in tensor memory (sf_ready[s])
       if (!mbar_wait_bounded(&sf_ready[s], static_cast<uint32_t>((i / S) & 1)) ||
           !mbar_wait_bounded(&full[s], static_cast<uint32_t>((i / S) & 1))) {
         *failed = 1;
@@ -385,11 +386,11 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     tc_commit(accum);         // every MMA issued above has completed
   } else if (warp == 3 && lane == 0) {
     // ---- scale mover ----
-    // Slot s is free for stage i: full[s] of stage i means the producers
+    // Slot s is free for stage i: sf_full[s] of stage i means the producers
     // refilled the stage, which waited for the MMAs of stage i - S.
     for (int i = 0; i < kb1 - kb0; ++i) {
       const int s = i % S;
-      if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((i / S) & 1))) {
+      if (!mbar_wait_bounded(&sf_full[s], static_cast<uint32_t>((i / S) & 1))) {
         *failed = 1;
         break;
       }
@@ -514,7 +515,7 @@ struct PCfg {
   }
   static constexpr size_t smem_bytes(int stages) {
     return 1024 + static_cast<size_t>(stages) * Cfg<BN, MX>::kStageBytes +
-           (3 * stages + 2 * kAcc + 2) * 8 + 8;
+           (4 * stages + 2 * kAcc + 2) * 8 + 8;
   }
 };
 
@@ -539,7 +540,8 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
   uint64_t* mma_done = acc_empty + P::kAcc;
   uint64_t* sf_ready = mma_done + 1;
   uint64_t* sf_done = sf_ready + S;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_done + 1);
+  uint64_t* sf_full = sf_done + 1;    // the stage's scale bytes have landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_full + S);
   volatile int* failed = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -554,6 +556,7 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
       mbar_init(&full[s], 2);
       mbar_init(&empty[s], 1);
       mbar_init(&sf_ready[s], 1);
+      mbar_init(&sf_full[s], 2);
     }
     mbar_init(sf_done, 1);
     for (int a = 0; a < P::kAcc; ++a) {
@@ -586,9 +589,6 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const int b_tile0 = n_tile * C::kSfTilesB;
       const int b_tiles = b_tiles_total - b_tile0 < C::kSfTilesB ? b_tiles_total - b_tile0
                                                                   : C::kSfTilesB;
-      const uint32_t stage_bytes =
-          load_a ? kTileBytesA + C::kSfBytesA
-                 : C::kTileBytesB + static_cast<uint32_t>(b_tiles) * C::kSfBytesA;
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
         const int s = it % S;
         if (it >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((it / S - 1) & 1))) {
@@ -597,34 +597,35 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
           break;
         }
         uint32_t sf_bytes = C::kSfBytesA;
-        uint32_t bytes = stage_bytes;
         if constexpr (RAG) {
-          if (kb == p.num_kb - 1) {   // fewer scale tiles in the ragged last block
+          if (kb == p.num_kb - 1)   // fewer scale tiles in the ragged last block
             sf_bytes = static_cast<uint32_t>(p.sf_tiles_last) * kSfTileBytes;
-            bytes = load_a ? kTileBytesA + sf_bytes
-                           : C::kTileBytesB + static_cast<uint32_t>(b_tiles) * sf_bytes;
-          }
         }
-        mbar_arrive_expect_tx(&full[s], bytes);
+        // the scales land on their own barrier (see the one-tile kernel)
+        mbar_arrive_expect_tx(&sf_full[s], load_a ? sf_bytes
+                                                  : static_cast<uint32_t>(b_tiles) * sf_bytes);
+        mbar_arrive_expect_tx(&full[s], load_a ? kTileBytesA : C::kTileBytesB);
         if (load_a) {
+          bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA,
+                   sfa_k + static_cast<size_t>(kb) * C::kSfBytesA, sf_bytes, &sf_full[s]);
           tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes,
                       m_tile * kBM, &full[s]);
-          bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA,
-                   sfa_k + static_cast<size_t>(kb) * C::kSfBytesA, sf_bytes, &full[s]);
         } else {
-          tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
-                      n_tile * BN, &full[s]);
           for (int q = 0; q < b_tiles; ++q)
             bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + q * C::kSfBytesA,
                      p.sfb + static_cast<size_t>(b_tile0 + q) * p.nkt * kSfTileBytes +
                          static_cast<size_t>(kb) * C::kSfBytesA,
-                     sf_bytes, &full[s]);
+                     sf_bytes, &sf_full[s]);
+          tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
+                      n_tile * BN, &full[s]);
         }
       }
     }
     if (!ok) {   // gave up: let the copies already issued land first
-      for (int j = it > S ? it - S : 0; j < it; ++j)
+      for (int j = it > S ? it - S : 0; j < it; ++j) {
         mbar_wait_bounded(&full[j % S], static_cast<uint32_t>((j / S) & 1));
+        mbar_wait_bounded(&sf_full[j % S], static_cast<uint32_t>((j / S) & 1));
+      }
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
@@ -674,7 +675,7 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const int total = my_tiles * p.num_kb;
     for (int it = 0; it < total; ++it) {
       const int s = it % S;
-      if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((it / S) & 1))) {
+      if (!mbar_wait_bounded(&sf_full[s], static_cast<uint32_t>((it / S) & 1))) {
         *failed = 1;
         break;
       }

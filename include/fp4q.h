@@ -223,15 +223,19 @@ FP4Q_API int fp4_gemm_variant(int64_t M, int64_t N, int64_t K, fp4_format_t form
  *   bias      [N] bf16 or NULL, added after alpha.
  *   residual  [M, N] bf16 or NULL, added last; may be `out` itself.
  *   out       [M, N] bf16, row-major.
- *   variant   tile schedule (the README's `variant`): -1 automatic; one CTA per
- *             output tile with 0 = 128 x 128 tiles (two CTAs per SM) or 1 = 128 x 256
- *             tiles; persistent, one CTA per SM walking the tiles, with 2 = 128 x 128
- *             (two accumulators in tensor memory) or 3 = 128 x 256; 4 = 128 x 128
- *             tiles with the K loop of each tile split over a thread-block cluster
- *             of up to 16 CTAs (partial tiles summed in rank order through
- *             distributed shared memory; chosen automatically when the output
- *             has fewer 128 x 128 tiles than half the SMs and K > 1536, e.g. the
- *             M = 41 decode product with K = 6144).
+ *   variant   tile schedule (the README's `variant`; fp4_gemm_variant reports
+ *             the automatic choice): -1 automatic; one CTA per output tile with
+ *             0 = 128 x 128 tiles (two CTAs per SM) or 1 = 128 x 256 tiles;
+ *             persistent CTAs walking the tiles, one accumulator each, loading
+ *             the next tile while the epilogue drains the last, with
+ *             2 = 128 x 128 (two CTAs per SM; automatic when the output has
+ *             more 128 x 128 tiles than twice the SMs) or 3 = 128 x 256 (one
+ *             per SM); 4 = 128 x 128 tiles with the K loop of each tile split
+ *             over a thread-block cluster of up to 16 CTAs (partial tiles
+ *             summed in rank order through distributed shared memory;
+ *             automatic when the output has at most half as many 128 x 128
+ *             tiles as SMs and K > 1536, e.g. the M = 41 decode product with
+ *             K = 6144).
  *   pdl       nonzero: launched as a programmatic dependent of the previous
  *             kernel on `stream`, so its prologue overlaps that kernel's tail
  *             (it waits for that kernel's results before reading anything).

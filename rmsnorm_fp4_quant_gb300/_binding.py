@@ -364,9 +364,10 @@ def gemm_nvfp4_bf16(a_packed, b_packed, sfa, sfb, alpha: float = 1.0, bias=None,
     """bf16 (M, N) = alpha * deq(A) @ deq(B)^T (+ bias) (+ residual) from packed
     NVFP4 operands (M, K/2) and (N, K/2) and their tiled scale buffers.
     fmt "mxfp4" takes MXFP4 operands (UE8M0 scale per 32 codes) instead.
-    variant: -1 automatic, 0 / 1 = one CTA per 128x128 / 128x256 output tile,
-    2 / 3 = persistent CTAs over 128x128 / 128x256 tiles, 4 = 128x128 tiles with
-    the K loop split over a cluster (automatic for few output tiles)."""
+    variant: -1 automatic (see fp4_gemm_variant), 0 / 1 = one CTA per 128x128 /
+    128x256 output tile, 2 / 3 = persistent CTAs over 128x128 / 128x256 tiles
+    (automatic for many tiles), 4 = 128x128 tiles with the K loop split over a
+    cluster (automatic for few output tiles and long K)."""
     torch = _torch()
     for name, t in (("a_packed", a_packed), ("b_packed", b_packed), ("sfa", sfa), ("sfb", sfb)):
         _check_cuda(t, name)

@@ -11,6 +11,13 @@ Operation (FlashInfer page ``add_rmsnorm_fp4quant.py``, ``add_rmsnorm_fp4quant``
 residual <- input + residual; y = residual / sqrt(mean(residual^2) + eps) * weight;
 y quantized to E2M1 with one scale per 16 (NVFP4, E4M3) or 32 (MXFP4, UE8M0)
 elements, scales row-major and/or in the 128x4 tiled layout.
+
+Around it: ``quantize_fp4`` (the same block quantization of x itself, FlashRT
+``quantize_fp4_sfa_*``), and the consumer GEMM on the tensor cores,
+``gemm_nvfp4_bf16`` / ``gemm_nvfp4_gelu`` (FlashRT ``nvfp4_gemm_*``: packed
+E2M1 operands and their tiled scales in, bf16 or NVFP4 out, NVFP4 or MXFP4
+operands, any K that is a multiple of 32), with ``fp4_gemm_variant`` and
+``fp4_launch_shape`` reporting the launches the library would make.
 """
 from ._binding import (  # noqa: F401
     FP4_DT_BF16,

@@ -218,7 +218,8 @@ def test_gemm_full_size_sampled_rows(variant):
 
 
 @pytest.mark.parametrize("K", [2048, 1568])
-def test_gemm_consumes_the_fused_producer_with_pdl(K):
+@pytest.mark.parametrize("variant", [-1, 0, 2])
+def test_gemm_consumes_the_fused_producer_with_pdl(K, variant):
     """The fused op writes A and its tiled scales, fp4_quantize writes B, and the
     GEMM is launched as a programmatic dependent of the quantize kernel.  The
     oracle runs the same chain on the CPU; the producer's bytes equal the
@@ -240,7 +241,7 @@ def test_gemm_consumes_the_fused_producer_with_pdl(K):
     pa, sa = fq.add_rmsnorm_fp4quant(xr, rr, w.cuda(), eps=wl.eps, fmt="nvfp4",
                                      sf_layout="swizzled")
     pb, sb = fq.quantize_fp4(wmat.cuda(), fmt="nvfp4", sf_layout="swizzled")
-    got = fq.gemm_nvfp4_bf16(pa, pb, sa, sb, pdl=True)
+    got = fq.gemm_nvfp4_bf16(pa, pb, sa, sb, pdl=True, variant=variant)
     torch.cuda.synchronize()
     same_a = np.array_equal(pa.cpu().numpy(), oa.packed) and np.array_equal(
         sa.cpu().numpy(), oa.sf_swizzled)
@@ -250,7 +251,8 @@ def test_gemm_consumes_the_fused_producer_with_pdl(K):
     check(got, g, K, "random")
 
 
-def test_gemm_consumes_the_mxfp4_producer():
+@pytest.mark.parametrize("variant", [-1, 2])
+def test_gemm_consumes_the_mxfp4_producer(variant):
     """The headline producer configuration (bf16 rows with outlier columns,
     MXFP4, tiled scales) feeding the MXFP4 GEMM with PDL, against the oracle's
     chain."""
@@ -268,7 +270,7 @@ def test_gemm_consumes_the_mxfp4_producer():
     pa, sa = fq.add_rmsnorm_fp4quant(x.cuda(), r.clone().cuda(), w.cuda(), eps=wl.eps,
                                      fmt="mxfp4", sf_layout="swizzled")
     pb, sb = fq.quantize_fp4(wmat.cuda(), fmt="mxfp4", sf_layout="swizzled")
-    got = fq.gemm_nvfp4_bf16(pa, pb, sa, sb, pdl=True, fmt="mxfp4")
+    got = fq.gemm_nvfp4_bf16(pa, pb, sa, sb, pdl=True, fmt="mxfp4", variant=variant)
     torch.cuda.synchronize()
     assert np.array_equal(pa.cpu().numpy(), oa.packed)
     assert np.array_equal(sa.cpu().numpy(), oa.sf_swizzled)

@@ -273,6 +273,9 @@ def test_gemm_variant_query(L):
     assert v(41, 1536, 6144, fp4_out=True)["variant"] == 0           # no split for FP4 output
     assert v(256, 256, 512, variant=3)["variant"] == 3
     assert L.fp4_gemm_variant(256, 256, 240, 0, 0, -1) == -1         # K % 32
+    assert L.fp4_gemm_variant(256, 256, 32, 0, 0, -1) >= 0           # one half K step
+    assert L.fp4_gemm_variant(41, 520, 288, 1, 0, -1) >= 0           # ragged last K block
+    assert L.fp4_gemm_variant(256, 256, 16, 0, 0, -1) == -1
     assert L.fp4_gemm_variant(256, 256, 512, 1, 0, 2) == 2           # MXFP4 persistent
     assert L.fp4_gemm_variant(256, 264, 512, 0, 1, -1) == -1         # FP4 output: N % 16
     assert L.fp4_gemm_variant(256, 256, 512, 2, 0, -1) == -1         # E4M3-B32 operands

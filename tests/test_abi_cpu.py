@@ -279,3 +279,49 @@ def test_gemm_variant_query(L):
     assert L.fp4_gemm_variant(256, 256, 512, 1, 0, 2) == 2           # MXFP4 persistent
     assert L.fp4_gemm_variant(256, 264, 512, 0, 1, -1) == -1         # FP4 output: N % 16
     assert L.fp4_gemm_variant(256, 256, 512, 2, 0, -1) == -1         # E4M3-B32 operands
+
+
+def _launch_shape_cases():
+    widths = sorted({64, 80, 96, 208, 256, 1536, 2080, 4096, 5120, 6144, 7168, 8224, 12288,
+                     16384, 17408} | {16 * k for k in range(4, 129, 7)})
+    for H in widths:
+        for M in (1, 3, 41, 128, 129, 512, 5000, 32768):
+            for fmt in (0, 1, 2):
+                yield M, H, fmt
+
+
+def test_launch_shape_invariants(L):
+    """Host-side choice of the fused launch (fp4_launch_shape, 152 SMs without
+    a device), over widths up to the register-resident limit, batch sizes and
+    formats: every chunk of a row has a thread, thread counts are whole warps
+    within the instance's limit, a cluster splits a row evenly (on 32-element
+    blocks for the 32-blocks formats), and the grid covers every row the
+    call writes (tiled layouts include the padding rows)."""
+    import rmsnorm_fp4_quant_gb300 as fq
+    checked = 0
+    for M, H, fmt in _launch_shape_cases():
+        if H % (16 if fmt == 0 else 32):
+            continue
+        for lay in (0, 1):
+            s = fq.fp4_launch_shape(M, H, 0, fmt, lay)
+            nchunk = H // 16
+            rows = M if lay == 0 else (M + 127) // 128 * 128
+            cpt, tpr, R, C = (s["chunks_per_thread"], s["threads_per_slice"],
+                              s["slices_per_cta"], s["cluster"])
+            assert 1 <= cpt <= 4 and tpr >= 2 and R >= 1, (M, H, s)
+            assert s["threads_per_cta"] == tpr * R and s["threads_per_cta"] % 32 == 0, (M, H, s)
+            assert s["threads_per_cta"] <= (1024 if cpt == 1 else 512), (M, H, s)
+            assert C in (1, 2, 4, 8) and nchunk % C == 0, (M, H, s)
+            if fmt != 0:
+                assert (nchunk // C) % 2 == 0, (M, H, s)      # whole 32-element blocks
+            assert tpr * cpt >= nchunk // C, (M, H, s)          # every chunk has a thread
+            if s["kernel"] == "fused_direct_kernel":
+                assert s["stages"] == 0
+                if C > 1:
+                    assert R == 1 and s["ctas"] == rows * C, (M, H, s)
+                else:
+                    assert s["ctas"] * R >= rows > (s["ctas"] - 1) * R, (M, H, s)
+            else:
+                assert s["stages"] >= 1 and 1 <= s["ctas"], (M, H, s)
+            checked += 1
+    assert checked > 500

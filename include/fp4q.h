@@ -8,13 +8,15 @@
  * M x H batch, with b = 16 (NVFP4) or 32 (MXFP4), nb = H / b:
  *
  *   h        = round_dtype(float(input) + float(residual))   -> residual (in place)
- *   rstd     = 1 / sqrt(sum(h^2) / H + eps)                   (fp32)
- *   y        = (h * rstd) * weight                            (fp32, never stored)
- *   per block of b elements:
+ *   rstd     = 1 / sqrt(sum(h^2) / H + eps)                   (fp32, each op rounded)
+ *   y        = (h * weight) * rstd                            (fp32: h * weight is exact,
+ *                                                              so y is rounded once)
+ *   per block of b elements (amax = max |y| over the block):
  *     NVFP4: scale = E4M3 nearest-even of min(amax / 6, 448)
  *     MXFP4: scale = UE8M0, the power of two at or above amax / 6
- *     code  = E2M1 nearest-even of y / scale on {0,.5,1,1.5,2,3,4,6}, saturating,
- *             sign in bit 3; a zero scale gives zero codes
+ *     code  = E2M1 nearest-even of y * rn(1 / scale) on {0,.5,1,1.5,2,3,4,6},
+ *             saturating, sign in bit 3 (the page's kernel scales by the
+ *             reciprocal of the decoded scale); a zero scale gives zero codes
  *   out_packed[m, j] = code[2j] | code[2j+1] << 4
  *
  * Scale layouts (same page, `is_sf_swizzled_layout`, `output_both_sf_layouts`):
@@ -72,8 +74,29 @@ typedef enum {
   FP4_ERR_INVALID_ARG = 1,       /* null pointer, bad enum, negative size, overlap */
   FP4_ERR_UNSUPPORTED_SHAPE = 2, /* H % b != 0, H < 64, or H above the maximum     */
   FP4_ERR_MISALIGNED = 3,        /* a pointer breaks the alignment rule below       */
-  FP4_ERR_CUDA = 4               /* the CUDA runtime reported an error on launch    */
+  FP4_ERR_CUDA = 4,              /* the CUDA runtime reported an error on launch    */
+  FP4_ERR_TIMEOUT = 5            /* a kernel gave up on a bounded wait (device status word) */
 } fp4_status_t;
+
+/*
+ * Device status word.  The kernels that wait on asynchronous copies (the
+ * wide-row fused kernel, which streams rows through a shared-memory ring
+ * filled by the copy engine, and every GEMM schedule) bound each wait at about
+ * one second of clock cycles.  A CTA whose wait runs out does not hang or
+ * trap: it stops, marks what it could not compute and returns, and the
+ * context stays usable.  The calls that take an optional `status` (a DEVICE
+ * pointer to one int32_t owned by the caller) then store FP4_ERR_TIMEOUT
+ * there.  The library never writes anything else to it and never clears it:
+ * zero it before the call, synchronise, and read it (fp4_read_device_status
+ * does the last two).  What a timed-out call leaves behind:
+ *   fused op: every scale byte of the rows the CTA did not finish is 0xFF
+ *             (NaN in E4M3 and in UE8M0); their codes, residual rows and y
+ *             rows are unspecified (the residual row may be the old value);
+ *   GEMM:     the output tiles of the CTA are NaN (bf16 out), or their scale
+ *             bytes 0xFF (NVFP4 out).
+ * The host-side return value of the call itself only reports what is known
+ * at launch (FP4_OK once the launch succeeded).
+ */
 
 /* Largest supported H: one CTA holds up to 32768 elements of a row in
  * registers and a thread-block cluster of up to 8 CTAs shares one row.  Above
@@ -110,7 +133,7 @@ FP4Q_API fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, c
  * captured CUDA graph picks up a new value).  global_scale: DEVICE pointer to
  * one positive finite fp32, or NULL for 1.  For the E4M3 formats each block
  * scale becomes E4M3(min(gs * amax / 6, 448)) and codes round from
- * y * (gs / scale) (so dequantised values are y * gs: a consumer divides by gs,
+ * y * rn(rn(1 / scale) * gs) (so dequantised values are y * gs: a consumer divides by gs,
  * e.g. gs = 448 * 6 / max|y| fills the E4M3 range); UE8M0 scales ignore it.
  * All other arguments as fp4_add_rmsnorm_quant.
  */
@@ -122,9 +145,10 @@ FP4Q_API fp4_status_t fp4_add_rmsnorm_quant_gs(const void* input, void* residual
                                                fp4q_stream_t stream);
 
 /*
- * fp4_add_rmsnorm_quant_ex - the general form of the fused op: strided rows
- * and an optional y output (API variants of the FlashInfer page's
- * `add_rmsnorm_fp4quant`, which views 3-D input as 2-D rows).
+ * fp4_add_rmsnorm_quant_ex - the general form of the fused op: strided rows,
+ * an optional y output, a device status word and programmatic dependent
+ * launch (API variants of the FlashInfer page's `add_rmsnorm_fp4quant`,
+ * which views 3-D input as 2-D rows).
  *
  *   input_row_stride, residual_row_stride  elements between consecutive rows
  *                  (0 = H); >= H and a multiple of 16 (rows start 32-byte
@@ -133,8 +157,17 @@ FP4Q_API fp4_status_t fp4_add_rmsnorm_quant_gs(const void* input, void* residual
  *                  (h * w) * rstd rounded to the storage dtype (the value the
  *                  codes quantize), for consumers that want it unquantized.
  *   global_scale   as in fp4_add_rmsnorm_quant_gs (NULL = 1).
- * Everything else as fp4_add_rmsnorm_quant; the outputs and y must not
- * overlap the inputs or each other.
+ *   status         DEVICE int32_t, 4-byte aligned, or NULL: receives
+ *                  FP4_ERR_TIMEOUT if a bounded wait ran out (see "Device
+ *                  status word" above); left untouched otherwise.
+ *   pdl            nonzero: launched as a programmatic dependent of the kernel
+ *                  before it on `stream` (e.g. the GEMM that produced `input`),
+ *                  so the launch overlaps that kernel's tail; the kernel waits
+ *                  for its results before reading anything.  Every kernel of
+ *                  this library lets its own dependents launch once its CTAs
+ *                  have issued their loads.
+ * Everything else as fp4_add_rmsnorm_quant; the outputs, y and status must
+ * not overlap the inputs or each other.
  */
 FP4Q_API fp4_status_t fp4_add_rmsnorm_quant_ex(const void* input, int64_t input_row_stride,
                                                void* residual, int64_t residual_row_stride,
@@ -143,7 +176,7 @@ FP4Q_API fp4_status_t fp4_add_rmsnorm_quant_ex(const void* input, int64_t input_
                                                fp4_format_t format, fp4_sf_layout_t sf_layout,
                                                uint8_t* out_packed, uint8_t* out_sf,
                                                uint8_t* out_sf_rowmajor, void* out_y,
-                                               fp4q_stream_t stream);
+                                               int32_t* status, int pdl, fp4q_stream_t stream);
 
 /*
  * fp4_quantize - block quantization of `input` [M, H] itself, without the
@@ -185,7 +218,8 @@ FP4Q_API int64_t fp4_sf_size_bytes(int64_t M, int64_t H, fp4_format_t format, fp
  * fp4_launch_shape - the launch the library would make for fp4_add_rmsnorm_quant
  * with these sizes on the current device (diagnostics; launches nothing).
  * Fills out[8] = {kernel (0 = persistent TMA-ring kernel, 1 = register-resident
- * kernel), chunks per thread, threads per row slice, row slices per CTA,
+ * kernel, 2 = persistent register-resident kernel with the next row group in
+ * flight), chunks per thread, threads per row slice, row slices per CTA,
  * CTAs per cluster, shared-memory ring stages, threads per CTA, CTAs}.
  * Returns FP4_OK, or the status fp4_add_rmsnorm_quant would return for the sizes.
  */
@@ -299,6 +333,72 @@ FP4Q_API fp4_status_t fp4_gemm_nvfp4_gelu_nvfp4(const uint8_t* a_packed,
                                                 int64_t K, uint8_t* out_packed,
                                                 uint8_t* out_sf, int variant, int pdl,
                                                 fp4q_stream_t stream);
+
+/* Output of the general GEMM entry point fp4_gemm_ex. */
+typedef enum {
+  FP4_EPI_BF16 = 0,        /* alpha * product (+ bias) (+ residual) -> bf16 out   */
+  FP4_EPI_GELU_BF16 = 1,   /* GELU(alpha * product (+ bias)) -> bf16 out          */
+  FP4_EPI_GELU_NVFP4 = 2   /* GELU(...) -> NVFP4 codes + tiled scales (out_packed, out_sf) */
+} fp4_epilogue_t;
+
+/*
+ * fp4_gemm_ex - the general form of the four GEMM entry points above: operand
+ * `format` (FP4_NVFP4 or FP4_MXFP4; FP4_EPI_GELU_NVFP4 takes NVFP4 only), the
+ * `epilogue`, and a device `status` word (DEVICE int32_t, 4-byte aligned, or
+ * NULL) that receives FP4_ERR_TIMEOUT when a CTA's bounded wait ran out (its
+ * tiles are then NaN, or 0xFF scale bytes for NVFP4 output; see "Device status
+ * word").  `residual` is used by FP4_EPI_BF16 only; `out` by the bf16
+ * epilogues, `out_packed` / `out_sf` by FP4_EPI_GELU_NVFP4.  Every other
+ * argument, check and variant as fp4_gemm_nvfp4_bf16 /
+ * fp4_gemm_nvfp4_gelu_nvfp4; the four named entry points are this call with
+ * status = NULL.
+ */
+FP4Q_API fp4_status_t fp4_gemm_ex(const uint8_t* a_packed, const uint8_t* b_packed,
+                                  const uint8_t* sfa, const uint8_t* sfb, fp4_format_t format,
+                                  fp4_epilogue_t epilogue, float alpha, const void* bias,
+                                  const void* residual, int64_t M, int64_t N, int64_t K, void* out,
+                                  uint8_t* out_packed, uint8_t* out_sf, int variant, int pdl,
+                                  int32_t* status, fp4q_stream_t stream);
+
+/*
+ * fp4_read_device_status - synchronises `stream`, then copies the device
+ * status word back and returns it as a status: FP4_OK (0) or FP4_ERR_TIMEOUT;
+ * FP4_ERR_INVALID_ARG for a NULL or misaligned pointer or a value that is no
+ * status; FP4_ERR_CUDA if the synchronisation or the copy failed.  Blocks the
+ * calling thread; not for use inside stream capture.
+ */
+FP4Q_API fp4_status_t fp4_read_device_status(const int32_t* status, fp4q_stream_t stream);
+
+/*
+ * Debug build.  `python -m rmsnorm_fp4_quant_gb300.build --debug` also builds
+ * libfp4q_debug.so: the same entry points compiled with checks of every
+ * global address a kernel computes against the extent of its buffer (an
+ * access outside it is counted and skipped, never made), and with a fault
+ * injector for the bounded waits.  The default libfp4q.so carries neither.
+ *
+ * fp4_debug_build - 1 in the debug build, 0 in the default one.
+ *
+ * fp4_debug_configure - process-wide knobs of the debug build, applied to
+ * every later launch (FP4_ERR_INVALID_ARG in the default build):
+ *   wait_limit_cycles  clock cycles each bounded wait allows (> 0; about one
+ *                      second, 2e9, unless changed);
+ *   shrink_bytes       bytes taken off every buffer extent the checks use
+ *                      (>= 0; 0 for the real extents), so a test can see the
+ *                      checks catch the accesses near the end of a buffer;
+ *   drop_kernel        0 none, 1 the wide-row fused kernel, 2 the GEMM: CTA
+ *                      `drop_cta` arrives on a stage's barrier expecting the
+ *                      bytes of a copy it then never issues, at ring iteration
+ *                      (fused) or K-block count (GEMM) `drop_iter`, so that
+ *                      the wait on that stage runs out with nothing in flight
+ *                      for it and the kernel's timeout path runs;
+ *   violations         DEVICE uint32_t counter (4-byte aligned) that the
+ *                      checks increment, or NULL (not counted).
+ * These knobs are for tests; no default build reads them.
+ */
+FP4Q_API int fp4_debug_build(void);
+FP4Q_API fp4_status_t fp4_debug_configure(int64_t wait_limit_cycles, int64_t shrink_bytes,
+                                          int drop_kernel, int drop_cta, int drop_iter,
+                                          uint32_t* violations);
 
 /* Static, NUL-terminated description of a status code. */
 FP4Q_API const char* fp4_status_string(fp4_status_t status);

@@ -18,6 +18,8 @@ Around it: ``quantize_fp4`` (the same block quantization of x itself, FlashRT
 E2M1 operands and their tiled scales in, bf16 or NVFP4 out, NVFP4 or MXFP4
 operands, any K that is a multiple of 32), with ``fp4_gemm_variant`` and
 ``fp4_launch_shape`` reporting the launches the library would make.
+Kernels that wait on asynchronous copies bound every wait; a call given a
+device ``status`` word learns of a wait that ran out (``read_device_status``).
 """
 from ._binding import (  # noqa: F401
     FP4_DT_BF16,
@@ -28,6 +30,15 @@ from ._binding import (  # noqa: F401
     FP4_SF_BOTH,
     FP4_SF_ROWMAJOR,
     FP4_SF_SWIZZLED,
+    FP4_OK,
+    FP4_ERR_INVALID_ARG,
+    FP4_ERR_UNSUPPORTED_SHAPE,
+    FP4_ERR_MISALIGNED,
+    FP4_ERR_CUDA,
+    FP4_ERR_TIMEOUT,
+    FP4_EPI_BF16,
+    FP4_EPI_GELU_BF16,
+    FP4_EPI_GELU_NVFP4,
     Fp4Error,
     add_rmsnorm_fp4quant,
     dequant,
@@ -41,13 +52,20 @@ from ._binding import (  # noqa: F401
     fp4_gemm_nvfp4_gelu_bf16,
     fp4_gemm_nvfp4_gelu_nvfp4,
     fp4_gemm_nvfp4_bf16,
+    fp4_gemm_ex,
+    fp4_read_device_status,
+    read_device_status,
     fp4_quantize,
     fp4_last_cuda_error,
     fp4_launch_shape,
     fp4_gemm_variant,
     fp4_sf_size_bytes,
     fp4_status_string,
+    debug_lib,
+    fp4_debug_build,
+    fp4_debug_configure,
     lib,
     lib_path,
+    using_library,
     quantize_fp4,
 )

@@ -1,21 +1,27 @@
 """ctypes binding of libfp4q.so: argument marshalling only, no computation."""
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional, Tuple
 
-from .build import LIBPATH
+from .build import DEBUG_LIBPATH, LIBPATH
 
 FP4_DT_BF16, FP4_DT_FP16 = 0, 1
 FP4_NVFP4, FP4_MXFP4, FP4_E4M3_B32 = 0, 1, 2
 FP4_SF_ROWMAJOR, FP4_SF_SWIZZLED, FP4_SF_BOTH = 0, 1, 2
+FP4_OK, FP4_ERR_INVALID_ARG, FP4_ERR_UNSUPPORTED_SHAPE, FP4_ERR_MISALIGNED = 0, 1, 2, 3
+FP4_ERR_CUDA, FP4_ERR_TIMEOUT = 4, 5
+FP4_EPI_BF16, FP4_EPI_GELU_BF16, FP4_EPI_GELU_NVFP4 = 0, 1, 2
 
 _FORMATS = {"nvfp4": FP4_NVFP4, "mxfp4": FP4_MXFP4, "e4m3b32": FP4_E4M3_B32}
 _LAYOUTS = {"rowmajor": FP4_SF_ROWMAJOR, "swizzled": FP4_SF_SWIZZLED, "both": FP4_SF_BOTH}
 _BLOCK = {FP4_NVFP4: 16, FP4_MXFP4: 32, FP4_E4M3_B32: 32}
 
 _lib = None
+_debug_lib = None
+_override = None     # the library the calls below go to inside `using_library`
 
 
 class Fp4Error(RuntimeError):
@@ -32,14 +38,41 @@ def lib_path() -> str:
 
 
 def lib() -> ctypes.CDLL:
-    """Loads libfp4q.so (once).  Raises if it has not been built."""
+    """Loads libfp4q.so (once) and returns it (or the library selected with
+    `using_library`).  Raises if it has not been built."""
     global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(LIBPATH):
-        raise RuntimeError(f"{LIBPATH} is missing: build it with "
-                           "`python -m rmsnorm_fp4_quant_gb300.build` (needs nvcc)")
-    L = ctypes.CDLL(LIBPATH)
+    if _override is not None:
+        return _override
+    if _lib is None:
+        _lib = _open(LIBPATH, "python -m rmsnorm_fp4_quant_gb300.build")
+    return _lib
+
+
+def debug_lib() -> ctypes.CDLL:
+    """Loads libfp4q_debug.so, the build with bounds checks and the fault
+    injector (include/fp4q.h, "Debug build").  Raises if it has not been built."""
+    global _debug_lib
+    if _debug_lib is None:
+        _debug_lib = _open(DEBUG_LIBPATH, "python -m rmsnorm_fp4_quant_gb300.build --debug")
+    return _debug_lib
+
+
+@contextlib.contextmanager
+def using_library(L: ctypes.CDLL):
+    """Inside the block every call of this module goes to `L` (e.g. debug_lib())."""
+    global _override
+    old = _override
+    _override = L
+    try:
+        yield L
+    finally:
+        _override = old
+
+
+def _open(path: str, how: str) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `{how}` (needs nvcc)")
+    L = ctypes.CDLL(path)
     vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     L.fp4_add_rmsnorm_quant.argtypes = [vp, vp, vp, ctypes.c_float, i64, i64, ci, ci, ci,
                                         vp, vp, vp, vp]
@@ -48,7 +81,7 @@ def lib() -> ctypes.CDLL:
                                            vp, vp, vp, vp]
     L.fp4_add_rmsnorm_quant_gs.restype = ci
     L.fp4_add_rmsnorm_quant_ex.argtypes = [vp, i64, vp, i64, vp, vp, ctypes.c_float, i64, i64,
-                                           ci, ci, ci, vp, vp, vp, vp, vp]
+                                           ci, ci, ci, vp, vp, vp, vp, vp, ci, vp]
     L.fp4_add_rmsnorm_quant_ex.restype = ci
     L.fp4_quantize.argtypes = [vp, vp, i64, i64, ci, ci, ci, vp, vp, vp, vp]
     L.fp4_quantize.restype = ci
@@ -75,7 +108,15 @@ def lib() -> ctypes.CDLL:
     L.fp4_gemm_nvfp4_gelu_nvfp4.restype = ci
     L.fp4_gemm_variant.argtypes = [i64, i64, i64, ci, ci, ci]
     L.fp4_gemm_variant.restype = ci
-    _lib = L
+    L.fp4_gemm_ex.argtypes = [vp, vp, vp, vp, ci, ci, ctypes.c_float, vp, vp, i64, i64, i64,
+                              vp, vp, vp, ci, ci, vp, vp]
+    L.fp4_gemm_ex.restype = ci
+    L.fp4_read_device_status.argtypes = [vp, vp]
+    L.fp4_read_device_status.restype = ci
+    L.fp4_debug_build.argtypes = []
+    L.fp4_debug_build.restype = ci
+    L.fp4_debug_configure.argtypes = [i64, i64, ci, ci, ci, vp]
+    L.fp4_debug_configure.restype = ci
     return L
 
 
@@ -105,12 +146,13 @@ def fp4_add_rmsnorm_quant_ex(input_ptr: int, input_row_stride: int, residual_ptr
                              residual_row_stride: int, weight_ptr: int, global_scale_ptr: int,
                              eps: float, M: int, H: int, dtype: int, fmt: int, sf_layout: int,
                              out_packed_ptr: int, out_sf_ptr: int, out_sf_rowmajor_ptr: int,
-                             out_y_ptr: int, stream: int) -> int:
+                             out_y_ptr: int, status_ptr: int, pdl: int, stream: int) -> int:
     return lib().fp4_add_rmsnorm_quant_ex(input_ptr, input_row_stride, residual_ptr,
                                           residual_row_stride, weight_ptr, global_scale_ptr or None,
                                           eps, M, H, dtype, fmt, sf_layout, out_packed_ptr,
                                           out_sf_ptr, out_sf_rowmajor_ptr or None,
-                                          out_y_ptr or None, stream or None)
+                                          out_y_ptr or None, status_ptr or None, pdl,
+                                          stream or None)
 
 
 def fp4_quantize(input_ptr: int, global_scale_ptr: int, M: int, H: int, dtype: int, fmt: int,
@@ -159,6 +201,30 @@ def fp4_gemm_nvfp4_gelu_nvfp4(a_packed_ptr: int, b_packed_ptr: int, sfa_ptr: int
                                            out_sf_ptr, variant, pdl, stream or None)
 
 
+def fp4_gemm_ex(a_packed_ptr: int, b_packed_ptr: int, sfa_ptr: int, sfb_ptr: int, fmt: int,
+                epilogue: int, alpha: float, bias_ptr: int, residual_ptr: int, M: int, N: int,
+                K: int, out_ptr: int, out_packed_ptr: int, out_sf_ptr: int, variant: int,
+                pdl: int, status_ptr: int, stream: int) -> int:
+    return lib().fp4_gemm_ex(a_packed_ptr, b_packed_ptr, sfa_ptr, sfb_ptr, fmt, epilogue, alpha,
+                             bias_ptr or None, residual_ptr or None, M, N, K, out_ptr or None,
+                             out_packed_ptr or None, out_sf_ptr or None, variant, pdl,
+                             status_ptr or None, stream or None)
+
+
+def fp4_read_device_status(status_ptr: int, stream: int) -> int:
+    return lib().fp4_read_device_status(status_ptr or None, stream or None)
+
+
+def fp4_debug_build() -> int:
+    return lib().fp4_debug_build()
+
+
+def fp4_debug_configure(wait_limit_cycles: int, shrink_bytes: int, drop_kernel: int,
+                        drop_cta: int, drop_iter: int, violations_ptr: int) -> int:
+    return lib().fp4_debug_configure(wait_limit_cycles, shrink_bytes, drop_kernel, drop_cta,
+                                     drop_iter, violations_ptr or None)
+
+
 def fp4_sf_size_bytes(M: int, H: int, fmt: int, layout: int) -> int:
     return lib().fp4_sf_size_bytes(M, H, fmt, layout)
 
@@ -182,7 +248,8 @@ def fp4_launch_shape(M: int, H: int, dtype: int, fmt: int, sf_layout: int) -> di
     if st != 0:
         raise Fp4Error(st, "fp4_launch_shape")
     d = dict(zip(_SHAPE_KEYS, list(out)))
-    d["kernel"] = "fused_tma_kernel" if d["kernel"] == 0 else "fused_direct_kernel"
+    d["kernel"] = {0: "fused_tma_kernel", 1: "fused_direct_kernel",
+                   2: "fused_stream_kernel"}[d["kernel"]]
     return d
 
 
@@ -273,17 +340,39 @@ def _row_stride(t, name) -> int:
     raise ValueError(f"{name} must be contiguous or a 2-D view with unit column stride")
 
 
+def _status_ptr(status) -> int:
+    if status is None:
+        return 0
+    torch = _torch()
+    _check_cuda(status, "status")
+    if status.dtype != torch.int32 or status.numel() != 1:
+        raise ValueError("status must be a CUDA int32 tensor with one element")
+    return status.data_ptr()
+
+
+def read_device_status(status, stream=None) -> int:
+    """Synchronises the stream and returns the device status word as a status
+    code (FP4_OK or FP4_ERR_TIMEOUT)."""
+    st = fp4_read_device_status(_status_ptr(status), _stream_handle(stream))
+    if st not in (FP4_OK, FP4_ERR_TIMEOUT):
+        raise Fp4Error(st, "fp4_read_device_status")
+    return st
+
+
 def add_rmsnorm_fp4quant(input, residual, weight, eps: float = 1e-6, fmt: str = "nvfp4",
                          sf_layout: str = "rowmajor", out_packed=None, out_sf=None,
                          out_sf_rowmajor=None, global_scale=None, return_y: bool = False,
-                         out_y=None, stream=None) -> Tuple:
+                         out_y=None, status=None, pdl: bool = False, stream=None) -> Tuple:
     """residual += input (in place); returns (packed, sf) or, for
     sf_layout="both", (packed, sf_tiled, sf_rowmajor), with y (the normalised,
     weighted rows in the input dtype) appended when return_y is set or out_y
     given.  ``input`` may be 2-D (M, H), a 2-D view with a row stride, or 3-D
     (B, S, H); packed has the same leading shape with H/2 bytes.  Scale buffers
     are uint8: row-major (M, H/b), tiled flat.  ``global_scale``: optional CUDA
-    float32 tensor of one element (E4M3 formats)."""
+    float32 tensor of one element (E4M3 formats).  ``status``: optional CUDA
+    int32 tensor of one element that receives FP4_ERR_TIMEOUT if a kernel
+    gave up on a bounded wait (never cleared by the call).  ``pdl``: launch as
+    a programmatic dependent of the previous kernel on the stream."""
     xs = _row_stride(input, "input")
     rs = _row_stride(residual, "residual")
     _check_cuda(weight, "weight")
@@ -311,7 +400,7 @@ def add_rmsnorm_fp4quant(input, residual, weight, eps: float = 1e-6, fmt: str = 
                                   out_packed.data_ptr(), out_sf.data_ptr(),
                                   out_sf_rowmajor.data_ptr() if out_sf_rowmajor is not None else 0,
                                   out_y.data_ptr() if out_y is not None else 0,
-                                  _stream_handle(stream))
+                                  _status_ptr(status), 1 if pdl else 0, _stream_handle(stream))
     if st != 0:
         raise Fp4Error(st, "fp4_add_rmsnorm_quant")
     outs = (out_packed, out_sf, out_sf_rowmajor) if lay == FP4_SF_BOTH else (out_packed, out_sf)
@@ -360,14 +449,17 @@ def dequant(packed, sf, M: int, H: int, fmt: str = "nvfp4", sf_layout: str = "ro
 
 
 def gemm_nvfp4_bf16(a_packed, b_packed, sfa, sfb, alpha: float = 1.0, bias=None, residual=None,
-                    out=None, variant: int = -1, pdl: bool = False, stream=None, fmt="nvfp4"):
+                    out=None, variant: int = -1, pdl: bool = False, stream=None, fmt="nvfp4",
+                    status=None):
     """bf16 (M, N) = alpha * deq(A) @ deq(B)^T (+ bias) (+ residual) from packed
     NVFP4 operands (M, K/2) and (N, K/2) and their tiled scale buffers.
     fmt "mxfp4" takes MXFP4 operands (UE8M0 scale per 32 codes) instead.
     variant: -1 automatic (see fp4_gemm_variant), 0 / 1 = one CTA per 128x128 /
     128x256 output tile, 2 / 3 = persistent CTAs over 128x128 / 128x256 tiles
     (automatic for many tiles), 4 = 128x128 tiles with the K loop split over a
-    cluster (automatic for few output tiles and long K)."""
+    cluster (automatic for few output tiles and long K).  status: optional CUDA
+    int32 tensor of one element that receives FP4_ERR_TIMEOUT if a kernel gave
+    up on a bounded wait (fp4_gemm_ex)."""
     torch = _torch()
     for name, t in (("a_packed", a_packed), ("b_packed", b_packed), ("sfa", sfa), ("sfb", sfb)):
         _check_cuda(t, name)
@@ -387,11 +479,19 @@ def gemm_nvfp4_bf16(a_packed, b_packed, sfa, sfb, alpha: float = 1.0, bias=None,
     _check_cuda(out, "out")
     if fmt not in ("nvfp4", "mxfp4"):
         raise ValueError("fmt must be 'nvfp4' or 'mxfp4'")
-    call = fp4_gemm_nvfp4_bf16 if fmt == "nvfp4" else fp4_gemm_mxfp4_bf16
-    st = call(a_packed.data_ptr(), b_packed.data_ptr(), sfa.data_ptr(), sfb.data_ptr(),
-              float(alpha), bias.data_ptr() if bias is not None else 0,
-              residual.data_ptr() if residual is not None else 0, M, N, K, out.data_ptr(),
-              int(variant), 1 if pdl else 0, _stream_handle(stream))
+    if status is None:
+        call = fp4_gemm_nvfp4_bf16 if fmt == "nvfp4" else fp4_gemm_mxfp4_bf16
+        st = call(a_packed.data_ptr(), b_packed.data_ptr(), sfa.data_ptr(), sfb.data_ptr(),
+                  float(alpha), bias.data_ptr() if bias is not None else 0,
+                  residual.data_ptr() if residual is not None else 0, M, N, K, out.data_ptr(),
+                  int(variant), 1 if pdl else 0, _stream_handle(stream))
+    else:
+        st = fp4_gemm_ex(a_packed.data_ptr(), b_packed.data_ptr(), sfa.data_ptr(),
+                         sfb.data_ptr(), _FORMATS[fmt], FP4_EPI_BF16, float(alpha),
+                         bias.data_ptr() if bias is not None else 0,
+                         residual.data_ptr() if residual is not None else 0, M, N, K,
+                         out.data_ptr(), 0, 0, int(variant), 1 if pdl else 0,
+                         _status_ptr(status), _stream_handle(stream))
     if st != 0:
         raise Fp4Error(st, f"fp4_gemm_{fmt}_bf16")
     return out

@@ -5,7 +5,12 @@ one shared library with the CUDA runtime linked statically, so the library
 loads on any machine with a driver and no matching libcudart.  Rebuilds only
 when a source or header is newer than the library.
 
-    python -m rmsnorm_fp4_quant_gb300.build [--force] [--verbose]
+With --debug (or build(debug=True)) the same sources are compiled with
+-DFP4Q_DEBUG_CHECKS into libfp4q_debug.so: every computed global address is
+checked against its buffer's extent and a fault injector for the bounded waits
+is compiled in (include/fp4q.h, "Debug build").
+
+    python -m rmsnorm_fp4_quant_gb300.build [--force] [--verbose] [--debug]
 """
 from __future__ import annotations
 
@@ -23,6 +28,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIBNAME = "libfp4q.so"
 LIBPATH = os.path.join(LIBDIR, LIBNAME)
+DEBUG_LIBPATH = os.path.join(LIBDIR, "libfp4q_debug.so")
+DEBUG_FLAGS = ["-DFP4Q_DEBUG_CHECKS"]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -46,24 +53,26 @@ def _deps():
         glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIBPATH):
+def up_to_date(path: str = LIBPATH) -> bool:
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIBPATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
     """Compile and link; returns the library path."""
-    if not force and up_to_date():
-        return LIBPATH
+    libpath = DEBUG_LIBPATH if debug else LIBPATH
+    if not force and up_to_date(libpath):
+        return libpath
     nvcc = nvcc_path()
-    objdir = os.path.join(LIBDIR, "obj")
+    objdir = os.path.join(LIBDIR, "obj_debug" if debug else "obj")
     os.makedirs(objdir, exist_ok=True)
+    flags = [*extra_flags, *(DEBUG_FLAGS if debug else [])]
 
     def compile_one(src):
         obj = os.path.join(objdir, os.path.basename(src) + ".o")
-        cmd = [nvcc, *ARCH_FLAGS, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH_FLAGS, *NVCC_FLAGS, *flags, "-c", src, "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{res.stdout}\n{res.stderr}")
@@ -74,13 +83,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     srcs = _sources()
     with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIBPATH + ".tmp"
+    tmp = libpath + ".tmp"
     cmd = [nvcc, *ARCH_FLAGS, "-shared", "-cudart", "static", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIBPATH)
-    return LIBPATH
+    os.replace(tmp, libpath)
+    return libpath
 
 
 if __name__ == "__main__":
@@ -90,4 +99,4 @@ if __name__ == "__main__":
     if extra:
         force = True
         verbose = True
-    print(build(force=force, verbose=verbose, extra_flags=extra))
+    print(build(force=force, verbose=verbose, extra_flags=extra, debug="--debug" in sys.argv))

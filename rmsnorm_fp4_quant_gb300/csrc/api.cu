@@ -4,6 +4,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/fp4q.h"
 #include "fp4q_launch.h"
@@ -14,6 +15,8 @@ cudaError_t launch_fused_bf16(int fmt, const FusedShape& s, const FusedParams& p
 cudaError_t launch_fused_fp16(int fmt, const FusedShape& s, const FusedParams& p, cudaStream_t st);
 int tma_ctas_per_sm_bf16(int fmt, int cpt, int threads, size_t smem);
 int tma_ctas_per_sm_fp16(int fmt, int cpt, int threads, size_t smem);
+int stream_ctas_per_sm_bf16(int fmt, int cpt, int threads);
+int stream_ctas_per_sm_fp16(int fmt, int cpt, int threads);
 
 // Tuning constants of the launch-shape choice (compile-time, overridable with -D).
 #ifndef FP4Q_TMA_CTA_THREADS
@@ -34,6 +37,20 @@ int tma_ctas_per_sm_fp16(int fmt, int cpt, int threads, size_t smem);
 #ifndef FP4Q_DIRECT_CTA_THREADS
 #define FP4Q_DIRECT_CTA_THREADS 128     // target threads of a direct-kernel CTA
 #endif
+#ifndef FP4Q_STREAM
+#define FP4Q_STREAM 1                   // long batches of narrow rows: persistent stream kernel
+#endif
+#ifndef FP4Q_STREAM_CTA_THREADS
+#define FP4Q_STREAM_CTA_THREADS 256     // target threads of a stream-kernel CTA
+#endif
+#ifndef FP4Q_STREAM_MAX_CPT
+#define FP4Q_STREAM_MAX_CPT 4           // chunks per thread allowed in the stream kernel
+#endif
+#ifndef FP4Q_STREAM_MIN_GROUPS
+#define FP4Q_STREAM_MIN_GROUPS 4        // row groups per resident CTA for the stream kernel
+#endif
+
+static_assert(kStatusTimeout == FP4_ERR_TIMEOUT, "device and host timeout status differ");
 
 namespace {
 
@@ -88,11 +105,12 @@ int round_tpr(int chunks, int cpt) {
 // Chunks per thread and slice width for `chunks` chunks: fewest idle lanes,
 // ties broken in the order 2, 1, 3, 4 (fewer registers first, then more
 // work per thread).  min_tpr forces whole warps where the kernel needs them.
-bool pick_cpt(int chunks, int min_tpr, int* cpt_out, int* tpr_out) {
+bool pick_cpt(int chunks, int min_tpr, int* cpt_out, int* tpr_out, int max_cpt = 4) {
   static const int order[4] = {2, 1, 3, 4};
   int best = -1, best_tpr = 0, best_waste = 1 << 30;
   for (int i = 0; i < 4; ++i) {
     const int cpt = order[i];
+    if (cpt > max_cpt) continue;
     int tpr = round_tpr(chunks, cpt);
     if (tpr < min_tpr) tpr = min_tpr;
     if (tpr > max_threads_for_cpt(cpt)) continue;
@@ -141,7 +159,38 @@ bool choose_fused_shape(int64_t M, int64_t rows, int H, int fmt, int dtype, int 
     out->threads = tpr;
     out->smem = 0;
     out->grid = rows * cluster;
+    out->sms = num_sms;
     return true;
+  }
+
+  if (H < FP4Q_TMA_MIN_H && FP4Q_STREAM) {
+    // Long batches: persistent CTAs with the next row group in flight, when
+    // every resident CTA gets several groups.
+    int cpt, tpr;
+    if (pick_cpt(nchunk, 2, &cpt, &tpr, FP4Q_STREAM_MAX_CPT)) {
+      int R = tpr >= FP4Q_STREAM_CTA_THREADS ? 1 : FP4Q_STREAM_CTA_THREADS / tpr;
+      while ((tpr * R) % 32) ++R;                         // whole warps
+      if (tpr * R <= max_threads_for_cpt(cpt)) {
+        const int per = dtype == 0 ? stream_ctas_per_sm_bf16(fmt, cpt, tpr * R)
+                                   : stream_ctas_per_sm_fp16(fmt, cpt, tpr * R);
+        const int64_t resident = static_cast<int64_t>(per) * num_sms;
+        const int64_t groups = (rows + R - 1) / R;
+        if (per > 0 && groups >= FP4Q_STREAM_MIN_GROUPS * resident) {
+          out->path = kPathStream;
+          out->cpt = cpt;
+          out->tpr = tpr;
+          out->rows_per_cta = R;
+          out->cluster = 1;
+          out->chunks_per_cta = nchunk;
+          out->stages = 0;
+          out->threads = tpr * R;
+          out->smem = 0;
+          out->grid = resident;
+          out->sms = num_sms;
+          return true;
+        }
+      }
+    }
   }
 
   if (H < FP4Q_TMA_MIN_H) {
@@ -163,6 +212,7 @@ bool choose_fused_shape(int64_t M, int64_t rows, int H, int fmt, int dtype, int 
     out->threads = tpr * R;
     out->smem = 0;
     out->grid = (rows + R - 1) / R;
+    out->sms = num_sms;
     return true;
   }
 
@@ -200,6 +250,7 @@ bool choose_fused_shape(int64_t M, int64_t rows, int H, int fmt, int dtype, int 
   out->threads = tpr * R;
   out->smem = smem;
   out->grid = grid;
+  out->sms = num_sms;
   return true;
 }
 
@@ -217,6 +268,18 @@ int record_cuda_error(cudaError_t err) {
 }
 
 int sm_count_current_device() { return num_sms_current_device(); }
+
+#ifdef FP4Q_DEBUG_CHECKS
+namespace {
+std::mutex g_debug_mu;
+DebugKnobs g_debug = {kWaitLimitCycles, 0, 0, -1, -1, nullptr};
+}  // namespace
+
+DebugKnobs debug_knobs() {
+  std::lock_guard<std::mutex> lock(g_debug_mu);
+  return g_debug;
+}
+#endif
 
 }  // namespace fp4q
 
@@ -248,6 +311,7 @@ const char* fp4_status_string(fp4_status_t s) {
     case FP4_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
     case FP4_ERR_MISALIGNED: return "misaligned pointer";
     case FP4_ERR_CUDA: return "CUDA error";
+    case FP4_ERR_TIMEOUT: return "a kernel gave up on a bounded wait (timeout)";
     default: return "unknown status";
   }
 }
@@ -282,20 +346,29 @@ static fp4_status_t record_cuda_status(cudaError_t err) {
   return static_cast<fp4_status_t>(record_cuda_error(err));
 }
 
-// Output-side checks shared by the fused op and the standalone quantize.
-static fp4_status_t check_outputs(int64_t M, int64_t H, fp4_format_t format,
-                                  fp4_sf_layout_t sf_layout, const void* act, int64_t act_bytes,
-                                  const uint8_t* out_packed, const uint8_t* out_sf,
-                                  const uint8_t* out_sf_rowmajor) {
+// A buffer the call touches, for the overlap checks.
+struct Extent {
+  const void* p;
+  int64_t bytes;
+};
+
+// True if any two of the non-null extents overlap.
+static bool any_overlap(const Extent* e, int n) {
+  for (int i = 0; i < n; ++i)
+    for (int j = i + 1; j < n; ++j)
+      if (e[i].p && e[j].p && overlap(e[i].p, e[i].bytes, e[j].p, e[j].bytes)) return true;
+  return false;
+}
+
+// Output-side checks shared by the fused op and the standalone quantize:
+// presence and alignment of the outputs.
+static fp4_status_t check_outputs(fp4_sf_layout_t sf_layout, const uint8_t* out_packed,
+                                  const uint8_t* out_sf, const uint8_t* out_sf_rowmajor) {
   if (!out_packed || !out_sf) return FP4_ERR_INVALID_ARG;
   if (sf_layout == FP4_SF_BOTH && !out_sf_rowmajor) return FP4_ERR_INVALID_ARG;
   if (!aligned(out_packed, 8)) return FP4_ERR_MISALIGNED;
   // padding of the tiled buffer is zeroed with 4-byte stores
   if (sf_layout != FP4_SF_ROWMAJOR && !aligned(out_sf, 4)) return FP4_ERR_MISALIGNED;
-  const int64_t sf_bytes = fp4_sf_size_bytes(M, H, format, sf_layout);
-  if (overlap(out_packed, M * H / 2, out_sf, sf_bytes) ||
-      overlap(out_packed, M * H / 2, act, act_bytes) || overlap(out_sf, sf_bytes, act, act_bytes))
-    return FP4_ERR_INVALID_ARG;
   return FP4_OK;
 }
 
@@ -304,7 +377,7 @@ static fp4_status_t fused_call(const void* input, int64_t x_stride, void* residu
                                float eps, int64_t M, int64_t H, fp4_dtype_t dtype,
                                fp4_format_t format, fp4_sf_layout_t sf_layout,
                                uint8_t* out_packed, uint8_t* out_sf, uint8_t* out_sf_rowmajor,
-                               void* out_y, fp4q_stream_t stream) {
+                               void* out_y, int32_t* status, int pdl, fp4q_stream_t stream) {
   if (dtype != FP4_DT_BF16 && dtype != FP4_DT_FP16) return FP4_ERR_INVALID_ARG;
   if (!valid_format(format) || !valid_layout(sf_layout)) return FP4_ERR_INVALID_ARG;
   if (M < 0 || H <= 0 || !(eps >= 0.0f)) return FP4_ERR_INVALID_ARG;
@@ -318,21 +391,29 @@ static fp4_status_t fused_call(const void* input, int64_t x_stride, void* residu
   if (!input || !residual || !weight) return FP4_ERR_INVALID_ARG;
   // rows start on 32-byte boundaries (256-bit accesses, bulk copies)
   if (!aligned(input, 32) || !aligned(residual, 32) || !aligned(weight, 32) ||
-      !aligned(global_scale, 4) || !aligned(out_y, 32) || x_stride % 16 || r_stride % 16)
+      !aligned(global_scale, 4) || !aligned(out_y, 32) || !aligned(status, 4) ||
+      x_stride % 16 || r_stride % 16)
     return FP4_ERR_MISALIGNED;
+  const fp4_status_t st = check_outputs(sf_layout, out_packed, out_sf, out_sf_rowmajor);
+  if (st != FP4_OK) return st;
+  // Nothing the call writes may overlap anything else it reads or writes.
+  // The input and the weight are only read, so they may share memory with
+  // each other (and the global scale with either).
   const int64_t x_bytes = ((M - 1) * x_stride + H) * 2;
   const int64_t r_bytes = ((M - 1) * r_stride + H) * 2;
-  const int64_t y_bytes = M * H * 2;
-  if (overlap(input, x_bytes, residual, r_bytes)) return FP4_ERR_INVALID_ARG;
-  const fp4_status_t st = check_outputs(M, H, format, sf_layout, residual, r_bytes, out_packed,
-                                        out_sf, out_sf_rowmajor);
-  if (st != FP4_OK) return st;
-  if (out_y) {
-    const int64_t sf_bytes = fp4_sf_size_bytes(M, H, format, sf_layout);
-    if (overlap(out_y, y_bytes, input, x_bytes) || overlap(out_y, y_bytes, residual, r_bytes) ||
-        overlap(out_y, y_bytes, out_packed, M * H / 2) || overlap(out_y, y_bytes, out_sf, sf_bytes))
-      return FP4_ERR_INVALID_ARG;
-  }
+  const int64_t nb = H / b;
+  const Extent writes[] = {{residual, r_bytes},
+                           {out_packed, M * H / 2},
+                           {out_sf, fp4_sf_size_bytes(M, H, format, sf_layout)},
+                           {sf_layout == FP4_SF_BOTH ? out_sf_rowmajor : nullptr, M * nb},
+                           {out_y, M * H * 2},
+                           {status, 4}};
+  constexpr int kWrites = sizeof(writes) / sizeof(writes[0]);
+  if (any_overlap(writes, kWrites)) return FP4_ERR_INVALID_ARG;
+  const Extent reads[] = {{input, x_bytes}, {weight, H * 2}, {global_scale, 4}};
+  for (const Extent& w : writes)
+    for (const Extent& r : reads)
+      if (w.p && r.p && overlap(w.p, w.bytes, r.p, r.bytes)) return FP4_ERR_INVALID_ARG;
 
   FusedShape shape;
   const int64_t rows = sf_layout == FP4_SF_ROWMAJOR ? M : (M + 127) / 128 * 128;
@@ -355,6 +436,7 @@ static fp4_status_t fused_call(const void* input, int64_t x_stride, void* residu
                                            : nullptr;
   p.gs = global_scale;
   p.y = out_y;
+  p.status = status;
   p.x_stride = x_stride;
   p.r_stride = r_stride;
   p.eps = eps;
@@ -370,11 +452,13 @@ static fp4_status_t fused_call(const void* input, int64_t x_stride, void* residu
   p.chunks_per_cta = shape.chunks_per_cta;
   p.stages = shape.stages;
   p.groups = (rows + shape.rows_per_cta - 1) / shape.rows_per_cta;
+  FP4Q_SET_DEBUG(p);
 
-  cudaError_t err = launch_fused(dtype == FP4_DT_BF16 ? 0 : 1, static_cast<int>(format), shape,
-                                 p, reinterpret_cast<cudaStream_t>(stream));
-  if (err == cudaSuccess) err = cudaGetLastError();
-  return record_cuda_status(err);
+  shape.pdl = pdl ? 1 : 0;
+  // cudaLaunchKernelEx reports this launch's own errors; the thread's sticky
+  // last error (which may belong to the caller) is left alone
+  return record_cuda_status(launch_fused(dtype == FP4_DT_BF16 ? 0 : 1, static_cast<int>(format),
+                                         shape, p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void* weight,
@@ -383,7 +467,7 @@ fp4_status_t fp4_add_rmsnorm_quant(const void* input, void* residual, const void
                                    uint8_t* out_packed, uint8_t* out_sf,
                                    uint8_t* out_sf_rowmajor, fp4q_stream_t stream) {
   return fused_call(input, H, residual, H, weight, nullptr, eps, M, H, dtype, format, sf_layout,
-                    out_packed, out_sf, out_sf_rowmajor, nullptr, stream);
+                    out_packed, out_sf, out_sf_rowmajor, nullptr, nullptr, 0, stream);
 }
 
 fp4_status_t fp4_add_rmsnorm_quant_gs(const void* input, void* residual, const void* weight,
@@ -393,7 +477,7 @@ fp4_status_t fp4_add_rmsnorm_quant_gs(const void* input, void* residual, const v
                                       uint8_t* out_sf, uint8_t* out_sf_rowmajor,
                                       fp4q_stream_t stream) {
   return fused_call(input, H, residual, H, weight, global_scale, eps, M, H, dtype, format,
-                    sf_layout, out_packed, out_sf, out_sf_rowmajor, nullptr, stream);
+                    sf_layout, out_packed, out_sf, out_sf_rowmajor, nullptr, nullptr, 0, stream);
 }
 
 fp4_status_t fp4_add_rmsnorm_quant_ex(const void* input, int64_t input_row_stride,
@@ -402,11 +486,11 @@ fp4_status_t fp4_add_rmsnorm_quant_ex(const void* input, int64_t input_row_strid
                                       int64_t M, int64_t H, fp4_dtype_t dtype,
                                       fp4_format_t format, fp4_sf_layout_t sf_layout,
                                       uint8_t* out_packed, uint8_t* out_sf,
-                                      uint8_t* out_sf_rowmajor, void* out_y,
-                                      fp4q_stream_t stream) {
+                                      uint8_t* out_sf_rowmajor, void* out_y, int32_t* status,
+                                      int pdl, fp4q_stream_t stream) {
   return fused_call(input, input_row_stride, residual, residual_row_stride, weight, global_scale,
                     eps, M, H, dtype, format, sf_layout, out_packed, out_sf, out_sf_rowmajor,
-                    out_y, stream);
+                    out_y, status, pdl, stream);
 }
 
 fp4_status_t fp4_quantize(const void* input, const float* global_scale, int64_t M, int64_t H,
@@ -421,9 +505,16 @@ fp4_status_t fp4_quantize(const void* input, const float* global_scale, int64_t 
   if (M == 0) return FP4_OK;
   if (!input) return FP4_ERR_INVALID_ARG;
   if (!aligned(input, 32) || !aligned(global_scale, 4)) return FP4_ERR_MISALIGNED;
-  const fp4_status_t st = check_outputs(M, H, format, sf_layout, input, M * H * 2, out_packed,
-                                        out_sf, out_sf_rowmajor);
+  const fp4_status_t st = check_outputs(sf_layout, out_packed, out_sf, out_sf_rowmajor);
   if (st != FP4_OK) return st;
+  const Extent writes[] = {{out_packed, M * H / 2},
+                           {out_sf, fp4_sf_size_bytes(M, H, format, sf_layout)},
+                           {sf_layout == FP4_SF_BOTH ? out_sf_rowmajor : nullptr, M * (H / b)}};
+  if (any_overlap(writes, 3)) return FP4_ERR_INVALID_ARG;
+  for (const Extent& w : writes)
+    if (w.p && (overlap(w.p, w.bytes, input, M * H * 2) ||
+                (global_scale && overlap(w.p, w.bytes, global_scale, 4))))
+      return FP4_ERR_INVALID_ARG;
   QuantParams p{};
   p.x = input;
   p.packed = out_packed;
@@ -438,9 +529,45 @@ fp4_status_t fp4_quantize(const void* input, const float* global_scale, int64_t 
   p.nchunk = static_cast<int>(H / 16);
   p.nb = static_cast<int>(H / b);
   p.nkt = (p.nb + 3) / 4;
+  FP4Q_SET_DEBUG(p);
   return record_cuda_status(launch_quantize(dtype == FP4_DT_BF16 ? 0 : 1, static_cast<int>(format), p,
                                      num_sms_current_device(),
                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp4_debug_build(void) {
+#ifdef FP4Q_DEBUG_CHECKS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+fp4_status_t fp4_debug_configure(int64_t wait_limit_cycles, int64_t shrink_bytes, int drop_kernel,
+                                 int drop_cta, int drop_iter, uint32_t* violations) {
+#ifdef FP4Q_DEBUG_CHECKS
+  if (wait_limit_cycles <= 0 || shrink_bytes < 0 || drop_kernel < 0 || drop_kernel > 2)
+    return FP4_ERR_INVALID_ARG;
+  if (violations && !aligned(violations, 4)) return FP4_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_debug_mu);
+  g_debug = DebugKnobs{wait_limit_cycles, shrink_bytes, drop_kernel, drop_cta, drop_iter,
+                       reinterpret_cast<unsigned int*>(violations)};
+  return FP4_OK;
+#else
+  (void)wait_limit_cycles; (void)shrink_bytes; (void)drop_kernel; (void)drop_cta;
+  (void)drop_iter; (void)violations;
+  return FP4_ERR_INVALID_ARG;   // the knobs exist in the debug build only
+#endif
+}
+
+fp4_status_t fp4_read_device_status(const int32_t* status, fp4q_stream_t stream) {
+  if (!status || !aligned(status, 4)) return FP4_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  int32_t v = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&v, status, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return record_cuda_status(e);
+  return v == FP4_OK || v == FP4_ERR_TIMEOUT ? static_cast<fp4_status_t>(v) : FP4_ERR_INVALID_ARG;
 }
 
 fp4_status_t fp4_dequant(const uint8_t* packed, const uint8_t* sf, int64_t M, int64_t H,

@@ -7,6 +7,7 @@
 namespace fp4q {
 
 constexpr long long kWaitLimitCycles = 2000000000LL;   // ~1 s at 2 GHz
+constexpr int kStatusTimeout = 5;                      // FP4_ERR_TIMEOUT of the C ABI
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -32,12 +33,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
                : "=r"(done) : "r"(smem_addr(bar)), "r"(parity) : "memory");
   return done != 0;
 }
-// Bounded wait for phase `parity` of `bar`; false if it did not complete.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Bounded wait for phase `parity` of `bar`; false if it did not complete
+// within `limit` clock cycles.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long start = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - start > kWaitLimitCycles) return false;
+    if (clock64() - start > limit) return false;
   }
   return true;
 }
@@ -80,6 +83,18 @@ __device__ __forceinline__ float4 ld_peer_f32x4(uint32_t remote) {
   asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote) : "memory");
   return v;
+}
+
+// --- programmatic dependent launch ---------------------------------------------
+// Wait until the preceding grid on the stream has completed and its writes are
+// visible / allow the next grid to be scheduled (it still waits for this grid's
+// completion in its own griddep_wait).  Both are no-ops when the launch has no
+// programmatic-serialization attribute.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 }  // namespace fp4q

@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "debug_checks.h"
+
 namespace fp4q {
 
 // Shared by the C entry points (api.cu, gemm_api.cu).
@@ -33,6 +35,7 @@ struct FusedParams {
   uint8_t* sf_rm;
   const float* gs;     // device global scale (one fp32) or null for 1
   void* y;             // optional [M, H] dtype output of y (dense), or null
+  int* status;         // optional device status word: set to the timeout status on a timeout
   int64_t x_stride;    // elements between rows of x
   int64_t r_stride;    // elements between rows of the residual
   float eps;
@@ -47,11 +50,27 @@ struct FusedParams {
   int cluster;         // CTAs per row (direct kernel), 1 otherwise
   int chunks_per_cta;  // nchunk / cluster
   int stages;          // shared-memory ring depth (TMA kernel)
-  int64_t groups;      // ceil(rows / rows_per_cta) (TMA kernel)
+  int64_t groups;      // ceil(rows / rows_per_cta) (persistent kernels)
+  FP4Q_DEBUG_FIELD     // debug build only: checks and fault injection
 };
+
+// Byte extents of the buffers of a fused call, as the C ABI defines them.
+__host__ __device__ inline long long x_extent(const FusedParams& p) {
+  return ((p.M - 1) * p.x_stride + p.H) * 2;
+}
+__host__ __device__ inline long long r_extent(const FusedParams& p) {
+  return ((p.M - 1) * p.r_stride + p.H) * 2;
+}
+__host__ __device__ inline long long packed_extent(int64_t M, int H) {
+  return M * static_cast<long long>(H) / 2;
+}
+__host__ __device__ inline long long tiled_extent(int64_t M, int nkt) {
+  return (M + 127) / 128 * static_cast<long long>(nkt) * 512;
+}
 
 constexpr int kPathTma = 0;       // persistent CTAs, TMA bulk-copy row ring
 constexpr int kPathDirect = 1;    // register-resident rows, optionally one row per cluster
+constexpr int kPathStream = 2;    // persistent CTAs, register-resident rows, next row in flight
 
 // Launch shape chosen on the host for one (M, H, format, dtype).
 struct FusedShape {
@@ -65,6 +84,8 @@ struct FusedShape {
   int threads;         // tpr * rows_per_cta
   size_t smem;         // dynamic shared memory bytes
   int64_t grid;        // CTAs
+  int sms;             // SMs the grid was sized for (persistent paths)
+  int pdl;             // launch as a programmatic dependent of the previous kernel
 };
 
 // Picks the launch shape; returns false when the shape cannot be handled.
@@ -107,6 +128,7 @@ struct QuantParams {
   int nb;
   int nkt;
   int evict_first;     // read the input with the L2 evict-first policy (set by the launcher)
+  FP4Q_DEBUG_FIELD     // debug build only: checks
 };
 
 cudaError_t launch_quantize(int dtype, int fmt, const QuantParams& p, int num_sms,

@@ -36,9 +36,9 @@ __device__ __forceinline__ float load_global_scale(const float* gs) {
 // this thread's partial sum of h^2 (exact squares from the mixed-precision
 // FMA; two fp32 lanes: even / odd elements, chunk order).
 template <typename T, int CPT>
-__device__ __forceinline__ float add_and_write_back(Chunk (&h)[CPT], const Chunk (&rr)[CPT],
-                                                    T* rrow, int c0, int tpr, int c_end,
-                                                    bool row_ok) {
+__device__ __forceinline__ float add_and_write_back(const FusedParams& p, Chunk (&h)[CPT],
+                                                    const Chunk (&rr)[CPT], T* rrow, int c0,
+                                                    int tpr, int c_end, bool row_ok) {
   float2 ss2 = make_float2(0.0f, 0.0f);
 #pragma unroll
   for (int k = 0; k < CPT; ++k) {
@@ -50,7 +50,7 @@ __device__ __forceinline__ float add_and_write_back(Chunk (&h)[CPT], const Chunk
         h[k].u[j] = u;
         Pair<T>::sq_acc(u, ss2);
       }
-      st_stream(rrow + c * 16, h[k]);
+      if (FP4Q_IN_RANGE(p, rrow + c * 16, 32, p.r, r_extent(p))) st_stream(rrow + c * 16, h[k]);
     }
   }
   return ss2.x + ss2.y;
@@ -85,7 +85,8 @@ __device__ __forceinline__ void quantize_and_store(const Chunk (&h)[CPT], float 
     float y[16];
     float amax = 0.0f;
     if (ok) {
-      const Chunk wc = ld_cached_ro(wvec + c * 16);
+      Chunk wc = {};
+      if (FP4Q_IN_RANGE(p, wvec + c * 16, 32, p.w, 2LL * p.H)) wc = ld_cached_ro(wvec + c * 16);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float2 yy = __fmul2_rn(Pair<T>::mul(h[k].u[j], wc.u[j]), rstd2);   // (h * w) * rstd
@@ -102,7 +103,8 @@ __device__ __forceinline__ void quantize_and_store(const Chunk (&h)[CPT], float 
       Chunk yc;
 #pragma unroll
       for (int j = 0; j < 8; ++j) yc.u[j] = Pair<T>::from_f32(y[2 * j], y[2 * j + 1]);
-      st_stream(static_cast<T*>(p.y) + static_cast<size_t>(row) * p.H + c * 16, yc);
+      T* yp = static_cast<T*>(p.y) + static_cast<size_t>(row) * p.H + c * 16;
+      if (FP4Q_IN_RANGE(p, yp, 32, p.y, 2LL * p.M * p.H)) st_stream(yp, yc);
     }
     if (ok) {
       float v[16];
@@ -124,17 +126,23 @@ __device__ __forceinline__ void quantize_and_store(const Chunk (&h)[CPT], float 
       }
       const uint64_t packed = static_cast<uint64_t>(e2m1_pack8(v)) |
                               (static_cast<uint64_t>(e2m1_pack8(v + 8)) << 32);
-      st_u64(prow + static_cast<size_t>(c) * 8, packed);
+      if (FP4Q_IN_RANGE(p, prow + static_cast<size_t>(c) * 8, 8, p.packed, packed_extent(p.M, p.H)))
+        st_u64(prow + static_cast<size_t>(c) * 8, packed);
 
       const bool owner = !Fmt<FMT>::kBlock32 || ((c & 1) == 0);
       if (owner) {
         const int kb = Fmt<FMT>::kBlock32 ? (c >> 1) : c;
-        if (p.sf_rm) st_u8(p.sf_rm + static_cast<size_t>(row) * p.nb + kb, code);
+        uint8_t* rm = p.sf_rm + static_cast<size_t>(row) * p.nb + kb;
+        if (p.sf_rm && FP4Q_IN_RANGE(p, rm, 1, p.sf_rm, static_cast<long long>(p.M) * p.nb))
+          st_u8(rm, code);
         if (p.sf_tiled) {
-          st_u8(p.sf_tiled + tiled_sf_offset(row, kb, p.nkt), code);
+          uint8_t* tl = p.sf_tiled + tiled_sf_offset(row, kb, p.nkt);
+          if (FP4Q_IN_RANGE(p, tl, 1, p.sf_tiled, tiled_extent(p.M, p.nkt))) st_u8(tl, code);
           if (kb == p.nb - 1) {   // k padding of the last 4-block group
-            for (int kk = p.nb; kk < 4 * p.nkt; ++kk)
-              st_u8(p.sf_tiled + tiled_sf_offset(row, kk, p.nkt), 0u);
+            for (int kk = p.nb; kk < 4 * p.nkt; ++kk) {
+              uint8_t* pad = p.sf_tiled + tiled_sf_offset(row, kk, p.nkt);
+              if (FP4Q_IN_RANGE(p, pad, 1, p.sf_tiled, tiled_extent(p.M, p.nkt))) st_u8(pad, 0u);
+            }
           }
         }
       }
@@ -146,7 +154,10 @@ __device__ __forceinline__ void quantize_and_store(const Chunk (&h)[CPT], float 
 // nkt four-byte groups.
 __device__ __forceinline__ void zero_tiled_row(const FusedParams& p, int64_t row, int lane,
                                                int tpr) {
-  for (int g = lane; g < p.nkt; g += tpr) st_u32(p.sf_tiled + tiled_sf_offset(row, 4 * g, p.nkt), 0u);
+  for (int g = lane; g < p.nkt; g += tpr) {
+    uint8_t* q = p.sf_tiled + tiled_sf_offset(row, 4 * g, p.nkt);
+    if (FP4Q_IN_RANGE(p, q, 4, p.sf_tiled, tiled_extent(p.M, p.nkt))) st_u32(q, 0u);
+  }
 }
 
 // Marks a row whose inputs never arrived: every scale byte of the slice set
@@ -158,8 +169,12 @@ __device__ __forceinline__ void mark_row_failed(const FusedParams& p, int64_t ro
   for (int c = c0; c < c_end; c += tpr) {
     if (Fmt<FMT>::kBlock32 && (c & 1)) continue;
     const int kb = Fmt<FMT>::kBlock32 ? (c >> 1) : c;
-    if (p.sf_rm) st_u8(p.sf_rm + static_cast<size_t>(row) * p.nb + kb, 0xFFu);
-    if (p.sf_tiled) st_u8(p.sf_tiled + tiled_sf_offset(row, kb, p.nkt), 0xFFu);
+    uint8_t* rm = p.sf_rm + static_cast<size_t>(row) * p.nb + kb;
+    if (p.sf_rm && FP4Q_IN_RANGE(p, rm, 1, p.sf_rm, static_cast<long long>(p.M) * p.nb))
+      st_u8(rm, 0xFFu);
+    uint8_t* tl = p.sf_tiled + tiled_sf_offset(row, kb, p.nkt);
+    if (p.sf_tiled && FP4Q_IN_RANGE(p, tl, 1, p.sf_tiled, tiled_extent(p.M, p.nkt)))
+      st_u8(tl, 0xFFu);
   }
 }
 

@@ -57,17 +57,19 @@ fused_direct_kernel(const FusedParams p) {
   const T* xrow = static_cast<const T*>(p.x) + xoff;
   T* rrow = static_cast<T*>(p.r) + (EX ? rsafe * static_cast<size_t>(p.r_stride) : xoff);
 
+  griddep_wait();                            // inputs may come from the kernel before (PDL)
   Chunk h[CPT];
   Chunk rr[CPT];
 #pragma unroll
   for (int k = 0; k < CPT; ++k) {
     const int c = c0 + k * tpr;
     if (row_ok && c < c_end) {
-      h[k] = ld_stream_ro(xrow + c * 16);
-      rr[k] = ld_stream_rw(rrow + c * 16);
+      if (FP4Q_IN_RANGE(p, xrow + c * 16, 32, p.x, x_extent(p))) h[k] = ld_stream_ro(xrow + c * 16);
+      if (FP4Q_IN_RANGE(p, rrow + c * 16, 32, p.r, r_extent(p))) rr[k] = ld_stream_rw(rrow + c * 16);
     }
   }
-  float ss = add_and_write_back<T, CPT>(h, rr, rrow, c0, tpr, c_end, row_ok);
+  griddep_launch_dependents();
+  float ss = add_and_write_back<T, CPT>(p, h, rr, rrow, c0, tpr, c_end, row_ok);
 
   // slice reduction: shuffles within the slice's lanes, then its warps in order
   const int width = tpr < 32 ? tpr : 32;

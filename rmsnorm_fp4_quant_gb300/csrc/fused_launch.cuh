@@ -1,31 +1,32 @@
 // fused_launch.cuh - launch helpers instantiated once per storage dtype.
 #pragma once
 
-#include <atomic>
 #include <mutex>
 
 #include "fused_direct.cuh"
+#include "fused_stream.cuh"
 #include "fused_tma.cuh"
 
 namespace fp4q {
 
 template <typename T, int FMT, int CPT, bool EX>
 cudaError_t raise_smem_limit(size_t smem) {
-  // the limit is a per-device function attribute: raise it when a launch
-  // needs more than any earlier one on this device
-  static std::atomic<size_t> done[64];
+  // The limit is a per-device function attribute, only ever raised: a launch
+  // that needs more than any earlier one on this device raises it to its own
+  // need.  The check, the attribute call and the record happen under one
+  // lock, so two host threads cannot lower the limit below what either has
+  // launched with.
+  static size_t done[64] = {};
+  static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_relaxed) >= smem)
-    return cudaSuccess;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev] >= smem) return cudaSuccess;
   e = cudaFuncSetAttribute(fused_tma_kernel<T, FMT, CPT, EX>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e == cudaSuccess && dev >= 0 && dev < 64) {
-    size_t cur = done[dev].load(std::memory_order_relaxed);
-    while (cur < smem && !done[dev].compare_exchange_weak(cur, smem)) {
-    }
-  }
+  if (e == cudaSuccess) done[dev] = smem;
   return e;
 }
 
@@ -53,6 +54,52 @@ int ctas_per_sm_one(int threads, size_t smem) {
     last[dev] = Last{threads, smem, n};
   }
   return n;
+}
+
+// CTAs of a fused_stream_kernel instance resident per SM at `threads` threads
+// (cached per device: calls repeat the same launch shape).
+template <typename T, int FMT, int CPT, bool EX>
+int stream_ctas_per_sm_one(int threads) {
+  struct Last { int threads; int n; };
+  static Last last[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const bool cacheable = dev >= 0 && dev < 64;
+  if (cacheable) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (last[dev].n > 0 && last[dev].threads == threads) return last[dev].n;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_stream_kernel<T, FMT, CPT, EX>,
+                                                    threads, 0) != cudaSuccess)
+    return 0;
+  if (cacheable) {
+    std::lock_guard<std::mutex> lock(mu);
+    last[dev] = Last{threads, n};
+  }
+  return n;
+}
+
+template <typename T, int FMT>
+int stream_ctas_per_sm_fmt(int cpt, int threads) {
+  switch (cpt) {
+    case 1: return stream_ctas_per_sm_one<T, FMT, 1, false>(threads);
+    case 2: return stream_ctas_per_sm_one<T, FMT, 2, false>(threads);
+    case 3: return stream_ctas_per_sm_one<T, FMT, 3, false>(threads);
+    case 4: return stream_ctas_per_sm_one<T, FMT, 4, false>(threads);
+    default: return 0;
+  }
+}
+
+template <typename T>
+int stream_ctas_per_sm_dtype(int fmt, int cpt, int threads) {
+  switch (fmt) {
+    case kFmtNV: return stream_ctas_per_sm_fmt<T, kFmtNV>(cpt, threads);
+    case kFmtMX: return stream_ctas_per_sm_fmt<T, kFmtMX>(cpt, threads);
+    case kFmtE4B32: return stream_ctas_per_sm_fmt<T, kFmtE4B32>(cpt, threads);
+    default: return 0;
+  }
 }
 
 template <typename T, int FMT>
@@ -84,19 +131,34 @@ cudaError_t launch_one(const FusedShape& s, const FusedParams& p, cudaStream_t s
   cfg.gridDim = dim3(static_cast<unsigned>(s.grid), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(s.threads), 1, 1);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
   cfg.numAttrs = 0;
+  if (s.pdl) {
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    ++cfg.numAttrs;
+  }
   if (s.path == kPathDirect) {
     if (s.cluster > 1) {
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = static_cast<unsigned>(s.cluster);
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.numAttrs = 1;
+      attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+      attr[cfg.numAttrs].val.clusterDim.x = static_cast<unsigned>(s.cluster);
+      attr[cfg.numAttrs].val.clusterDim.y = 1;
+      attr[cfg.numAttrs].val.clusterDim.z = 1;
+      ++cfg.numAttrs;
     }
     cfg.dynamicSmemBytes = 0;
     return cudaLaunchKernelEx(&cfg, fused_direct_kernel<T, FMT, CPT, EX>, p);
+  }
+  if (s.path == kPathStream) {
+    if (EX) {   // the general instance may hold fewer CTAs per SM: never more than resident
+      const int per = stream_ctas_per_sm_one<T, FMT, CPT, EX>(s.threads);
+      if (per <= 0) return cudaErrorInvalidConfiguration;
+      const int64_t resident = static_cast<int64_t>(per) * s.sms;
+      if (resident < s.grid) cfg.gridDim.x = static_cast<unsigned>(resident);
+    }
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, fused_stream_kernel<T, FMT, CPT, EX>, p);
   }
   const cudaError_t e = raise_smem_limit<T, FMT, CPT, EX>(s.smem);
   if (e != cudaSuccess) return e;

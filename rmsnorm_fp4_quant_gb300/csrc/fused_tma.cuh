@@ -21,8 +21,14 @@
 //
 // Every mbarrier wait is bounded (~1 s of clock cycles).  A CTA whose wait
 // runs out agrees on it with __syncthreads_or, marks the scale bytes of its
-// remaining rows 0xFF (NaN in E4M3 and UE8M0), lets thread 0 wait (bounded)
-// for its copies still in flight, and returns.
+// remaining rows 0xFF (NaN in E4M3 and UE8M0), stores the timeout status in
+// the caller's status word (if any), lets thread 0 drain the copies still in
+// flight, and returns.  The drain waits, each bounded the same way, for every
+// stage that has a copy issued; a stage whose wait ran out because the bytes
+// it expects never arrive holds no copy that could still land.  A bulk copy
+// from device memory that has been issued either completes or faults the
+// context, so once those waits end no copy can still be writing into this
+// CTA's shared memory.
 #pragma once
 
 #include "async_copy.cuh"
@@ -74,12 +80,14 @@ fused_tma_kernel(const FusedParams p) {
     const uint32_t nrows = left <= 0 ? 0u : static_cast<uint32_t>(left < R ? left : R);
     const uint32_t bytes = nrows * 2u * H;
     mbar_arrive_expect_tx(&full[s], 2u * bytes);   // zero bytes completes the phase at once
+    if (FP4Q_DROP(p, 1, static_cast<int>(b), static_cast<int>(it))) return;   // debug build
     if (bytes) {
       uint8_t* st = smem + static_cast<size_t>(s) * 2u * half_stage;
       // rows of a stage are contiguous in memory (strided rows run with R = 1)
-      bulk_g2s(st, static_cast<const T*>(p.x) + row0 * (EX ? p.x_stride : H), bytes, &full[s]);
-      bulk_g2s(st + half_stage, static_cast<const T*>(p.r) + row0 * (EX ? p.r_stride : H), bytes,
-               &full[s]);
+      const T* xs = static_cast<const T*>(p.x) + row0 * (EX ? p.x_stride : H);
+      const T* rs = static_cast<const T*>(p.r) + row0 * (EX ? p.r_stride : H);
+      if (FP4Q_IN_RANGE(p, xs, bytes, p.x, x_extent(p))) bulk_g2s(st, xs, bytes, &full[s]);
+      if (FP4Q_IN_RANGE(p, rs, bytes, p.r, r_extent(p))) bulk_g2s(st + half_stage, rs, bytes, &full[s]);
     }
   };
 
@@ -88,9 +96,11 @@ fused_tma_kernel(const FusedParams p) {
     mbar_init_fence();
   }
   __syncthreads();
+  griddep_wait();                            // inputs may come from the kernel before (PDL)
   if (tid == 0) {
     for (int64_t it = 0; it < n_iter && it < S; ++it) issue(it);
   }
+  griddep_launch_dependents();
 
   const int warp = tid >> 5;
   const int wpr = tpr >> 5;                         // warps per slice (tpr >= 32)
@@ -101,7 +111,7 @@ fused_tma_kernel(const FusedParams p) {
     const int64_t row = (b + it * G) * R + grp;
     const bool row_ok = row < p.M;
 
-    const bool ok = mbar_wait_bounded(&full[s], parity);
+    const bool ok = mbar_wait_bounded(&full[s], parity, FP4Q_WAIT_LIMIT(p));
     Chunk h[CPT];
     Chunk rr[CPT];
     if (ok && row_ok) {
@@ -118,7 +128,7 @@ fused_tma_kernel(const FusedParams p) {
     }
     T* rrow = static_cast<T*>(p.r) + static_cast<size_t>(row_ok ? row : 0) *
                                          static_cast<size_t>(EX ? p.r_stride : H);
-    float ss = add_and_write_back<T, CPT>(h, rr, rrow, lane, tpr, c_end, ok && row_ok);
+    float ss = add_and_write_back<T, CPT>(p, h, rr, rrow, lane, tpr, c_end, ok && row_ok);
 
     const int width = tpr < 32 ? tpr : 32;
     for (int o = width >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(kFullMask, ss, o);
@@ -130,8 +140,10 @@ fused_tma_kernel(const FusedParams p) {
       for (int64_t j = it; j < n_iter; ++j)
         mark_row_failed<FMT>(p, (b + j * G) * R + grp, lane, tpr, c_end);
       if (tid == 0) {
+        if (p.status) atomicExch(p.status, kStatusTimeout);
+        // stages it .. it + S - 1 were issued (the last refill was issue(it - 1 + S))
         for (int64_t j = it; j < n_iter && j < it + S; ++j)
-          mbar_wait_bounded(&full[j % S], static_cast<uint32_t>((j / S) & 1));
+          mbar_wait_bounded(&full[j % S], static_cast<uint32_t>((j / S) & 1), FP4Q_WAIT_LIMIT(p));
       }
       return;
     }

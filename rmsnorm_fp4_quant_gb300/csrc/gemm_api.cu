@@ -50,7 +50,7 @@ fp4_status_t gemm_call(bool mx, int epilogue, const uint8_t* a_packed, const uin
                        const uint8_t* sfa, const uint8_t* sfb, float alpha, const void* bias,
                        const void* residual, int64_t M, int64_t N, int64_t K, void* out,
                        uint8_t* out_packed, uint8_t* out_sf, int variant, int pdl,
-                       fp4q_stream_t stream) {
+                       int32_t* status, fp4q_stream_t stream) {
   const bool fp4_out = epilogue == kEpiGeluFp4;
   if (M < 0 || N < 0 || K <= 0) return FP4_ERR_INVALID_ARG;
   if (variant < -1 || variant > 4) return FP4_ERR_INVALID_ARG;
@@ -94,6 +94,15 @@ fp4_status_t gemm_call(bool mx, int epilogue, const uint8_t* a_packed, const uin
   // by the same thread), but not partly overlap it
   if (residual && residual != out && abi_overlap(out, out_bytes, residual, out_bytes))
     return FP4_ERR_INVALID_ARG;
+  if (status) {   // the status word overlaps nothing else the call touches
+    if (!abi_aligned(status, 4)) return FP4_ERR_MISALIGNED;
+    const void* bufs[9] = {a_packed, b_packed, sfa, sfb, bias, residual, out, out_packed, out_sf};
+    const int64_t sizes[9] = {M * K / 2, N * K / 2, sfa_bytes, sfb_bytes, N * 2, M * N * 2,
+                              out_bytes, fp4_out ? M * N / 2 : 0,
+                              fp4_out ? fp4_sf_size_bytes(M, N, FP4_NVFP4, FP4_SF_SWIZZLED) : 0};
+    for (int i = 0; i < 9; ++i)
+      if (bufs[i] && abi_overlap(status, 4, bufs[i], sizes[i])) return FP4_ERR_INVALID_ARG;
+  }
   GemmParams p{};
   p.sfa = sfa;
   p.sfb = sfb;
@@ -102,6 +111,7 @@ fp4_status_t gemm_call(bool mx, int epilogue, const uint8_t* a_packed, const uin
   p.out = static_cast<uint16_t*>(out);
   p.out_packed = out_packed;
   p.out_sf = out_sf;
+  p.status = reinterpret_cast<int*>(status);
   p.epilogue = epilogue;
   p.out_nkt = static_cast<int>((N / 16 + 3) / 4);
   p.rows_out = static_cast<int>(fp4_out ? (M + 127) / 128 * 128 : M);
@@ -137,6 +147,7 @@ fp4_status_t gemm_call(bool mx, int epilogue, const uint8_t* a_packed, const uin
   p.nkt = 0;        // filled by the launcher
   p.num_kb = 0;
   p.tmem_cols = 0;
+  FP4Q_SET_DEBUG(p);
   cudaError_t e = launch_gemm_nvfp4(a_packed, b_packed, p, bn, persistent, mx, pdl,
                                     reinterpret_cast<cudaStream_t>(stream));
   // a cluster of this many CTAs may not fit: halve it until one does
@@ -158,7 +169,7 @@ fp4_status_t fp4_gemm_nvfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packe
                                  int64_t K, void* out, int variant, int pdl,
                                  fp4q_stream_t stream) {
   return gemm_call(false, kEpiPlain, a_packed, b_packed, sfa, sfb, alpha, bias, residual, M, N,
-                   K, out, nullptr, nullptr, variant, pdl, stream);
+                   K, out, nullptr, nullptr, variant, pdl, nullptr, stream);
 }
 
 fp4_status_t fp4_gemm_mxfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
@@ -167,7 +178,7 @@ fp4_status_t fp4_gemm_mxfp4_bf16(const uint8_t* a_packed, const uint8_t* b_packe
                                  int64_t K, void* out, int variant, int pdl,
                                  fp4q_stream_t stream) {
   return gemm_call(true, kEpiPlain, a_packed, b_packed, sfa, sfb, alpha, bias, residual, M, N, K,
-                   out, nullptr, nullptr, variant, pdl, stream);
+                   out, nullptr, nullptr, variant, pdl, nullptr, stream);
 }
 
 fp4_status_t fp4_gemm_nvfp4_gelu_bf16(const uint8_t* a_packed, const uint8_t* b_packed,
@@ -175,7 +186,7 @@ fp4_status_t fp4_gemm_nvfp4_gelu_bf16(const uint8_t* a_packed, const uint8_t* b_
                                       const void* bias, int64_t M, int64_t N, int64_t K,
                                       void* out, int variant, int pdl, fp4q_stream_t stream) {
   return gemm_call(false, kEpiGelu, a_packed, b_packed, sfa, sfb, alpha, bias, nullptr, M, N, K,
-                   out, nullptr, nullptr, variant, pdl, stream);
+                   out, nullptr, nullptr, variant, pdl, nullptr, stream);
 }
 
 fp4_status_t fp4_gemm_nvfp4_gelu_nvfp4(const uint8_t* a_packed, const uint8_t* b_packed,
@@ -184,7 +195,31 @@ fp4_status_t fp4_gemm_nvfp4_gelu_nvfp4(const uint8_t* a_packed, const uint8_t* b
                                        uint8_t* out_packed, uint8_t* out_sf, int variant,
                                        int pdl, fp4q_stream_t stream) {
   return gemm_call(false, kEpiGeluFp4, a_packed, b_packed, sfa, sfb, alpha, bias, nullptr, M, N,
-                   K, nullptr, out_packed, out_sf, variant, pdl, stream);
+                   K, nullptr, out_packed, out_sf, variant, pdl, nullptr, stream);
+}
+
+fp4_status_t fp4_gemm_ex(const uint8_t* a_packed, const uint8_t* b_packed, const uint8_t* sfa,
+                         const uint8_t* sfb, fp4_format_t format, fp4_epilogue_t epilogue,
+                         float alpha, const void* bias, const void* residual, int64_t M,
+                         int64_t N, int64_t K, void* out, uint8_t* out_packed, uint8_t* out_sf,
+                         int variant, int pdl, int32_t* status, fp4q_stream_t stream) {
+  if (format != FP4_NVFP4 && format != FP4_MXFP4) return FP4_ERR_INVALID_ARG;
+  const bool mx = format == FP4_MXFP4;
+  switch (epilogue) {
+    case FP4_EPI_BF16:
+      return gemm_call(mx, kEpiPlain, a_packed, b_packed, sfa, sfb, alpha, bias, residual, M, N,
+                       K, out, nullptr, nullptr, variant, pdl, status, stream);
+    case FP4_EPI_GELU_BF16:
+      if (residual) return FP4_ERR_INVALID_ARG;
+      return gemm_call(mx, kEpiGelu, a_packed, b_packed, sfa, sfb, alpha, bias, nullptr, M, N, K,
+                       out, nullptr, nullptr, variant, pdl, status, stream);
+    case FP4_EPI_GELU_NVFP4:
+      if (mx || residual) return FP4_ERR_INVALID_ARG;
+      return gemm_call(false, kEpiGeluFp4, a_packed, b_packed, sfa, sfb, alpha, bias, nullptr, M,
+                       N, K, nullptr, out_packed, out_sf, variant, pdl, status, stream);
+    default:
+      return FP4_ERR_INVALID_ARG;
+  }
 }
 
 int fp4_gemm_variant(int64_t M, int64_t N, int64_t K, fp4_format_t format, int fp4_out,

@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "debug_checks.h"
+
 namespace fp4q {
 
 // NVFP4 x NVFP4 -> bf16 GEMM (bf16 tensors as raw 16-bit words).
@@ -19,6 +21,7 @@ struct GemmParams {
   uint16_t* out;               // [M, N] bf16 (kEpiPlain, kEpiGelu)
   uint8_t* out_packed;         // [M, N/2] E2M1 codes (kEpiGeluFp4)
   uint8_t* out_sf;             // tiled E4M3 scales of the output (kEpiGeluFp4)
+  int* status;                 // optional device status word: the timeout status on a timeout
   int epilogue;                // kEpi*
   int out_nkt;                 // ceil(N / 64): scale groups per output row (kEpiGeluFp4)
   int rows_out;                // rows the epilogue visits: M, or 128 * ceil(M / 128) (kEpiGeluFp4)
@@ -32,6 +35,7 @@ struct GemmParams {
   int stages;                  // shared-memory ring depth, 2..6
   int split;                   // CTAs of a cluster sharing one tile's K loop (1 = none)
   uint32_t tmem_cols;          // tensor-memory columns taken per CTA
+  FP4Q_DEBUG_FIELD             // debug build only: checks and fault injection
 };
 
 // K % 32 == 0, N % 8 == 0, a / b 16-byte aligned (checked by the caller);

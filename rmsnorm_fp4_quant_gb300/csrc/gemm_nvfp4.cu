@@ -43,7 +43,8 @@
 // Every mbarrier wait is bounded.  A producer or MMA wait that runs out marks
 // the CTA failed: the producer waits (bounded) for its copies in flight, the
 // MMA issuer still commits so the epilogue wait ends once its MMAs are done,
-// the tile is written as NaN, and tensor memory is freed before the exit.
+// the tile is written as NaN, the caller's status word (if any) receives the
+// timeout status, and tensor memory is freed before the exit.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -128,7 +129,7 @@ __device__ __forceinline__ void epilogue_values(const GemmParams& p, const float
   const float nan = __int_as_float(0x7fc00000);
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = bad ? nan : acc[i] * p.alpha;
-  if (p.bias) {
+  if (p.bias && FP4Q_IN_RANGE(p, p.bias + n, 16, p.bias, 2LL * p.N)) {
     const uint4 b = *reinterpret_cast<const uint4*>(p.bias + n);
     const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
@@ -153,7 +154,8 @@ __device__ __forceinline__ void store8(const GemmParams& p, const float (&acc)[8
   float v[8];
   epilogue_values(p, acc, n, bad, v);
   const size_t off = static_cast<size_t>(row) * static_cast<size_t>(p.N) + n;
-  if (p.residual) {
+  const long long out_bytes = 2LL * p.M * p.N;
+  if (p.residual && FP4Q_IN_RANGE(p, p.residual + off, 16, p.residual, out_bytes)) {
     const uint4 rr = *reinterpret_cast<const uint4*>(p.residual + off);
     const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
 #pragma unroll
@@ -168,19 +170,24 @@ __device__ __forceinline__ void store8(const GemmParams& p, const float (&acc)[8
   o.y = bf16x2_bits(v[2], v[3]);
   o.z = bf16x2_bits(v[4], v[5]);
   o.w = bf16x2_bits(v[6], v[7]);
-  *reinterpret_cast<uint4*>(p.out + off) = o;
+  if (FP4Q_IN_RANGE(p, p.out + off, 16, p.out, out_bytes)) *reinterpret_cast<uint4*>(p.out + off) = o;
 }
 
 // FP4 output of 16 values (one NVFP4 block) of one row at column n: the
 // producer's rules (E4M3 scale of amax / 6, codes of v * rn(1/s)), codes to
 // the packed output, the scale byte to the tiled scale buffer (k padding of
 // the row's last group zeroed by the last block).  `row_valid` false writes
-// the zero scale byte of a padding row.
+// the zero scale byte of a padding row; `bad` (the tile's inputs never
+// arrived) writes the scale byte 0xFF (NaN in E4M3) and zero codes.
 __device__ __forceinline__ void store_fp4_block16(const GemmParams& p, const float (&v)[16],
-                                                  int row, int n, bool row_valid) {
+                                                  int row, int n, bool row_valid, bool bad) {
   const int kb = n >> 4;
   uint32_t code = 0;
-  if (row_valid) {
+  if (row_valid && bad) {
+    code = 0xFFu;
+    uint8_t* pk = p.out_packed + static_cast<size_t>(row) * static_cast<size_t>(p.N / 2) + n / 2;
+    if (FP4Q_IN_RANGE(p, pk, 8, p.out_packed, packed_extent(p.M, p.N))) st_u64(pk, 0ull);
+  } else if (row_valid) {
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; i += 2) amax = max_abs3(amax, v[i], v[i + 1]);
@@ -191,13 +198,17 @@ __device__ __forceinline__ void store_fp4_block16(const GemmParams& p, const flo
     for (int i = 0; i < 16; ++i) q[i] = inv_s > 0.0f ? v[i] * inv_s : 0.0f;
     const uint64_t packed = static_cast<uint64_t>(e2m1_pack8(q)) |
                             (static_cast<uint64_t>(e2m1_pack8(q + 8)) << 32);
-    st_u64(p.out_packed + static_cast<size_t>(row) * static_cast<size_t>(p.N / 2) + n / 2,
-           packed);
+    uint8_t* pk = p.out_packed + static_cast<size_t>(row) * static_cast<size_t>(p.N / 2) + n / 2;
+    if (FP4Q_IN_RANGE(p, pk, 8, p.out_packed, packed_extent(p.M, p.N))) st_u64(pk, packed);
   }
-  st_u8(p.out_sf + tiled_sf_offset(row, kb, p.out_nkt), code);
-  if (kb == p.N / 16 - 1)
-    for (int kk = kb + 1; kk < 4 * p.out_nkt; ++kk)
-      st_u8(p.out_sf + tiled_sf_offset(row, kk, p.out_nkt), 0u);
+  uint8_t* sfp = p.out_sf + tiled_sf_offset(row, kb, p.out_nkt);
+  if (FP4Q_IN_RANGE(p, sfp, 1, p.out_sf, tiled_extent(p.M, p.out_nkt))) st_u8(sfp, code);
+  if (kb == p.N / 16 - 1) {
+    for (int kk = kb + 1; kk < 4 * p.out_nkt; ++kk) {
+      uint8_t* pad = p.out_sf + tiled_sf_offset(row, kk, p.out_nkt);
+      if (FP4Q_IN_RANGE(p, pad, 1, p.out_sf, tiled_extent(p.M, p.out_nkt))) st_u8(pad, 0u);
+    }
+  }
 }
 
 // 32 accumulator columns (raw fp32 bits from tensor memory) of one row.  Rows
@@ -223,7 +234,7 @@ __device__ __forceinline__ void store_columns32(const GemmParams& p, const uint3
           for (int i = 0; i < 8; ++i) v[8 * q + i] = out8[i];
         }
       }
-      store_fp4_block16(p, v, row, n, row_valid);
+      store_fp4_block16(p, v, row, n, row_valid, bad);
     }
     return;
   }
@@ -304,6 +315,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  int issued = 0;    // K blocks a producer thread issued copies for
 
   if ((warp == 0 || warp == 2) && lane == 0) {
     // ---- producers: warp 0 A and its scales, warp 2 B and its scales ----
@@ -319,7 +331,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     for (; i < kb1 - kb0; ++i) {
       const int kb = kb0 + i;
       const int s = i % S;
-      if (i >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((i / S - 1) & 1))) {
+      if (i >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((i / S - 1) & 1),
+                                        FP4Q_WAIT_LIMIT(p))) {
         *failed = 1;
         break;
       }
@@ -334,33 +347,33 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                 : static_cast<uint32_t>(b_tiles) * sf_bytes);
       mbar_arrive_expect_tx(&full[s], load_a ? kTileBytesA : C::kTileBytesB);
       if (load_a) {
-        bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA,
-                 sfa_k + static_cast<size_t>(kb) * C::kSfBytesA, sf_bytes, &sf_full[s]);
-        tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes,
-                    m_tile * kBM, &full[s]);
+        const uint8_t* src = sfa_k + static_cast<size_t>(kb) * C::kSfBytesA;
+        if (FP4Q_IN_RANGE(p, src, sf_bytes, p.sfa, tiled_extent(p.M, p.nkt)))
+          bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA, src, sf_bytes, &sf_full[s]);
+        // debug build: one CTA never issues one A tile (fault injection)
+        if (!FP4Q_DROP(p, 2, static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x), i))
+          tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes,
+                      m_tile * kBM, &full[s]);
       } else {
-        for (int t = 0; t < b_tiles; ++t)
-          bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + t * C::kSfBytesA,
-                   p.sfb + (static_cast<size_t>(b_tile0 + t) * p.nkt) * kSfTileBytes +
-                       static_cast<size_t>(kb) * C::kSfBytesA,
-                   sf_bytes, &sf_full[s]);
+        for (int t = 0; t < b_tiles; ++t) {
+          const uint8_t* src = p.sfb + (static_cast<size_t>(b_tile0 + t) * p.nkt) * kSfTileBytes +
+                               static_cast<size_t>(kb) * C::kSfBytesA;
+          if (FP4Q_IN_RANGE(p, src, sf_bytes, p.sfb, tiled_extent(p.N, p.nkt)))
+            bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + t * C::kSfBytesA, src,
+                     sf_bytes, &sf_full[s]);
+        }
         tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
                     n_tile * BN, &full[s]);
       }
     }
-    if (i < kb1 - kb0) {   // gave up: let the copies already issued land first
-      for (int j = i > S ? i - S : 0; j < i; ++j) {
-        mbar_wait_bounded(&full[j % S], static_cast<uint32_t>((j / S) & 1));
-        mbar_wait_bounded(&sf_full[j % S], static_cast<uint32_t>((j / S) & 1));
-      }
-    }
+    issued = i;
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
     for (int i = 0; i < kb1 - kb0; ++i) {
       const int s = i % S;
       // the operand tiles (full[s]) and the scales in tensor memory (sf_ready[s])
-      if (!mbar_wait_bounded(&sf_ready[s], static_cast<uint32_t>((i / S) & 1)) ||
-          !mbar_wait_bounded(&full[s], static_cast<uint32_t>((i / S) & 1))) {
+      if (!mbar_wait_bounded(&sf_ready[s], static_cast<uint32_t>((i / S) & 1), FP4Q_WAIT_LIMIT(p)) ||
+          !mbar_wait_bounded(&full[s], static_cast<uint32_t>((i / S) & 1), FP4Q_WAIT_LIMIT(p))) {
         *failed = 1;
         break;
       }
@@ -390,7 +403,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     // refilled the stage, which waited for the MMAs of stage i - S.
     for (int i = 0; i < kb1 - kb0; ++i) {
       const int s = i % S;
-      if (!mbar_wait_bounded(&sf_full[s], static_cast<uint32_t>((i / S) & 1))) {
+      if (!mbar_wait_bounded(&sf_full[s], static_cast<uint32_t>((i / S) & 1), FP4Q_WAIT_LIMIT(p))) {
         *failed = 1;
         break;
       }
@@ -417,14 +430,25 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
       tc_commit(&sf_ready[s]);
     }
     tc_commit(sf_done);       // no copy may still be running when tensor memory is freed
-    mbar_wait_bounded(sf_done, 0);
+    mbar_wait_bounded(sf_done, 0, FP4Q_WAIT_LIMIT(p));
   }
   __syncthreads();            // roles done; a failure flag is visible to all
+  if (*failed != 0 && (warp == 0 || warp == 2) && lane == 0) {
+    // A failed CTA may have stopped consuming stages it still has copies in
+    // flight for: each producer waits (bounded) for the last S stages it
+    // filled - earlier ones were consumed by MMAs, so their copies landed -
+    // before anything here can end the CTA.
+    for (int j = issued > S ? issued - S : 0; j < issued; ++j) {
+      mbar_wait_bounded(&full[j % S], static_cast<uint32_t>((j / S) & 1), FP4Q_WAIT_LIMIT(p));
+      mbar_wait_bounded(&sf_full[j % S], static_cast<uint32_t>((j / S) & 1), FP4Q_WAIT_LIMIT(p));
+    }
+  }
 
   // ---- epilogue ----
-  const bool acc_ok = mbar_wait_bounded(accum, 0);
+  const bool acc_ok = mbar_wait_bounded(accum, 0, FP4Q_WAIT_LIMIT(p));
   tc_fence_after_sync();
   const bool bad = !acc_ok || *failed != 0;
+  if (bad && threadIdx.x == 0 && p.status) atomicExch(p.status, kStatusTimeout);
   griddep_launch_dependents();
 
   const int row = m_tile * kBM + warp * 32 + lane;
@@ -482,6 +506,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
   tc_fence_before_sync();
   __syncthreads();
+  if (threadIdx.x == 0 && *failed != 0 && p.status) atomicExch(p.status, kStatusTimeout);
   if (warp == 0) tmem_dealloc(tmem, p.tmem_cols);
 }
 
@@ -575,6 +600,7 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  int issued = 0;    // K blocks a producer thread issued copies for, over all tiles
 
   if ((warp == 0 || warp == 6) && lane == 0) {
     // ---- producers: warp 0 A and its scales, warp 6 B and its scales ----
@@ -591,7 +617,8 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                                   : C::kSfTilesB;
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
         const int s = it % S;
-        if (it >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((it / S - 1) & 1))) {
+        if (it >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((it / S - 1) & 1),
+                                          FP4Q_WAIT_LIMIT(p))) {
           *failed = 1;
           ok = false;
           break;
@@ -606,27 +633,27 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                   : static_cast<uint32_t>(b_tiles) * sf_bytes);
         mbar_arrive_expect_tx(&full[s], load_a ? kTileBytesA : C::kTileBytesB);
         if (load_a) {
-          bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA,
-                   sfa_k + static_cast<size_t>(kb) * C::kSfBytesA, sf_bytes, &sf_full[s]);
-          tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes,
-                      m_tile * kBM, &full[s]);
+          const uint8_t* src = sfa_k + static_cast<size_t>(kb) * C::kSfBytesA;
+          if (FP4Q_IN_RANGE(p, src, sf_bytes, p.sfa, tiled_extent(p.M, p.nkt)))
+            bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA, src, sf_bytes, &sf_full[s]);
+          // debug build: one CTA never issues one A tile (fault injection)
+          if (!FP4Q_DROP(p, 2, static_cast<int>(blockIdx.x), it))
+            tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes,
+                        m_tile * kBM, &full[s]);
         } else {
-          for (int q = 0; q < b_tiles; ++q)
-            bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + q * C::kSfBytesA,
-                     p.sfb + static_cast<size_t>(b_tile0 + q) * p.nkt * kSfTileBytes +
-                         static_cast<size_t>(kb) * C::kSfBytesA,
-                     sf_bytes, &sf_full[s]);
+          for (int q = 0; q < b_tiles; ++q) {
+            const uint8_t* src = p.sfb + static_cast<size_t>(b_tile0 + q) * p.nkt * kSfTileBytes +
+                                 static_cast<size_t>(kb) * C::kSfBytesA;
+            if (FP4Q_IN_RANGE(p, src, sf_bytes, p.sfb, tiled_extent(p.N, p.nkt)))
+              bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + q * C::kSfBytesA, src,
+                       sf_bytes, &sf_full[s]);
+          }
           tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
                       n_tile * BN, &full[s]);
         }
       }
     }
-    if (!ok) {   // gave up: let the copies already issued land first
-      for (int j = it > S ? it - S : 0; j < it; ++j) {
-        mbar_wait_bounded(&full[j % S], static_cast<uint32_t>((j / S) & 1));
-        mbar_wait_bounded(&sf_full[j % S], static_cast<uint32_t>((j / S) & 1));
-      }
-    }
+    issued = it;
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
     int it = 0;
@@ -634,7 +661,8 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
     for (int i = 0; i < my_tiles && ok; ++i) {
       const int a = i % P::kAcc;
       // the epilogue has read this accumulator out (first use: passes at once)
-      if (!mbar_wait_bounded(&acc_empty[a], static_cast<uint32_t>(((i / P::kAcc) & 1) ^ 1))) {
+      if (!mbar_wait_bounded(&acc_empty[a], static_cast<uint32_t>(((i / P::kAcc) & 1) ^ 1),
+                             FP4Q_WAIT_LIMIT(p))) {
         *failed = 1;
         break;
       }
@@ -642,8 +670,8 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const uint32_t d_t = tmem + static_cast<uint32_t>(a * BN);
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
         const int s = it % S;
-        if (!mbar_wait_bounded(&sf_ready[s], static_cast<uint32_t>((it / S) & 1)) ||
-            !mbar_wait_bounded(&full[s], static_cast<uint32_t>((it / S) & 1))) {
+        if (!mbar_wait_bounded(&sf_ready[s], static_cast<uint32_t>((it / S) & 1), FP4Q_WAIT_LIMIT(p)) ||
+            !mbar_wait_bounded(&full[s], static_cast<uint32_t>((it / S) & 1), FP4Q_WAIT_LIMIT(p))) {
           *failed = 1;
           ok = false;
           break;
@@ -665,17 +693,21 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
         }
         tc_commit(&empty[s]);
       }
-      tc_commit(&acc_full[a]);   // this tile's MMAs (or those issued before a failure) are done
+      // this tile's MMAs are done.  Not after a failure: the epilogue's own
+      // wait then runs out and marks the tile, so it never depends on seeing
+      // the failure flag through the asynchronous arrive
+      if (!ok) break;
+      tc_commit(&acc_full[a]);
     }
     // tensor memory is freed below only after every MMA issued here has completed
     tc_commit(mma_done);
-    mbar_wait_bounded(mma_done, 0);
+    mbar_wait_bounded(mma_done, 0, FP4Q_WAIT_LIMIT(p));
   } else if (warp == 7 && lane == 0) {
     // ---- scale mover: stage it's scales into its tensor-memory slot ----
     const int total = my_tiles * p.num_kb;
     for (int it = 0; it < total; ++it) {
       const int s = it % S;
-      if (!mbar_wait_bounded(&sf_full[s], static_cast<uint32_t>((it / S) & 1))) {
+      if (!mbar_wait_bounded(&sf_full[s], static_cast<uint32_t>((it / S) & 1), FP4Q_WAIT_LIMIT(p))) {
         *failed = 1;
         break;
       }
@@ -700,7 +732,7 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
       tc_commit(&sf_ready[s]);
     }
     tc_commit(sf_done);
-    mbar_wait_bounded(sf_done, 0);
+    mbar_wait_bounded(sf_done, 0, FP4Q_WAIT_LIMIT(p));
   } else if (warp >= 2 && warp <= 5) {
     // ---- epilogue ----
     const int quarter = warp & 3;
@@ -711,8 +743,9 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const int m_tile = t / n_tiles, n_tile = t - (t / n_tiles) * n_tiles;
       const int a = i % P::kAcc;
       const int row = m_tile * kBM + quarter * 32 + lane;
-      if (ok) ok = mbar_wait_bounded(&acc_full[a], static_cast<uint32_t>((i / P::kAcc) & 1));
+      if (ok) ok = mbar_wait_bounded(&acc_full[a], static_cast<uint32_t>((i / P::kAcc) & 1), FP4Q_WAIT_LIMIT(p));
       ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-wide
+      if (!ok && lane == 0) *failed = 1;
       tc_fence_after_sync();
       if (i == my_tiles - 1) griddep_launch_dependents();
       const bool bad = !ok || *failed != 0;
@@ -734,8 +767,18 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
       }
     }
   }
+  __syncthreads();            // every role done; a failure flag is visible to all
+  if (*failed != 0 && (warp == 0 || warp == 6) && lane == 0) {
+    // as in the one-tile kernel: the last S stages each producer filled
+    // have landed before the CTA ends
+    for (int j = issued > S ? issued - S : 0; j < issued; ++j) {
+      mbar_wait_bounded(&full[j % S], static_cast<uint32_t>((j / S) & 1), FP4Q_WAIT_LIMIT(p));
+      mbar_wait_bounded(&sf_full[j % S], static_cast<uint32_t>((j / S) & 1), FP4Q_WAIT_LIMIT(p));
+    }
+  }
   tc_fence_before_sync();
   __syncthreads();
+  if (threadIdx.x == 0 && *failed != 0 && p.status) atomicExch(p.status, kStatusTimeout);
   if (warp == 1) tmem_dealloc(tmem, p.tmem_cols);
 }
 

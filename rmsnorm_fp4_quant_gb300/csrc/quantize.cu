@@ -12,6 +12,7 @@
 // scheduler); where SEGS does not divide the row's segments the last run is
 // ragged and its missing segments are skipped.  Rows >= M (padding rows of
 // the tiled scale layout) only write zero scale bytes.
+#include "async_copy.cuh"
 #include "fused_common.cuh"
 
 namespace fp4q {
@@ -55,14 +56,22 @@ __device__ __forceinline__ void quantize_chunk(const QuantParams& p, const Chunk
     }
     const uint64_t packed = static_cast<uint64_t>(e2m1_pack8(v)) |
                             (static_cast<uint64_t>(e2m1_pack8(v + 8)) << 32);
-    st_u64(p.packed + row * static_cast<int64_t>(p.H / 2) + static_cast<int64_t>(c) * 8, packed);
+    uint8_t* pk = p.packed + row * static_cast<int64_t>(p.H / 2) + static_cast<int64_t>(c) * 8;
+    if (FP4Q_IN_RANGE(p, pk, 8, p.packed, packed_extent(p.M, p.H))) st_u64(pk, packed);
   }
   if (owner) {
-    if (p.sf_rm && have) st_u8(p.sf_rm + row * p.nb + kb, code);
+    uint8_t* rm = p.sf_rm + row * p.nb + kb;
+    if (p.sf_rm && have && FP4Q_IN_RANGE(p, rm, 1, p.sf_rm, static_cast<long long>(p.M) * p.nb))
+      st_u8(rm, code);
     if (p.sf_tiled) {
-      st_u8(p.sf_tiled + tiled_sf_offset(row, kb, p.nkt), code);
-      if (kb == p.nb - 1)                   // k padding of the last 4-block group
-        for (int kk = p.nb; kk < 4 * p.nkt; ++kk) st_u8(p.sf_tiled + tiled_sf_offset(row, kk, p.nkt), 0u);
+      uint8_t* tl = p.sf_tiled + tiled_sf_offset(row, kb, p.nkt);
+      if (FP4Q_IN_RANGE(p, tl, 1, p.sf_tiled, tiled_extent(p.M, p.nkt))) st_u8(tl, code);
+      if (kb == p.nb - 1) {                 // k padding of the last 4-block group
+        for (int kk = p.nb; kk < 4 * p.nkt; ++kk) {
+          uint8_t* pad = p.sf_tiled + tiled_sf_offset(row, kk, p.nkt);
+          if (FP4Q_IN_RANGE(p, pad, 1, p.sf_tiled, tiled_extent(p.M, p.nkt))) st_u8(pad, 0u);
+        }
+      }
     }
   }
 }
@@ -75,6 +84,7 @@ __global__ void __launch_bounds__(256, SEGS >= 3 ? 4 : 1) quantize_kernel(const 
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (row >= p.rows) return;                          // whole warps leave together
+  griddep_wait();                                     // input from the kernel before (PDL)
   const bool have_row = row < p.M;
   const T* xrow = static_cast<const T*>(p.x) + row * p.H;
   int c[SEGS];
@@ -84,10 +94,11 @@ __global__ void __launch_bounds__(256, SEGS >= 3 ? 4 : 1) quantize_kernel(const 
   for (int u = 0; u < SEGS; ++u) {                    // all loads first
     c[u] = (blockIdx.y * SEGS + u) * 32 + lane;
     have[u] = have_row && c[u] < p.nchunk;
-    if (have[u])
+    if (have[u] && FP4Q_IN_RANGE(p, xrow + c[u] * 16, 32, p.x, 2LL * p.M * p.H))
       xc[u] = p.evict_first ? ld_stream_ro_evict_first(xrow + c[u] * 16)
                             : ld_stream_ro(xrow + c[u] * 16);
   }
+  griddep_launch_dependents();
 #pragma unroll
   for (int u = 0; u < SEGS; ++u) quantize_chunk<T, FMT>(p, xc[u], have[u], row, c[u], gs);
 }

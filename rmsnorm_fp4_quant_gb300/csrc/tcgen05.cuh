@@ -107,7 +107,7 @@ __device__ __forceinline__ void tmem_load_32cols(uint32_t taddr, uint32_t (&r)[3
       : "memory");
 }
 
-// --- TMA and grid control -----------------------------------------------------
+// --- TMA ----------------------------------------------------------------------
 // Tiled 2-D load of the box at (x, y) of `map` (x in elements of the innermost
 // dimension, a multiple of 16 bytes) into shared memory, counted on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
@@ -121,15 +121,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 }
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-// Programmatic dependent launch: wait for the preceding grid's results / let
-// the next grid start its prologue.  No-ops without the launch attribute.
-__device__ __forceinline__ void griddep_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void griddep_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 }  // namespace fp4q

@@ -29,3 +29,22 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def parity_log(request):
+    """(workload, excused exceptions, elements) of every whole-workload parity
+    check, printed at the end of the run."""
+    log = []
+    request.config._fp4q_parity_log = log
+    return log
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    log = getattr(config, "_fp4q_parity_log", None)
+    if not log:
+        return
+    terminalreporter.write_sep("-", "whole-workload parity: every row against the oracle")
+    for name, exc, n in log:
+        terminalreporter.write_line(f"{name}: {exc} excused boundary exceptions in {n} elements "
+                                    f"({exc / max(n, 1):.2e}; bound 1e-4)")

@@ -1,6 +1,6 @@
 """Helpers for the GPU-vs-oracle parity tests.
 
-Acceptance rule (stated for this path):
+Acceptance rule (stated for this path; the numpy part is tests/acceptance.py):
   * the updated residual is bit-exact;
   * scale bytes and E2M1 codes are bit-exact, except where the oracle's
     pre-rounding value lies within 1e-5 relative of a rounding boundary - an
@@ -22,35 +22,16 @@ import torch
 import oracle
 import rmsnorm_fp4_quant_gb300 as fq
 
-BOUNDARY_REL = 1e-5
-MAX_EXCEPTION_FRAC = 1e-4
-E2M1_MIDS = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
-_E4M3_VALS = None
-
-
-def e4m3_midpoints():
-    global _E4M3_VALS
-    if _E4M3_VALS is None:
-        vals = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8)).astype(np.float64)
-        _E4M3_VALS = (vals[:-1] + vals[1:]) / 2
-    return _E4M3_VALS
-
-
-def near(values, bounds, rel=BOUNDARY_REL):
-    """True where a value lies within `rel` (relative) of any boundary."""
-    v = np.abs(np.asarray(values, np.float64)).reshape(-1)
-    b = np.asarray(bounds, np.float64)
-    i = np.clip(np.searchsorted(b, v), 1, len(b) - 1)
-    d = np.minimum(np.abs(v - b[i - 1]), np.abs(v - b[i]))
-    return (d <= rel * np.maximum(v, 1e-30)).reshape(np.shape(values))
-
-
-def near_pow2(values, rel=BOUNDARY_REL):
-    v = np.asarray(values, np.float64)
-    with np.errstate(divide="ignore"):
-        lg = np.log2(np.where(v > 0, v, 1.0))
-    nearest = np.exp2(np.round(lg))
-    return (np.abs(v - nearest) <= rel * v) & (v > 0)
+from acceptance import (  # noqa: F401  (re-exported for the tests)
+    BOUNDARY_REL,
+    E2M1_MIDS,
+    MAX_EXCEPTION_FRAC,
+    check_rows,
+    e4m3_midpoints,
+    near,
+    near_pow2,
+    tiled_padding_is_zero,
+)
 
 
 @dataclasses.dataclass
@@ -107,57 +88,21 @@ def gpu_scale_codes(g: GpuOut, M, H, fmt, layout, rows=None):
 
 def compare(g: GpuOut, o: oracle.OracleResult, fmt, layout, dtype, M_full, H,
             check_padding=True):
-    """Apply the acceptance rule to the GPU rows held in `g` against the
-    oracle result `o` computed on exactly those rows.  Returns a stats dict."""
+    """Apply the acceptance rule (tests/acceptance.py) to the GPU rows held in
+    `g` against the oracle result `o` computed on exactly those rows, with
+    the exception fraction taken over these rows.  Returns a stats dict."""
     rows = g.rows
     assert o.packed.shape[0] == len(rows)
-    b = oracle.block_size(fmt)
-    nb = H // b
-    # 1. residual (the standalone quantize has none)
-    if g.residual_bits is not None:
-        want_bits = (o.residual.view(np.uint32) >> 16).astype(np.uint16) if dtype == "bf16" \
-            else o.residual.astype(np.float16).view(np.uint16)
-        bad_res = np.argwhere(g.residual_bits != want_bits)
-        assert bad_res.size == 0, f"residual differs at {bad_res[:5].tolist()}"
-
-    # 2. scales
+    nb = H // oracle.block_size(fmt)
     g_sc = gpu_scale_codes(g, M_full, H, fmt, "rowmajor" if layout == "rowmajor" else "swizzled",
                            rows)
-    sc_bad = g_sc != o.scale_codes
-    if oracle.e4m3_scaled(fmt):
-        sc_excusable = near(o.t, e4m3_midpoints())
-    else:
-        sc_excusable = near_pow2(o.t)
-    unexcused = sc_bad & ~sc_excusable
-    assert not unexcused.any(), (
-        f"scale bytes differ away from a boundary at {np.argwhere(unexcused)[:5].tolist()}: "
-        f"gpu {g_sc[unexcused][:5]} oracle {o.scale_codes[unexcused][:5]} t {o.t[unexcused][:5]}")
+    n_exc = check_rows(o, g.residual_bits, g_sc, g.packed, fmt, dtype)
     if layout == "both":
         rm = g.sf_rm.reshape(M_full, nb)[rows]
         assert np.array_equal(rm, g_sc), "row-major and tiled scale buffers disagree"
-
-    # 3. codes
-    g_codes = np.empty((len(rows), H), np.uint8)
-    pk = g.packed
-    g_codes[:, 0::2] = pk & 0xF
-    g_codes[:, 1::2] = pk >> 4
-    code_bad = g_codes != o.codes
-    block_excused = np.repeat(sc_bad, b, axis=1)
-    code_excusable = near(np.abs(o.v), E2M1_MIDS) | block_excused
-    unexcused = code_bad & ~code_excusable
-    assert not unexcused.any(), (
-        f"codes differ away from a boundary at {np.argwhere(unexcused)[:5].tolist()}: "
-        f"gpu {g_codes[unexcused][:8]} oracle {o.codes[unexcused][:8]} v {o.v[unexcused][:8]}")
-    n_exc = int(code_bad.sum() + sc_bad.sum())
     assert n_exc <= MAX_EXCEPTION_FRAC * o.codes.size, f"{n_exc} exceptions in {o.codes.size}"
-
-    # 4. tiled padding
     if check_padding and layout in ("swizzled", "both"):
-        nkt = (nb + 3) // 4
-        mask = np.ones(g.sf.size, bool)
-        mm, kk = np.meshgrid(np.arange(M_full), np.arange(nb), indexing="ij")
-        mask[oracle.swizzled_sf_offset(mm, kk, nkt).reshape(-1)] = False
-        assert np.all(g.sf[mask] == 0), "tiled padding bytes are not zero"
+        assert tiled_padding_is_zero(g.sf, M_full, nb), "tiled padding bytes are not zero"
     return {"exceptions": n_exc, "elements": int(o.codes.size)}
 
 

@@ -39,7 +39,8 @@ def test_header_declares_the_boundary():
     for want in ("fp4_add_rmsnorm_quant", "fp4_add_rmsnorm_quant_gs", "fp4_quantize",
                  "fp4_dequant", "fp4_sf_size_bytes", "fp4_launch_shape",
                  "fp4_status_string", "fp4_last_cuda_error", "fp4_gemm_nvfp4_bf16",
-                 "fp4_gemm_mxfp4_bf16", "fp4_gemm_nvfp4_gelu_bf16", "fp4_gemm_nvfp4_gelu_nvfp4"):
+                 "fp4_gemm_mxfp4_bf16", "fp4_gemm_nvfp4_gelu_bf16", "fp4_gemm_nvfp4_gelu_nvfp4",
+                 "fp4_add_rmsnorm_quant_ex", "fp4_gemm_ex", "fp4_read_device_status"):
         assert want in names
 
 
@@ -78,9 +79,25 @@ def test_sf_size_rejects_bad_arguments(L):
 
 
 def test_status_strings(L):
-    for s in range(5):
+    for s in range(6):
         assert fq.fp4_status_string(s) and fq.fp4_status_string(s) != "unknown status"
+    assert "timeout" in fq.fp4_status_string(fq.FP4_ERR_TIMEOUT)
     assert fq.fp4_status_string(99) == "unknown status"
+
+
+def test_status_codes_match_the_header(L):
+    text = open(os.path.join(ROOT, "include", "fp4q.h")).read()
+    for name in ("FP4_OK", "FP4_ERR_INVALID_ARG", "FP4_ERR_UNSUPPORTED_SHAPE",
+                 "FP4_ERR_MISALIGNED", "FP4_ERR_CUDA", "FP4_ERR_TIMEOUT", "FP4_EPI_BF16",
+                 "FP4_EPI_GELU_BF16", "FP4_EPI_GELU_NVFP4"):
+        m = re.search(rf"\b{name}\s*=\s*(\d+)", text)
+        assert m and int(m.group(1)) == getattr(fq, name), name
+
+
+def test_read_device_status_rejects_bad_pointers(L):
+    # rejected before the stream or the pointer is touched
+    assert fq.fp4_read_device_status(0, 0) == fq.FP4_ERR_INVALID_ARG
+    assert fq.fp4_read_device_status(A + 2, 0) == fq.FP4_ERR_INVALID_ARG
 
 
 # Fake, never-dereferenced addresses: every call below must fail validation.
@@ -169,14 +186,41 @@ def test_quantize_validation(L, kwargs, status):
     (dict(y=B + 64), 1),               # y inside the residual
     (dict(y=P + 32), 1),               # y over the packed output
     (dict(xs=512, r=A + 512), 1),      # strided input overlapping the residual
+    (dict(st=S2 + 2), 3),              # status word must be 4-byte aligned
+    (dict(st=P + 64), 1),              # status word inside the packed output
+    (dict(st=A + 64), 1),              # status word inside the input
+    (dict(lay=2, s2=P + 16), 1),       # row-major scales of "both" over the packed output
+    (dict(lay=2, s2=B + 32), 1),       # ... over the residual
+    (dict(lay=2, s2=A), 1),            # ... over the input
+    (dict(lay=2, s2=S + 4), 1),        # ... over the tiled scales
+    (dict(p=A + 128), 1),              # packed output inside the input
+    (dict(p=W), 1),                    # packed output over the weight
+    (dict(s=W + 32), 1),               # scales over the weight
+    (dict(y=W), 1),                    # y over the weight
+    (dict(gs=P + 4), 1),               # global scale read from the packed output
 ])
 def test_fused_ex_validation(L, kwargs, status):
     a = dict(x=A, xs=0, r=B, rs=0, w=W, gs=0, eps=1e-6, M=4, H=256, dt=0, f=0, lay=0, p=P, s=S,
-             s2=0, y=0)
+             s2=0, y=0, st=0, pdl=0)
     a.update(kwargs)
     st = fq.fp4_add_rmsnorm_quant_ex(a["x"], a["xs"], a["r"], a["rs"], a["w"], a["gs"], a["eps"],
                                      a["M"], a["H"], a["dt"], a["f"], a["lay"], a["p"], a["s"],
-                                     a["s2"], a["y"], 0)
+                                     a["s2"], a["y"], a["st"], a["pdl"], 0)
+    assert st == status
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(p=A + 256), 1),              # packed output inside the input
+    (dict(lay=2, s2=P + 8), 1),        # row-major scales over the packed output
+    (dict(lay=2, s2=S), 1),            # row-major scales over the tiled ones
+    (dict(lay=2, s2=A + 64), 1),       # row-major scales inside the input
+    (dict(gs=P), 1),                   # global scale read from the packed output
+])
+def test_quantize_overlap_validation(L, kwargs, status):
+    a = dict(x=A, gs=0, M=4, H=256, dt=0, f=0, lay=0, p=P, s=S, s2=0)
+    a.update(kwargs)
+    st = fq.fp4_quantize(a["x"], a["gs"], a["M"], a["H"], a["dt"], a["f"], a["lay"], a["p"],
+                         a["s"], a["s2"], 0)
     assert st == status
 
 
@@ -208,6 +252,62 @@ def test_gemm_validation(L, kwargs, status):
                                 a["residual"], a["M"], a["N"], a["K"], a["out"], a["variant"],
                                 a["pdl"], 0)
     assert st == status
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(fmt=2), 1), (dict(fmt=7), 1),          # E4M3-B32 operands, bad enum
+    (dict(epi=3), 1), (dict(epi=-1), 1),
+    (dict(epi=2, fmt=1), 1),                     # NVFP4 output takes NVFP4 operands only
+    (dict(epi=1, residual=B + (1 << 20)), 1),    # GELU takes no residual
+    (dict(epi=2, residual=B + (1 << 20)), 1),
+    (dict(st=S2 + 1), 3),                        # status word alignment
+    (dict(st=G_OUT + 256), 1),                   # status word inside the output
+    (dict(st=A + 4), 1),                         # ... inside A
+    (dict(epi=2, out=0, p=P, s=G_OUT, st=P + 16), 1),   # ... inside the packed output
+    (dict(K=48), 2), (dict(variant=7), 1),
+    (dict(M=0, a=0, b=0, out=0), 0),
+])
+def test_gemm_ex_validation(L, kwargs, status):
+    a = dict(a=A, b=B, sfa=S, sfb=S2, fmt=0, epi=0, alpha=1.0, bias=0, residual=0, M=256, N=256,
+             K=512, out=G_OUT, p=0, s=0, variant=-1, pdl=0, st=0)
+    a.update(kwargs)
+    st = fq.fp4_gemm_ex(a["a"], a["b"], a["sfa"], a["sfb"], a["fmt"], a["epi"], a["alpha"],
+                        a["bias"], a["residual"], a["M"], a["N"], a["K"], a["out"], a["p"],
+                        a["s"], a["variant"], a["pdl"], a["st"], 0)
+    assert st == status
+
+
+def test_default_build_has_no_debug_knobs(L):
+    assert L.fp4_debug_build() == 0
+    assert fq.fp4_debug_configure(1000, 0, 1, 0, 0, 0) == fq.FP4_ERR_INVALID_ARG
+
+
+@pytest.fixture(scope="module")
+def D(L):
+    fbuild.build(debug=True)
+    return fq.debug_lib()
+
+
+def test_debug_build_exports_the_same_entry_points(D):
+    assert D.fp4_debug_build() == 1
+    for name in _declared_functions():
+        assert ctypes.cast(getattr(D, name), ctypes.c_void_p).value, name
+
+
+@pytest.mark.parametrize("args,status", [
+    ((2_000_000_000, 0, 0, -1, -1, 0), 0),
+    ((20_000, 1, 2, 0, 1, A), 0),
+    ((0, 0, 0, -1, -1, 0), 1),             # the wait limit must be positive
+    ((1000, -1, 0, -1, -1, 0), 1),         # negative shrink
+    ((1000, 0, 3, 0, 0, 0), 1),            # no kernel 3
+    ((1000, 0, 1, 0, 0, A + 2), 3),        # counter alignment
+])
+def test_debug_configure_validation(D, args, status):
+    """Host only: the knobs are stored, nothing is launched or dereferenced."""
+    try:
+        assert D.fp4_debug_configure(*args) == status
+    finally:
+        D.fp4_debug_configure(2_000_000_000, 0, 0, -1, -1, None)
 
 
 def test_library_exports_only_the_declared_entry_points(L):

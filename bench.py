@@ -52,9 +52,10 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--rows", type=int, default=None,
                     help="override the workload's M (smaller cases for profiling)")
-    ap.add_argument("--op", choices=["fused", "quantize", "gemm"], default="fused",
-                    help="fused add+RMSNorm+quantize (default), the standalone quantize, or "
-                         "the NVFP4 GEMM that consumes them (--gemm picks the shape)")
+    ap.add_argument("--op", choices=["fused", "quantize", "gemm", "chain"], default="fused",
+                    help="fused add+RMSNorm+quantize (default), the standalone quantize, "
+                         "the NVFP4 GEMM that consumes them (--gemm picks the shape), or the "
+                         "chain fused op -> GEMM on the rows of the GEMM's A operand")
     ap.add_argument("--gemm", default="G4_M8192_N7168_K7168",
                     help="GEMM workload for --op gemm")
     ap.add_argument("--gemm-format", choices=["nvfp4", "mxfp4"], default="nvfp4",
@@ -965,8 +966,107 @@ def run_gemm(args):
         print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# a decode step's chain: add + RMSNorm + NVFP4 quantization of M rows, then the
+# projection that consumes the codes and tiled scales
+# ---------------------------------------------------------------------------
+CHAIN_METRIC = "fused add+RMSNorm+NVFP4 quant -> NVFP4 GEMM chain, us per step"
+
+
+def run_chain(args):
+    """One step = fp4_add_rmsnorm_quant_ex on M x K rows (bf16, NVFP4, tiled
+    scales) followed by fp4_gemm_nvfp4_bf16 of its codes against an N x K
+    NVFP4 weight, both launched with and without programmatic dependent
+    launch; enough copies of the inputs, weights and outputs rotate that one
+    pass moves more than twice the L2, and a pass of steps is replayed as a
+    CUDA graph (as a decode loop would run it)."""
+    import torch
+
+    import rmsnorm_fp4_quant_gb300 as fq
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    L = fq.lib()
+    gw = workloads.GEMM_CONFIGS[args.gemm]
+    M, N, K = gw.M, gw.N, gw.K
+    wl = workloads.Workload("chain", M, K, "bf16", "nvfp4", "swizzled", 1e-6, seed=gw.seed)
+    x, r, w = workloads.make_inputs(wl, dev)
+    _, b, _, sfb = gemm_operands(gw, dev)
+    sf_bytes = fq.fp4_sf_size_bytes(M, K, fq.FP4_NVFP4, fq.FP4_SF_SWIZZLED)
+    per_step = wl.algorithmic_bytes() + gw.algorithmic_bytes()
+    rot = max(1, -(-2 * L2_BYTES // per_step))
+    sets = []
+    for _ in range(rot):
+        sets.append({"x": x.clone(), "xn": -x, "r": r.clone(), "b": b.clone(), "sfb": sfb.clone(),
+                     "p": torch.empty(M, K // 2, dtype=torch.uint8, device=dev),
+                     "s": torch.empty(sf_bytes, dtype=torch.uint8, device=dev),
+                     "o": torch.empty(M, N, dtype=torch.bfloat16, device=dev)})
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+
+    def step(c, xs, pdl):
+        st = L.fp4_add_rmsnorm_quant_ex(xs.data_ptr(), K, c["r"].data_ptr(), K, w.data_ptr(),
+                                        None, 1e-6, M, K, fq.FP4_DT_BF16, fq.FP4_NVFP4,
+                                        fq.FP4_SF_SWIZZLED, c["p"].data_ptr(), c["s"].data_ptr(),
+                                        None, None, None, pdl, sh)
+        if st != 0:
+            raise fq.Fp4Error(st, "chain: fused")
+        st = L.fp4_gemm_nvfp4_bf16(c["p"].data_ptr(), c["b"].data_ptr(), c["s"].data_ptr(),
+                                   c["sfb"].data_ptr(), 1.0, None, None, M, N, K,
+                                   c["o"].data_ptr(), -1, pdl, sh)
+        if st != 0:
+            raise fq.Fp4Error(st, "chain: gemm")
+
+    results = {}
+    for pdl in (0, 1):
+        def one_pass():
+            for c in sets:
+                step(c, c["x"], pdl)
+            for c in sets:
+                step(c, c["xn"], pdl)
+        with torch.cuda.stream(stream):
+            one_pass()
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                one_pass()
+            for _ in range(max(3, args.warmup)):
+                graph.replay()
+        stream.synchronize()
+        reps = max(1, -(-args.steps // (2 * rot)))
+        a = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            e.record(stream)
+        stream.synchronize()
+        results[pdl] = a.elapsed_time(e) * 1e3 / (reps * 2 * rot)
+    line = {"metric": CHAIN_METRIC, "value": round(results[1], 3), "unit": "us",
+            "n_gpus": 1, "steps": reps * 2 * rot, "warmup": args.warmup,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 in, e2m1 x e2m1 -> f32, bf16 out", "data": "synthetic",
+            "config": {"workload": f"chain_{gw.name}", "M": M, "N": N, "K": K,
+                       "l2": "%d copies of inputs, weights and outputs rotated (%.0f MB per "
+                             "pass vs 129 MB L2), one pass captured as a CUDA graph"
+                             % (rot, 2 * rot * per_step / 1e6),
+                       "fused_kernel": fq.fp4_launch_shape(M, K, 0, 0, 1)["kernel"],
+                       "gemm": fq.fp4_gemm_variant(M, N, K)},
+            "us_per_step_without_pdl": round(results[0], 3),
+            "us_per_step_with_pdl": round(results[1], 3),
+            "gpu_launches": 2 * reps * 2 * rot}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.op == "chain":
+        run_chain(args)
+        return
     if args.op == "gemm":
         if args.impl == "reference":
             run_gemm_reference(args)

@@ -38,7 +38,7 @@ int stream_ctas_per_sm_fp16(int fmt, int cpt, int threads);
 #define FP4Q_DIRECT_CTA_THREADS 128     // target threads of a direct-kernel CTA
 #endif
 #ifndef FP4Q_STREAM
-#define FP4Q_STREAM 1                   // long batches of narrow rows: persistent stream kernel
+#define FP4Q_STREAM 0                   // long batches of narrow rows: persistent stream kernel
 #endif
 #ifndef FP4Q_STREAM_CTA_THREADS
 #define FP4Q_STREAM_CTA_THREADS 256     // target threads of a stream-kernel CTA

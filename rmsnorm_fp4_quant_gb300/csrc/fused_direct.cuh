@@ -28,8 +28,16 @@ __device__ __forceinline__ void st_peer_f32(float* local_slot, uint32_t peer, fl
   asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(remote), "f"(v) : "memory");
 }
 
+// Register budget: the launch bound of the instance, or a cap on the one- and
+// two-chunk instances (more CTAs resident per SM) when FP4Q_DIRECT_MAXNREG is set.
+#if defined(FP4Q_DIRECT_MAXNREG) && FP4Q_DIRECT_MAXNREG > 0
+#define FP4Q_DIRECT_REGS(CPT) __maxnreg__((CPT) <= 2 ? FP4Q_DIRECT_MAXNREG : 128)
+#else
+#define FP4Q_DIRECT_REGS(CPT) __launch_bounds__(max_threads_for_cpt(CPT))
+#endif
+
 template <typename T, int FMT, int CPT, bool EX>
-__global__ void __launch_bounds__(max_threads_for_cpt(CPT))
+__global__ void FP4Q_DIRECT_REGS(CPT)
 fused_direct_kernel(const FusedParams p) {
   __shared__ float warp_part[32];
   __shared__ float cluster_part[16];

@@ -51,8 +51,14 @@ __host__ __device__ constexpr size_t tma_smem_bytes(int stages, int rows_per_cta
   return static_cast<size_t>(stages) * 4u * rows_per_cta * H + 8u * stages + 2u * 32u * 4u;
 }
 
+#if defined(FP4Q_TMA_MAXNREG) && FP4Q_TMA_MAXNREG > 0
+#define FP4Q_TMA_REGS(CPT) __maxnreg__((CPT) <= 2 ? FP4Q_TMA_MAXNREG : 128)
+#else
+#define FP4Q_TMA_REGS(CPT) __launch_bounds__(max_threads_for_cpt(CPT))
+#endif
+
 template <typename T, int FMT, int CPT, bool EX>
-__global__ void __launch_bounds__(max_threads_for_cpt(CPT))
+__global__ void FP4Q_TMA_REGS(CPT)
 fused_tma_kernel(const FusedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int S = p.stages;

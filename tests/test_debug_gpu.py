@@ -93,7 +93,7 @@ def test_checks_find_nothing_and_change_nothing(D):
         torch.cuda.synchronize()
         for ta, tb in zip(qd, qr):
             assert torch.equal(ta, tb), ("quantize", M, H)
-    assert kinds >= {"fused_direct_kernel", "fused_tma_kernel", "fused_stream_kernel"}, kinds
+    assert kinds >= {"fused_direct_kernel", "fused_tma_kernel"}, kinds
     # the GEMM: every schedule, both operand formats, the epilogues
     for (M, N, K) in [(128, 128, 256), (300, 520, 768), (41, 1536, 6144), (1024, 1024, 1024)]:
         for fmt in ("nvfp4", "mxfp4"):

@@ -49,6 +49,9 @@ int stream_ctas_per_sm_fp16(int fmt, int cpt, int threads);
 #ifndef FP4Q_STREAM_MIN_GROUPS
 #define FP4Q_STREAM_MIN_GROUPS 4        // row groups per resident CTA for the stream kernel
 #endif
+#ifndef FP4Q_WARP_ROWS
+#define FP4Q_WARP_ROWS 0                // prefer a whole row in one warp when no lane idles
+#endif
 
 static_assert(kStatusTimeout == FP4_ERR_TIMEOUT, "device and host timeout status differ");
 
@@ -108,6 +111,19 @@ int round_tpr(int chunks, int cpt) {
 bool pick_cpt(int chunks, int min_tpr, int* cpt_out, int* tpr_out, int max_cpt = 4) {
   static const int order[4] = {2, 1, 3, 4};
   int best = -1, best_tpr = 0, best_waste = 1 << 30;
+  if (FP4Q_WARP_ROWS && min_tpr <= 32) {
+    // a row in one warp, no idle lane: the slice reduction is shuffles only
+    for (int i = 0; i < 4; ++i) {
+      const int cpt = order[i];
+      if (cpt > max_cpt) continue;
+      const int tpr = round_tpr(chunks, cpt);
+      if (tpr <= 32 && tpr >= min_tpr && tpr * cpt == chunks) {
+        *cpt_out = cpt;
+        *tpr_out = tpr;
+        return true;
+      }
+    }
+  }
   for (int i = 0; i < 4; ++i) {
     const int cpt = order[i];
     if (cpt > max_cpt) continue;

@@ -518,7 +518,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
 //   one lane each     continuous stream of K blocks over all the CTA's tiles
 //                     through the S-stage ring (never drains between tiles);
 //   warp 1            tensor-memory allocation; one lane issues the MMAs;
-//   warps 2..5        epilogue, lane quarter = warp % 4;
+//   warps 2..5        epilogue, lane quarter = warp % 4 (and warps 8..11, the
+//                     other half of the columns, with FP4Q_GEMM_EPI8);
 //   warp 7, one lane  scale mover: each stage's scale tiles into that stage's
 //                     tensor-memory slot, committed to sf_ready[s].
 // While the epilogue reads a tile's accumulator out (acc_empty), the
@@ -527,8 +528,17 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
 // other CTA's MMAs run meanwhile.  This is the automatic schedule for large
 // NVFP4 products (238 us on 8192 x 7168 x 7168 against 244 us for one CTA
 // per tile in the same run).
+#ifndef FP4Q_GEMM_EPI8
+#define FP4Q_GEMM_EPI8 0     // 256-wide persistent tiles drained by eight epilogue warps
+#endif
+
 template <int BN, bool MX>
 struct PCfg {
+  // Epilogue warps: four (one per tensor-memory lane quarter), or eight for
+  // 256-wide tiles (two per quarter, each draining half of the columns), so
+  // the single accumulator is handed back to the MMAs sooner.
+  static constexpr int kEpiWarps = (BN == 256 && FP4Q_GEMM_EPI8) ? 8 : 4;
+  static constexpr int kThreads = 256 + (kEpiWarps - 4) * 32;
   // One accumulator: a 128-wide tile then needs 128 + S * 32 <= 256 tensor-
   // memory columns, so two CTAs share an SM and one's epilogue overlaps the
   // other's MMAs (measured faster than one CTA per SM with two accumulators
@@ -545,7 +555,7 @@ struct PCfg {
 };
 
 template <int BN, bool MX, bool RAG>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(PCfg<BN, MX>::kThreads, 1)
 gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
                              const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
   using C = Cfg<BN, MX>;
@@ -586,7 +596,7 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
     mbar_init(sf_done, 1);
     for (int a = 0; a < P::kAcc; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);   // one arrival per epilogue warp
+      mbar_init(&acc_empty[a], P::kEpiWarps);   // one arrival per epilogue warp
     }
     mbar_init(mma_done, 1);
     *failed = 0;
@@ -733,9 +743,11 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
     }
     tc_commit(sf_done);
     mbar_wait_bounded(sf_done, 0, FP4Q_WAIT_LIMIT(p));
-  } else if (warp >= 2 && warp <= 5) {
-    // ---- epilogue ----
+  } else if ((warp >= 2 && warp <= 5) || warp >= 8) {
+    // ---- epilogue: warps 2..5 (and 8..11) ----
     const int quarter = warp & 3;
+    constexpr int kCols = BN / (P::kEpiWarps / 4);    // columns each warp drains
+    const int c_lo = warp >= 8 ? kCols : 0;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     bool ok = true;
     for (int i = 0; i < my_tiles; ++i) {
@@ -751,7 +763,7 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const bool bad = !ok || *failed != 0;
       if (ok) {
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = c_lo; c < c_lo + kCols; c += 32) {
           uint32_t r[32];
           tmem_load_32cols(tmem + lane_off + static_cast<uint32_t>(a * BN + c), r);
           if (row < p.rows_out) store_columns32(p, r, row, n_tile * BN + c, bad);
@@ -763,7 +775,8 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
         uint32_t r[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) r[c] = 0;
-        for (int c = 0; c < BN; c += 32) store_columns32(p, r, row, n_tile * BN + c, true);
+        for (int c = c_lo; c < c_lo + kCols; c += 32)
+          store_columns32(p, r, row, n_tile * BN + c, true);
       }
     }
   }
@@ -1014,7 +1027,7 @@ cudaError_t launch_persistent(const uint8_t* a, const uint8_t* b, GemmParams p, 
   static PrepTable table;
   Prep* pr = nullptr;
   // as many CTAs per SM as tensor memory holds: two 128-wide, one 256-wide
-  cudaError_t e = prepare(table, kernel, 256, smem_need, p.tmem_cols, p.stages, &pr);
+  cudaError_t e = prepare(table, kernel, P::kThreads, smem_need, p.tmem_cols, p.stages, &pr);
   if (e != cudaSuccess) return e;
   const int sms = sm_count();
   if (sms < 1) return cudaErrorInvalidDevice;
@@ -1022,7 +1035,7 @@ cudaError_t launch_persistent(const uint8_t* a, const uint8_t* b, GemmParams p, 
   const int64_t resident = static_cast<int64_t>(sms) * static_cast<int64_t>(512 / p.tmem_cols);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(tiles < resident ? tiles : resident), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.blockDim = dim3(P::kThreads, 1, 1);
   cfg.dynamicSmemBytes = pr->smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -68,6 +68,8 @@ def parse_args():
     ap.add_argument("--format", default=None, help="override the workload's format")
     ap.add_argument("--y-out", action="store_true",
                     help="also write y (the normalised rows, input dtype): +2H bytes per row")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="launch the fused calls without programmatic dependent launch")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
@@ -401,10 +403,14 @@ def run_ours(args, wl):
         gs_t = torch.tensor([args.global_scale], dtype=torch.float32, device=dev)
     gp = gs_t.data_ptr() if gs_t is not None else None
     y_t, yp = None, None
+    # consecutive calls are programmatic dependents of the call before (the
+    # way a serving stream chains its kernels): each launch is scheduled
+    # during the previous call's last CTAs and waits for its results
+    pdl_on = 0 if args.no_pdl else 1
     if args.op == "quantize":
         qcall = L.fp4_quantize
 
-        def step(i):
+        def step(i, pdl=0):
             st = qcall(ptrs[i & 1], gp, M, H, dt, fmt, lay, pp, sp, s2, sh)
             if st != 0:
                 raise fq.Fp4Error(st, "fp4_quantize")
@@ -413,9 +419,9 @@ def run_ours(args, wl):
         y_t = torch.empty(M, H, dtype=x.dtype, device=dev) if args.y_out else None
         yp = y_t.data_ptr() if y_t is not None else None
 
-        def step(i):
+        def step(i, pdl=pdl_on):
             st = call(ptrs[i & 1], H, rp, H, wp, gp, eps, M, H, dt, fmt, lay, pp, sp, s2, yp,
-                      None, 0, sh)
+                      None, pdl, sh)
             if st != 0:
                 raise fq.Fp4Error(st, "fp4_add_rmsnorm_quant")
 
@@ -446,7 +452,7 @@ def run_ours(args, wl):
                 st = L.fp4_add_rmsnorm_quant_ex(
                     xs.data_ptr(), H, c["r"].data_ptr(), H, wp, gp, eps, M, H, dt, fmt, lay,
                     c["p"].data_ptr(), c["s"].data_ptr(), s2p,
-                    c["y"].data_ptr() if c["y"] is not None else None, None, 0, sh)
+                    c["y"].data_ptr() if c["y"] is not None else None, None, pdl_on, sh)
             if st != 0:
                 raise fq.Fp4Error(st, "graph step")
 
@@ -512,12 +518,27 @@ def run_ours(args, wl):
             ev[i][1].record(stream)
     stream.synchronize()
     kern_ms = [a.elapsed_time(b) for a, b in ev]
+    # the same K calls without programmatic dependent launch (reported beside)
+    no_pdl_ms = None
+    if graph is None and args.op == "fused" and pdl_on:
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a0.record(stream)
+            for i in range(K):
+                step(i, 0)
+            a1.record(stream)
+        stream.synchronize()
+        no_pdl_ms = a0.elapsed_time(a1) / K
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     clocks = None
-    if sampler:
+    if sampler and args.clock_seconds <= 0:
+        clocks = sampler.summary(wall0, wall1)
+        sampler.stop()
+    elif sampler:
         # The timed region of a short run lasts a millisecond or so, shorter
         # than the sampling period; the clock record comes from a sustained
         # loop of the same calls right after it (outside the timed region).
@@ -604,7 +625,7 @@ def run_ours(args, wl):
                 st = L.fp4_add_rmsnorm_quant_ex(
                     b["x"].data_ptr(), H, b["r"].data_ptr(), H, b["w"].data_ptr(), gp, eps, M, H,
                     dt, fmt, lay, b["p"].data_ptr(), b["s"].data_ptr(), s2p,
-                    b["y"].data_ptr() if b["y"] is not None else None, None, 0, sh)
+                    b["y"].data_ptr() if b["y"] is not None else None, None, pdl_on, sh)
             if st != 0:
                 raise fq.Fp4Error(st, "e2e step")
             b["done"].record(stream)
@@ -648,7 +669,8 @@ def run_ours(args, wl):
         for other in large_workloads():
             if other.name == wl.name:
                 continue
-            configs.append(time_config(L, fq, other, dev, stream, args.config_steps, peak_gbs))
+            configs.append(time_config(L, fq, other, dev, stream, args.config_steps, peak_gbs,
+                                       pdl_on))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.op == "fused":
@@ -661,7 +683,7 @@ def run_ours(args, wl):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": wl.name, "op": args.op, "global_scale": args.global_scale,
-                       "y_out": bool(args.y_out),
+                       "y_out": bool(args.y_out), "pdl": bool(pdl_on) and args.op == "fused",
                        "M": M, "H": H, "format": wl.fmt,
                        "sf_layout": wl.sf_layout, "io_dtype": wl.dtype, "eps": wl.eps,
                        "algorithmic_bytes_per_step": alg,
@@ -682,7 +704,11 @@ def run_ours(args, wl):
                          "traffic": traffic, "traffic_source": traffic_src,
                          "kernel": kernel_name, "launch": shape,
                          "kernel_ms_mean": round(kern_mean, 5),
-                         "kernel_ms_event_pairs_median": round(statistics.median(kern_ms), 5)},
+                         "kernel_ms_event_pairs_median": round(statistics.median(kern_ms), 5),
+                         "no_pdl": None if no_pdl_ms is None else {
+                             "kernel_ms_mean": round(no_pdl_ms, 5),
+                             "achieved": round(alg / (no_pdl_ms * 1e-3) / 1e9, 1),
+                             "frac": round(alg / (no_pdl_ms * 1e-3) / 1e9 / peak, 4)}},
             "clocks": clocks, "e2e": e2e, "gpu_launches": K, "cpu_baseline": cpu,
             "configs": configs,
         }
@@ -697,11 +723,13 @@ def large_workloads():
     return [workloads.C3, workloads.C4] + [w for w in workloads.sweep() if w.M == 32768]
 
 
-def time_config(L, fq, wl, dev, stream, steps: int, peak: float):
+def time_config(L, fq, wl, dev, stream, steps: int, peak: float, pdl: int = 1):
     """One large workload: inputs drawn on the device, `steps` calls timed
     back to back between two events on `stream` after 5 warm-up calls
-    (consecutive calls alternate x and -x), each call one launch.  Every one
-    of these moves more than twice the L2 per call, so no flush is needed."""
+    (consecutive calls alternate x and -x, each a programmatic dependent of
+    the one before when `pdl`), each call one launch; then the same without
+    programmatic dependent launch.  Every one of these moves more than twice
+    the L2 per call, so no flush is needed."""
     import torch
     M, H = wl.M, wl.H
     fmt = {"nvfp4": fq.FP4_NVFP4, "mxfp4": fq.FP4_MXFP4, "e4m3b32": fq.FP4_E4M3_B32}[wl.fmt]
@@ -717,33 +745,39 @@ def time_config(L, fq, wl, dev, stream, steps: int, peak: float):
     sh = stream.cuda_stream
     s2 = sf_rm.data_ptr() if sf_rm is not None else None
 
-    def step(i):
+    def step(i, pdl_i):
         st = L.fp4_add_rmsnorm_quant_ex(xs[i & 1].data_ptr(), H, r.data_ptr(), H, w.data_ptr(),
                                         None, float(wl.eps), M, H, dt, fmt, lay,
-                                        packed.data_ptr(), sf.data_ptr(), s2, None, None, 0, sh)
+                                        packed.data_ptr(), sf.data_ptr(), s2, None, None, pdl_i,
+                                        sh)
         if st != 0:
             raise fq.Fp4Error(st, wl.name)
 
-    torch.cuda.synchronize(dev)
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        for i in range(5):
-            step(i)
-        a.record(stream)
-        for i in range(steps):
-            step(i)
-        b.record(stream)
-    stream.synchronize()
-    ms = a.elapsed_time(b) / steps
+    def timed(pdl_i):
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for i in range(5):
+                step(i, pdl_i)
+            a.record(stream)
+            for i in range(steps):
+                step(i, pdl_i)
+            b.record(stream)
+        stream.synchronize()
+        return a.elapsed_time(b) / steps
+
+    ms = timed(pdl)
+    ms_no_pdl = timed(0) if pdl else ms
     alg = wl.algorithmic_bytes()
     shape = fq.fp4_launch_shape(M, H, dt, fmt, lay)
     del x, r, w, xs, packed, sf, sf_rm
     torch.cuda.empty_cache()
-    return {"workload": wl.name, "ms_per_step": round(ms, 5), "steps": steps,
+    return {"workload": wl.name, "ms_per_step": round(ms, 5), "steps": steps, "pdl": bool(pdl),
             "algorithmic_bytes": alg, "gbs": round(alg / (ms * 1e-3) / 1e9, 1),
             "frac": round(alg / (ms * 1e-3) / 1e9 / peak, 4), "kernel": shape["kernel"],
-            "launch": shape}
+            "launch": shape, "no_pdl": {"ms_per_step": round(ms_no_pdl, 5),
+                                        "frac": round(alg / (ms_no_pdl * 1e-3) / 1e9 / peak, 4)}}
 
 
 # ---------------------------------------------------------------------------

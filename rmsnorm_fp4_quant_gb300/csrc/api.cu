@@ -50,7 +50,7 @@ int stream_ctas_per_sm_fp16(int fmt, int cpt, int threads);
 #define FP4Q_STREAM_MIN_GROUPS 4        // row groups per resident CTA for the stream kernel
 #endif
 #ifndef FP4Q_WARP_ROWS
-#define FP4Q_WARP_ROWS 0                // prefer a whole row in one warp when no lane idles
+#define FP4Q_WARP_ROWS 1                // prefer a whole row in one warp when no lane idles
 #endif
 
 static_assert(kStatusTimeout == FP4_ERR_TIMEOUT, "device and host timeout status differ");
@@ -214,8 +214,11 @@ bool choose_fused_shape(int64_t M, int64_t rows, int H, int fmt, int dtype, int 
     int cpt, tpr;
     if (!pick_cpt(nchunk, 2, &cpt, &tpr)) return false;
     int R = tpr >= FP4Q_DIRECT_CTA_THREADS ? 1 : FP4Q_DIRECT_CTA_THREADS / tpr;
-    const int64_t per_sm = (M + num_sms - 1) / num_sms;   // short batches: spread rows first
-    if (per_sm < R) R = static_cast<int>(per_sm < 1 ? 1 : per_sm);
+    // short batches: at least one CTA per SM before rows are stacked in a CTA
+    if (M < static_cast<int64_t>(R) * num_sms) {
+      const int64_t fit = M / num_sms;
+      R = static_cast<int>(fit < 1 ? 1 : fit);
+    }
     while ((tpr * R) % 32) ++R;                           // whole warps
     if (tpr * R > max_threads_for_cpt(cpt)) return false;
     out->path = kPathDirect;

@@ -110,7 +110,7 @@ def measured_hbm_peak():
 KERNEL_SOURCES = {
     "fused": ("api.cu", "async_copy.cuh", "fp4q_device.cuh", "fp4q_launch.h", "fused_bf16.cu",
               "fused_common.cuh", "fused_direct.cuh", "fused_fp16.cu", "fused_launch.cuh",
-              "fused_stream.cuh", "fused_tma.cuh"),
+              "fused_tma.cuh", "debug_checks.h"),
     "quantize": ("api.cu", "fp4q_device.cuh", "fp4q_launch.h", "quantize.cu"),
     "gemm": ("async_copy.cuh", "fp4q_device.cuh", "gemm_api.cu", "gemm_launch.h", "gemm_nvfp4.cu",
              "tcgen05.cuh"),
@@ -410,8 +410,8 @@ def run_ours(args, wl):
     if args.op == "quantize":
         qcall = L.fp4_quantize
 
-        def step(i, pdl=0):
-            st = qcall(ptrs[i & 1], gp, M, H, dt, fmt, lay, pp, sp, s2, sh)
+        def step(i, pdl=pdl_on):
+            st = qcall(ptrs[i & 1], gp, M, H, dt, fmt, lay, pp, sp, s2, pdl, sh)
             if st != 0:
                 raise fq.Fp4Error(st, "fp4_quantize")
     else:
@@ -447,7 +447,7 @@ def run_ours(args, wl):
             s2p = c["s2"].data_ptr() if c["s2"] is not None else None
             if args.op == "quantize":
                 st = L.fp4_quantize(xs.data_ptr(), gp, M, H, dt, fmt, lay, c["p"].data_ptr(),
-                                    c["s"].data_ptr(), s2p, sh)
+                                    c["s"].data_ptr(), s2p, pdl_on, sh)
             else:
                 st = L.fp4_add_rmsnorm_quant_ex(
                     xs.data_ptr(), H, c["r"].data_ptr(), H, wp, gp, eps, M, H, dt, fmt, lay,
@@ -520,7 +520,7 @@ def run_ours(args, wl):
     kern_ms = [a.elapsed_time(b) for a, b in ev]
     # the same K calls without programmatic dependent launch (reported beside)
     no_pdl_ms = None
-    if graph is None and args.op == "fused" and pdl_on:
+    if graph is None and pdl_on:
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
@@ -620,7 +620,7 @@ def run_ours(args, wl):
             s2p = b["s2"].data_ptr() if b["s2"] is not None else None
             if args.op == "quantize":
                 st = L.fp4_quantize(b["x"].data_ptr(), gp, M, H, dt, fmt, lay, b["p"].data_ptr(),
-                                    b["s"].data_ptr(), s2p, sh)
+                                    b["s"].data_ptr(), s2p, pdl_on, sh)
             else:
                 st = L.fp4_add_rmsnorm_quant_ex(
                     b["x"].data_ptr(), H, b["r"].data_ptr(), H, b["w"].data_ptr(), gp, eps, M, H,
@@ -683,7 +683,7 @@ def run_ours(args, wl):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": wl.name, "op": args.op, "global_scale": args.global_scale,
-                       "y_out": bool(args.y_out), "pdl": bool(pdl_on) and args.op == "fused",
+                       "y_out": bool(args.y_out), "pdl": bool(pdl_on),
                        "M": M, "H": H, "format": wl.fmt,
                        "sf_layout": wl.sf_layout, "io_dtype": wl.dtype, "eps": wl.eps,
                        "algorithmic_bytes_per_step": alg,

@@ -185,12 +185,14 @@ FP4Q_API fp4_status_t fp4_add_rmsnorm_quant_ex(const void* input, int64_t input_
  * `quantize_fp4_sfa_fp16`).  The same layouts serve as the GEMM's A-operand
  * scales (rows = M) or B-operand scales (rows = N).  input 32-byte aligned,
  * H a multiple of the block size (>= 16); global_scale as in
- * fp4_add_rmsnorm_quant_gs; outputs as fp4_add_rmsnorm_quant.
+ * fp4_add_rmsnorm_quant_gs; outputs as fp4_add_rmsnorm_quant; pdl as in
+ * fp4_add_rmsnorm_quant_ex (launched as a programmatic dependent of the
+ * kernel before it on `stream`, e.g. the kernel that produced `input`).
  */
 FP4Q_API fp4_status_t fp4_quantize(const void* input, const float* global_scale, int64_t M, int64_t H,
                                    fp4_dtype_t dtype, fp4_format_t format, fp4_sf_layout_t sf_layout,
                                    uint8_t* out_packed, uint8_t* out_sf, uint8_t* out_sf_rowmajor,
-                                   fp4q_stream_t stream);
+                                   int pdl, fp4q_stream_t stream);
 
 /*
  * fp4_dequant - validation helper: out[m, i] = E2M1 value of code (m, i) times
@@ -218,8 +220,7 @@ FP4Q_API int64_t fp4_sf_size_bytes(int64_t M, int64_t H, fp4_format_t format, fp
  * fp4_launch_shape - the launch the library would make for fp4_add_rmsnorm_quant
  * with these sizes on the current device (diagnostics; launches nothing).
  * Fills out[8] = {kernel (0 = persistent TMA-ring kernel, 1 = register-resident
- * kernel, 2 = persistent register-resident kernel with the next row group in
- * flight), chunks per thread, threads per row slice, row slices per CTA,
+ * kernel), chunks per thread, threads per row slice, row slices per CTA,
  * CTAs per cluster, shared-memory ring stages, threads per CTA, CTAs}.
  * Returns FP4_OK, or the status fp4_add_rmsnorm_quant would return for the sizes.
  */

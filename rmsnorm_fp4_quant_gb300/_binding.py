@@ -83,7 +83,7 @@ def _open(path: str, how: str) -> ctypes.CDLL:
     L.fp4_add_rmsnorm_quant_ex.argtypes = [vp, i64, vp, i64, vp, vp, ctypes.c_float, i64, i64,
                                            ci, ci, ci, vp, vp, vp, vp, vp, ci, vp]
     L.fp4_add_rmsnorm_quant_ex.restype = ci
-    L.fp4_quantize.argtypes = [vp, vp, i64, i64, ci, ci, ci, vp, vp, vp, vp]
+    L.fp4_quantize.argtypes = [vp, vp, i64, i64, ci, ci, ci, vp, vp, vp, ci, vp]
     L.fp4_quantize.restype = ci
     L.fp4_dequant.argtypes = [vp, vp, i64, i64, ci, ci, vp, vp]
     L.fp4_dequant.restype = ci
@@ -157,9 +157,9 @@ def fp4_add_rmsnorm_quant_ex(input_ptr: int, input_row_stride: int, residual_ptr
 
 def fp4_quantize(input_ptr: int, global_scale_ptr: int, M: int, H: int, dtype: int, fmt: int,
                  sf_layout: int, out_packed_ptr: int, out_sf_ptr: int, out_sf_rowmajor_ptr: int,
-                 stream: int) -> int:
+                 pdl: int, stream: int) -> int:
     return lib().fp4_quantize(input_ptr, global_scale_ptr or None, M, H, dtype, fmt, sf_layout,
-                              out_packed_ptr, out_sf_ptr, out_sf_rowmajor_ptr or None,
+                              out_packed_ptr, out_sf_ptr, out_sf_rowmajor_ptr or None, pdl,
                               stream or None)
 
 
@@ -248,8 +248,7 @@ def fp4_launch_shape(M: int, H: int, dtype: int, fmt: int, sf_layout: int) -> di
     if st != 0:
         raise Fp4Error(st, "fp4_launch_shape")
     d = dict(zip(_SHAPE_KEYS, list(out)))
-    d["kernel"] = {0: "fused_tma_kernel", 1: "fused_direct_kernel",
-                   2: "fused_stream_kernel"}[d["kernel"]]
+    d["kernel"] = "fused_tma_kernel" if d["kernel"] == 0 else "fused_direct_kernel"
     return d
 
 
@@ -408,9 +407,11 @@ def add_rmsnorm_fp4quant(input, residual, weight, eps: float = 1e-6, fmt: str = 
 
 
 def quantize_fp4(x, fmt: str = "nvfp4", sf_layout: str = "swizzled", global_scale=None,
-                 out_packed=None, out_sf=None, out_sf_rowmajor=None, stream=None) -> Tuple:
+                 out_packed=None, out_sf=None, out_sf_rowmajor=None, pdl: bool = False,
+                 stream=None) -> Tuple:
     """Block-quantize x (M, H) or (B, S, H) itself (no add, no norm); returns
-    (packed, sf) or (packed, sf_tiled, sf_rowmajor) for sf_layout="both"."""
+    (packed, sf) or (packed, sf_tiled, sf_rowmajor) for sf_layout="both".
+    ``pdl``: launch as a programmatic dependent of the previous kernel."""
     _check_cuda(x, "x")
     dt = _dtype_code(x)
     f = _FORMATS[fmt]
@@ -425,7 +426,7 @@ def quantize_fp4(x, fmt: str = "nvfp4", sf_layout: str = "swizzled", global_scal
     st = fp4_quantize(x.data_ptr(), _gs_ptr(global_scale), M, H, dt, f, lay,
                       out_packed.data_ptr(), out_sf.data_ptr(),
                       out_sf_rowmajor.data_ptr() if out_sf_rowmajor is not None else 0,
-                      _stream_handle(stream))
+                      1 if pdl else 0, _stream_handle(stream))
     if st != 0:
         raise Fp4Error(st, "fp4_quantize")
     if lay == FP4_SF_BOTH:

@@ -15,8 +15,6 @@ cudaError_t launch_fused_bf16(int fmt, const FusedShape& s, const FusedParams& p
 cudaError_t launch_fused_fp16(int fmt, const FusedShape& s, const FusedParams& p, cudaStream_t st);
 int tma_ctas_per_sm_bf16(int fmt, int cpt, int threads, size_t smem);
 int tma_ctas_per_sm_fp16(int fmt, int cpt, int threads, size_t smem);
-int stream_ctas_per_sm_bf16(int fmt, int cpt, int threads);
-int stream_ctas_per_sm_fp16(int fmt, int cpt, int threads);
 
 // Tuning constants of the launch-shape choice (compile-time, overridable with -D).
 #ifndef FP4Q_TMA_CTA_THREADS
@@ -36,18 +34,6 @@ int stream_ctas_per_sm_fp16(int fmt, int cpt, int threads);
 #endif
 #ifndef FP4Q_DIRECT_CTA_THREADS
 #define FP4Q_DIRECT_CTA_THREADS 128     // target threads of a direct-kernel CTA
-#endif
-#ifndef FP4Q_STREAM
-#define FP4Q_STREAM 0                   // long batches of narrow rows: persistent stream kernel
-#endif
-#ifndef FP4Q_STREAM_CTA_THREADS
-#define FP4Q_STREAM_CTA_THREADS 256     // target threads of a stream-kernel CTA
-#endif
-#ifndef FP4Q_STREAM_MAX_CPT
-#define FP4Q_STREAM_MAX_CPT 4           // chunks per thread allowed in the stream kernel
-#endif
-#ifndef FP4Q_STREAM_MIN_GROUPS
-#define FP4Q_STREAM_MIN_GROUPS 4        // row groups per resident CTA for the stream kernel
 #endif
 #ifndef FP4Q_WARP_ROWS
 #define FP4Q_WARP_ROWS 1                // prefer a whole row in one warp when no lane idles
@@ -108,14 +94,13 @@ int round_tpr(int chunks, int cpt) {
 // Chunks per thread and slice width for `chunks` chunks: fewest idle lanes,
 // ties broken in the order 2, 1, 3, 4 (fewer registers first, then more
 // work per thread).  min_tpr forces whole warps where the kernel needs them.
-bool pick_cpt(int chunks, int min_tpr, int* cpt_out, int* tpr_out, int max_cpt = 4) {
+bool pick_cpt(int chunks, int min_tpr, int* cpt_out, int* tpr_out) {
   static const int order[4] = {2, 1, 3, 4};
   int best = -1, best_tpr = 0, best_waste = 1 << 30;
   if (FP4Q_WARP_ROWS && min_tpr <= 32) {
     // a row in one warp, no idle lane: the slice reduction is shuffles only
     for (int i = 0; i < 4; ++i) {
       const int cpt = order[i];
-      if (cpt > max_cpt) continue;
       const int tpr = round_tpr(chunks, cpt);
       if (tpr <= 32 && tpr >= min_tpr && tpr * cpt == chunks) {
         *cpt_out = cpt;
@@ -126,7 +111,6 @@ bool pick_cpt(int chunks, int min_tpr, int* cpt_out, int* tpr_out, int max_cpt =
   }
   for (int i = 0; i < 4; ++i) {
     const int cpt = order[i];
-    if (cpt > max_cpt) continue;
     int tpr = round_tpr(chunks, cpt);
     if (tpr < min_tpr) tpr = min_tpr;
     if (tpr > max_threads_for_cpt(cpt)) continue;
@@ -175,38 +159,7 @@ bool choose_fused_shape(int64_t M, int64_t rows, int H, int fmt, int dtype, int 
     out->threads = tpr;
     out->smem = 0;
     out->grid = rows * cluster;
-    out->sms = num_sms;
     return true;
-  }
-
-  if (H < FP4Q_TMA_MIN_H && FP4Q_STREAM) {
-    // Long batches: persistent CTAs with the next row group in flight, when
-    // every resident CTA gets several groups.
-    int cpt, tpr;
-    if (pick_cpt(nchunk, 2, &cpt, &tpr, FP4Q_STREAM_MAX_CPT)) {
-      int R = tpr >= FP4Q_STREAM_CTA_THREADS ? 1 : FP4Q_STREAM_CTA_THREADS / tpr;
-      while ((tpr * R) % 32) ++R;                         // whole warps
-      if (tpr * R <= max_threads_for_cpt(cpt)) {
-        const int per = dtype == 0 ? stream_ctas_per_sm_bf16(fmt, cpt, tpr * R)
-                                   : stream_ctas_per_sm_fp16(fmt, cpt, tpr * R);
-        const int64_t resident = static_cast<int64_t>(per) * num_sms;
-        const int64_t groups = (rows + R - 1) / R;
-        if (per > 0 && groups >= FP4Q_STREAM_MIN_GROUPS * resident) {
-          out->path = kPathStream;
-          out->cpt = cpt;
-          out->tpr = tpr;
-          out->rows_per_cta = R;
-          out->cluster = 1;
-          out->chunks_per_cta = nchunk;
-          out->stages = 0;
-          out->threads = tpr * R;
-          out->smem = 0;
-          out->grid = resident;
-          out->sms = num_sms;
-          return true;
-        }
-      }
-    }
   }
 
   if (H < FP4Q_TMA_MIN_H) {
@@ -231,7 +184,6 @@ bool choose_fused_shape(int64_t M, int64_t rows, int H, int fmt, int dtype, int 
     out->threads = tpr * R;
     out->smem = 0;
     out->grid = (rows + R - 1) / R;
-    out->sms = num_sms;
     return true;
   }
 
@@ -269,7 +221,6 @@ bool choose_fused_shape(int64_t M, int64_t rows, int H, int fmt, int dtype, int 
   out->threads = tpr * R;
   out->smem = smem;
   out->grid = grid;
-  out->sms = num_sms;
   return true;
 }
 
@@ -514,7 +465,7 @@ fp4_status_t fp4_add_rmsnorm_quant_ex(const void* input, int64_t input_row_strid
 
 fp4_status_t fp4_quantize(const void* input, const float* global_scale, int64_t M, int64_t H,
                           fp4_dtype_t dtype, fp4_format_t format, fp4_sf_layout_t sf_layout,
-                          uint8_t* out_packed, uint8_t* out_sf, uint8_t* out_sf_rowmajor,
+                          uint8_t* out_packed, uint8_t* out_sf, uint8_t* out_sf_rowmajor, int pdl,
                           fp4q_stream_t stream) {
   if (dtype != FP4_DT_BF16 && dtype != FP4_DT_FP16) return FP4_ERR_INVALID_ARG;
   if (!valid_format(format) || !valid_layout(sf_layout)) return FP4_ERR_INVALID_ARG;
@@ -550,8 +501,7 @@ fp4_status_t fp4_quantize(const void* input, const float* global_scale, int64_t 
   p.nkt = (p.nb + 3) / 4;
   FP4Q_SET_DEBUG(p);
   return record_cuda_status(launch_quantize(dtype == FP4_DT_BF16 ? 0 : 1, static_cast<int>(format), p,
-                                     num_sms_current_device(),
-                                     reinterpret_cast<cudaStream_t>(stream)));
+                                            pdl, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int fp4_debug_build(void) {

@@ -50,7 +50,7 @@ struct FusedParams {
   int cluster;         // CTAs per row (direct kernel), 1 otherwise
   int chunks_per_cta;  // nchunk / cluster
   int stages;          // shared-memory ring depth (TMA kernel)
-  int64_t groups;      // ceil(rows / rows_per_cta) (persistent kernels)
+  int64_t groups;      // ceil(rows / rows_per_cta) (TMA kernel)
   FP4Q_DEBUG_FIELD     // debug build only: checks and fault injection
 };
 
@@ -70,7 +70,6 @@ __host__ __device__ inline long long tiled_extent(int64_t M, int nkt) {
 
 constexpr int kPathTma = 0;       // persistent CTAs, TMA bulk-copy row ring
 constexpr int kPathDirect = 1;    // register-resident rows, optionally one row per cluster
-constexpr int kPathStream = 2;    // persistent CTAs, register-resident rows, next row in flight
 
 // Launch shape chosen on the host for one (M, H, format, dtype).
 struct FusedShape {
@@ -84,7 +83,6 @@ struct FusedShape {
   int threads;         // tpr * rows_per_cta
   size_t smem;         // dynamic shared memory bytes
   int64_t grid;        // CTAs
-  int sms;             // SMs the grid was sized for (persistent paths)
   int pdl;             // launch as a programmatic dependent of the previous kernel
 };
 
@@ -131,7 +129,7 @@ struct QuantParams {
   FP4Q_DEBUG_FIELD     // debug build only: checks
 };
 
-cudaError_t launch_quantize(int dtype, int fmt, const QuantParams& p, int num_sms,
+cudaError_t launch_quantize(int dtype, int fmt, const QuantParams& p, int pdl,
                             cudaStream_t stream);
 
 }  // namespace fp4q

@@ -9,7 +9,4 @@ cudaError_t launch_fused_bf16(int fmt, const FusedShape& s, const FusedParams& p
 int tma_ctas_per_sm_bf16(int fmt, int cpt, int threads, size_t smem) {
   return ctas_per_sm_dtype<__nv_bfloat16>(fmt, cpt, threads, smem);
 }
-int stream_ctas_per_sm_bf16(int fmt, int cpt, int threads) {
-  return stream_ctas_per_sm_dtype<__nv_bfloat16>(fmt, cpt, threads);
-}
 }  // namespace fp4q

@@ -4,7 +4,6 @@
 #include <mutex>
 
 #include "fused_direct.cuh"
-#include "fused_stream.cuh"
 #include "fused_tma.cuh"
 
 namespace fp4q {
@@ -56,52 +55,6 @@ int ctas_per_sm_one(int threads, size_t smem) {
   return n;
 }
 
-// CTAs of a fused_stream_kernel instance resident per SM at `threads` threads
-// (cached per device: calls repeat the same launch shape).
-template <typename T, int FMT, int CPT, bool EX>
-int stream_ctas_per_sm_one(int threads) {
-  struct Last { int threads; int n; };
-  static Last last[64] = {};
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  const bool cacheable = dev >= 0 && dev < 64;
-  if (cacheable) {
-    std::lock_guard<std::mutex> lock(mu);
-    if (last[dev].n > 0 && last[dev].threads == threads) return last[dev].n;
-  }
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_stream_kernel<T, FMT, CPT, EX>,
-                                                    threads, 0) != cudaSuccess)
-    return 0;
-  if (cacheable) {
-    std::lock_guard<std::mutex> lock(mu);
-    last[dev] = Last{threads, n};
-  }
-  return n;
-}
-
-template <typename T, int FMT>
-int stream_ctas_per_sm_fmt(int cpt, int threads) {
-  switch (cpt) {
-    case 1: return stream_ctas_per_sm_one<T, FMT, 1, false>(threads);
-    case 2: return stream_ctas_per_sm_one<T, FMT, 2, false>(threads);
-    case 3: return stream_ctas_per_sm_one<T, FMT, 3, false>(threads);
-    case 4: return stream_ctas_per_sm_one<T, FMT, 4, false>(threads);
-    default: return 0;
-  }
-}
-
-template <typename T>
-int stream_ctas_per_sm_dtype(int fmt, int cpt, int threads) {
-  switch (fmt) {
-    case kFmtNV: return stream_ctas_per_sm_fmt<T, kFmtNV>(cpt, threads);
-    case kFmtMX: return stream_ctas_per_sm_fmt<T, kFmtMX>(cpt, threads);
-    case kFmtE4B32: return stream_ctas_per_sm_fmt<T, kFmtE4B32>(cpt, threads);
-    default: return 0;
-  }
-}
-
 template <typename T, int FMT>
 int ctas_per_sm_fmt(int cpt, int threads, size_t smem) {
   switch (cpt) {
@@ -149,16 +102,6 @@ cudaError_t launch_one(const FusedShape& s, const FusedParams& p, cudaStream_t s
     }
     cfg.dynamicSmemBytes = 0;
     return cudaLaunchKernelEx(&cfg, fused_direct_kernel<T, FMT, CPT, EX>, p);
-  }
-  if (s.path == kPathStream) {
-    if (EX) {   // the general instance may hold fewer CTAs per SM: never more than resident
-      const int per = stream_ctas_per_sm_one<T, FMT, CPT, EX>(s.threads);
-      if (per <= 0) return cudaErrorInvalidConfiguration;
-      const int64_t resident = static_cast<int64_t>(per) * s.sms;
-      if (resident < s.grid) cfg.gridDim.x = static_cast<unsigned>(resident);
-    }
-    cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, fused_stream_kernel<T, FMT, CPT, EX>, p);
   }
   const cudaError_t e = raise_smem_limit<T, FMT, CPT, EX>(s.smem);
   if (e != cudaSuccess) return e;

@@ -513,13 +513,13 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
 // Persistent form: resident CTAs (two per SM for 128-wide tiles, one for
 // 256-wide) walk the output tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...
 // (row tile t / n_tiles, column tile t % n_tiles, so CTAs running together
-// share A's row panel).  Eight warps:
+// share A's row panel).  Eight warps (twelve for 256-wide tiles):
 //   warps 0 and 6,    producers (A and its scales / B and its scales): one
 //   one lane each     continuous stream of K blocks over all the CTA's tiles
 //                     through the S-stage ring (never drains between tiles);
 //   warp 1            tensor-memory allocation; one lane issues the MMAs;
-//   warps 2..5        epilogue, lane quarter = warp % 4 (and warps 8..11, the
-//                     other half of the columns, with FP4Q_GEMM_EPI8);
+//   warps 2..5        epilogue, lane quarter = warp % 4 (and, for 256-wide
+//                     tiles, warps 8..11 draining the other half of the columns);
 //   warp 7, one lane  scale mover: each stage's scale tiles into that stage's
 //                     tensor-memory slot, committed to sf_ready[s].
 // While the epilogue reads a tile's accumulator out (acc_empty), the
@@ -529,14 +529,15 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
 // NVFP4 products (238 us on 8192 x 7168 x 7168 against 244 us for one CTA
 // per tile in the same run).
 #ifndef FP4Q_GEMM_EPI8
-#define FP4Q_GEMM_EPI8 0     // 256-wide persistent tiles drained by eight epilogue warps
+#define FP4Q_GEMM_EPI8 1     // 256-wide persistent tiles drained by eight epilogue warps
 #endif
 
 template <int BN, bool MX>
 struct PCfg {
   // Epilogue warps: four (one per tensor-memory lane quarter), or eight for
   // 256-wide tiles (two per quarter, each draining half of the columns), so
-  // the single accumulator is handed back to the MMAs sooner.
+  // the single accumulator is handed back to the MMAs sooner (8192 x 7168 x
+  // 7168: 260.5 -> 241.9 us for the 256-wide schedule).
   static constexpr int kEpiWarps = (BN == 256 && FP4Q_GEMM_EPI8) ? 8 : 4;
   static constexpr int kThreads = 256 + (kEpiWarps - 4) * 32;
   // One accumulator: a 128-wide tile then needs 128 + S * 32 <= 256 tensor-

@@ -107,38 +107,44 @@ __global__ void __launch_bounds__(256, SEGS >= 3 ? 4 : 1) quantize_kernel(const 
 // ragged last run from 8 segments up (measured 2-11 % faster than runs of 2),
 // else 2 or 1.
 template <typename T, int FMT>
-cudaError_t launch_q_fmt(const QuantParams& p, cudaStream_t stream) {
+cudaError_t launch_q_fmt(const QuantParams& p, int pdl, cudaStream_t stream) {
   const int segs = (p.nchunk + 31) / 32;
   const int per = segs % 4 == 0 ? 4
                 : segs % 3 == 0 ? 3
                 : segs >= 8     ? 4
                 : segs % 2 == 0 ? 2 : 1;
-  const dim3 grid(static_cast<unsigned>((p.rows + 7) / 8),
-                  static_cast<unsigned>((segs + per - 1) / per));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((p.rows + 7) / 8),
+                     static_cast<unsigned>((segs + per - 1) / per));
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
   switch (per) {
-    case 4: quantize_kernel<T, FMT, 4><<<grid, 256, 0, stream>>>(p); break;
-    case 3: quantize_kernel<T, FMT, 3><<<grid, 256, 0, stream>>>(p); break;
-    case 2: quantize_kernel<T, FMT, 2><<<grid, 256, 0, stream>>>(p); break;
-    default: quantize_kernel<T, FMT, 1><<<grid, 256, 0, stream>>>(p); break;
+    case 4: return cudaLaunchKernelEx(&cfg, quantize_kernel<T, FMT, 4>, p);
+    case 3: return cudaLaunchKernelEx(&cfg, quantize_kernel<T, FMT, 3>, p);
+    case 2: return cudaLaunchKernelEx(&cfg, quantize_kernel<T, FMT, 2>, p);
+    default: return cudaLaunchKernelEx(&cfg, quantize_kernel<T, FMT, 1>, p);
   }
-  return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t launch_q(int fmt, const QuantParams& p, cudaStream_t stream) {
+cudaError_t launch_q(int fmt, const QuantParams& p, int pdl, cudaStream_t stream) {
   switch (fmt) {
-    case kFmtNV: return launch_q_fmt<T, kFmtNV>(p, stream);
-    case kFmtMX: return launch_q_fmt<T, kFmtMX>(p, stream);
-    case kFmtE4B32: return launch_q_fmt<T, kFmtE4B32>(p, stream);
+    case kFmtNV: return launch_q_fmt<T, kFmtNV>(p, pdl, stream);
+    case kFmtMX: return launch_q_fmt<T, kFmtMX>(p, pdl, stream);
+    case kFmtE4B32: return launch_q_fmt<T, kFmtE4B32>(p, pdl, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_quantize(int dtype, int fmt, const QuantParams& p, int num_sms,
+cudaError_t launch_quantize(int dtype, int fmt, const QuantParams& p, int pdl,
                             cudaStream_t stream) {
-  (void)num_sms;
   if (p.rows == 0) return cudaSuccess;
   if ((p.rows + 7) / 8 > INT32_MAX || (p.nchunk + 31) / 32 > 65535)
     return cudaErrorInvalidConfiguration;
@@ -147,7 +153,8 @@ cudaError_t launch_quantize(int dtype, int fmt, const QuantParams& p, int num_sm
   // 17408- and 32768-wide rows.
   QuantParams q = p;
   q.evict_first = p.H <= 8192 ? 1 : 0;
-  return dtype == 0 ? launch_q<__nv_bfloat16>(fmt, q, stream) : launch_q<__half>(fmt, q, stream);
+  return dtype == 0 ? launch_q<__nv_bfloat16>(fmt, q, pdl, stream)
+                     : launch_q<__half>(fmt, q, pdl, stream);
 }
 
 }  // namespace fp4q

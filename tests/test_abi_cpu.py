@@ -173,7 +173,7 @@ def test_quantize_validation(L, kwargs, status):
     a = dict(x=A, gs=0, M=4, H=256, dt=0, f=0, lay=0, p=P, s=S, s2=0)
     a.update(kwargs)
     st = fq.fp4_quantize(a["x"], a["gs"], a["M"], a["H"], a["dt"], a["f"], a["lay"], a["p"],
-                         a["s"], a["s2"], 0)
+                         a["s"], a["s2"], 0, 0)
     assert st == status
 
 
@@ -220,7 +220,7 @@ def test_quantize_overlap_validation(L, kwargs, status):
     a = dict(x=A, gs=0, M=4, H=256, dt=0, f=0, lay=0, p=P, s=S, s2=0)
     a.update(kwargs)
     st = fq.fp4_quantize(a["x"], a["gs"], a["M"], a["H"], a["dt"], a["f"], a["lay"], a["p"],
-                         a["s"], a["s2"], 0)
+                         a["s"], a["s2"], 0, 0)
     assert st == status
 
 

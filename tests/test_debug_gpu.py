@@ -56,8 +56,8 @@ def _fused(L, x, r, w, fmt, layout, status=None):
     return outs
 
 
-# every fused kernel path: register-resident rows, cluster rows, the TMA ring,
-# and the persistent stream kernel (long batches)
+# every fused kernel path: register-resident rows (also one row per warp, and
+# long batches), cluster rows, the TMA ring
 FUSED_SHAPES = [(1, 64), (3, 80), (127, 208), (129, 1536), (130, 5120), (129, 7168),
                 (41, 17408), (1, 32768), (2, 65536), (5000, 64), (2049, 208), (1999, 1536),
                 (700, 7168), (613, 17408), (333, 32768), (20000, 1536), (2500, 7168)]

@@ -64,14 +64,15 @@ cudaError_t launch_dequant(int fmt, const DequantParams& p, cudaStream_t stream)
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
   if (blocks > 152 * 64) blocks = 152 * 64;
-  const unsigned g = static_cast<unsigned>(blocks);
-  if (fmt == 0)
-    dequant_kernel<0><<<g, threads, 0, stream>>>(p);
-  else if (fmt == 1)
-    dequant_kernel<1><<<g, threads, 0, stream>>>(p);
-  else
-    dequant_kernel<2><<<g, threads, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.stream = stream;
+  // cudaLaunchKernelEx reports this launch's own error; the thread's sticky
+  // last error (which may be the caller's) is left alone
+  if (fmt == 0) return cudaLaunchKernelEx(&cfg, dequant_kernel<0>, p);
+  if (fmt == 1) return cudaLaunchKernelEx(&cfg, dequant_kernel<1>, p);
+  return cudaLaunchKernelEx(&cfg, dequant_kernel<2>, p);
 }
 
 }  // namespace fp4q

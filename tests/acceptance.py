@@ -123,3 +123,21 @@ def tiled_padding_is_zero(sf, M, nb):
     k = np.arange(nkt)[None, :, None, None, None] * 4 + np.arange(4)[None, None, None, None, :]
     pad = np.broadcast_to((m >= M) | (k >= nb), t.shape)
     return bool(np.all(t[pad] == 0))
+
+
+def quantize_block_task(args):
+    """Worker task: the oracle's standalone quantize on one block of rows and
+    the rule against the GPU's bytes for them; returns (exceptions, elements)."""
+    x_bits, dtype, fmt, packed, scale_bytes = args
+    o = oracle.quantize(bits_to_f32(x_bits, dtype), fmt, "rowmajor")
+    n = check_rows(o, None, scale_bytes, packed, fmt, dtype)
+    return n, int(o.codes.size)
+
+
+def gemm_block_bits_task(args):
+    """Worker task: the GEMM oracle's bf16 output bits for one block of rows
+    (its A rows and their tiled scales are passed alone; a block starts on a
+    128-row tile, so its scales are a contiguous slice of the tiled buffer)."""
+    a, b, sfa, sfb, M, N, K, fmt = args
+    g = oracle.gemm_bf16(a, b, sfa, sfb, M, N, K, fmt=fmt)
+    return (np.asarray(g.out, np.float32).view(np.uint32) >> 16).astype(np.uint16)

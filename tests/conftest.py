@@ -1,3 +1,4 @@
+import multiprocessing
 import os
 import sys
 
@@ -48,3 +49,22 @@ def pytest_terminal_summary(terminalreporter, exitstatus, config):
     for name, exc, n in log:
         terminalreporter.write_line(f"{name}: {exc} excused boundary exceptions in {n} elements "
                                     f"({exc / max(n, 1):.2e}; bound 1e-4)")
+
+
+@pytest.fixture(scope="session")
+def oracle_pool():
+    """Oracle workers for full-size parity: spawned (never forked after CUDA
+    is initialised), one per host core, single-threaded numpy each."""
+    n = max(1, min(32, len(os.sched_getaffinity(0))))
+    keep = os.environ.get("OMP_NUM_THREADS")
+    os.environ["OMP_NUM_THREADS"] = "1"
+    try:
+        p = multiprocessing.get_context("spawn").Pool(n)
+    finally:
+        if keep is None:
+            os.environ.pop("OMP_NUM_THREADS", None)
+        else:
+            os.environ["OMP_NUM_THREADS"] = keep
+    yield p
+    p.close()
+    p.join()

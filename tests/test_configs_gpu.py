@@ -7,9 +7,6 @@ acceptance rule (tests/acceptance.py) on it, and the excused exceptions are
 summed over the whole workload before the 1e-4 bound is applied.  The tiled
 padding is checked over the whole buffer, the two scale layouts against each
 other on every row, and small workloads also through the library's dequant."""
-import multiprocessing
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -32,25 +29,6 @@ SMALL_ELEMS = 1 << 22       # at most this many elements: also checked through f
 def _lib():
     fbuild.build()
     fq.lib()
-
-
-@pytest.fixture(scope="module")
-def pool():
-    """Oracle workers: spawned (never forked after CUDA is initialised), one
-    per host core, single-threaded numpy each."""
-    n = max(1, min(32, len(os.sched_getaffinity(0))))
-    keep = os.environ.get("OMP_NUM_THREADS")
-    os.environ["OMP_NUM_THREADS"] = "1"
-    try:
-        p = multiprocessing.get_context("spawn").Pool(n)
-    finally:
-        if keep is None:
-            os.environ.pop("OMP_NUM_THREADS", None)
-        else:
-            os.environ["OMP_NUM_THREADS"] = keep
-    yield p
-    p.close()
-    p.join()
 
 
 def _bits16(t):
@@ -112,12 +90,12 @@ def run_workload(wl: workloads.Workload, pool):
 
 @pytest.mark.parametrize("wl", [workloads.C1, workloads.C2, workloads.C3, workloads.C4],
                          ids=lambda w: w.name)
-def test_named_configs(wl, pool, parity_log):
-    stats = run_workload(wl, pool)
+def test_named_configs(wl, oracle_pool, parity_log):
+    stats = run_workload(wl, oracle_pool)
     parity_log.append((wl.name, stats["exceptions"], stats["elements"]))
 
 
 @pytest.mark.parametrize("wl", workloads.sweep(), ids=lambda w: w.name)
-def test_sweep(wl, pool, parity_log):
-    stats = run_workload(wl, pool)
+def test_sweep(wl, oracle_pool, parity_log):
+    stats = run_workload(wl, oracle_pool)
     parity_log.append((wl.name, stats["exceptions"], stats["elements"]))

@@ -17,6 +17,7 @@ import numpy as np
 import pytest
 import torch
 
+import acceptance
 import oracle
 import rmsnorm_fp4_quant_gb300 as fq
 import workloads
@@ -202,19 +203,33 @@ def test_gemm_residual_in_place():
     check(got, oracle_gemm(a, b, sfa, sfb, M, N, K, residual=res.float().numpy()), K, "exact")
 
 
-@pytest.mark.parametrize("variant", [-1] + VARIANTS)
-def test_gemm_full_size_sampled_rows(variant):
-    """The 8192 x 7168 x 7168 product in the launch configuration the
-    benchmark times (automatic variant) and in each tile schedule:
-    exact-kind operands, every column of 96 sampled rows (first and last row
-    tile, ragged spread) bit-exact."""
+@pytest.fixture(scope="module")
+def g4_exact(oracle_pool):
+    """The 8192 x 7168 x 7168 exact-kind product's operands and the oracle's
+    bf16 output bits for every row, computed once on spawned workers (one
+    512-row block of A each; a block starts on a 128-row tile, so its tiled
+    scales are a contiguous slice)."""
     wl = workloads.GEMM_CONFIGS["G4_M8192_N7168_K7168"]
     a, b, sfa, sfb = operands(wl.M, wl.N, wl.K, wl.seed, "exact")
-    got = gpu_gemm(a, b, sfa, sfb, variant=variant)
-    rows = np.unique(np.concatenate([np.arange(0, 32), np.arange(wl.M - 32, wl.M),
-                                     np.random.default_rng(0).integers(0, wl.M, 32)]))
-    g = oracle_gemm(a, b, sfa, sfb, wl.M, wl.N, wl.K, rows=rows)
-    check(got[torch.as_tensor(rows, device=got.device)], g, wl.K, "exact")
+    an, bn, san, sbn = a.numpy(), b.numpy(), sfa.numpy(), sfb.numpy()
+    tile_bytes = (wl.K // 64) * 512                        # one 128-row tile of NVFP4 scales
+    blk = 512
+    tasks = [(an[r0:r0 + blk], bn, san[r0 // 128 * tile_bytes:(r0 + blk) // 128 * tile_bytes], sbn,
+              blk, wl.N, wl.K, "nvfp4") for r0 in range(0, wl.M, blk)]
+    bits = np.concatenate(oracle_pool.map(acceptance.gemm_block_bits_task, tasks, chunksize=1))
+    return wl, (a, b, sfa, sfb), bits
+
+
+@pytest.mark.parametrize("variant", [-1] + VARIANTS)
+def test_gemm_full_size_every_row(variant, g4_exact):
+    """The 8192 x 7168 x 7168 product in the launch configuration the
+    benchmark times (automatic variant) and in each tile schedule:
+    exact-kind operands, every output element bit-exact."""
+    wl, ops, want = g4_exact
+    got = gpu_gemm(*ops, variant=variant)
+    got_bits = got.view(torch.int16).cpu().numpy().view(np.uint16)
+    bad = np.argwhere(got_bits != want)
+    assert bad.size == 0, f"{len(bad)} of {want.size} outputs differ, first at {bad[:4].tolist()}"
 
 
 @pytest.mark.parametrize("K", [2048, 1568])

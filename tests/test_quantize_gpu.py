@@ -9,6 +9,7 @@ import rmsnorm_fp4_quant_gb300 as fq
 import workloads
 from rmsnorm_fp4_quant_gb300 import build as fbuild
 
+import acceptance
 import parity
 
 pytestmark = pytest.mark.gpu
@@ -60,27 +61,52 @@ def test_quantize_three_d_and_empty():
     assert p.numel() == 0 and s.numel() == 0
 
 
-def _sample_rows(M, seed, n=96):
-    fixed = {0, 1, 31, 32, 127, 128, 129, M // 2, M - 129, M - 128, M - 2, M - 1}
-    rng = np.random.default_rng(seed)
-    rand = set(rng.choice(M, size=min(n, M), replace=False).tolist())
-    return np.array(sorted(r for r in fixed | rand if 0 <= r < M), dtype=np.int64)
-
-
 @pytest.mark.parametrize("name", ["C3_M8192_H7168_bf16_mxfp4_swizzled_outliers",
                                   "C4_M16384_H5120_fp16_nvfp4_both",
                                   "C5_M32768_H1536_bf16_nvfp4_swizzled",
                                   "C5_M32768_H6144_bf16_nvfp4_swizzled",
                                   "C5_M32768_H17408_bf16_mxfp4_swizzled",
                                   "C5_M32768_H32768_bf16_nvfp4_swizzled"])
-def test_quantize_full_size_sampled(name):
+def test_quantize_full_size_every_row(name, oracle_pool, parity_log):
     """The benchmarked quantize shapes at full size, in the launch the
-    benchmark times: sampled rows (tile edges, first/last, seeded random)
-    against the oracle, every padding byte of the tiled buffer checked."""
+    benchmark times: every row against the oracle (blocks of about 4M
+    elements on spawned workers, exceptions summed over the workload), the
+    two scale layouts against each other, every padding byte of the tiled
+    buffer."""
     wl = workloads.CONFIGS[name]
+    M, H = wl.M, wl.H
+    nb = H // wl.block
     x = workloads.make_inputs(wl, "cuda")[0]
-    rows = _sample_rows(wl.M, wl.seed)
-    xs = x.index_select(0, torch.from_numpy(rows).cuda()).float().cpu().numpy()
-    g = parity.run_quantize(x, wl.fmt, wl.sf_layout, rows=rows)
-    o = oracle.quantize(xs, wl.fmt, wl.sf_layout)
-    parity.compare(g, o, wl.fmt, wl.sf_layout, wl.dtype, wl.M, wl.H)
+    outs = fq.quantize_fp4(x, fmt=wl.fmt, sf_layout=wl.sf_layout)
+    torch.cuda.synchronize()
+    packed = outs[0]
+    sf = outs[1].cpu().numpy().reshape(-1)
+    if wl.sf_layout == "rowmajor":
+        rows_sf = sf.reshape(M, nb)
+    else:
+        assert acceptance.tiled_padding_is_zero(sf, M, nb)
+    sf_rm = outs[2].cpu().numpy().reshape(M, nb) if wl.sf_layout == "both" else None
+    step = max(1, (1 << 22) // H)
+
+    def task(a):
+        b = min(M, a + step)
+        if wl.sf_layout == "rowmajor":
+            sc = rows_sf[a:b]
+        else:
+            sc = sf[oracle.swizzled_sf_offset(np.arange(a, b)[:, None], np.arange(nb)[None, :],
+                                              (nb + 3) // 4)]
+            if sf_rm is not None:
+                assert np.array_equal(sf_rm[a:b], sc), f"scale layouts disagree in rows {a}.."
+        return (x[a:b].view(torch.int16).cpu().numpy().view(np.uint16), wl.dtype, wl.fmt,
+                packed[a:b].cpu().numpy(), sc)
+
+    starts = list(range(0, M, step))
+    n_exc = n_el = 0
+    for i in range(0, len(starts), 32):
+        tasks = [task(a) for a in starts[i:i + 32]]
+        for e, n in oracle_pool.map(acceptance.quantize_block_task, tasks, chunksize=1):
+            n_exc += e
+            n_el += n
+    assert n_el == M * H
+    assert n_exc <= acceptance.MAX_EXCEPTION_FRAC * n_el
+    parity_log.append((name + " (quantize)", n_exc, n_el))

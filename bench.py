@@ -462,6 +462,7 @@ def run_ours(args, wl):
             for c in copies:
                 step_copy(c, c["xn"])
 
+        torch.cuda.synchronize(dev)       # the copies were made on the default stream
         with torch.cuda.stream(stream):
             one_pass()
         stream.synchronize()
@@ -888,6 +889,7 @@ def run_gemm(args):
         if st != 0:
             raise fq.Fp4Error(st, "fp4_gemm_nvfp4_bf16")
 
+    torch.cuda.synchronize(dev)           # operands and copies were made on the default stream
     sampler = ClockSampler(gpu_smi_id(torch, dev)) if rank == 0 else None
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, rot)):
@@ -1038,6 +1040,7 @@ def run_chain(args):
                      "o": torch.empty(M, N, dtype=torch.bfloat16, device=dev)})
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
+    torch.cuda.synchronize(dev)           # inputs and copies were made on the default stream
 
     def step(c, xs, pdl):
         st = L.fp4_add_rmsnorm_quant_ex(xs.data_ptr(), K, c["r"].data_ptr(), K, w.data_ptr(),

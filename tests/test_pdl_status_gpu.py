@@ -39,6 +39,7 @@ def test_chained_calls_with_pdl(M, H, fmt):
     x, r, w = workloads.make_inputs(wl, "cpu")
     xd, rd, wd = x.cuda(), r.cuda(), w.cuda()
     stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())   # the inputs' uploads
     outs = []
     with torch.cuda.stream(stream):
         for _ in range(steps):
@@ -63,6 +64,7 @@ def test_quantize_with_pdl_reads_the_fused_output():
     x, r, w = workloads.make_inputs(wl, "cpu")
     xd, rd, wd = x.cuda(), r.cuda(), w.cuda()
     stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())   # the inputs' uploads
     with torch.cuda.stream(stream):
         fq.add_rmsnorm_fp4quant(xd, rd, wd, fmt="nvfp4", sf_layout="swizzled", stream=stream)
         pq, sq = fq.quantize_fp4(rd, fmt="nvfp4", sf_layout="swizzled", pdl=True, stream=stream)

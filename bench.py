@@ -126,9 +126,10 @@ def kernel_source_sha(op: str = "fused") -> str:
     return h.hexdigest()
 
 
-def gemm_profile_key(workload_name: str, fmt: str, kernel: str) -> str:
-    """The `workload:` key of a GEMM capture: shape, operand format, kernel."""
-    return f"{workload_name}_{fmt}_{kernel}"
+def gemm_profile_key(workload_name: str, fmt: str, kernel: str, tile_n: int) -> str:
+    """The `workload:` key of a GEMM capture: shape, operand format, kernel
+    and output-tile width (the persistent kernel runs 128- or 256-wide)."""
+    return f"{workload_name}_{fmt}_{kernel}_n{tile_n}"
 
 
 def recorded_traffic(workload_name: str, op: str = "fused"):
@@ -938,9 +939,10 @@ def run_gemm(args):
              "frac": round(gbs / hbm_peak, 4), "peak_source": f"{hbm_src} hbm_gbs"})
     sched = fq.fp4_gemm_variant(gw.M, gw.N, gw.K, 0 if args.gemm_format == "nvfp4" else 1,
                                 False, args.gemm_variant)
-    # a GEMM capture is keyed by shape, operand format and kernel
+    # a GEMM capture is keyed by shape, operand format, kernel and tile width
     traffic, traffic_src = recorded_traffic(gemm_profile_key(gw.name, args.gemm_format,
-                                                             sched["kernel"]), "gemm")
+                                                             sched["kernel"], sched["tile_n"]),
+                                            "gemm")
     roof.update({"traffic": traffic, "traffic_source": traffic_src,
                  "kernel": sched["kernel"], "schedule": sched, "kernel_ms_mean": round(ms, 5),
                  "algorithmic_bytes": alg, "flops": gw.flops()})

@@ -263,9 +263,9 @@ FP4Q_API int fp4_gemm_variant(int64_t M, int64_t N, int64_t K, fp4_format_t form
  *             0 = 128 x 128 tiles (two CTAs per SM) or 1 = 128 x 256 tiles;
  *             persistent CTAs walking the tiles, one accumulator each, loading
  *             the next tile while the epilogue drains the last, with
- *             2 = 128 x 128 (two CTAs per SM; automatic when the output has
- *             more 128 x 128 tiles than twice the SMs) or 3 = 128 x 256 (one
- *             per SM); 4 = 128 x 128 tiles with the K loop of each tile split
+ *             2 = 128 x 128 (two CTAs per SM) or 3 = 128 x 256 (one per SM;
+ *             automatic when the output has more 128 x 128 tiles than twice
+ *             the SMs); 4 = 128 x 128 tiles with the K loop of each tile split
  *             over a thread-block cluster of up to 16 CTAs (partial tiles
  *             summed in rank order through distributed shared memory;
  *             automatic when the output has at most half as many 128 x 128

@@ -33,6 +33,7 @@ struct GemmParams {
   int mma_last;                // K = 64 MMAs in the last K block (1..4)
   int sf_tiles_last;           // scale tiles per 128 rows in the last K block
   int stages;                  // shared-memory ring depth, 2..6
+  int sf_stages;               // scale ring depth of the persistent kernel: stages or stages + 1
   int split;                   // CTAs of a cluster sharing one tile's K loop (1 = none)
   uint32_t tmem_cols;          // tensor-memory columns taken per CTA
   FP4Q_DEBUG_FIELD             // debug build only: checks and fault injection

@@ -19,20 +19,21 @@
 //                      warp 2 B and its scales, each arriving once per stage
 //                      on each barrier (two threads issue a stage's copies in
 //                      about half the time one takes: 4 % on a large product).
-//   warp 3, one lane   scale mover.  As soon as a stage's scales have landed
-//                      (sf_full[s], before its operand tiles), copies its eight scale tiles into
-//                      the stage's tensor-memory slot (tcgen05.cp 32x128b,
-//                      repeated over the four lane quarters: a 512-byte tile is
-//                      exactly the image of 128 rows x 4 scales the
-//                      block-scaled MMA reads) and commits them to sf_ready[s],
-//                      so the copies of stage s + 1 run while stage s
-//                      multiplies (8 % on a large product against issuing them
-//                      from the MMA thread).
+//   warps 3 and 4,     scale movers.  As soon as a stage's scales have landed
+//   one lane each      (sf_full[s], before its operand tiles), copy its eight
+//                      scale tiles into the stage's tensor-memory slot
+//                      (tcgen05.cp 32x128b, repeated over the four lane
+//                      quarters: a 512-byte tile is exactly the image of 128
+//                      rows x 4 scales the block-scaled MMA reads), even tiles
+//                      by one and odd by the other, each committing to
+//                      sf_ready[s], so the copies of stage s + 1 run while
+//                      stage s multiplies.  Issuing a copy holds its thread for
+//                      tens of cycles, hence two.
 //   warp 1, one lane   MMA issuer.  Once the stage's scales are in tensor
 //                      memory, issues four K = 64 MMAs of kind mxf4nvf4 with
 //                      one E4M3 scale per 16 elements, and commits the stage
 //                      back (empty[s]).
-//   all four warps     epilogue.  Warp w owns accumulator lanes 32w..32w+31 (one
+//   warps 0..3         epilogue.  Warp w owns accumulator lanes 32w..32w+31 (one
 //                      output row per thread): 32 columns at a time from tensor
 //                      memory, alpha, bias and residual in fp32, one rounding to
 //                      bf16, 16-byte stores.
@@ -261,8 +262,12 @@ __device__ __forceinline__ void store_columns32(const GemmParams& p, const uint3
 // scale tiles that exist are issued (codes past K read as zero, so a half
 // step meets the tiled layout's k-padding scales).  A separate instance, so
 // the full-block loops of every other product stay as they are.
+// Threads of the one-tile kernel: four warps (roles, then the epilogue, one
+// tensor-memory lane quarter each) and a fifth, the second scale mover.
+constexpr int kTileThreads = 160;
+
 template <int BN, bool SPLIT, bool MX, bool RAG>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kTileThreads, 1)
 gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
                   const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
   using C = Cfg<BN, MX>;
@@ -297,10 +302,10 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 2);   // one arrival per producer
       mbar_init(&empty[s], 1);
-      mbar_init(&sf_ready[s], 1);
+      mbar_init(&sf_ready[s], 2);  // one commit per scale mover
       mbar_init(&sf_full[s], 2);   // one arrival per producer
     }
-    mbar_init(sf_done, 1);
+    mbar_init(sf_done, 2);
     mbar_init(accum, 1);
     *failed = 0;
     mbar_init_fence();
@@ -328,11 +333,11 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const int b_tiles = b_tiles_total - b_tile0 < C::kSfTilesB ? b_tiles_total - b_tile0
                                                                 : C::kSfTilesB;
     int i = 0;    // K blocks issued
+    int s = 0;    // ring slot of block i; ph = (i / S) & 1, by counters (no division per block)
+    uint32_t ph = 0;
     for (; i < kb1 - kb0; ++i) {
       const int kb = kb0 + i;
-      const int s = i % S;
-      if (i >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((i / S - 1) & 1),
-                                        FP4Q_WAIT_LIMIT(p))) {
+      if (i >= S && !mbar_wait_bounded(&empty[s], ph ^ 1u, FP4Q_WAIT_LIMIT(p))) {
         *failed = 1;
         break;
       }
@@ -365,15 +370,20 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
         tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
                     n_tile * BN, &full[s]);
       }
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
     issued = i;
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
+    int s = 0;
+    uint32_t ph = 0;
     for (int i = 0; i < kb1 - kb0; ++i) {
-      const int s = i % S;
       // the operand tiles (full[s]) and the scales in tensor memory (sf_ready[s])
-      if (!mbar_wait_bounded(&sf_ready[s], static_cast<uint32_t>((i / S) & 1), FP4Q_WAIT_LIMIT(p)) ||
-          !mbar_wait_bounded(&full[s], static_cast<uint32_t>((i / S) & 1), FP4Q_WAIT_LIMIT(p))) {
+      if (!mbar_wait_bounded(&sf_ready[s], ph, FP4Q_WAIT_LIMIT(p)) ||
+          !mbar_wait_bounded(&full[s], ph, FP4Q_WAIT_LIMIT(p))) {
         *failed = 1;
         break;
       }
@@ -395,15 +405,21 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                  sfb_t + 4 * C::kSfTilesB * C::atom(j), (i | j) != 0 ? 1u : 0u);
       }
       tc_commit(&empty[s]);   // the stage is free once these MMAs have read it
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
     tc_commit(accum);         // every MMA issued above has completed
-  } else if (warp == 3 && lane == 0) {
-    // ---- scale mover ----
+  } else if ((warp == 3 || warp == 4) && lane == 0) {
+    // ---- scale movers: even scale tiles by warp 3, odd by warp 4 ----
     // Slot s is free for stage i: sf_full[s] of stage i means the producers
     // refilled the stage, which waited for the MMAs of stage i - S.
+    const int mover = warp - 3;
+    int s = 0;
+    uint32_t ph = 0;
     for (int i = 0; i < kb1 - kb0; ++i) {
-      const int s = i % S;
-      if (!mbar_wait_bounded(&sf_full[s], static_cast<uint32_t>((i / S) & 1), FP4Q_WAIT_LIMIT(p))) {
+      if (!mbar_wait_bounded(&sf_full[s], ph, FP4Q_WAIT_LIMIT(p))) {
         *failed = 1;
         break;
       }
@@ -414,6 +430,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
       const uint32_t sfb_s = smem_addr(sSFB + static_cast<size_t>(s) * C::kSfBytesB);
 #pragma unroll
       for (int q = 0; q < C::kSfAtoms; ++q) {
+        if (q % 2 != mover) continue;
         if constexpr (RAG) {
           if (kb0 + i == p.num_kb - 1 && q >= p.sf_tiles_last) break;
         }
@@ -428,6 +445,10 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                          kSwizzleNone));
       }
       tc_commit(&sf_ready[s]);
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
     tc_commit(sf_done);       // no copy may still be running when tensor memory is freed
     mbar_wait_bounded(sf_done, 0, FP4Q_WAIT_LIMIT(p));
@@ -451,11 +472,12 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
   if (bad && threadIdx.x == 0 && p.status) atomicExch(p.status, kStatusTimeout);
   griddep_launch_dependents();
 
+  // warps 0..3 drain the accumulator, warp w its lanes 32w..32w+31
   const int row = m_tile * kBM + warp * 32 + lane;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
   if constexpr (!SPLIT) {
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = 0; c < BN && warp < 4; c += 32) {
       uint32_t r[32];
       tmem_load_32cols(lane_base + static_cast<uint32_t>(c), r);   // whole warp, unconditionally
       if (row >= p.rows_out) continue;
@@ -467,7 +489,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     float* part = reinterpret_cast<float*>(smem);
     const int local_row = warp * 32 + lane;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = 0; c < BN && warp < 4; c += 32) {
       uint32_t r[32];
       tmem_load_32cols(lane_base + static_cast<uint32_t>(c), r);
       if (row >= p.M) continue;
@@ -486,7 +508,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const int rows_valid = p.M - m_tile * kBM < kBM ? p.M - m_tile * kBM : kBM;
     constexpr int kChunks = BN / 8;
     const int items = rows_valid * kChunks;
-    for (int it = rank + split * static_cast<int>(threadIdx.x); it < items; it += split * 128) {
+    for (int it = rank + split * static_cast<int>(threadIdx.x); it < items;
+         it += split * kTileThreads) {
       const int rl = it / kChunks;
       const int ch = it - rl * kChunks;
       const uint32_t local = smem_addr(part + rl * kStride + ch * 8);
@@ -513,23 +536,34 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
 // Persistent form: resident CTAs (two per SM for 128-wide tiles, one for
 // 256-wide) walk the output tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...
 // (row tile t / n_tiles, column tile t % n_tiles, so CTAs running together
-// share A's row panel).  Eight warps (twelve for 256-wide tiles):
+// share A's row panel).  Nine warps (thirteen for 256-wide tiles):
 //   warps 0 and 6,    producers (A and its scales / B and its scales): one
 //   one lane each     continuous stream of K blocks over all the CTA's tiles
-//                     through the S-stage ring (never drains between tiles);
+//                     through the S-stage operand ring (never drains between
+//                     tiles);
 //   warp 1            tensor-memory allocation; one lane issues the MMAs;
 //   warps 2..5        epilogue, lane quarter = warp % 4 (and, for 256-wide
 //                     tiles, warps 8..11 draining the other half of the columns);
-//   warp 7, one lane  scale mover: each stage's scale tiles into that stage's
-//                     tensor-memory slot, committed to sf_ready[s].
+//   warp 7 and the    scale movers, one lane each: a K block's scale tiles
+//   last warp         into its tensor-memory slot (even tiles by one, odd by
+//                     the other), each committing to sf_ready[ss].
+// The scales have a ring of their own, SS = S + lead slots in shared and
+// tensor memory, and a producer issues K block it + lead's scales together
+// with block it's operands: the scale copy into tensor memory, which
+// completes only behind the MMAs already in the tensor pipe, then lands
+// while the block before is multiplied instead of after it.  Both rings are
+// freed by the same event - the MMAs of block it - S have completed (empty[s])
+// - since block it + lead - SS = it - S.  lead = 1 where shared and tensor
+// memory hold the extra slot at the CTA's occupancy, else 0.
 // While the epilogue reads a tile's accumulator out (acc_empty), the
 // producers already fill the ring with the next tile's K blocks, so a new
 // tile never waits for a CTA launch or a first load; with two CTAs per SM the
-// other CTA's MMAs run meanwhile.  This is the automatic schedule for large
-// NVFP4 products (238 us on 8192 x 7168 x 7168 against 244 us for one CTA
-// per tile in the same run).
+// other CTA's MMAs run meanwhile.
 #ifndef FP4Q_GEMM_EPI8
 #define FP4Q_GEMM_EPI8 1     // 256-wide persistent tiles drained by eight epilogue warps
+#endif
+#ifndef FP4Q_GEMM_SF_LEAD
+#define FP4Q_GEMM_SF_LEAD 1  // K blocks the persistent scale ring runs ahead (0 or 1)
 #endif
 
 template <int BN, bool MX>
@@ -539,24 +573,43 @@ struct PCfg {
   // the single accumulator is handed back to the MMAs sooner (8192 x 7168 x
   // 7168: 260.5 -> 241.9 us for the 256-wide schedule).
   static constexpr int kEpiWarps = (BN == 256 && FP4Q_GEMM_EPI8) ? 8 : 4;
-  static constexpr int kThreads = 256 + (kEpiWarps - 4) * 32;
-  // One accumulator: a 128-wide tile then needs 128 + S * 32 <= 256 tensor-
+  // Two scale movers: issuing a tensor-memory copy holds its thread for tens
+  // of cycles, and one thread's eight (twelve for 256-wide tiles) per K block
+  // trailed the MMAs (8192 x 7168 x 7168, 256-wide: 256.5 -> 218.8 us).
+  static constexpr int kMovers = 2;
+  static constexpr int kMover2Warp = 4 + kEpiWarps;   // after the epilogue warps
+  static constexpr int kThreads = 32 * (kMover2Warp + 1);
+  // One accumulator: a 128-wide tile then needs 128 + SS * 32 <= 256 tensor-
   // memory columns, so two CTAs share an SM and one's epilogue overlaps the
   // other's MMAs (measured faster than one CTA per SM with two accumulators
   // and six stages: 238 against 315 us on an 8192 x 7168 x 7168 product).
   static constexpr int kAcc = 1;
+  static constexpr int kCtasPerSm = BN == 128 ? 2 : 1;
   static constexpr uint32_t kSfCol = kAcc * BN;     // the scale slots after the accumulators
-  static constexpr uint32_t tmem_cols(int stages) {
-    return (kSfCol + Cfg<BN, MX>::kSfColsPerStage * stages) <= 256 ? 256u : 512u;
+  static constexpr uint32_t tmem_cols(int sf_stages) {
+    return (kSfCol + Cfg<BN, MX>::kSfColsPerStage * sf_stages) <= 256 ? 256u : 512u;
   }
-  static constexpr size_t smem_bytes(int stages) {
-    return 1024 + static_cast<size_t>(stages) * Cfg<BN, MX>::kStageBytes +
-           (4 * stages + 2 * kAcc + 2) * 8 + 8;
+  static constexpr size_t smem_bytes(int stages, int sf_stages) {
+    using C = Cfg<BN, MX>;
+    return 1024 + static_cast<size_t>(stages) * (kTileBytesA + C::kTileBytesB) +
+           static_cast<size_t>(sf_stages) * (C::kSfBytesA + C::kSfBytesB) +
+           (2 * stages + 2 * sf_stages + 2 * kAcc + 2) * 8 + 8;
+  }
+  // The scale ring's lead: 1 if the extra slot still fits kCtasPerSm CTAs in
+  // an SM's shared memory (228 KiB, 1 KiB of it reserved per CTA) and tensor
+  // memory (512 columns), else 0.
+  static constexpr int sf_lead(int stages) {
+    return FP4Q_GEMM_SF_LEAD > 0 &&
+                   kCtasPerSm * (smem_bytes(stages, stages + 1) + 1024) <= 228 * 1024 &&
+                   kCtasPerSm * tmem_cols(stages + 1) <= 512 &&
+                   kSfCol + Cfg<BN, MX>::kSfColsPerStage * (stages + 1) <= 512
+               ? 1
+               : 0;
   }
 };
 
 template <int BN, bool MX, bool RAG>
-__global__ void __launch_bounds__(PCfg<BN, MX>::kThreads, 1)
+__global__ void __launch_bounds__(PCfg<BN, MX>::kThreads, PCfg<BN, MX>::kCtasPerSm)
 gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
                              const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
   using C = Cfg<BN, MX>;
@@ -565,19 +618,21 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
+  const int SS = p.sf_stages;     // S or S + 1
+  const int lead = SS - S;
   uint8_t* sA = smem;
   uint8_t* sB = sA + static_cast<size_t>(S) * kTileBytesA;
   uint8_t* sSFA = sB + static_cast<size_t>(S) * C::kTileBytesB;
-  uint8_t* sSFB = sSFA + static_cast<size_t>(S) * C::kSfBytesA;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + static_cast<size_t>(S) * C::kSfBytesB);
+  uint8_t* sSFB = sSFA + static_cast<size_t>(SS) * C::kSfBytesA;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + static_cast<size_t>(SS) * C::kSfBytesB);
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;
   uint64_t* acc_empty = acc_full + P::kAcc;
   uint64_t* mma_done = acc_empty + P::kAcc;
-  uint64_t* sf_ready = mma_done + 1;
-  uint64_t* sf_done = sf_ready + S;
-  uint64_t* sf_full = sf_done + 1;    // the stage's scale bytes have landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_full + S);
+  uint64_t* sf_ready = mma_done + 1;  // a scale slot's tiles are in tensor memory
+  uint64_t* sf_done = sf_ready + SS;
+  uint64_t* sf_full = sf_done + 1;    // a scale slot's bytes have landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_full + SS);
   volatile int* failed = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -586,15 +641,18 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
   const int tiles = n_tiles * ((p.M + kBM - 1) / kBM);
   const int G = gridDim.x;
   const int my_tiles = blockIdx.x < tiles ? (tiles - 1 - blockIdx.x) / G + 1 : 0;
+  const int total = my_tiles * p.num_kb;    // K blocks over all of this CTA's tiles
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 2);
+      mbar_init(&full[s], 2);      // one arrival per producer
       mbar_init(&empty[s], 1);
-      mbar_init(&sf_ready[s], 1);
+    }
+    for (int s = 0; s < SS; ++s) {
+      mbar_init(&sf_ready[s], P::kMovers);   // one commit per mover
       mbar_init(&sf_full[s], 2);
     }
-    mbar_init(sf_done, 1);
+    mbar_init(sf_done, P::kMovers);
     for (int a = 0; a < P::kAcc; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], P::kEpiWarps);   // one arrival per epilogue warp
@@ -611,63 +669,103 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  int issued = 0;    // K blocks a producer thread issued copies for, over all tiles
+  int issued = 0;      // K blocks whose operand copies a producer thread issued
+  int issued_sf = 0;   // K blocks whose scale copies it issued
 
   if ((warp == 0 || warp == 6) && lane == 0) {
     // ---- producers: warp 0 A and its scales, warp 6 B and its scales ----
+    // Ring slots, phases and block coordinates advance by counters: this
+    // thread's issue rate bounds the ring, and a division by a runtime value
+    // per K block cost it more than its copies.
     const bool load_a = warp == 0;
     const int b_tiles_total = (p.N + 127) / 128;
-    int it = 0;   // K blocks issued over all tiles
-    bool ok = true;
-    for (int i = 0; i < my_tiles && ok; ++i) {
-      const int t = blockIdx.x + i * G;
-      const int m_tile = t / n_tiles, n_tile = t - (t / n_tiles) * n_tiles;
-      const uint8_t* sfa_k = p.sfa + static_cast<size_t>(m_tile) * p.nkt * kSfTileBytes;
-      const int b_tile0 = n_tile * C::kSfTilesB;
-      const int b_tiles = b_tiles_total - b_tile0 < C::kSfTilesB ? b_tiles_total - b_tile0
-                                                                  : C::kSfTilesB;
-      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-        const int s = it % S;
-        if (it >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((it / S - 1) & 1),
-                                          FP4Q_WAIT_LIMIT(p))) {
-          *failed = 1;
-          ok = false;
-          break;
+    struct Pos {         // a K block: its tile's coordinates and its index in the K loop
+      int t, m_tile, n_tile, kb;
+    };
+    auto at_tile = [&](int t, Pos& q) {
+      q.t = t;
+      q.m_tile = t / n_tiles;
+      q.n_tile = t - q.m_tile * n_tiles;
+      q.kb = 0;
+    };
+    auto advance = [&](Pos& q) {
+      if (++q.kb == p.num_kb) at_tile(q.t + G, q);
+    };
+    // block q's scales into scale slot ss
+    auto issue_scales = [&](const Pos& q, int ss) {
+      uint32_t sf_bytes = C::kSfBytesA;
+      if constexpr (RAG) {
+        if (q.kb == p.num_kb - 1)   // fewer scale tiles in the ragged last block
+          sf_bytes = static_cast<uint32_t>(p.sf_tiles_last) * kSfTileBytes;
+      }
+      if (load_a) {
+        mbar_arrive_expect_tx(&sf_full[ss], sf_bytes);
+        const uint8_t* src = p.sfa + static_cast<size_t>(q.m_tile) * p.nkt * kSfTileBytes +
+                             static_cast<size_t>(q.kb) * C::kSfBytesA;
+        if (FP4Q_IN_RANGE(p, src, sf_bytes, p.sfa, tiled_extent(p.M, p.nkt)))
+          bulk_g2s(sSFA + static_cast<size_t>(ss) * C::kSfBytesA, src, sf_bytes, &sf_full[ss]);
+      } else {
+        // B's 128-row scale tiles of this column tile that exist
+        const int b_tile0 = q.n_tile * C::kSfTilesB;
+        const int b_tiles = b_tiles_total - b_tile0 < C::kSfTilesB ? b_tiles_total - b_tile0
+                                                                    : C::kSfTilesB;
+        mbar_arrive_expect_tx(&sf_full[ss], static_cast<uint32_t>(b_tiles) * sf_bytes);
+        for (int u = 0; u < b_tiles; ++u) {
+          const uint8_t* src = p.sfb + static_cast<size_t>(b_tile0 + u) * p.nkt * kSfTileBytes +
+                               static_cast<size_t>(q.kb) * C::kSfBytesA;
+          if (FP4Q_IN_RANGE(p, src, sf_bytes, p.sfb, tiled_extent(p.N, p.nkt)))
+            bulk_g2s(sSFB + static_cast<size_t>(ss) * C::kSfBytesB + u * C::kSfBytesA, src,
+                     sf_bytes, &sf_full[ss]);
         }
-        uint32_t sf_bytes = C::kSfBytesA;
-        if constexpr (RAG) {
-          if (kb == p.num_kb - 1)   // fewer scale tiles in the ragged last block
-            sf_bytes = static_cast<uint32_t>(p.sf_tiles_last) * kSfTileBytes;
-        }
-        // the scales land on their own barrier (see the one-tile kernel)
-        mbar_arrive_expect_tx(&sf_full[s], load_a ? sf_bytes
-                                                  : static_cast<uint32_t>(b_tiles) * sf_bytes);
-        mbar_arrive_expect_tx(&full[s], load_a ? kTileBytesA : C::kTileBytesB);
-        if (load_a) {
-          const uint8_t* src = sfa_k + static_cast<size_t>(kb) * C::kSfBytesA;
-          if (FP4Q_IN_RANGE(p, src, sf_bytes, p.sfa, tiled_extent(p.M, p.nkt)))
-            bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA, src, sf_bytes, &sf_full[s]);
-          // debug build: one CTA never issues one A tile (fault injection)
-          if (!FP4Q_DROP(p, 2, static_cast<int>(blockIdx.x), it))
-            tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes,
-                        m_tile * kBM, &full[s]);
-        } else {
-          for (int q = 0; q < b_tiles; ++q) {
-            const uint8_t* src = p.sfb + static_cast<size_t>(b_tile0 + q) * p.nkt * kSfTileBytes +
-                                 static_cast<size_t>(kb) * C::kSfBytesA;
-            if (FP4Q_IN_RANGE(p, src, sf_bytes, p.sfb, tiled_extent(p.N, p.nkt)))
-              bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + q * C::kSfBytesA, src,
-                       sf_bytes, &sf_full[s]);
-          }
-          tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
-                      n_tile * BN, &full[s]);
-        }
+      }
+    };
+    Pos op, sc;              // block it, and block it + lead (its scales go out with it)
+    at_tile(blockIdx.x, op);
+    sc = op;
+    int ss = 0;              // scale slot of block it + lead
+    // blocks 0 .. lead-1: their scale slots start free
+    for (; issued_sf < lead && issued_sf < total; ++issued_sf) {
+      issue_scales(sc, ss);
+      advance(sc);
+      if (++ss == SS) ss = 0;
+    }
+    int it = 0, s = 0;
+    uint32_t ph = 0;         // it = round * S + s, ph = round & 1
+    for (; it < total; ++it) {
+      // the MMAs of block it - S have completed: operand slot s and scale
+      // slot (it + lead) % SS (last used by that same block) are free
+      if (it >= S && !mbar_wait_bounded(&empty[s], ph ^ 1u, FP4Q_WAIT_LIMIT(p))) {
+        *failed = 1;
+        break;
+      }
+      if (it + lead < total) {
+        issue_scales(sc, ss);
+        issued_sf = it + lead + 1;
+        advance(sc);
+        if (++ss == SS) ss = 0;
+      }
+      mbar_arrive_expect_tx(&full[s], load_a ? kTileBytesA : C::kTileBytesB);
+      if (load_a) {
+        // debug build: one CTA never issues one A tile (fault injection)
+        if (!FP4Q_DROP(p, 2, static_cast<int>(blockIdx.x), it))
+          tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, op.kb * kBKBytes,
+                      op.m_tile * kBM, &full[s]);
+      } else {
+        tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, op.kb * kBKBytes,
+                    op.n_tile * BN, &full[s]);
+      }
+      advance(op);
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
       }
     }
     issued = it;
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
     int it = 0;
+    int s = 0, ss = 0;         // operand and scale slots of block it
+    uint32_t ph = 0, sph = 0;  // their phases
     bool ok = true;
     for (int i = 0; i < my_tiles && ok; ++i) {
       const int a = i % P::kAcc;
@@ -680,15 +778,14 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
       tc_fence_after_sync();
       const uint32_t d_t = tmem + static_cast<uint32_t>(a * BN);
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-        const int s = it % S;
-        if (!mbar_wait_bounded(&sf_ready[s], static_cast<uint32_t>((it / S) & 1), FP4Q_WAIT_LIMIT(p)) ||
-            !mbar_wait_bounded(&full[s], static_cast<uint32_t>((it / S) & 1), FP4Q_WAIT_LIMIT(p))) {
+        if (!mbar_wait_bounded(&sf_ready[ss], sph, FP4Q_WAIT_LIMIT(p)) ||
+            !mbar_wait_bounded(&full[s], ph, FP4Q_WAIT_LIMIT(p))) {
           *failed = 1;
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t sfa_t = tmem + P::kSfCol + static_cast<uint32_t>(s) * C::kSfColsPerStage;
+        const uint32_t sfa_t = tmem + P::kSfCol + static_cast<uint32_t>(ss) * C::kSfColsPerStage;
         const uint32_t sfb_t = sfa_t + C::kSfColsA;
         const uint32_t a_s = smem_addr(sA + static_cast<size_t>(s) * kTileBytesA);
         const uint32_t b_s = smem_addr(sB + static_cast<size_t>(s) * C::kTileBytesB);
@@ -703,6 +800,14 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                    sfb_t + 4 * C::kSfTilesB * C::atom(j), (kb | j) != 0 ? 1u : 0u);
         }
         tc_commit(&empty[s]);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+        if (++ss == SS) {
+          ss = 0;
+          sph ^= 1u;
+        }
       }
       // this tile's MMAs are done.  Not after a failure: the epilogue's own
       // wait then runs out and marks the tile, so it never depends on seeing
@@ -713,38 +818,48 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
     // tensor memory is freed below only after every MMA issued here has completed
     tc_commit(mma_done);
     mbar_wait_bounded(mma_done, 0, FP4Q_WAIT_LIMIT(p));
-  } else if (warp == 7 && lane == 0) {
-    // ---- scale mover: stage it's scales into its tensor-memory slot ----
-    const int total = my_tiles * p.num_kb;
-    for (int it = 0; it < total; ++it) {
-      const int s = it % S;
-      if (!mbar_wait_bounded(&sf_full[s], static_cast<uint32_t>((it / S) & 1), FP4Q_WAIT_LIMIT(p))) {
+  } else if ((warp == 7 || warp == P::kMover2Warp) && lane == 0) {
+    // ---- scale movers: block j's scale tiles into tensor-memory slot j % SS.
+    // The slot is free: sf_full of block j means a producer saw the MMAs of
+    // block j - SS (its last reader) complete before issuing these bytes.
+    const int mover = warp == 7 ? 0 : 1;
+    int ss = 0, kb = 0;
+    uint32_t sph = 0;
+    for (int j = 0; j < total; ++j) {
+      if (!mbar_wait_bounded(&sf_full[ss], sph, FP4Q_WAIT_LIMIT(p))) {
         *failed = 1;
         break;
       }
       tc_fence_after_sync();
-      const uint32_t sfa_t = tmem + P::kSfCol + static_cast<uint32_t>(s) * C::kSfColsPerStage;
+      const uint32_t sfa_t = tmem + P::kSfCol + static_cast<uint32_t>(ss) * C::kSfColsPerStage;
       const uint32_t sfb_t = sfa_t + C::kSfColsA;
-      const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(s) * C::kSfBytesA);
-      const uint32_t sfb_s = smem_addr(sSFB + static_cast<size_t>(s) * C::kSfBytesB);
+      const uint32_t sfa_s = smem_addr(sSFA + static_cast<size_t>(ss) * C::kSfBytesA);
+      const uint32_t sfb_s = smem_addr(sSFB + static_cast<size_t>(ss) * C::kSfBytesB);
 #pragma unroll
-      for (int j = 0; j < C::kSfAtoms; ++j) {
+      for (int q = 0; q < C::kSfAtoms; ++q) {
+        if (q % P::kMovers != mover) continue;
         if constexpr (RAG) {
-          if (it % p.num_kb == p.num_kb - 1 && j >= p.sf_tiles_last) break;
+          if (kb == p.num_kb - 1 && q >= p.sf_tiles_last) break;
         }
-        tmem_copy_32x128b_x4(sfa_t + 4 * j,
-                             smem_desc(sfa_s + j * kSfTileBytes, 0, 128, kSwizzleNone));
+        // scale tile q: 32 rows of 16 bytes, 8-row groups 128 bytes apart
+        tmem_copy_32x128b_x4(sfa_t + 4 * q,
+                             smem_desc(sfa_s + q * kSfTileBytes, 0, 128, kSwizzleNone));
 #pragma unroll
-        for (int q = 0; q < C::kSfTilesB; ++q)
-          tmem_copy_32x128b_x4(sfb_t + 4 * (C::kSfTilesB * j + q),
-                               smem_desc(sfb_s + q * C::kSfBytesA + j * kSfTileBytes, 0, 128,
+        for (int u = 0; u < C::kSfTilesB; ++u)
+          tmem_copy_32x128b_x4(sfb_t + 4 * (C::kSfTilesB * q + u),
+                               smem_desc(sfb_s + u * C::kSfBytesA + q * kSfTileBytes, 0, 128,
                                          kSwizzleNone));
       }
-      tc_commit(&sf_ready[s]);
+      tc_commit(&sf_ready[ss]);
+      if (++ss == SS) {
+        ss = 0;
+        sph ^= 1u;
+      }
+      if (++kb == p.num_kb) kb = 0;
     }
     tc_commit(sf_done);
     mbar_wait_bounded(sf_done, 0, FP4Q_WAIT_LIMIT(p));
-  } else if ((warp >= 2 && warp <= 5) || warp >= 8) {
+  } else if ((warp >= 2 && warp <= 5) || (warp >= 8 && warp < P::kMover2Warp)) {
     // ---- epilogue: warps 2..5 (and 8..11) ----
     const int quarter = warp & 3;
     constexpr int kCols = BN / (P::kEpiWarps / 4);    // columns each warp drains
@@ -783,12 +898,13 @@ gemm_nvfp4_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
   }
   __syncthreads();            // every role done; a failure flag is visible to all
   if (*failed != 0 && (warp == 0 || warp == 6) && lane == 0) {
-    // as in the one-tile kernel: the last S stages each producer filled
-    // have landed before the CTA ends
-    for (int j = issued > S ? issued - S : 0; j < issued; ++j) {
+    // as in the one-tile kernel: the last S operand blocks and the last SS
+    // scale blocks each producer issued have landed before the CTA ends
+    // (earlier ones were consumed, so their copies completed)
+    for (int j = issued > S ? issued - S : 0; j < issued; ++j)
       mbar_wait_bounded(&full[j % S], static_cast<uint32_t>((j / S) & 1), FP4Q_WAIT_LIMIT(p));
-      mbar_wait_bounded(&sf_full[j % S], static_cast<uint32_t>((j / S) & 1), FP4Q_WAIT_LIMIT(p));
-    }
+    for (int j = issued_sf > SS ? issued_sf - SS : 0; j < issued_sf; ++j)
+      mbar_wait_bounded(&sf_full[j % SS], static_cast<uint32_t>((j / SS) & 1), FP4Q_WAIT_LIMIT(p));
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -969,13 +1085,13 @@ cudaError_t launch_bn(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
   if (smem_need > 227 * 1024) return cudaErrorInvalidValue;
   static PrepTable table;
   Prep* pr = nullptr;
-  cudaError_t e = prepare(table, kernel, 128, smem_need, p.tmem_cols, p.stages, &pr);
+  cudaError_t e = prepare(table, kernel, kTileThreads, smem_need, p.tmem_cols, p.stages, &pr);
   if (e != cudaSuccess) return e;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((p.N + BN - 1) / BN) * (SPLIT ? p.split : 1),
                      static_cast<unsigned>((p.M + kBM - 1) / kBM), 1);
-  cfg.blockDim = dim3(128, 1, 1);
+  cfg.blockDim = dim3(kTileThreads, 1, 1);
   cfg.dynamicSmemBytes = pr->smem;
   cfg.stream = stream;
   if (SPLIT && !cluster_fits(pr, kernel, cfg, p.split)) return cudaErrorInvalidConfiguration;
@@ -1019,11 +1135,12 @@ cudaError_t launch_persistent(const uint8_t* a, const uint8_t* b, GemmParams p, 
   CUtensorMap ta, tb;
   if (!operand_map(&ta, a, p.M, p.K / 2, kBM) || !operand_map(&tb, b, p.N, p.K / 2, BN))
     return cudaErrorInvalidValue;
-  if (P::kSfCol + C::kSfColsPerStage * static_cast<uint32_t>(p.stages) > 512)
+  p.sf_stages = p.stages + P::sf_lead(p.stages);
+  if (P::kSfCol + C::kSfColsPerStage * static_cast<uint32_t>(p.sf_stages) > 512)
     return cudaErrorInvalidValue;   // accumulators and scale slots must fit tensor memory
-  p.tmem_cols = P::tmem_cols(p.stages);
+  p.tmem_cols = P::tmem_cols(p.sf_stages);
   set_k_blocks(p, MX);
-  const size_t smem_need = P::smem_bytes(p.stages);
+  const size_t smem_need = P::smem_bytes(p.stages, p.sf_stages);
   if (smem_need > 227 * 1024) return cudaErrorInvalidValue;
   static PrepTable table;
   Prep* pr = nullptr;

@@ -364,12 +364,12 @@ def test_gemm_variant_query(L):
     variant comes back as given, rejected sizes give -1."""
     import rmsnorm_fp4_quant_gb300 as fq
     v = fq.fp4_gemm_variant
-    assert v(8192, 7168, 7168)["variant"] == 2                       # many tiles, NVFP4
+    assert v(8192, 7168, 7168)["variant"] == 3                       # many tiles, NVFP4
     assert v(8192, 7168, 7168)["kernel"] == "gemm_nvfp4_persistent_kernel"
-    assert v(8192, 7168, 7168, fmt=1)["variant"] == 2                # MXFP4 as well
+    assert v(8192, 7168, 7168, fmt=1)["variant"] == 3                # MXFP4 as well
     assert v(41, 1536, 6144)["split_k"]                              # few tiles, long K
     assert v(41, 4608, 1536)["variant"] == 0                         # few tiles, 6 K blocks
-    assert v(8192, 7168, 7168, fp4_out=True)["variant"] == 2
+    assert v(8192, 7168, 7168, fp4_out=True)["variant"] == 3
     assert v(41, 1536, 6144, fp4_out=True)["variant"] == 0           # no split for FP4 output
     assert v(256, 256, 512, variant=3)["variant"] == 3
     assert L.fp4_gemm_variant(256, 256, 240, 0, 0, -1) == -1         # K % 32

@@ -59,17 +59,17 @@ def test_committed_profiles_are_well_formed():
         assert 0.5 < traffic / workloads.C3.algorithmic_bytes() < 1.1
 
 
-def test_gemm_profile_keys_name_format_and_kernel():
-    """Each GEMM capture is keyed by shape, operand format and kernel, so a
-    line never reports another schedule's or format's DRAM bytes."""
+def test_gemm_profile_keys_name_format_kernel_and_tile():
+    """Each GEMM capture is keyed by shape, operand format, kernel and tile
+    width, so a line never reports another schedule's or format's DRAM bytes."""
     import glob
     import re
     for p in glob.glob(os.path.join(ROOT, "profiles", "gemm_*kernel__*.md")):
         key = re.search(r"^workload:\s*(\S+)", open(p).read(), re.M).group(1)
         kernel = os.path.basename(p).split("__")[0]
-        assert key.endswith(kernel), p
+        assert re.fullmatch(r".*_" + kernel + r"_n(128|256)", key), p
         assert "_nvfp4_" in key or "_mxfp4_" in key, p
-    assert bench.gemm_profile_key("G4", "nvfp4", "k") == "G4_nvfp4_k"
+    assert bench.gemm_profile_key("G4", "nvfp4", "k", 256) == "G4_nvfp4_k_n256"
 
 
 def test_kernel_source_hash_covers_only_each_kernels_files():

@@ -233,7 +233,7 @@ def test_gemm_full_size_every_row(variant, g4_exact):
 
 
 @pytest.mark.parametrize("K", [2048, 1568])
-@pytest.mark.parametrize("variant", [-1, 0, 2])
+@pytest.mark.parametrize("variant", [-1, 0, 2, 3])
 def test_gemm_consumes_the_fused_producer_with_pdl(K, variant):
     """The fused op writes A and its tiled scales, fp4_quantize writes B, and the
     GEMM is launched as a programmatic dependent of the quantize kernel.  The
@@ -266,7 +266,7 @@ def test_gemm_consumes_the_fused_producer_with_pdl(K, variant):
     check(got, g, K, "random")
 
 
-@pytest.mark.parametrize("variant", [-1, 2])
+@pytest.mark.parametrize("variant", [-1, 2, 3])
 def test_gemm_consumes_the_mxfp4_producer(variant):
     """The headline producer configuration (bf16 rows with outlier columns,
     MXFP4, tiled scales) feeding the MXFP4 GEMM with PDL, against the oracle's
@@ -302,7 +302,7 @@ import parity  # noqa: E402
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 256), (41, 4608, 1536), (300, 520, 768),
                                    (77, 264, 352)])
-@pytest.mark.parametrize("variant", [0, 1, 4])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
 def test_gemm_gelu_bf16(M, N, K, variant):
     """GELU(alpha * product + bias) in bf16.  Exact-kind operands make the
     GELU argument exact; the GPU's erff-based GELU and one bf16 rounding keep

@@ -106,8 +106,8 @@ struct Cfg {
   }
   static constexpr size_t smem_bytes(int stages) {
     // 1 KiB of alignment slack (the 128-byte swizzle wants 1 KiB-aligned
-    // tiles), the ring, 4S + 2 mbarriers, the tensor-memory address, a flag
-    return 1024 + static_cast<size_t>(stages) * kStageBytes + (4 * stages + 2) * 8 + 8;
+    // tiles), the ring, 4S + 3 mbarriers, the tensor-memory address, a flag
+    return 1024 + static_cast<size_t>(stages) * kStageBytes + (4 * stages + 3) * 8 + 8;
   }
 };
 
@@ -286,7 +286,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
   uint64_t* sf_ready = accum + 1;     // the stage's scales are in tensor memory
   uint64_t* sf_done = sf_ready + S;   // every scale copy has completed
   uint64_t* sf_full = sf_done + 1;    // the stage's scale bytes have landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_full + S);
+  uint64_t* recv_bar = sf_full + S;   // split K: the peers' partial rows have landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_bar + 1);
   volatile int* failed = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -307,6 +308,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     }
     mbar_init(sf_done, 2);
     mbar_init(accum, 1);
+    mbar_init(recv_bar, 1);
     *failed = 0;
     mbar_init_fence();
     tma_prefetch_map(&tmap_a);
@@ -346,7 +348,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
         if (kb == p.num_kb - 1)     // fewer scale tiles in the ragged last block
           sf_bytes = static_cast<uint32_t>(p.sf_tiles_last) * kSfTileBytes;
       }
-      // the scales land on their own barrier, so the scale mover copies them
+      // the scales land on their own barrier, so the scale movers copy them
       // into tensor memory while the operand tiles are still arriving
       mbar_arrive_expect_tx(&sf_full[s], load_a ? sf_bytes
                                                 : static_cast<uint32_t>(b_tiles) * sf_bytes);
@@ -475,55 +477,128 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
   // warps 0..3 drain the accumulator, warp w its lanes 32w..32w+31
   const int row = m_tile * kBM + warp * 32 + lane;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  // The tile in fp32 in the drained ring, rows 16 bytes apart beyond BN
+  // floats (a warp's row-per-lane float4 stores then take the minimum four
+  // shared-memory wavefronts), so that it leaves in row order: a thread per
+  // row storing its own 16-byte pieces scattered a warp's stores over 32 rows
+  // and held each warp about 1100 cycles per 32 columns.
+  constexpr int kStride = BN + 4;
+  constexpr int kChunks = BN / 8;     // 8-column pieces of a row
+  float* part = reinterpret_cast<float*>(smem);
+  const int local_row = warp * 32 + lane;
+  const int rows_valid = p.M - m_tile * kBM < kBM ? p.M - m_tile * kBM : kBM;
   if constexpr (!SPLIT) {
+    if (p.epilogue == kEpiGeluFp4) {
+      // NVFP4 output: a thread quantizes its own row's 16-element blocks
 #pragma unroll 1
-    for (int c = 0; c < BN && warp < 4; c += 32) {
-      uint32_t r[32];
-      tmem_load_32cols(lane_base + static_cast<uint32_t>(c), r);   // whole warp, unconditionally
-      if (row >= p.rows_out) continue;
-      store_columns32(p, r, row, n_tile * BN + c, bad);
+      for (int c = 0; c < BN && warp < 4; c += 32) {
+        uint32_t r[32];
+        tmem_load_32cols(lane_base + static_cast<uint32_t>(c), r);   // whole warp, unconditionally
+        if (row >= p.rows_out) continue;
+        store_columns32(p, r, row, n_tile * BN + c, bad);
+      }
+    } else {
+#pragma unroll 1
+      for (int c = 0; c < BN && warp < 4; c += 32) {
+        uint32_t r[32];
+        tmem_load_32cols(lane_base + static_cast<uint32_t>(c), r);   // whole warp, unconditionally
+        if (local_row >= rows_valid) continue;
+        float4* dst = reinterpret_cast<float4*>(part + local_row * kStride + c);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                               __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+      }
+      __syncthreads();
+      // consecutive threads take consecutive 8-column pieces of a row
+      for (int it = static_cast<int>(threadIdx.x); it < rows_valid * kChunks; it += kTileThreads) {
+        const int rl = it / kChunks;
+        const int ch = it - rl * kChunks;
+        const float4 lo = *reinterpret_cast<const float4*>(part + rl * kStride + ch * 8);
+        const float4 hi = *reinterpret_cast<const float4*>(part + rl * kStride + ch * 8 + 4);
+        const float acc[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        store8(p, acc, m_tile * kBM + rl, n_tile * BN + ch * 8, bad);
+      }
     }
   } else {
-    // partial tile -> own shared memory, rows 16 bytes apart beyond BN floats
-    constexpr int kStride = BN + 4;
-    float* part = reinterpret_cast<float*>(smem);
-    const int local_row = warp * 32 + lane;
+    // Partial tile -> own shared memory (NaN if this CTA's inputs never
+    // arrived, so every sum it enters is NaN).  Rank q owns rows
+    // [q * rows_valid / split, (q + 1) * rows_valid / split) of the tile: after
+    // a cluster barrier every rank bulk-copies (TMA engine, shared to shared)
+    // the rows each other rank owns into that rank's receive slot for it, and
+    // each owner sums its rows over the ranks in rank order - the same sum on
+    // every run.  Reading the peers' partials with per-thread remote loads
+    // instead took about 230 cycles per load, one after another.
+    const float nan = __int_as_float(0x7fc00000);
 #pragma unroll 1
     for (int c = 0; c < BN && warp < 4; c += 32) {
       uint32_t r[32];
       tmem_load_32cols(lane_base + static_cast<uint32_t>(c), r);
-      if (row >= p.M) continue;
+      if (local_row >= rows_valid) continue;
       float4* dst = reinterpret_cast<float4*>(part + local_row * kStride + c);
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                             __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+        dst[q] = bad ? make_float4(nan, nan, nan, nan)
+                     : make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                   __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
     }
     if (bad && threadIdx.x == 0) *failed = 1;
-    cluster_arrive_release();
+    constexpr uint32_t kRowBytes = kStride * sizeof(float);
+    const int slot_rows = (rows_valid + split - 1) / split;
+    float* recv = part + kBM * kStride;       // slot q: the rows from rank q
+    const int my0 = rank * rows_valid / split;
+    const int my1 = (rank + 1) * rows_valid / split;
+    if (threadIdx.x == 0)
+      mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((split - 1) * (my1 - my0)) * kRowBytes);
+    fence_proxy_async_smem();   // the partial, written above, is read by the copies below
+    cluster_arrive_release();   // every rank's partial and receive barrier are ready
     cluster_wait_acquire();
-    bool any_bad = false;
-    for (int q = 0; q < split; ++q)
-      any_bad |= ld_peer_u32(peer_smem_addr(smem_addr(const_cast<int*>(failed)), q)) != 0;
-    const int rows_valid = p.M - m_tile * kBM < kBM ? p.M - m_tile * kBM : kBM;
-    constexpr int kChunks = BN / 8;
-    const int items = rows_valid * kChunks;
-    for (int it = rank + split * static_cast<int>(threadIdx.x); it < items;
-         it += split * kTileThreads) {
-      const int rl = it / kChunks;
-      const int ch = it - rl * kChunks;
-      const uint32_t local = smem_addr(part + rl * kStride + ch * 8);
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int q = 0; q < split; ++q) {   // rank order: the same sum on every run
-        const uint32_t a = peer_smem_addr(local, q);
-        const float4 lo = ld_peer_f32x4(a);
-        const float4 hi = ld_peer_f32x4(a + 16);
-        acc[0] += lo.x; acc[1] += lo.y; acc[2] += lo.z; acc[3] += lo.w;
-        acc[4] += hi.x; acc[5] += hi.y; acc[6] += hi.z; acc[7] += hi.w;
+    // lane 0 of each warp issues the copies to every fifth peer (issuing one
+    // holds its thread about 200 cycles)
+    if (lane == 0) {
+      for (int q = warp; q < split; q += kTileThreads / 32) {
+        const int r0 = q * rows_valid / split;
+        const int r1 = (q + 1) * rows_valid / split;
+        if (q == rank || r1 <= r0) continue;
+        bulk_s2cluster(peer_smem_addr(smem_addr(recv + rank * slot_rows * kStride),
+                                      static_cast<uint32_t>(q)),
+                       smem_addr(part + r0 * kStride), static_cast<uint32_t>(r1 - r0) * kRowBytes,
+                       peer_smem_addr(smem_addr(recv_bar), static_cast<uint32_t>(q)));
       }
-      store8(p, acc, m_tile * kBM + rl, n_tile * BN + ch * 8, any_bad);
     }
-    cluster_arrive_release();   // every peer has read this CTA's partial
+    const bool got = mbar_wait_bounded(recv_bar, 0, FP4Q_WAIT_LIMIT(p));
+    if (!got && threadIdx.x == 0) *failed = 1;
+    // This CTA's incoming copies have landed.  Once every rank has arrived
+    // here, every copy out of this CTA's partial has landed too: the wait for
+    // that, before the CTA may end, comes after the sums below.  Nothing is
+    // read on the strength of this arrival (the copies' completion is already
+    // a fact), so it needs no release.
+    cluster_arrive_relaxed();
+    const int items = (my1 - my0) * kChunks;
+    for (int it = static_cast<int>(threadIdx.x); it < items; it += kTileThreads) {
+      const int rl = it / kChunks;          // row within the owned rows
+      const int ch = it - rl * kChunks;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // rank order; four ranks' loads issued before their adds
+      for (int q0 = 0; q0 < split; q0 += 4) {
+        float4 lo[4], hi[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int q = q0 + u < split ? q0 + u : split - 1;
+          const float* src = q == rank ? part + (my0 + rl) * kStride + ch * 8
+                                       : recv + (q * slot_rows + rl) * kStride + ch * 8;
+          lo[u] = *reinterpret_cast<const float4*>(src);
+          hi[u] = *reinterpret_cast<const float4*>(src + 4);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (q0 + u >= split) break;
+          acc[0] += lo[u].x; acc[1] += lo[u].y; acc[2] += lo[u].z; acc[3] += lo[u].w;
+          acc[4] += hi[u].x; acc[5] += hi[u].y; acc[6] += hi[u].z; acc[7] += hi[u].w;
+        }
+      }
+      store8(p, acc, m_tile * kBM + my0 + rl, n_tile * BN + ch * 8, !got);
+    }
     cluster_wait_acquire();
   }
 
@@ -1078,6 +1153,19 @@ cudaError_t launch_bn(const uint8_t* a, const uint8_t* b, GemmParams p, int pdl,
   auto kernel = gemm_nvfp4_kernel<BN, SPLIT, MX, RAG>;
   CUtensorMap ta, tb;
   if (!operand_map(&ta, a, p.M, p.K / 2, kBM) || !operand_map(&tb, b, p.N, p.K / 2, BN))
+    return cudaErrorInvalidValue;
+  // The epilogue stages the fp32 tile (128 rows of BN + 4 floats) in the
+  // drained operand ring; split K also receives there the rows each peer
+  // sends (a slot of ceil(rows / split) rows per rank).  A deeper ring makes
+  // the room where the default one is too small.
+  const int64_t tile_rows = p.M < kBM ? p.M : kBM;
+  const size_t stage_floats =
+      static_cast<size_t>(kBM) * (BN + 4) +
+      (SPLIT ? static_cast<size_t>(p.split) * ((tile_rows + p.split - 1) / p.split) * (BN + 4) : 0);
+  while (static_cast<size_t>(p.stages) * (kTileBytesA + C::kTileBytesB) <
+             stage_floats * sizeof(float) && p.stages < 6)
+    ++p.stages;
+  if (static_cast<size_t>(p.stages) * (kTileBytesA + C::kTileBytesB) < stage_floats * sizeof(float))
     return cudaErrorInvalidValue;
   p.tmem_cols = C::tmem_cols(p.stages);
   set_k_blocks(p, MX);

@@ -107,6 +107,22 @@ __device__ __forceinline__ void tmem_load_32cols(uint32_t taddr, uint32_t (&r)[3
       : "memory");
 }
 
+// --- shared memory across the cluster -----------------------------------------
+// Makes this thread's generic-proxy writes to its CTA's shared memory visible
+// to the async proxy (bulk copies issued after a later barrier read them).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Shared -> shared bulk copy (TMA engine) into a CTA of the cluster: dst and
+// bar are shared::cluster addresses (mapa), src is this CTA's; both 16-byte
+// aligned, bytes a multiple of 16; completion counted on bar, in dst's CTA.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst, uint32_t src, uint32_t bytes,
+                                               uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(dst), "r"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
 // --- TMA ----------------------------------------------------------------------
 // Tiled 2-D load of the box at (x, y) of `map` (x in elements of the innermost
 // dimension, a multiple of 16 bytes) into shared memory, counted on `bar`.

@@ -121,6 +121,24 @@ def test_gemm_exact_operands_bit_exact(M, N, K, alpha, variant):
     check(got, oracle_gemm(a, b, sfa, sfb, M, N, K, alpha=alpha), K, "exact")
 
 
+# Split K (variant 4) reduces through the ranks' shared memory: each rank owns
+# rows [q * rows / split, (q + 1) * rows / split) of the tile and receives
+# those rows of every other rank's partial.  Shapes where most ranks own no row
+# (1 or 5 rows over 16 ranks), a full 128-row tile over 16 ranks (the receive
+# slots then need a deeper ring than the default), and a ragged K.
+SPLIT_SHAPES = [(1, 8, 4096), (5, 264, 4096), (128, 128, 8192), (41, 1536, 6144),
+                (130, 264, 4000)]
+
+
+@pytest.mark.parametrize("M,N,K", SPLIT_SHAPES)
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+def test_gemm_split_k_reduction_bit_exact(M, N, K, fmt):
+    a, b, sfa, sfb = operands(M, N, K, seed=M + 7 * N + K, kind="exact", fmt=fmt)
+    assert fq.fp4_gemm_variant(M, N, K, fmt=0 if fmt == "nvfp4" else 1, variant=4)["split_k"]
+    got = gpu_gemm(a, b, sfa, sfb, alpha=0.5, variant=4, fmt=fmt)
+    check(got, oracle_gemm(a, b, sfa, sfb, M, N, K, alpha=0.5, fmt=fmt), K, "exact")
+
+
 # K not a multiple of 256: a ragged last K block of 1-4 K = 64 steps, the last
 # of them possibly half past K (codes there read as zero, scales are the
 # k-padding of the tiled layout)

@@ -34,9 +34,11 @@
 //                      one E4M3 scale per 16 elements, and commits the stage
 //                      back (empty[s]).
 //   warps 0..3         epilogue.  Warp w owns accumulator lanes 32w..32w+31 (one
-//                      output row per thread): 32 columns at a time from tensor
-//                      memory, alpha, bias and residual in fp32, one rounding to
-//                      bf16, 16-byte stores.
+//                      output row per thread), read 32 columns at a time from
+//                      tensor memory into the drained ring as fp32; then all
+//                      five warps write the tile out row by row (consecutive
+//                      threads on consecutive 16-byte pieces) with alpha, bias
+//                      and residual in fp32 and one rounding to bf16.
 //
 // Two CTAs fit an SM (S = 3 stages: 108 KiB of shared memory and 256 tensor-
 // memory columns each), so one CTA's epilogue overlaps the other's main loop.

@@ -1014,8 +1014,9 @@ CHAIN_METRIC = "fused add+RMSNorm+NVFP4 quant -> NVFP4 GEMM chain, us per step"
 def run_chain(args):
     """One step = fp4_add_rmsnorm_quant_ex on M x K rows (bf16, NVFP4, tiled
     scales) followed by fp4_gemm_nvfp4_bf16 of its codes against an N x K
-    NVFP4 weight, both launched with and without programmatic dependent
-    launch; enough copies of the inputs, weights and outputs rotate that one
+    NVFP4 weight, launched without programmatic dependent launch, with it
+    (pdl = 1), and with it and the weights declared static (the GEMM's pdl =
+    2: its B copies start before the dependency wait); enough copies of the inputs, weights and outputs rotate that one
     pass moves more than twice the L2, and a pass of steps is replayed as a
     CUDA graph (as a decode loop would run it)."""
     import torch
@@ -1044,7 +1045,9 @@ def run_chain(args):
     sh = stream.cuda_stream
     torch.cuda.synchronize(dev)           # inputs and copies were made on the default stream
 
-    def step(c, xs, pdl):
+    def step(c, xs, mode):
+        pdl = 1 if mode else 0          # the fused call: PDL on or off
+        gemm_pdl = mode                 # the GEMM: 0, 1, or 2 (static weights)
         st = L.fp4_add_rmsnorm_quant_ex(xs.data_ptr(), K, c["r"].data_ptr(), K, w.data_ptr(),
                                         None, 1e-6, M, K, fq.FP4_DT_BF16, fq.FP4_NVFP4,
                                         fq.FP4_SF_SWIZZLED, c["p"].data_ptr(), c["s"].data_ptr(),
@@ -1053,17 +1056,17 @@ def run_chain(args):
             raise fq.Fp4Error(st, "chain: fused")
         st = L.fp4_gemm_nvfp4_bf16(c["p"].data_ptr(), c["b"].data_ptr(), c["s"].data_ptr(),
                                    c["sfb"].data_ptr(), 1.0, None, None, M, N, K,
-                                   c["o"].data_ptr(), -1, pdl, sh)
+                                   c["o"].data_ptr(), -1, gemm_pdl, sh)
         if st != 0:
             raise fq.Fp4Error(st, "chain: gemm")
 
     results = {}
-    for pdl in (0, 1):
+    for mode in (0, 1, 2):
         def one_pass():
             for c in sets:
-                step(c, c["x"], pdl)
+                step(c, c["x"], mode)
             for c in sets:
-                step(c, c["xn"], pdl)
+                step(c, c["xn"], mode)
         with torch.cuda.stream(stream):
             one_pass()
         stream.synchronize()
@@ -1083,8 +1086,8 @@ def run_chain(args):
                 graph.replay()
             e.record(stream)
         stream.synchronize()
-        results[pdl] = a.elapsed_time(e) * 1e3 / (reps * 2 * rot)
-    line = {"metric": CHAIN_METRIC, "value": round(results[1], 3), "unit": "us",
+        results[mode] = a.elapsed_time(e) * 1e3 / (reps * 2 * rot)
+    line = {"metric": CHAIN_METRIC, "value": round(results[2], 3), "unit": "us",
             "n_gpus": 1, "steps": reps * 2 * rot, "warmup": args.warmup,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16 in, e2m1 x e2m1 -> f32, bf16 out", "data": "synthetic",
@@ -1096,6 +1099,7 @@ def run_chain(args):
                        "gemm": fq.fp4_gemm_variant(M, N, K)},
             "us_per_step_without_pdl": round(results[0], 3),
             "us_per_step_with_pdl": round(results[1], 3),
+            "us_per_step_with_pdl_static_weights": round(results[2], 3),
             "gpu_launches": 2 * reps * 2 * rot}
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -271,9 +271,14 @@ FP4Q_API int fp4_gemm_variant(int64_t M, int64_t N, int64_t K, fp4_format_t form
  *             automatic when the output has at most half as many 128 x 128
  *             tiles as SMs and K > 1536, e.g. the M = 41 decode product with
  *             K = 6144).
- *   pdl       nonzero: launched as a programmatic dependent of the previous
- *             kernel on `stream`, so its prologue overlaps that kernel's tail
- *             (it waits for that kernel's results before reading anything).
+ *   pdl       1: launched as a programmatic dependent of the previous kernel
+ *             on `stream`, so its prologue overlaps that kernel's tail (it
+ *             waits for that kernel's results before reading anything).
+ *             2: the same, and the caller states that the previous kernel
+ *             writes neither b_packed nor sfb (weights, as in a decode step
+ *             after the fused op): the one-CTA-per-tile and split-K schedules
+ *             then start B's first ring of copies before the wait.  0: none.
+ *             Other values: FP4_ERR_INVALID_ARG.
  * K must be a multiple of 32 (a packed row a whole number of 16-byte units;
  * the FlashRT contract's K % 16 otherwise) and N of 8; every pointer 16-byte
  * aligned; out must not overlap the inputs (except residual == out).  When K

@@ -449,8 +449,13 @@ def dequant(packed, sf, M: int, H: int, fmt: str = "nvfp4", sf_layout: str = "ro
     return out
 
 
+def _pdl_mode(pdl) -> int:
+    """False / True -> 0 / 1; an int is passed on as given (2: static weights)."""
+    return int(pdl) if not isinstance(pdl, bool) else (1 if pdl else 0)
+
+
 def gemm_nvfp4_bf16(a_packed, b_packed, sfa, sfb, alpha: float = 1.0, bias=None, residual=None,
-                    out=None, variant: int = -1, pdl: bool = False, stream=None, fmt="nvfp4",
+                    out=None, variant: int = -1, pdl=False, stream=None, fmt="nvfp4",
                     status=None):
     """bf16 (M, N) = alpha * deq(A) @ deq(B)^T (+ bias) (+ residual) from packed
     NVFP4 operands (M, K/2) and (N, K/2) and their tiled scale buffers.
@@ -458,9 +463,11 @@ def gemm_nvfp4_bf16(a_packed, b_packed, sfa, sfb, alpha: float = 1.0, bias=None,
     variant: -1 automatic (see fp4_gemm_variant), 0 / 1 = one CTA per 128x128 /
     128x256 output tile, 2 / 3 = persistent CTAs over 128x128 / 128x256 tiles
     (automatic for many tiles), 4 = 128x128 tiles with the K loop split over a
-    cluster (automatic for few output tiles and long K).  status: optional CUDA
-    int32 tensor of one element that receives FP4_ERR_TIMEOUT if a kernel gave
-    up on a bounded wait (fp4_gemm_ex)."""
+    cluster (automatic for few output tiles and long K).  pdl: False / True (0 /
+    1), or 2 when the kernel before this one writes neither b_packed nor sfb
+    (B's first copies then start before the dependency wait).  status: optional
+    CUDA int32 tensor of one element that receives FP4_ERR_TIMEOUT if a kernel
+    gave up on a bounded wait (fp4_gemm_ex)."""
     torch = _torch()
     for name, t in (("a_packed", a_packed), ("b_packed", b_packed), ("sfa", sfa), ("sfb", sfb)):
         _check_cuda(t, name)
@@ -485,13 +492,13 @@ def gemm_nvfp4_bf16(a_packed, b_packed, sfa, sfb, alpha: float = 1.0, bias=None,
         st = call(a_packed.data_ptr(), b_packed.data_ptr(), sfa.data_ptr(), sfb.data_ptr(),
                   float(alpha), bias.data_ptr() if bias is not None else 0,
                   residual.data_ptr() if residual is not None else 0, M, N, K, out.data_ptr(),
-                  int(variant), 1 if pdl else 0, _stream_handle(stream))
+                  int(variant), _pdl_mode(pdl), _stream_handle(stream))
     else:
         st = fp4_gemm_ex(a_packed.data_ptr(), b_packed.data_ptr(), sfa.data_ptr(),
                          sfb.data_ptr(), _FORMATS[fmt], FP4_EPI_BF16, float(alpha),
                          bias.data_ptr() if bias is not None else 0,
                          residual.data_ptr() if residual is not None else 0, M, N, K,
-                         out.data_ptr(), 0, 0, int(variant), 1 if pdl else 0,
+                         out.data_ptr(), 0, 0, int(variant), _pdl_mode(pdl),
                          _status_ptr(status), _stream_handle(stream))
     if st != 0:
         raise Fp4Error(st, f"fp4_gemm_{fmt}_bf16")
@@ -517,7 +524,7 @@ def gemm_nvfp4_gelu(a_packed, b_packed, sfa, sfb, alpha: float = 1.0, bias=None,
         out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         st = fp4_gemm_nvfp4_gelu_bf16(a_packed.data_ptr(), b_packed.data_ptr(), sfa.data_ptr(),
                                       sfb.data_ptr(), float(alpha), bp, M, N, K, out.data_ptr(),
-                                      int(variant), 1 if pdl else 0, _stream_handle(stream))
+                                      int(variant), _pdl_mode(pdl), _stream_handle(stream))
         if st != 0:
             raise Fp4Error(st, "fp4_gemm_nvfp4_gelu_bf16")
         return out
@@ -528,7 +535,7 @@ def gemm_nvfp4_gelu(a_packed, b_packed, sfa, sfb, alpha: float = 1.0, bias=None,
                      device=dev)
     st = fp4_gemm_nvfp4_gelu_nvfp4(a_packed.data_ptr(), b_packed.data_ptr(), sfa.data_ptr(),
                                    sfb.data_ptr(), float(alpha), bp, M, N, K, packed.data_ptr(),
-                                   sf.data_ptr(), int(variant), 1 if pdl else 0,
+                                   sf.data_ptr(), int(variant), _pdl_mode(pdl),
                                    _stream_handle(stream))
     if st != 0:
         raise Fp4Error(st, "fp4_gemm_nvfp4_gelu_nvfp4")

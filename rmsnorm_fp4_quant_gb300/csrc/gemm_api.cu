@@ -56,6 +56,7 @@ fp4_status_t gemm_call(bool mx, int epilogue, const uint8_t* a_packed, const uin
   const bool fp4_out = epilogue == kEpiGeluFp4;
   if (M < 0 || N < 0 || K <= 0) return FP4_ERR_INVALID_ARG;
   if (variant < -1 || variant > 4) return FP4_ERR_INVALID_ARG;
+  if (pdl < 0 || pdl > 2) return FP4_ERR_INVALID_ARG;
   if (fp4_out && variant == 4) return FP4_ERR_INVALID_ARG;   // split K stores 8-column groups
   if (K % 32 != 0 || N % (fp4_out ? 16 : 8) != 0) return FP4_ERR_UNSUPPORTED_SHAPE;
   if (M > INT32_MAX - 128 || N > INT32_MAX - 128 || K > INT32_MAX / 2)
@@ -132,6 +133,7 @@ fp4_status_t gemm_call(bool mx, int epilogue, const uint8_t* a_packed, const uin
   p.stages = !persistent ? FP4Q_GEMM_STAGES : bn == 128 ? FP4Q_GEMM_PSTAGES_128
                                                         : FP4Q_GEMM_PSTAGES_256;
   p.split = 1;
+  p.b_static = pdl == 2 ? 1 : 0;
   if (v == 4) {
     int64_t sk = tiles128 > 0 ? sms / tiles128 : 1;
     if (sk > 16) sk = 16;

@@ -35,6 +35,7 @@ struct GemmParams {
   int stages;                  // shared-memory ring depth, 2..6
   int sf_stages;               // scale ring depth of the persistent kernel: stages or stages + 1
   int split;                   // CTAs of a cluster sharing one tile's K loop (1 = none)
+  int b_static;                // 1: the kernel before this one (PDL) writes neither B nor its scales
   uint32_t tmem_cols;          // tensor-memory columns taken per CTA
   FP4Q_DEBUG_FIELD             // debug build only: checks and fault injection
 };

@@ -316,6 +316,41 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     tma_prefetch_map(&tmap_a);
     tma_prefetch_map(&tmap_b);
   }
+  // B's 128-row scale tiles of this column tile that exist (the last column
+  // tile may cover fewer rows than BN)
+  const int b_tile0 = n_tile * C::kSfTilesB;
+  const int b_tiles_total = (p.N + 127) / 128;
+  const int b_tiles = b_tiles_total - b_tile0 < C::kSfTilesB ? b_tiles_total - b_tile0
+                                                              : C::kSfTilesB;
+  // block i's B tile and its scales into ring slot s (the B producer)
+  auto issue_b = [&](int i, int s) {
+    const int kb = kb0 + i;
+    uint32_t sf_bytes = C::kSfBytesA;
+    if constexpr (RAG) {
+      if (kb == p.num_kb - 1)     // fewer scale tiles in the ragged last block
+        sf_bytes = static_cast<uint32_t>(p.sf_tiles_last) * kSfTileBytes;
+    }
+    mbar_arrive_expect_tx(&sf_full[s], static_cast<uint32_t>(b_tiles) * sf_bytes);
+    mbar_arrive_expect_tx(&full[s], C::kTileBytesB);
+    for (int t = 0; t < b_tiles; ++t) {
+      const uint8_t* src = p.sfb + (static_cast<size_t>(b_tile0 + t) * p.nkt) * kSfTileBytes +
+                           static_cast<size_t>(kb) * C::kSfBytesA;
+      if (FP4Q_IN_RANGE(p, src, sf_bytes, p.sfb, tiled_extent(p.N, p.nkt)))
+        bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + t * C::kSfBytesA, src,
+                 sf_bytes, &sf_full[s]);
+    }
+    tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
+                n_tile * BN, &full[s]);
+  };
+  // When the caller states that the kernel before this one writes neither B
+  // nor its scales (pdl = 2: weights), B's first ring of copies leaves before
+  // the dependency wait and streams in during that kernel's tail.
+  const int b_early = p.b_static ? (kb1 - kb0 < S ? kb1 - kb0 : S) : 0;
+  if (b_early > 0) {
+    __syncthreads();            // the barriers above are initialised
+    if (warp == 2 && lane == 0)
+      for (int i = 0; i < b_early; ++i) issue_b(i, i);
+  }
   // A and its scales may come from the kernel before this one (PDL); tensor
   // memory is taken only after it, since that kernel may still hold some
   griddep_wait();
@@ -330,12 +365,6 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
     // ---- producers: warp 0 A and its scales, warp 2 B and its scales ----
     const bool load_a = warp == 0;
     const uint8_t* sfa_k = p.sfa + static_cast<size_t>(m_tile) * p.nkt * kSfTileBytes;
-    // B's 128-row scale tiles of this column tile that exist (the last column
-    // tile may cover fewer rows than BN)
-    const int b_tile0 = n_tile * C::kSfTilesB;
-    const int b_tiles_total = (p.N + 127) / 128;
-    const int b_tiles = b_tiles_total - b_tile0 < C::kSfTilesB ? b_tiles_total - b_tile0
-                                                                : C::kSfTilesB;
     int i = 0;    // K blocks issued
     int s = 0;    // ring slot of block i; ph = (i / S) & 1, by counters (no division per block)
     uint32_t ph = 0;
@@ -345,6 +374,14 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
         *failed = 1;
         break;
       }
+      if (!load_a) {
+        if (i >= b_early) issue_b(i, s);   // the first b_early blocks left before the wait
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+        continue;
+      }
       uint32_t sf_bytes = C::kSfBytesA;
       if constexpr (RAG) {
         if (kb == p.num_kb - 1)     // fewer scale tiles in the ragged last block
@@ -352,28 +389,15 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
       }
       // the scales land on their own barrier, so the scale movers copy them
       // into tensor memory while the operand tiles are still arriving
-      mbar_arrive_expect_tx(&sf_full[s], load_a ? sf_bytes
-                                                : static_cast<uint32_t>(b_tiles) * sf_bytes);
-      mbar_arrive_expect_tx(&full[s], load_a ? kTileBytesA : C::kTileBytesB);
-      if (load_a) {
-        const uint8_t* src = sfa_k + static_cast<size_t>(kb) * C::kSfBytesA;
-        if (FP4Q_IN_RANGE(p, src, sf_bytes, p.sfa, tiled_extent(p.M, p.nkt)))
-          bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA, src, sf_bytes, &sf_full[s]);
-        // debug build: one CTA never issues one A tile (fault injection)
-        if (!FP4Q_DROP(p, 2, static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x), i))
-          tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes,
-                      m_tile * kBM, &full[s]);
-      } else {
-        for (int t = 0; t < b_tiles; ++t) {
-          const uint8_t* src = p.sfb + (static_cast<size_t>(b_tile0 + t) * p.nkt) * kSfTileBytes +
-                               static_cast<size_t>(kb) * C::kSfBytesA;
-          if (FP4Q_IN_RANGE(p, src, sf_bytes, p.sfb, tiled_extent(p.N, p.nkt)))
-            bulk_g2s(sSFB + static_cast<size_t>(s) * C::kSfBytesB + t * C::kSfBytesA, src,
-                     sf_bytes, &sf_full[s]);
-        }
-        tma_load_2d(sB + static_cast<size_t>(s) * C::kTileBytesB, &tmap_b, kb * kBKBytes,
-                    n_tile * BN, &full[s]);
-      }
+      mbar_arrive_expect_tx(&sf_full[s], sf_bytes);
+      mbar_arrive_expect_tx(&full[s], kTileBytesA);
+      const uint8_t* src = sfa_k + static_cast<size_t>(kb) * C::kSfBytesA;
+      if (FP4Q_IN_RANGE(p, src, sf_bytes, p.sfa, tiled_extent(p.M, p.nkt)))
+        bulk_g2s(sSFA + static_cast<size_t>(s) * C::kSfBytesA, src, sf_bytes, &sf_full[s]);
+      // debug build: one CTA never issues one A tile (fault injection)
+      if (!FP4Q_DROP(p, 2, static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x), i))
+        tma_load_2d(sA + static_cast<size_t>(s) * kTileBytesA, &tmap_a, kb * kBKBytes,
+                    m_tile * kBM, &full[s]);
       if (++s == S) {
         s = 0;
         ph ^= 1u;

@@ -243,6 +243,7 @@ G_OUT = A + (6 << 32)
     (dict(M=0, a=0, b=0, out=0), 0),   # empty: nothing launched
     (dict(N=0), 0),
     (dict(variant=5), 1), (dict(variant=-2), 1),
+    (dict(pdl=3), 1), (dict(pdl=-1), 1),          # 0, 1 or 2 (static weights)
 ])
 def test_gemm_validation(L, kwargs, status):
     a = dict(a=A, b=B, sfa=S, sfb=S2, alpha=1.0, bias=0, residual=0, M=256, N=256, K=512,
@@ -264,7 +265,7 @@ def test_gemm_validation(L, kwargs, status):
     (dict(st=G_OUT + 256), 1),                   # status word inside the output
     (dict(st=A + 4), 1),                         # ... inside A
     (dict(epi=2, out=0, p=P, s=G_OUT, st=P + 16), 1),   # ... inside the packed output
-    (dict(K=48), 2), (dict(variant=7), 1),
+    (dict(K=48), 2), (dict(variant=7), 1), (dict(pdl=3), 1),
     (dict(M=0, a=0, b=0, out=0), 0),
 ])
 def test_gemm_ex_validation(L, kwargs, status):

@@ -139,6 +139,20 @@ def test_gemm_split_k_reduction_bit_exact(M, N, K, fmt):
     check(got, oracle_gemm(a, b, sfa, sfb, M, N, K, alpha=0.5, fmt=fmt), K, "exact")
 
 
+@pytest.mark.parametrize("M,N,K,variant", [(41, 1536, 6144, 4), (130, 264, 4000, 4),
+                                           (41, 4608, 1536, 0), (256, 768, 2048, 3)])
+def test_gemm_repeats_bit_identical(M, N, K, variant):
+    """The split-K reduction sums the ranks in a fixed order and the epilogues
+    write each output once, so repeated launches give identical bytes."""
+    a, b, sfa, sfb = operands(M, N, K, seed=M * 3 + N + K, kind="random")
+    dev = [t.cuda() for t in (a, b, sfa, sfb)]
+    first = fq.gemm_nvfp4_bf16(*dev, alpha=0.5, variant=variant)
+    outs = [fq.gemm_nvfp4_bf16(*dev, alpha=0.5, variant=variant) for _ in range(10)]
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o.view(torch.int16), first.view(torch.int16))
+
+
 # K not a multiple of 256: a ragged last K block of 1-4 K = 64 steps, the last
 # of them possibly half past K (codes there read as zero, scales are the
 # k-padding of the tiled layout)

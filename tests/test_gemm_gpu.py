@@ -298,22 +298,26 @@ def test_gemm_consumes_the_fused_producer_with_pdl(K, variant):
     check(got, g, K, "random")
 
 
-@pytest.mark.parametrize("M,N,K,variant", [(41, 4608, 1536, -1), (41, 1536, 6144, -1),
-                                           (300, 512, 1568, 0), (300, 512, 1568, 4),
-                                           (256, 768, 2048, 3)])
-def test_gemm_static_weights_pdl2(M, N, K, variant):
+@pytest.mark.parametrize("M,N,K,variant,fmt", [(41, 4608, 1536, -1, "nvfp4"),
+                                               (41, 1536, 6144, -1, "nvfp4"),
+                                               (300, 512, 1568, 0, "nvfp4"),
+                                               (300, 512, 1568, 4, "nvfp4"),
+                                               (256, 768, 2048, 3, "nvfp4"),
+                                               (41, 4608, 1536, -1, "mxfp4"),
+                                               (300, 512, 1600, 4, "mxfp4")])
+def test_gemm_static_weights_pdl2(M, N, K, variant, fmt):
     """A decode step's chain with static weights: B is quantized once and
     synchronised; then, three times, the fused op updates the residual and
     writes A, and the GEMM is launched with pdl = 2 (its B copies start before
     the dependency wait).  Every step's product matches the oracle GEMM of the
     operands that step's producer wrote."""
     steps = 3
-    wl = workloads.Workload("static_b", M, K, "bf16", "nvfp4", "swizzled", 1e-6, seed=M + K)
+    wl = workloads.Workload("static_b", M, K, "bf16", fmt, "swizzled", 1e-6, seed=M + K)
     x, r, w = workloads.make_inputs(wl, "cpu")
-    wmat = workloads.make_rows(workloads.Workload("wmat_s", N, K, "bf16", "nvfp4", "swizzled",
+    wmat = workloads.make_rows(workloads.Workload("wmat_s", N, K, "bf16", fmt, "swizzled",
                                                   1e-6, seed=N + 5), "x", 0, N, "cpu")
-    ob = oracle.quantize(wmat.float().numpy(), "nvfp4", "swizzled")
-    pb, sb = fq.quantize_fp4(wmat.cuda(), fmt="nvfp4", sf_layout="swizzled")
+    ob = oracle.quantize(wmat.float().numpy(), fmt, "swizzled")
+    pb, sb = fq.quantize_fp4(wmat.cuda(), fmt=fmt, sf_layout="swizzled")
     torch.cuda.synchronize()
     xr, rr, wr = x.cuda(), r.clone().cuda(), w.cuda()
     stream = torch.cuda.Stream()
@@ -321,10 +325,10 @@ def test_gemm_static_weights_pdl2(M, N, K, variant):
     outs = []
     with torch.cuda.stream(stream):
         for _ in range(steps):
-            pa, sa = fq.add_rmsnorm_fp4quant(xr, rr, wr, eps=wl.eps, fmt="nvfp4",
+            pa, sa = fq.add_rmsnorm_fp4quant(xr, rr, wr, eps=wl.eps, fmt=fmt,
                                              sf_layout="swizzled", pdl=True, stream=stream)
             outs.append((pa, sa, fq.gemm_nvfp4_bf16(pa, pb, sa, sb, pdl=2, variant=variant,
-                                                    stream=stream)))
+                                                    stream=stream, fmt=fmt)))
     stream.synchronize()
     assert np.array_equal(pb.cpu().numpy(), ob.packed)
     assert np.array_equal(sb.cpu().numpy(), ob.sf_swizzled)
@@ -332,7 +336,7 @@ def test_gemm_static_weights_pdl2(M, N, K, variant):
     # producer wrote (the producer's own parity is tested on its own)
     for pa, sa, got in outs:
         g = oracle.gemm_bf16(pa.cpu().numpy(), ob.packed, sa.cpu().numpy(), ob.sf_swizzled,
-                             M, N, K)
+                             M, N, K, fmt=fmt)
         check(got, g, K, "random")
 
 
